@@ -1,0 +1,331 @@
+"""Seeded synthetic workloads for the HiSparse decode-time swap-in resolver.
+
+This module only *generates inputs*: sequence lengths, per-step top-k index
+sets, KV row bytes and backup rows.  It holds none of the resolver's
+arithmetic (no hit test, no LRU, no victim choice), so both the CPU oracle
+(tests only) and the CUDA path can be fed from it without sharing any of the
+method's logic.
+
+Random numbers come from one counter-based generator, splitmix64
+(Steele, Lea & Flood, "Fast splittable pseudorandom number generators",
+OOPSLA 2014): output i of a stream with key K is mix(K + (i + 1) * 0x9E3779B97F4A7C15).
+Integers in [0, n) are drawn as ((u >> 32) * n) >> 32, so draws are exact
+integer arithmetic and identical on every machine.
+
+Workload shapes follow the pages' decode setting: the user guide's example
+config (top_k 2048, device_buffer_size 6144, host_to_device_ratio 10), its
+40K-token random-input benchmark, and MLA-sized KV rows (fp8 e4m3 latent +
+fp32 scales + bf16 rope = 656 B, or 576 bf16 values = 1152 B).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_MASK32 = np.uint64(0xFFFFFFFF)
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    """splitmix64 finaliser on a uint64 array (wrapping arithmetic)."""
+    z = np.asarray(z, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def _mix_scalar(x: int) -> int:
+    return int(_mix(np.array([x & 0xFFFFFFFFFFFFFFFF], dtype=np.uint64))[0])
+
+
+def stream_key(seed: int, *ids: int) -> int:
+    """Derive an independent stream key from a seed and integer ids."""
+    k = _mix_scalar(seed)
+    for i in ids:
+        k = _mix_scalar(k ^ ((i * 0xD1B54A32D192ED03) & 0xFFFFFFFFFFFFFFFF))
+    return k
+
+
+class Stream:
+    """A sequential splitmix64 stream (keyed, counter-based)."""
+
+    def __init__(self, key: int):
+        self.key = np.uint64(key & 0xFFFFFFFFFFFFFFFF)
+        self.ctr = 0
+
+    def u64(self, n: int) -> np.ndarray:
+        idx = np.arange(self.ctr + 1, self.ctr + 1 + n, dtype=np.uint64)
+        self.ctr += n
+        with np.errstate(over="ignore"):
+            return _mix(self.key + idx * _GOLDEN)
+
+    def below(self, n: int, bound) -> np.ndarray:
+        """n integers uniform in [0, bound) (bound scalar or array, < 2^32)."""
+        u = self.u64(n) >> np.uint64(32)
+        b = np.asarray(bound, dtype=np.uint64)
+        return ((u * b) >> np.uint64(32)).astype(np.int64)
+
+    def unit(self, n: int) -> np.ndarray:
+        """n doubles uniform in [0, 1) with 53 random bits."""
+        return (self.u64(n) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+# --------------------------------------------------------------------------
+# Workload configurations
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class Workload:
+    """One synthetic decode workload (shapes of the pages' decode setting)."""
+
+    name: str
+    config_no: int
+    num_requests: int
+    num_layers: int
+    anchor_of_layer: List[int]      # -1: layer owns its top-k and hot state
+    steps: int                      # decode steps
+    substeps: int                   # swap-in calls per decode step (spec verify)
+    top_k: int
+    device_buffer_size: int
+    row_bytes: int
+    row_kind: str                   # "bf16" or "mla_fp8"
+    host_to_device_ratio: int
+    keep: int                       # indices kept from the previous set
+    new_mix: str                    # "uniform" or "mixture"
+    backup: bool                    # one backup row per request per layer per step
+    seq_lens0: np.ndarray           # int32 [R], lengths before step 0
+    seed: int
+
+    @property
+    def growth(self) -> int:
+        return self.steps if self.backup else 0
+
+    @property
+    def host_capacity(self) -> np.ndarray:
+        """Tokens of host storage per request: the context plus growth."""
+        return (self.seq_lens0.astype(np.int64) + self.growth).astype(np.int64)
+
+    def seq_lens_at(self, step: int) -> np.ndarray:
+        if self.backup:
+            return (self.seq_lens0 + step).astype(np.int32)
+        return self.seq_lens0.astype(np.int32)
+
+    @property
+    def anchors(self) -> List[int]:
+        return [l for l in range(self.num_layers) if self.anchor_of_layer[l] < 0]
+
+
+def _seed(config_no: int) -> int:
+    return 0x48530000 + config_no
+
+
+def make_config(config_no: int, *, steps: Optional[int] = None,
+                num_requests: Optional[int] = None) -> Workload:
+    """The five workloads; ``steps``/``num_requests`` shrink a config for tests."""
+    seed = _seed(config_no)
+    if config_no == 1:
+        # Tiny check: 4 requests, seq_len {400,3000,5000,8000}, k 256, D 512,
+        # 576 bf16 values per row, 70% of each set redrawn from the previous.
+        R = 4
+        w = Workload("tiny", 1, R, 1, [-1], 8, 1, 256, 512, 1152, "bf16", 10,
+                     int(round(0.7 * 256)), "uniform", False,
+                     np.array([400, 3000, 5000, 8000], dtype=np.int32), seed)
+    elif config_no == 2:
+        # The guide's decode setting: 32 x 40000 tokens, k 2048, D 6144, ratio
+        # 10, 656 B MLA fp8 rows, 80% reuse, new indices from the mixture.
+        R = 32
+        w = Workload("decode_40k", 2, R, 1, [-1], 64, 1, 2048, 6144, 656,
+                     "mla_fp8", 10, int(round(0.8 * 2048)), "mixture", False,
+                     np.full(R, 40000, dtype=np.int32), seed)
+    elif config_no == 3:
+        # Mixed lengths U[2048, 81920], 4 independent layers, 60% reuse,
+        # eager backup of one row per request per layer per step.
+        R = 128
+        st = Stream(stream_key(seed, 0xC3))
+        lens = (2048 + st.below(R, 81920 - 2048 + 1)).astype(np.int32)
+        w = Workload("mixed_len", 3, R, 4, [-1, -1, -1, -1], 32, 1, 2048, 6144,
+                     656, "mla_fp8", 10, int(round(0.6 * 2048)), "mixture", True,
+                     lens, seed)
+    elif config_no == 4:
+        # Shared-index prefetch: 1 anchor + 3 skip layers, 64 x 65536 tokens,
+        # 70% reuse.  Ratio 11: 64*65536 tokens exceed 10 x 64 x 6144 slots.
+        R = 64
+        w = Workload("shared_index", 4, R, 4, [-1, 0, 0, 0], 32, 1, 2048, 6144,
+                     656, "mla_fp8", 11, int(round(0.7 * 2048)), "mixture", False,
+                     np.full(R, 65536, dtype=np.int32), seed)
+    elif config_no == 5:
+        # Stress + speculative verify: 256 x 32768, D 4096, bf16 1152 B rows,
+        # 3 sub-steps per step at 50% overlap, backup once per decode step.
+        R = 256
+        w = Workload("spec_verify", 5, R, 1, [-1], 16, 3, 2048, 4096, 1152,
+                     "bf16", 10, 1024, "mixture", True,
+                     np.full(R, 32768, dtype=np.int32), seed)
+    else:
+        raise ValueError(f"unknown config {config_no}")
+    if steps is not None:
+        w.steps = steps
+    if num_requests is not None and num_requests != w.num_requests:
+        w.num_requests = num_requests
+        w.seq_lens0 = w.seq_lens0[:num_requests].copy()
+    return w
+
+
+# --------------------------------------------------------------------------
+# Top-k index sets
+# --------------------------------------------------------------------------
+
+class _ZipfRecency:
+    """Inverse-CDF sampler of recency d in [0, S) with P(d) ~ (d+1)^-s."""
+
+    def __init__(self, s: float, max_len: int):
+        w = np.power(np.arange(1, max_len + 1, dtype=np.float64), -s)
+        self.cum = np.cumsum(w)
+
+    def sample(self, u: np.ndarray, S: int) -> np.ndarray:
+        total = self.cum[S - 1]
+        d = np.searchsorted(self.cum[:S], u * total, side="right")
+        return np.minimum(d, S - 1)
+
+
+class TopkSource:
+    """Per-(layer, request) top-k sequences of distinct token indices.
+
+    Step 0 draws ``top_k`` distinct indices; each later call keeps ``keep``
+    of the previous set (a uniform subset) and draws the rest from the
+    workload's mixture, rejecting duplicates.  Each set is emitted in a
+    random order, as an indexer's score order would be.
+    """
+
+    def __init__(self, w: Workload, layer: int, request: int):
+        self.w = w
+        self.st = Stream(stream_key(w.seed, 0x70, layer, request))
+        self.prev: Optional[np.ndarray] = None
+        self.zipf: Optional[_ZipfRecency] = None
+
+    def _draw_new(self, n: int, S: int, exclude: np.ndarray) -> np.ndarray:
+        taken = np.zeros(S, dtype=bool)
+        taken[exclude] = True
+        out: List[np.ndarray] = []
+        need = n
+        while need > 0:
+            c = max(2 * need, 64)
+            if self.w.new_mix == "uniform":
+                cand = self.st.below(c, S)
+            else:
+                coin = self.st.below(c, 2)
+                uni = self.st.below(c, S)
+                if self.zipf is None:
+                    self.zipf = _ZipfRecency(1.1, int(self.w.host_capacity.max()))
+                d = self.zipf.sample(self.st.unit(c), S)
+                cand = np.where(coin == 0, uni, S - 1 - d)
+            # keep first occurrences, in draw order, of indices not yet taken
+            _, first = np.unique(cand, return_index=True)
+            first.sort()
+            cand = cand[first]
+            cand = cand[~taken[cand]][:need]
+            taken[cand] = True
+            out.append(cand)
+            need -= cand.size
+        return np.concatenate(out)
+
+    def next(self, S: int) -> np.ndarray:
+        k = self.w.top_k
+        if S < k:
+            raise ValueError("sequence shorter than top_k")
+        if self.prev is None:
+            cur = self._draw_new(k, S, np.zeros(0, dtype=np.int64))
+        else:
+            order = np.argsort(self.st.u64(self.prev.size), kind="stable")
+            kept = self.prev[order[: self.w.keep]]
+            kept = kept[kept < S]
+            new = self._draw_new(k - kept.size, S, kept)
+            cur = np.concatenate([kept, new])
+        perm = np.argsort(self.st.u64(cur.size), kind="stable")
+        cur = cur[perm]
+        self.prev = cur
+        return cur.astype(np.int32)
+
+
+def topk_schedule(w: Workload) -> Dict[int, np.ndarray]:
+    """All top-k inputs: {anchor layer: int32 [steps*substeps][R][k]}.
+
+    Call c of a layer is decode step c // substeps; sets chain across
+    sub-steps and decode steps alike.
+    """
+    out = {}
+    calls = w.steps * w.substeps
+    for l in w.anchors:
+        arr = np.empty((calls, w.num_requests, w.top_k), dtype=np.int32)
+        for r in range(w.num_requests):
+            src = TopkSource(w, l, r)
+            for c in range(calls):
+                S = int(w.seq_lens_at(c // w.substeps)[r])
+                arr[c, r] = src.next(S)
+        out[l] = arr
+    return out
+
+
+# --------------------------------------------------------------------------
+# KV row bytes
+# --------------------------------------------------------------------------
+
+def _row_words(w: Workload, layer: int, request: int, tokens: np.ndarray,
+               nwords: int) -> np.ndarray:
+    """uint64 [len(tokens)][nwords], a pure function of (layer, request, token)."""
+    key = np.uint64(stream_key(w.seed, 0x52, layer, request))
+    t = np.asarray(tokens, dtype=np.uint64)[:, None]
+    i = np.arange(nwords, dtype=np.uint64)[None, :]
+    with np.errstate(over="ignore"):
+        ctr = t * np.uint64(nwords) + i + np.uint64(1)
+        return _mix(key + ctr * _GOLDEN)
+
+
+def _to_bf16_bits(f: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (round to nearest even), returning uint16 bits."""
+    b = np.asarray(f, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return b.astype(np.uint16)
+
+
+def kv_rows(w: Workload, layer: int, request: int, tokens) -> np.ndarray:
+    """uint8 [len(tokens)][row_bytes]: the KV rows of these token positions.
+
+    "mla_fp8" (656 B): 512 fp8 e4m3 latent bytes (random, never the NaN
+    codes 0x7F/0xFF) + 4 fp32 scales uniform in [2^-8, 1] + 64 bf16 rope
+    values uniform in [-1, 1].  "bf16": row_bytes/2 bf16 values in [-1, 1].
+    """
+    tokens = np.atleast_1d(np.asarray(tokens, dtype=np.int64))
+    n = tokens.size
+    B = w.row_bytes
+    if w.row_kind == "mla_fp8":
+        assert B == 656
+        words = _row_words(w, layer, request, tokens, 64 + 2 + 32)
+        latent = words[:, :64].copy().view(np.uint8).reshape(n, 512)
+        latent[latent == 0x7F] = 0x7E
+        latent[latent == 0xFF] = 0xFE
+        u32 = words[:, 64:].copy().view(np.uint32).reshape(n, 68)
+        sc = (2.0 ** -8 + (1.0 - 2.0 ** -8) * (u32[:, :4] >> 8) * (2.0 ** -24)).astype(np.float32)
+        rope = _to_bf16_bits((u32[:, 4:] >> 8).astype(np.float64) * (2.0 ** -23) - 1.0)
+        return np.concatenate([latent, sc.view(np.uint8).reshape(n, 16),
+                               rope.view(np.uint8).reshape(n, 128)], axis=1)
+    if w.row_kind == "bf16":
+        nv = B // 2
+        words = _row_words(w, layer, request, tokens, (nv + 1) // 2)
+        u32 = words.copy().view(np.uint32).reshape(n, -1)[:, :nv]
+        vals = _to_bf16_bits((u32 >> 8).astype(np.float64) * (2.0 ** -23) - 1.0)
+        return vals.view(np.uint8).reshape(n, B)
+    raise ValueError(w.row_kind)
+
+
+def fill_host_rows(w: Workload, layer: int, request: int, dst: np.ndarray,
+                   upto: int, chunk: int = 8192) -> None:
+    """Write rows [0, upto) of (layer, request) into dst ([cap][B] uint8)."""
+    for t0 in range(0, upto, chunk):
+        t1 = min(upto, t0 + chunk)
+        dst[t0:t1] = kv_rows(w, layer, request, np.arange(t0, t1))

@@ -1,0 +1,368 @@
+/*
+ * hisparse_oracle.c -- plain, slow, single-threaded CPU oracle of the HiSparse
+ * decode-time swap-in resolver.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and
+ * the benchmark's CPU-baseline leg load this file's library.  The product
+ * path (the CUDA library) never calls it, and this file shares no code,
+ * header, table or helper with it.
+ *
+ * Citations name the two pages the method is taken from:
+ *   [Arch]  "HiSparse local KV offload architecture" (vLLM design doc)
+ *   [Guide] "HiSparse: Hierarchical Sparse Attention" (SGLang user guide)
+ *
+ * The method is an exact data-structure algorithm (no floating point): each
+ * function below writes out its definition step by step, in the order the
+ * pages give, and uses the C library's qsort as the only "library step".
+ *
+ * Points the pages leave open, and the reading taken here:
+ *   - fast path iff seq_len <= device_buffer_size ([Guide] Decode Workflow);
+ *     it changes no map, LRU entry or plan;
+ *   - misses are handled in ascending token order, victims are the non-hit
+ *     slots in ascending (last_used, slot) order, miss i goes to victim i;
+ *   - the LRU clock ("tick") of a hot state advances by one on every swap-in
+ *     call, starting at 1; prefill stamps 0; every slot selected by a call
+ *     (hit or refilled) gets last_used = tick;
+ *   - top-k entries are -1 (padding, resolves to -1) or distinct positions in
+ *     [0, seq_len); anything else sets a per-request status, leaves that
+ *     request's state untouched and writes -1 to all its outputs.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define HSO_OK 0
+#define HSO_BAD_INDEX 1     /* an entry outside {-1} U [0, seq_len) */
+#define HSO_DUPLICATE 2     /* a position selected twice            */
+#define HSO_BAD_SEQ_LEN 3   /* seq_len outside [0, host capacity]   */
+#define HSO_BAD_POSITION 4  /* backup position outside [0, capacity) */
+
+typedef struct hs_oracle {
+    int R, L, k, D;
+    int64_t B;
+    int track_bytes;
+    int *anchor;          /* [L]; -1 = the layer owns its hot state          */
+    int64_t *cap;         /* [R]; host token capacity per request           */
+    int64_t *host_off;    /* [R]; first host token row of each request      */
+    int64_t total_cap;
+    /* hot state, allocated only for layers with anchor == -1 */
+    int32_t **tok2slot;   /* [L] -> [total_cap]  token -> slot or -1        */
+    int32_t **slot2tok;   /* [L] -> [R*D]        slot -> token or -1        */
+    uint32_t **last_used; /* [L] -> [R*D]        LRU stamp of each slot     */
+    uint32_t *tick;       /* [L]                 stamp of the latest call   */
+    /* bytes (only with track_bytes) */
+    uint8_t **host;       /* [L] -> [total_cap * B]  pinned host pool       */
+    uint8_t **dev;        /* [L] -> [R * D * B]      device hot buffer      */
+} hs_oracle;
+
+static void hso_free(hs_oracle *o)
+{
+    if (!o) return;
+    for (int l = 0; l < o->L; ++l) {
+        if (o->tok2slot) free(o->tok2slot[l]);
+        if (o->slot2tok) free(o->slot2tok[l]);
+        if (o->last_used) free(o->last_used[l]);
+        if (o->host) free(o->host[l]);
+        if (o->dev) free(o->dev[l]);
+    }
+    free(o->tok2slot); free(o->slot2tok); free(o->last_used); free(o->tick);
+    free(o->host); free(o->dev);
+    free(o->anchor); free(o->cap); free(o->host_off);
+    free(o);
+}
+
+void hso_destroy(hs_oracle *o) { hso_free(o); }
+
+hs_oracle *hso_create(int R, int L, int64_t B, int k, int D,
+                      const int *anchor_of_layer, const int64_t *host_capacity,
+                      int track_bytes)
+{
+    if (R <= 0 || L <= 0 || B <= 0 || k <= 0 || D <= 0 || k > D) return NULL;
+    hs_oracle *o = (hs_oracle *)calloc(1, sizeof(hs_oracle));
+    if (!o) return NULL;
+    o->R = R; o->L = L; o->B = B; o->k = k; o->D = D;
+    o->track_bytes = track_bytes;
+    o->anchor = (int *)malloc(sizeof(int) * (size_t)L);
+    o->cap = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
+    o->host_off = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
+    o->tok2slot = (int32_t **)calloc((size_t)L, sizeof(int32_t *));
+    o->slot2tok = (int32_t **)calloc((size_t)L, sizeof(int32_t *));
+    o->last_used = (uint32_t **)calloc((size_t)L, sizeof(uint32_t *));
+    o->tick = (uint32_t *)calloc((size_t)L, sizeof(uint32_t));
+    o->host = (uint8_t **)calloc((size_t)L, sizeof(uint8_t *));
+    o->dev = (uint8_t **)calloc((size_t)L, sizeof(uint8_t *));
+    if (!o->anchor || !o->cap || !o->host_off || !o->tok2slot || !o->slot2tok ||
+        !o->last_used || !o->tick || !o->host || !o->dev) { hso_free(o); return NULL; }
+    int64_t off = 0;
+    for (int r = 0; r < R; ++r) {
+        o->cap[r] = host_capacity[r];
+        o->host_off[r] = off;
+        off += host_capacity[r];
+    }
+    o->total_cap = off;
+    for (int l = 0; l < L; ++l) {
+        o->anchor[l] = anchor_of_layer ? anchor_of_layer[l] : -1;
+        if (o->anchor[l] >= L || o->anchor[l] == l) { hso_free(o); return NULL; }
+        if (o->anchor[l] < 0) {
+            /* [Arch] Ownership: the hot-row map and LRU belong to the
+             * per-cache runtime; index-sharing followers hold none
+             * ([Arch] Performance invariants). */
+            o->tok2slot[l] = (int32_t *)malloc(sizeof(int32_t) * (size_t)o->total_cap);
+            o->slot2tok[l] = (int32_t *)malloc(sizeof(int32_t) * (size_t)R * D);
+            o->last_used[l] = (uint32_t *)calloc((size_t)R * D, sizeof(uint32_t));
+            if (!o->tok2slot[l] || !o->slot2tok[l] || !o->last_used[l]) { hso_free(o); return NULL; }
+            for (int64_t i = 0; i < o->total_cap; ++i) o->tok2slot[l][i] = -1;
+            for (int64_t i = 0; i < (int64_t)R * D; ++i) o->slot2tok[l][i] = -1;
+        }
+        if (track_bytes) {
+            o->host[l] = (uint8_t *)calloc((size_t)(o->total_cap * B), 1);
+            o->dev[l] = (uint8_t *)calloc((size_t)((int64_t)R * D * B), 1);
+            if (!o->host[l] || !o->dev[l]) { hso_free(o); return NULL; }
+        }
+    }
+    return o;
+}
+
+uint8_t *hso_host_row(hs_oracle *o, int layer, int r, int64_t t)
+{
+    if (!o->track_bytes) return NULL;
+    return o->host[layer] + (o->host_off[r] + t) * o->B;
+}
+
+uint8_t *hso_dev_row(hs_oracle *o, int layer, int r, int64_t s)
+{
+    if (!o->track_bytes) return NULL;
+    return o->dev[layer] + ((int64_t)r * o->D + s) * o->B;
+}
+
+/* Copy host row t of request r into device slot s of the same layer. */
+static void copy_row(hs_oracle *o, int layer, int r, int32_t t, int32_t s)
+{
+    if (!o->track_bytes) return;
+    memcpy(hso_dev_row(o, layer, r, s), hso_host_row(o, layer, r, t), (size_t)o->B);
+}
+
+/*
+ * Prefill: the hot buffer of every request starts with the most recent
+ * n = min(S, D) tokens, slot i holding token S - n + i, all stamped 0.
+ * ([Guide] Decode Workflow: for S <= D "all KV is already in the buffer",
+ * which fixes slot = token in that case.)
+ */
+int hso_prefill(hs_oracle *o, const int32_t *seq_lens)
+{
+    for (int r = 0; r < o->R; ++r)
+        if (seq_lens[r] < 0 || seq_lens[r] > o->cap[r]) return -1;
+    for (int l = 0; l < o->L; ++l) {
+        for (int r = 0; r < o->R; ++r) {
+            int32_t S = seq_lens[r];
+            int32_t n = S < o->D ? S : o->D;
+            if (o->anchor[l] < 0) {
+                int32_t *t2s = o->tok2slot[l] + o->host_off[r];
+                int32_t *s2t = o->slot2tok[l] + (int64_t)r * o->D;
+                uint32_t *lu = o->last_used[l] + (int64_t)r * o->D;
+                for (int64_t t = 0; t < o->cap[r]; ++t) t2s[t] = -1;
+                for (int32_t s = 0; s < o->D; ++s) { s2t[s] = -1; lu[s] = 0; }
+                for (int32_t i = 0; i < n; ++i) {
+                    s2t[i] = S - n + i;
+                    t2s[S - n + i] = i;
+                }
+            }
+            for (int32_t i = 0; i < n; ++i) copy_row(o, l, r, S - n + i, i);
+        }
+        o->tick[l] = 0;
+    }
+    return 0;
+}
+
+/* Sort keys for the misses (ascending token). */
+static int cmp_i32(const void *a, const void *b)
+{
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/* Sort keys for LRU candidates: ascending (last_used, slot). */
+typedef struct { uint32_t last_used; int32_t slot; } lru_key;
+static int cmp_lru(const void *a, const void *b)
+{
+    const lru_key *x = (const lru_key *)a, *y = (const lru_key *)b;
+    if (x->last_used != y->last_used) return x->last_used < y->last_used ? -1 : 1;
+    return (x->slot > y->slot) - (x->slot < y->slot);
+}
+
+/* Validate one request's top-k row; returns a status code. */
+static int32_t validate(const int32_t *topk, int k, int32_t S)
+{
+    int32_t *v = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+    int n = 0, bad = 0;
+    for (int j = 0; j < k; ++j) {
+        if (topk[j] == -1) continue;
+        if (topk[j] < 0 || topk[j] >= S) { bad = 1; continue; }
+        v[n++] = topk[j];
+    }
+    int32_t st = HSO_OK;
+    if (bad) st = HSO_BAD_INDEX;
+    else {
+        qsort(v, (size_t)n, sizeof(int32_t), cmp_i32);
+        for (int i = 1; i < n; ++i)
+            if (v[i] == v[i - 1]) { st = HSO_DUPLICATE; break; }
+    }
+    free(v);
+    return st;
+}
+
+/*
+ * One request of one swap-in call on hot-state layer `a`
+ * ([Guide] Decode Workflow, swap-in step; [Arch] Hot lookup and LRU).
+ */
+static void swap_in_request(hs_oracle *o, int a, int r, const int32_t *topk,
+                            int32_t S, uint32_t tick, int32_t *out,
+                            int32_t *plan, int32_t *count, int32_t *status)
+{
+    const int k = o->k, D = o->D;
+    *count = 0;
+    if (S < 0 || S > o->cap[r]) *status = HSO_BAD_SEQ_LEN;
+    else *status = validate(topk, k, S);
+    if (*status != HSO_OK) {
+        for (int j = 0; j < k; ++j) out[j] = -1;
+        return;
+    }
+
+    /* Short sequence: every KV row is already in the buffer, slot = token. */
+    if (S <= D) {
+        for (int j = 0; j < k; ++j) out[j] = topk[j];
+        return;
+    }
+
+    int32_t *t2s = o->tok2slot[a] + o->host_off[r];
+    int32_t *s2t = o->slot2tok[a] + (int64_t)r * D;
+    uint32_t *lu = o->last_used[a] + (int64_t)r * D;
+
+    /* Hit detection: a token is hot iff the token->slot map holds a slot. */
+    char *is_hit_slot = (char *)calloc((size_t)D, 1);
+    int32_t *miss = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+    int m = 0;
+    for (int j = 0; j < k; ++j) {
+        int32_t t = topk[j];
+        if (t < 0) continue;
+        if (t2s[t] >= 0) is_hit_slot[t2s[t]] = 1;
+        else miss[m++] = t;
+    }
+    /* Misses are handled in ascending token order. */
+    qsort(miss, (size_t)m, sizeof(int32_t), cmp_i32);
+
+    /* LRU victims: the m non-hit slots with the smallest (last_used, slot). */
+    lru_key *cand = (lru_key *)malloc(sizeof(lru_key) * (size_t)D);
+    int nc = 0;
+    for (int32_t s = 0; s < D; ++s)
+        if (!is_hit_slot[s]) { cand[nc].last_used = lu[s]; cand[nc].slot = s; ++nc; }
+    qsort(cand, (size_t)nc, sizeof(lru_key), cmp_lru);
+    /* k <= D and every hit uses one slot, so m <= k - hits <= D - hits = nc. */
+
+    /* Refill: miss i evicts victim i and is copied from pinned host memory. */
+    for (int i = 0; i < m; ++i) {
+        int32_t v = cand[i].slot, t = miss[i];
+        if (s2t[v] >= 0) t2s[s2t[v]] = -1;
+        s2t[v] = t;
+        t2s[t] = v;
+        plan[2 * i] = t;
+        plan[2 * i + 1] = v;
+        copy_row(o, a, r, t, v);
+    }
+    *count = m;
+
+    /* Outputs in input order; every selected slot is stamped with the tick. */
+    for (int j = 0; j < k; ++j) {
+        int32_t t = topk[j];
+        if (t < 0) { out[j] = -1; continue; }
+        out[j] = t2s[t];
+        lu[t2s[t]] = tick;
+    }
+    free(is_hit_slot); free(miss); free(cand);
+}
+
+/*
+ * hso_swap_in: resolve one call's top-k rows for every request.
+ *   topk   [R][k] int32     out    [R][k] int32
+ *   plan   [R][k][2] int32  (token, slot) pairs, first count[r] valid
+ *   count  [R] int32        status [R] int32
+ * Returns -1 if `layer` holds no hot state of its own.
+ */
+int hso_swap_in(hs_oracle *o, int layer, const int32_t *topk, const int32_t *seq_lens,
+                int32_t *out, int32_t *plan, int32_t *count, int32_t *status)
+{
+    if (layer < 0 || layer >= o->L || o->anchor[layer] >= 0) return -1;
+    uint32_t tick = ++o->tick[layer];
+    for (int r = 0; r < o->R; ++r)
+        swap_in_request(o, layer, r, topk + (int64_t)r * o->k, seq_lens[r], tick,
+                        out + (int64_t)r * o->k, plan + (int64_t)r * o->k * 2,
+                        count + r, status + r);
+    return 0;
+}
+
+/*
+ * Replay a recorded miss plan on another layer's KV storage
+ * ([Guide] Shared-index prefetch): for every (token, slot) pair, copy that
+ * layer's host row into that layer's device slot.  No map or LRU changes.
+ */
+int hso_replay(hs_oracle *o, const int32_t *plan, const int32_t *count, int layer)
+{
+    if (layer < 0 || layer >= o->L) return -1;
+    for (int r = 0; r < o->R; ++r)
+        for (int i = 0; i < count[r]; ++i)
+            copy_row(o, layer, r, plan[((int64_t)r * o->k + i) * 2],
+                     plan[((int64_t)r * o->k + i) * 2 + 1]);
+    return 0;
+}
+
+/*
+ * Eager backup ([Guide] Decode Workflow): each request's newest KV row goes
+ * to host position positions[r] (-1 skips the request); the position is the
+ * request's current seq_len.  A position inside the device buffer (< D)
+ * belongs to a short sequence, whose buffer holds every token at
+ * slot = token, so device slot p is written as well and, for a layer with
+ * hot state, the maps pair slot p with token p (their stamps are left as
+ * they are).
+ */
+int hso_backup(hs_oracle *o, int layer, const uint8_t *rows, const int32_t *positions,
+               int32_t *status)
+{
+    if (layer < 0 || layer >= o->L) return -1;
+    for (int r = 0; r < o->R; ++r) {
+        int32_t p = positions[r];
+        status[r] = HSO_OK;
+        if (p == -1) continue;
+        if (p < 0 || p >= o->cap[r]) { status[r] = HSO_BAD_POSITION; continue; }
+        if (o->track_bytes)
+            memcpy(hso_host_row(o, layer, r, p), rows + (int64_t)r * o->B, (size_t)o->B);
+        if (p < o->D) {
+            if (o->track_bytes)
+                memcpy(hso_dev_row(o, layer, r, p), rows + (int64_t)r * o->B, (size_t)o->B);
+            if (o->anchor[layer] < 0) {
+                int32_t *t2s = o->tok2slot[layer] + o->host_off[r];
+                int32_t *s2t = o->slot2tok[layer] + (int64_t)r * o->D;
+                /* unlink whatever slot p and token p were paired with */
+                if (s2t[p] >= 0 && s2t[p] != p) t2s[s2t[p]] = -1;
+                if (t2s[p] >= 0 && t2s[p] != p) s2t[t2s[p]] = -1;
+                s2t[p] = p;
+                t2s[p] = p;
+            }
+        }
+    }
+    return 0;
+}
+
+/* Copy out a hot-state layer's maps, LRU stamps and tick. */
+int hso_state(hs_oracle *o, int layer, int32_t *slot2tok, uint32_t *last_used,
+              int32_t *tok2slot, uint32_t *tick)
+{
+    if (layer < 0 || layer >= o->L || o->anchor[layer] >= 0) return -1;
+    size_t nd = (size_t)o->R * o->D;
+    if (slot2tok) memcpy(slot2tok, o->slot2tok[layer], nd * sizeof(int32_t));
+    if (last_used) memcpy(last_used, o->last_used[layer], nd * sizeof(uint32_t));
+    if (tok2slot) memcpy(tok2slot, o->tok2slot[layer], (size_t)o->total_cap * sizeof(int32_t));
+    if (tick) *tick = o->tick[layer];
+    return 0;
+}
+
+int64_t hso_total_capacity(const hs_oracle *o) { return o->total_cap; }

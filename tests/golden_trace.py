@@ -1,0 +1,49 @@
+"""Parser for the hand-derived single-request traces in tests/golden/."""
+
+from __future__ import annotations
+
+import os
+from typing import Dict, List, Tuple
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _ints(s: str) -> List[int]:
+    return [int(x) for x in s.split(",")] if s and s != "-" else []
+
+
+def _kv(tokens: List[str]) -> Dict[str, str]:
+    return dict(t.split("=", 1) for t in tokens)
+
+
+def load(name: str) -> Tuple[Dict[str, int], List[Tuple[str, dict]]]:
+    """Returns (layout {D,k,cap}, [(op, args)]), op in prefill/call/backup."""
+    layout, ops = None, []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            head, *rest = line.split()
+            kv = _kv(rest)
+            if head == "layout":
+                layout = {k: int(v) for k, v in kv.items()}
+            elif head == "prefill":
+                ops.append(("prefill", {"S": int(kv["S"])}))
+            elif head == "call":
+                ops.append(("call", {"S": int(kv["S"]), "topk": _ints(kv["topk"])}))
+            elif head == "expect":
+                plan = [] if kv["plan"] == "-" else \
+                    [tuple(int(x) for x in p.split(":")) for p in kv["plan"].split(",")]
+                ops[-1][1]["expect"] = {
+                    "out": _ints(kv["out"]), "plan": plan, "status": int(kv["status"]),
+                    "slot2tok": _ints(kv["slot2tok"]), "last_used": _ints(kv["last_used"])}
+            elif head == "backup":
+                ops.append(("backup", {"pos": int(kv["pos"])}))
+            else:
+                raise ValueError(head)
+    return layout, ops
+
+
+def names() -> List[str]:
+    return sorted(n for n in os.listdir(GOLDEN) if n.endswith(".txt"))

@@ -1,0 +1,116 @@
+"""The oracle's pins catch plausible mistakes (CPU only).
+
+Each case plants one mistake in a temporary copy of the oracle's C source,
+builds it with gcc, and checks that at least one pin (golden traces, the
+recency-list model, invariants, closed forms) rejects the planted oracle.
+The oracle in the repository is never modified.
+"""
+
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle as O
+from golden_trace import names
+import test_oracle as T
+
+SRC = os.path.join(os.path.dirname(O.__file__), "hisparse_oracle.c")
+
+# (id, original text, planted mistake)
+MUTANTS = [
+    ("lru_newest_first",
+     "return x->last_used < y->last_used ? -1 : 1;",
+     "return x->last_used < y->last_used ? 1 : -1;"),
+    ("slot_tiebreak_reversed",
+     "return (x->slot > y->slot) - (x->slot < y->slot);",
+     "return (x->slot < y->slot) - (x->slot > y->slot);"),
+    ("misses_not_sorted",
+     "qsort(miss, (size_t)m, sizeof(int32_t), cmp_i32);",
+     ";"),
+    ("evicted_token_not_unmapped",
+     "if (s2t[v] >= 0) t2s[s2t[v]] = -1;",
+     ";"),
+    ("hits_not_stamped",
+     "lu[t2s[t]] = tick;",
+     "if (!is_hit_slot[t2s[t]]) lu[t2s[t]] = tick;"),
+    ("hit_slots_evictable",
+     "if (!is_hit_slot[s]) { cand[nc]",
+     "if (1) { cand[nc]"),
+    ("fast_path_strict",
+     "if (S <= D) {\n        for (int j = 0; j < k; ++j) out[j] = topk[j];",
+     "if (S < D) {\n        for (int j = 0; j < k; ++j) out[j] = topk[j];"),
+    ("prefill_oldest_tokens",
+     "s2t[i] = S - n + i;\n                    t2s[S - n + i] = i;",
+     "s2t[i] = i;\n                    t2s[i] = i;"),
+    ("tick_not_advanced",
+     "uint32_t tick = ++o->tick[layer];",
+     "uint32_t tick = o->tick[layer] + 1;"),
+    ("copy_transposed",
+     "copy_row(o, a, r, t, v);",
+     "copy_row(o, a, r, v, t);"),
+    ("plan_transposed",
+     "plan[2 * i] = t;\n        plan[2 * i + 1] = v;",
+     "plan[2 * i] = v;\n        plan[2 * i + 1] = t;"),
+    ("duplicates_accepted",
+     "if (v[i] == v[i - 1]) { st = HSO_DUPLICATE; break; }",
+     ";"),
+    ("error_keeps_outputs",
+     "for (int j = 0; j < k; ++j) out[j] = -1;\n        return;",
+     "return;"),
+    ("backup_skips_device",
+     "memcpy(hso_dev_row(o, layer, r, p), rows + (int64_t)r * o->B, (size_t)o->B);",
+     ";"),
+    ("replay_wrong_layer",
+     "copy_row(o, layer, r, plan[((int64_t)r * o->k + i) * 2],",
+     "copy_row(o, 0, r, plan[((int64_t)r * o->k + i) * 2],"),
+]
+
+
+def run_all_pins(lib_path):
+    """Names of the pins that reject the oracle at lib_path."""
+    failed = []
+    for n in names():
+        try:
+            if T.run_trace_on_oracle(n, lib_path) is not None:
+                failed.append("golden:" + n)
+        except Exception:
+            failed.append("golden:" + n)
+    for D, S, k, nc in [(3, 5, 2, 3), (4, 7, 3, 2)]:
+        progs = T._exhaustive_programs(S, k, nc)
+        try:
+            if T.compare_with_model(D, k, [S] * len(progs), progs, lib_path) is not None:
+                failed.append(f"exhaustive:{D},{S},{k}")
+        except Exception:
+            failed.append(f"exhaustive:{D},{S},{k}")
+    for pin in T.PINS:
+        try:
+            pin(lib_path)
+        except Exception:
+            failed.append(pin.__name__)
+    return failed
+
+
+@pytest.mark.parametrize("mid,orig,planted", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, mid, orig, planted):
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"mutation anchor for {mid} not unique"
+    mut = tmp_path / f"oracle_{mid}.c"
+    mut.write_text(src.replace(orig, planted))
+    lib = tmp_path / f"liboracle_{mid}.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-w", "-shared", "-fPIC",
+                           "-o", str(lib), str(mut)])
+    # run the pins in a child process: a planted mistake may also crash it
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = ("import sys; sys.path[:0] = [%r, %r]; import test_oracle_mutants as M; "
+            "f = M.run_all_pins(%r); print(f); sys.exit(3 if f else 0)"
+            % (here, os.path.dirname(here), str(lib)))
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         timeout=600)
+    assert res.returncode != 0, f"no pin rejects the planted mistake {mid}"
+
+
+def test_unmodified_oracle_passes_all_pins():
+    assert run_all_pins(O.build()) == []
