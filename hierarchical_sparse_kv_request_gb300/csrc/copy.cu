@@ -1,0 +1,205 @@
+// copy.cu -- plan replay, eager backup and prefill kernels.
+//
+// Sources: [Guide] "HiSparse: Hierarchical Sparse Attention" -- Shared-index
+// prefetch (skip layers replay the anchor's miss plan with a copy-only kernel
+// on a small fixed grid) and Decode Workflow (eager backup of the newest
+// token's KV to host; short sequences keep every token in the buffer).
+#include "hs_common.cuh"
+
+namespace hs {
+namespace {
+
+constexpr int REPLAY_NT = 512;
+constexpr int REPLAY_UNROLL = 8;
+
+// Copy every (token -> slot) pair of a plan, host row -> device slot, for one
+// layer.  Work items are 16-byte chunks of the rows, numbered over the
+// concatenation of all requests' plan rows; each CTA first builds the prefix
+// sum of plan counts in shared memory (clamped to [0, k]), then walks its
+// items with COPY_UNROLL host loads in flight per thread.  Pairs whose token
+// or slot is out of range are skipped.
+__global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
+{
+    extern __shared__ __align__(16) uint32_t rows_before[];  // [R + 1]
+    __shared__ uint32_t warp_tot[32];
+    if (a.programmatic) {
+        // wait for the resolve grid that writes the plan (griddepcontrol.wait)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+    const int R = a.g.R, k = a.g.k, D = a.g.D;
+    const int tid = threadIdx.x;
+
+    // exclusive prefix of counts over requests (R <= 8192: 16 per thread)
+    const int per = (R + REPLAY_NT - 1) / REPLAY_NT;
+    const int r0 = min(tid * per, R), r1 = min(r0 + per, R);
+    uint32_t local = 0;
+    for (int r = r0; r < r1; ++r) local += (uint32_t)min(max(a.plan_counts[r], 0), k);
+    uint32_t total_rows;
+    uint32_t run = block_exclusive_scan<REPLAY_NT>(local, warp_tot, total_rows);
+    for (int r = r0; r < r1; ++r) {
+        rows_before[r] = run;
+        run += (uint32_t)min(max(a.plan_counts[r], 0), k);
+    }
+    if (tid == 0) rows_before[R] = total_rows;
+    __syncthreads();
+
+    const int CH = a.g.chunks;
+    const int64_t B = a.g.B;
+    const uint64_t total = (uint64_t)total_rows * CH;
+    const uint64_t stride = (uint64_t)gridDim.x * REPLAY_NT;
+    for (uint64_t e = (uint64_t)blockIdx.x * REPLAY_NT + tid; e < total;
+         e += stride * REPLAY_UNROLL) {
+        const uint8_t *src[REPLAY_UNROLL];
+        uint8_t *dst[REPLAY_UNROLL];
+#pragma unroll
+        for (int u = 0; u < REPLAY_UNROLL; ++u) {
+            src[u] = nullptr;
+            dst[u] = nullptr;
+            const uint64_t ee = e + u * stride;
+            if (ee >= total) continue;
+            const uint32_t row = (uint32_t)(ee / CH);
+            const int c = (int)(ee - (uint64_t)row * CH);
+            int lo = 0, hi = R;  // last r with rows_before[r] <= row
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (rows_before[mid] <= row) lo = mid; else hi = mid;
+            }
+            const int r = lo;
+            const uint32_t i = row - rows_before[r];
+            const int32_t *pr = a.plan_rows + ((int64_t)r * k + i) * 2;
+            const int32_t tok = pr[0], slot = pr[1];
+            if (tok < 0 || (int64_t)tok >= a.g.host_cap[r] || slot < 0 || slot >= D) continue;
+            src[u] = a.store.host + (a.g.host_off[r] + tok) * B + c * 16;
+            dst[u] = a.store.dev + ((int64_t)r * D + slot) * B + c * 16;
+        }
+        uint4 v[REPLAY_UNROLL];
+#pragma unroll
+        for (int u = 0; u < REPLAY_UNROLL; ++u)
+            if (src[u]) v[u] = ld_host_v4(src[u]);
+#pragma unroll
+        for (int u = 0; u < REPLAY_UNROLL; ++u)
+            if (src[u]) st_v4(dst[u], v[u]);
+    }
+}
+
+// Backup: one thread per 16-byte chunk of each request's new row.
+__global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
+{
+    const int CH = a.g.chunks;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= (int64_t)a.g.R * CH) return;
+    const int r = (int)(e / CH), c = (int)(e - (int64_t)r * CH);
+    const int32_t p = a.positions[r];
+    if (p == -1) return;
+    const int64_t cap = a.g.host_cap[r];
+    if (p < 0 || (int64_t)p >= cap) {
+        if (c == 0) a.status[r] = kStatusBadPosition;
+        return;
+    }
+    const int64_t B = a.g.B;
+    const int D = a.g.D;
+    const uint4 v = ld_dev_v4(a.rows + (int64_t)r * B + c * 16);
+    st_v4(a.host + (a.g.host_off[r] + p) * B + c * 16, v);
+    if (p < D) {
+        st_v4(a.dev + ((int64_t)r * D + p) * B + c * 16, v);
+        if (c == 0 && a.st.tok2slot) {
+            int32_t *t2s = a.st.tok2slot + a.g.host_off[r];
+            int32_t *s2t = a.st.slot2tok + (int64_t)r * D;
+            const int32_t old_tok = s2t[p], old_slot = t2s[p];
+            if (old_tok >= 0 && old_tok != p) t2s[old_tok] = -1;
+            if (old_slot >= 0 && old_slot != p) s2t[old_slot] = -1;
+            s2t[p] = p;
+            t2s[p] = p;
+        }
+    }
+}
+
+// Prefill: grid (blocks per request, R, L).  For request r, n = min(S, D):
+// slot i <- token S-n+i.  Every map entry is written with its final value,
+// so blocks never race.
+__global__ void __launch_bounds__(256) prefill_kernel(const int32_t *seq_lens,
+                                                      const LayerDescDev *layers, Geometry g,
+                                                      int32_t *status)
+{
+    const int r = blockIdx.y, l = blockIdx.z;
+    const int32_t S = seq_lens[r];
+    if (S == -1) return;
+    const int64_t cap = g.host_cap[r];
+    if (S < 0 || (int64_t)S > cap) {
+        if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusBadSeqLen;
+        return;
+    }
+    if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusOk;
+    const LayerDescDev L = layers[l];
+    const int D = g.D;
+    const int32_t n = S < D ? S : D;
+    const int64_t off = g.host_off[r];
+    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t gs = (int64_t)gridDim.x * blockDim.x;
+    if (L.st.tok2slot) {
+        int32_t *t2s = L.st.tok2slot + off;
+        for (int64_t t = gt; t < cap; t += gs)
+            t2s[t] = (t >= S - n && t < S) ? (int32_t)(t - (S - n)) : -1;
+        int32_t *s2t = L.st.slot2tok + (int64_t)r * D;
+        uint32_t *lu = L.st.last_used + (int64_t)r * D;
+        uint16_t *lru = L.st.lru + (int64_t)r * D;
+        for (int64_t s = gt; s < D; s += gs) {
+            s2t[s] = s < n ? (int32_t)(S - n + s) : -1;
+            lu[s] = 0u;
+            lru[s] = (uint16_t)s;
+        }
+        if (gt == 0) L.st.tick[r] = 0u;
+    }
+    const int CH = g.chunks;
+    const int64_t B = g.B;
+    const int64_t total = (int64_t)n * CH;
+    for (int64_t e = gt; e < total; e += gs) {
+        const int64_t i = e / CH;
+        const int c = (int)(e - i * CH);
+        const uint4 v = ld_host_v4(L.host + (off + S - n + i) * B + c * 16);
+        st_v4(L.dev + ((int64_t)r * D + i) * B + c * 16, v);
+    }
+}
+
+}  // namespace
+
+size_t replay_smem_bytes(int R) { return (size_t)(R + 1) * 4; }
+
+cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s)
+{
+    const size_t smem = replay_smem_bytes(a.g.R);
+    cudaError_t e = cudaFuncSetAttribute(replay_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_ctas);
+    cfg.blockDim = dim3(REPLAY_NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (a.programmatic) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, replay_kernel, a);
+}
+
+cudaError_t launch_backup(const BackupLaunch &a, cudaStream_t s)
+{
+    const int64_t n = (int64_t)a.g.R * a.g.chunks;
+    const int blocks = (int)((n + 255) / 256);
+    backup_kernel<<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const int32_t *seq_lens, const LayerDescDev *layers, int num_layers,
+                           const Geometry &g, int32_t *status, cudaStream_t s)
+{
+    dim3 grid(8, g.R, num_layers);
+    prefill_kernel<<<grid, 256, 0, s>>>(seq_lens, layers, g, status);
+    return cudaGetLastError();
+}
+
+}  // namespace hs

@@ -1,0 +1,414 @@
+// hisparse.cu -- host side of the C ABI declared in include/hisparse.h and
+// include/hisparse_measure.h: layout validation, allocation of the pinned host
+// pool, hot buffers and hot state, and kernel launches.  No entry point that
+// takes a stream synchronises or reads device data back.
+//
+// [Arch] "HiSparse local KV offload architecture", Ownership: the per-cache
+// runtime owns the host/hot storage, the hot-row map and the LRU; Performance
+// invariants: no device readback, one kernel per call.  [Guide] "HiSparse:
+// Hierarchical Sparse Attention", HiSparse Config Parameters: top_k,
+// device_buffer_size, host_to_device_ratio, swap_in_block_size.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "hisparse.h"
+#include "hisparse_measure.h"
+#include "hs_common.cuh"
+
+struct hisparse_handle {
+    int device = 0;
+    int num_sms = 0;
+    int32_t R = 0, L = 0, k = 0, D = 0, ratio = 0;
+    int64_t B = 0;
+    int32_t chunks = 0;
+    std::vector<int32_t> anchor;
+    std::vector<int64_t> cap, off;
+    int64_t total_cap = 0, max_cap = 0;
+    uint8_t *host_pool = nullptr;      // pinned [L][total_cap][B]
+    uint8_t *host_pool_dev = nullptr;  // the same memory, device address
+    uint8_t *dev_buf = nullptr;        // [L][R][D][B]
+    int64_t *d_off = nullptr, *d_cap = nullptr;
+    int32_t *d_status = nullptr;
+    int32_t *d_zero = nullptr;         // [R] zeros, for the initial prefill
+    std::vector<hs::HotState> state;   // per layer; tok2slot null for skip layers
+    hs::LayerDescDev *d_layers = nullptr;
+    int32_t *d_plan_rows = nullptr, *d_plan_counts = nullptr;  // split-copy plan
+    int32_t copy_mode = HISPARSE_COPY_FUSED;
+};
+
+namespace {
+
+hs::Geometry geometry(const hisparse_handle *h)
+{
+    hs::Geometry g;
+    g.R = h->R;
+    g.k = h->k;
+    g.D = h->D;
+    g.B = h->B;
+    g.chunks = h->chunks;
+    g.host_off = h->d_off;
+    g.host_cap = h->d_cap;
+    return g;
+}
+
+hs::LayerStore layer_store(const hisparse_handle *h, int layer)
+{
+    hs::LayerStore s;
+    s.host = h->host_pool_dev + (int64_t)layer * h->total_cap * h->B;
+    s.dev = h->dev_buf + (int64_t)layer * h->R * h->D * h->B;
+    return s;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? HISPARSE_OK : HISPARSE_ERR_CUDA; }
+
+template <class T>
+cudaError_t dev_alloc(T **p, size_t count)
+{
+    return cudaMalloc(reinterpret_cast<void **>(p), count * sizeof(T));
+}
+
+void release(hisparse_handle *h)
+{
+    if (!h) return;
+    for (auto &st : h->state) {
+        cudaFree(st.tok2slot);
+        cudaFree(st.slot2tok);
+        cudaFree(st.last_used);
+        cudaFree(st.lru);
+        cudaFree(st.tick);
+    }
+    cudaFree(h->d_layers);
+    cudaFree(h->d_plan_rows);
+    cudaFree(h->d_plan_counts);
+    cudaFree(h->d_status);
+    cudaFree(h->d_zero);
+    cudaFree(h->d_off);
+    cudaFree(h->d_cap);
+    cudaFree(h->dev_buf);
+    if (h->host_pool) cudaFreeHost(h->host_pool);
+    delete h;
+}
+
+int validate_layout(const hisparse_layout *l)
+{
+    if (l->num_requests < 1 || l->num_layers < 1 || l->row_bytes <= 0 || l->top_k < 1 ||
+        l->device_buffer_size < 1 || l->host_to_device_ratio < 1 || l->swap_in_block_size < 0)
+        return HISPARSE_ERR_LAYOUT;
+    if (l->row_bytes % 16 != 0) return HISPARSE_ERR_LAYOUT;
+    if (l->top_k > l->device_buffer_size) return HISPARSE_ERR_LAYOUT;
+    if (!l->host_capacity) return HISPARSE_ERR_INVALID_ARG;
+    if (l->num_requests > HISPARSE_MAX_REQUESTS || l->top_k > HISPARSE_MAX_TOP_K ||
+        l->device_buffer_size > HISPARSE_MAX_DEVICE_BUFFER)
+        return HISPARSE_ERR_UNSUPPORTED;
+    bool any_owner = false;
+    for (int i = 0; i < l->num_layers; ++i) {
+        const int a = l->anchor_of_layer ? l->anchor_of_layer[i] : -1;
+        if (a < -1 || a >= l->num_layers || a == i) return HISPARSE_ERR_LAYOUT;
+        if (a >= 0 && l->anchor_of_layer[a] != -1) return HISPARSE_ERR_LAYOUT;
+        any_owner |= a == -1;
+    }
+    if (!any_owner) return HISPARSE_ERR_LAYOUT;
+    int64_t total = 0;
+    for (int r = 0; r < l->num_requests; ++r) {
+        const int64_t c = l->host_capacity[r];
+        if (c < 0) return HISPARSE_ERR_LAYOUT;
+        if (c > HISPARSE_MAX_HOST_CAPACITY) return HISPARSE_ERR_UNSUPPORTED;
+        total += c;
+    }
+    if (total < 1) return HISPARSE_ERR_LAYOUT;
+    const int64_t limit = (int64_t)l->host_to_device_ratio * l->num_requests * l->device_buffer_size;
+    if (total > limit) return HISPARSE_ERR_CAPACITY;
+    return HISPARSE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hisparse_version(void) { return 100; }
+
+const char *hisparse_error_string(int code)
+{
+    switch (code) {
+    case HISPARSE_OK: return "ok";
+    case HISPARSE_ERR_INVALID_ARG: return "invalid argument";
+    case HISPARSE_ERR_LAYOUT: return "inconsistent layout";
+    case HISPARSE_ERR_CAPACITY: return "host capacity exceeds host_to_device_ratio * R * D";
+    case HISPARSE_ERR_LAYER: return "layer out of range or without hot state";
+    case HISPARSE_ERR_CUDA: return "CUDA runtime error";
+    case HISPARSE_ERR_NO_MEMORY: return "out of pinned or device memory";
+    case HISPARSE_ERR_UNSUPPORTED: return "size beyond this library's limits";
+    case HISPARSE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    default: return "unknown error";
+    }
+}
+
+int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
+{
+    if (!out) return HISPARSE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!layout) return HISPARSE_ERR_INVALID_ARG;
+    int rc = validate_layout(layout);
+    if (rc != HISPARSE_OK) return rc;
+
+    hisparse_handle *h = new (std::nothrow) hisparse_handle;
+    if (!h) return HISPARSE_ERR_NO_MEMORY;
+    h->R = layout->num_requests;
+    h->L = layout->num_layers;
+    h->k = layout->top_k;
+    h->D = layout->device_buffer_size;
+    h->B = layout->row_bytes;
+    h->chunks = (int32_t)(h->B / 16);
+    h->ratio = layout->host_to_device_ratio;
+    h->anchor.resize(h->L);
+    for (int i = 0; i < h->L; ++i) h->anchor[i] = layout->anchor_of_layer ? layout->anchor_of_layer[i] : -1;
+    h->cap.assign(layout->host_capacity, layout->host_capacity + h->R);
+    h->off.resize(h->R);
+    for (int r = 0; r < h->R; ++r) {
+        h->off[r] = h->total_cap;
+        h->total_cap += h->cap[r];
+        if (h->cap[r] > h->max_cap) h->max_cap = h->cap[r];
+    }
+
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        release(h);
+        return HISPARSE_ERR_CUDA;
+    }
+    int max_smem = 0;
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
+    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap) > (size_t)max_smem ||
+        hs::replay_smem_bytes(h->R) > (size_t)max_smem) {
+        release(h);
+        return HISPARSE_ERR_UNSUPPORTED;
+    }
+
+    // Pinned host pool, mapped into the device address space.  A test hook
+    // makes this allocation fail on request so the failure path is exercised.
+    const size_t pool_bytes = (size_t)h->L * h->total_cap * h->B;
+    const char *fail = std::getenv("HISPARSE_TEST_FAIL_PINNED_ALLOC");
+    if ((fail && fail[0] == '1') ||
+        cudaHostAlloc(reinterpret_cast<void **>(&h->host_pool), pool_bytes,
+                      cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+        h->host_pool = nullptr;
+        cudaGetLastError();
+        release(h);
+        return HISPARSE_ERR_NO_MEMORY;
+    }
+    std::memset(h->host_pool, 0, pool_bytes);
+    if (cudaHostGetDevicePointer(reinterpret_cast<void **>(&h->host_pool_dev), h->host_pool, 0) !=
+        cudaSuccess) {
+        release(h);
+        return HISPARSE_ERR_CUDA;
+    }
+
+    const size_t buf_bytes = (size_t)h->L * h->R * h->D * h->B;
+    const size_t RD = (size_t)h->R * h->D;
+    bool ok = dev_alloc(&h->dev_buf, buf_bytes) == cudaSuccess &&
+              dev_alloc(&h->d_off, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(&h->d_cap, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(&h->d_status, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(&h->d_zero, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(&h->d_layers, (size_t)h->L) == cudaSuccess &&
+              dev_alloc(&h->d_plan_rows, (size_t)h->R * h->k * 2) == cudaSuccess &&
+              dev_alloc(&h->d_plan_counts, (size_t)h->R) == cudaSuccess;
+    h->state.assign(h->L, hs::HotState{nullptr, nullptr, nullptr, nullptr, nullptr});
+    for (int l = 0; ok && l < h->L; ++l) {
+        if (h->anchor[l] >= 0) continue;
+        hs::HotState &st = h->state[l];
+        ok = dev_alloc(&st.tok2slot, (size_t)h->total_cap) == cudaSuccess &&
+             dev_alloc(&st.slot2tok, RD) == cudaSuccess &&
+             dev_alloc(&st.last_used, RD) == cudaSuccess &&
+             dev_alloc(&st.lru, RD) == cudaSuccess &&
+             dev_alloc(&st.tick, (size_t)h->R) == cudaSuccess;
+    }
+    if (!ok) {
+        cudaGetLastError();
+        release(h);
+        return HISPARSE_ERR_NO_MEMORY;
+    }
+
+    std::vector<hs::LayerDescDev> desc(h->L);
+    for (int l = 0; l < h->L; ++l) {
+        const hs::LayerStore s = layer_store(h, l);
+        desc[l].host = s.host;
+        desc[l].dev = s.dev;
+        desc[l].st = h->state[l];
+    }
+    cudaError_t e = cudaMemcpy(h->d_off, h->off.data(), sizeof(int64_t) * h->R, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(h->d_cap, h->cap.data(), sizeof(int64_t) * h->R, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(h->d_layers, desc.data(), sizeof(hs::LayerDescDev) * h->L, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(h->dev_buf, 0, buf_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->d_zero, 0, sizeof(int32_t) * h->R);
+    if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t) * h->R);
+    if (e == cudaSuccess) e = cudaMemset(h->d_plan_counts, 0, sizeof(int32_t) * h->R);
+    // empty hot state: seq_len 0 everywhere (maps -1, LRU in slot order, ticks 0)
+    if (e == cudaSuccess) e = hs::launch_prefill(h->d_zero, h->d_layers, h->L, geometry(h), h->d_status, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        release(h);
+        return HISPARSE_ERR_CUDA;
+    }
+    *out = h;
+    return HISPARSE_OK;
+}
+
+int hisparse_destroy(hisparse_t h)
+{
+    release(h);
+    return HISPARSE_OK;
+}
+
+int hisparse_host_rows(hisparse_t h, int32_t layer, int32_t request, void **host_ptr)
+{
+    if (!h || !host_ptr) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
+    if (request < 0 || request >= h->R) return HISPARSE_ERR_INVALID_ARG;
+    *host_ptr = h->host_pool + ((int64_t)layer * h->total_cap + h->off[request]) * h->B;
+    return HISPARSE_OK;
+}
+
+int hisparse_device_buffer(hisparse_t h, int32_t layer, void **dev_ptr)
+{
+    if (!h || !dev_ptr) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
+    *dev_ptr = layer_store(h, layer).dev;
+    return HISPARSE_OK;
+}
+
+int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream)
+{
+    if (!h || !seq_lens) return HISPARSE_ERR_INVALID_ARG;
+    return cuda_status(hs::launch_prefill(seq_lens, h->d_layers, h->L, geometry(h), h->d_status,
+                                          as_stream(stream)));
+}
+
+int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int32_t *seq_lens,
+                     int32_t *out_slot_ids, const hisparse_plan *out_plan, void *stream)
+{
+    if (!h || !topk_idx || !seq_lens || !out_slot_ids) return HISPARSE_ERR_INVALID_ARG;
+    if (out_plan && (!out_plan->rows || !out_plan->counts)) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L || h->anchor[layer] >= 0) return HISPARSE_ERR_LAYER;
+    hs::ResolveLaunch a;
+    a.topk = topk_idx;
+    a.seq_lens = seq_lens;
+    a.out = out_slot_ids;
+    a.status = h->d_status;
+    a.st = h->state[layer];
+    a.store = layer_store(h, layer);
+    a.g = geometry(h);
+    a.max_cap = (int32_t)h->max_cap;
+    const bool split = h->copy_mode == HISPARSE_COPY_SPLIT;
+    a.fused_copy = !split;
+    a.plan_rows = out_plan ? out_plan->rows : (split ? h->d_plan_rows : nullptr);
+    a.plan_counts = out_plan ? out_plan->counts : (split ? h->d_plan_counts : nullptr);
+    cudaError_t e = hs::launch_resolve(a, as_stream(stream));
+    if (e != cudaSuccess || !split) return cuda_status(e);
+    hs::ReplayLaunch c;
+    c.plan_rows = a.plan_rows;
+    c.plan_counts = a.plan_counts;
+    c.store = a.store;
+    c.g = a.g;
+    c.num_ctas = h->num_sms;
+    c.programmatic = true;
+    return cuda_status(hs::launch_replay(c, as_stream(stream)));
+}
+
+int hisparse_replay_plan(hisparse_t h, const hisparse_plan *plan, int32_t layer, int32_t num_ctas,
+                         void *stream)
+{
+    if (!h || !plan || !plan->rows || !plan->counts || num_ctas < 0) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
+    hs::ReplayLaunch c;
+    c.plan_rows = plan->rows;
+    c.plan_counts = plan->counts;
+    c.store = layer_store(h, layer);
+    c.g = geometry(h);
+    c.num_ctas = num_ctas ? num_ctas : 16;
+    c.programmatic = false;
+    return cuda_status(hs::launch_replay(c, as_stream(stream)));
+}
+
+int hisparse_backup(hisparse_t h, int32_t layer, const void *rows, const int32_t *positions,
+                    void *stream)
+{
+    if (!h || !rows || !positions) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
+    if (!aligned16(rows)) return HISPARSE_ERR_ALIGNMENT;
+    hs::BackupLaunch b;
+    b.rows = static_cast<const uint8_t *>(rows);
+    b.positions = positions;
+    const hs::LayerStore s = layer_store(h, layer);
+    b.host = const_cast<uint8_t *>(s.host);
+    b.dev = s.dev;
+    b.st = h->state[layer];
+    b.g = geometry(h);
+    b.status = h->d_status;
+    return cuda_status(hs::launch_backup(b, as_stream(stream)));
+}
+
+int hisparse_status(hisparse_t h, int32_t **dev_status)
+{
+    if (!h || !dev_status) return HISPARSE_ERR_INVALID_ARG;
+    *dev_status = h->d_status;
+    return HISPARSE_OK;
+}
+
+int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok, uint32_t *last_used,
+                        int32_t *tok2slot, int32_t *lru_order, uint32_t *ticks, void *stream)
+{
+    if (!h) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L || h->anchor[layer] >= 0) return HISPARSE_ERR_LAYER;
+    const hs::HotState &st = h->state[layer];
+    const size_t RD = (size_t)h->R * h->D;
+    cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+    if (e == cudaSuccess && slot2tok) e = cudaMemcpy(slot2tok, st.slot2tok, RD * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && last_used) e = cudaMemcpy(last_used, st.last_used, RD * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && tok2slot)
+        e = cudaMemcpy(tok2slot, st.tok2slot, (size_t)h->total_cap * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && lru_order) {
+        std::vector<uint16_t> tmp(RD);
+        e = cudaMemcpy(tmp.data(), st.lru, RD * 2, cudaMemcpyDeviceToHost);
+        for (size_t i = 0; e == cudaSuccess && i < RD; ++i) lru_order[i] = tmp[i];
+    }
+    if (e == cudaSuccess && ticks) e = cudaMemcpy(ticks, st.tick, (size_t)h->R * 4, cudaMemcpyDeviceToHost);
+    return cuda_status(e);
+}
+
+int hisparse_set_copy_mode(hisparse_t h, int32_t mode)
+{
+    if (!h || (mode != HISPARSE_COPY_FUSED && mode != HISPARSE_COPY_SPLIT)) return HISPARSE_ERR_INVALID_ARG;
+    h->copy_mode = mode;
+    return HISPARSE_OK;
+}
+
+// ---- measurement kernels ---------------------------------------------------
+
+int hisparse_synthetic_compute(float *buf, int64_t n, int32_t num_threads, int32_t iters, void *stream)
+{
+    if (!buf || num_threads < 1 || iters < 0 || n < num_threads) return HISPARSE_ERR_INVALID_ARG;
+    return cuda_status(hs::launch_synthetic_compute(buf, num_threads, iters, as_stream(stream)));
+}
+
+int hisparse_link_probe(const void *src, void *dst, int64_t bytes, int32_t num_ctas, void *stream)
+{
+    if (!src || !dst || bytes < 0 || bytes % 16 != 0 || num_ctas < 0) return HISPARSE_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return HISPARSE_ERR_ALIGNMENT;
+    if (bytes == 0) return HISPARSE_OK;
+    int ctas = num_ctas;
+    if (ctas == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&ctas, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return HISPARSE_ERR_CUDA;
+    }
+    return cuda_status(hs::launch_link_probe(src, dst, bytes, ctas, as_stream(stream)));
+}
+
+}  // extern "C"

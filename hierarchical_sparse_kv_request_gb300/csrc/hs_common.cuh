@@ -1,0 +1,171 @@
+// hs_common.cuh -- types and device helpers shared by the resolver's kernels.
+//
+// Sources (page title, section):
+//   [Guide] "HiSparse: Hierarchical Sparse Attention": Decode Workflow,
+//           Shared-index prefetch.
+//   [Arch]  "HiSparse local KV offload architecture": Hot lookup and LRU,
+//           Performance invariants.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace hs {
+
+constexpr int kStatusOk = 0;
+constexpr int kStatusBadIndex = 1;
+constexpr int kStatusDuplicate = 2;
+constexpr int kStatusBadSeqLen = 3;
+constexpr int kStatusBadPosition = 4;
+
+// Hot state of one state-owning layer.  Per request r:
+//   tok2slot[host_off[r] + t]  slot holding token t, or -1   (host_cap[r] ints)
+//   slot2tok[r*D + s]          token in slot s, or -1
+//   last_used[r*D + s]         tick of the last call that selected slot s
+//   lru[r*D + i]               the i-th least recently used slot; the list
+//                              is kept sorted by (last_used, slot)
+//   tick[r]                    ticks of the request's calls so far
+struct HotState {
+    int32_t *tok2slot;
+    int32_t *slot2tok;
+    uint32_t *last_used;
+    uint16_t *lru;
+    uint32_t *tick;
+};
+
+// Storage of one layer: the pinned host pool as seen from the device and
+// the device hot buffer.
+struct LayerStore {
+    const uint8_t *host;  // [total_cap][B] (device-visible pinned memory)
+    uint8_t *dev;         // [R][D][B]
+};
+
+struct Geometry {
+    int32_t R, k, D;
+    int64_t B;             // multiple of 16
+    int32_t chunks;        // B / 16
+    const int64_t *host_off;  // device [R]
+    const int64_t *host_cap;  // device [R]
+};
+
+// ---------------------------------------------------------------------------
+// Memory access helpers.
+// ---------------------------------------------------------------------------
+
+// 16-byte load of pinned host memory through the device's address space.
+// The host pool is read-only while a kernel reads it (backups are separate,
+// stream-ordered launches), so the non-coherent path is safe; L1 is bypassed
+// because every host byte is read once.
+__device__ __forceinline__ uint4 ld_host_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_dev_v4(const void *p)
+{
+    return *reinterpret_cast<const uint4 *>(p);
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v)
+{
+    *reinterpret_cast<uint4 *>(p) = v;
+}
+
+// ---------------------------------------------------------------------------
+// Block-wide exclusive prefix sum of one uint32 per thread.
+// `warp_tot` is shared scratch of NT/32 words.  The function starts and ends
+// with a barrier so it can be called back to back.
+// ---------------------------------------------------------------------------
+template <int NT>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *warp_tot,
+                                                         uint32_t &total)
+{
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < NW ? warp_tot[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < NW) warp_tot[lane] = w;  // inclusive warp totals
+    }
+    __syncthreads();
+    total = warp_tot[NW - 1];
+    return (warp ? warp_tot[warp - 1] : 0u) + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel launchers (defined in the .cu files).
+// ---------------------------------------------------------------------------
+struct ResolveLaunch {
+    const int32_t *topk;
+    const int32_t *seq_lens;
+    int32_t *out;
+    int32_t *plan_rows;    // may be null
+    int32_t *plan_counts;  // may be null
+    int32_t *status;
+    HotState st;
+    LayerStore store;
+    Geometry g;
+    int32_t max_cap;       // largest host capacity (sizes the miss bitmap)
+    bool fused_copy;
+};
+
+// Shared-memory bytes the resolve kernel needs for this geometry.
+size_t resolve_smem_bytes(int k, int D, int max_cap);
+int resolve_threads();
+cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s);
+
+struct ReplayLaunch {
+    const int32_t *plan_rows;
+    const int32_t *plan_counts;
+    LayerStore store;
+    Geometry g;
+    int num_ctas;
+    bool programmatic;  // launched right after a resolve (programmatic dependency)
+};
+size_t replay_smem_bytes(int R);
+cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s);
+
+struct BackupLaunch {
+    const uint8_t *rows;      // device [R][B]
+    const int32_t *positions; // device [R]
+    uint8_t *host;            // layer's pinned pool (device-visible)
+    uint8_t *dev;             // layer's hot buffer
+    HotState st;              // tok2slot == nullptr for a skip layer
+    Geometry g;
+    int32_t *status;
+};
+cudaError_t launch_backup(const BackupLaunch &a, cudaStream_t s);
+
+// Per-layer descriptor, kept in device memory for kernels that walk all
+// layers in one launch (prefill).  st.tok2slot == nullptr marks a skip layer.
+struct LayerDescDev {
+    const uint8_t *host;
+    uint8_t *dev;
+    HotState st;
+};
+cudaError_t launch_prefill(const int32_t *seq_lens, const LayerDescDev *layers, int num_layers,
+                           const Geometry &g, int32_t *status, cudaStream_t s);
+
+cudaError_t launch_synthetic_compute(float *buf, int32_t num_threads, int32_t iters,
+                                     cudaStream_t s);
+cudaError_t launch_link_probe(const void *src, void *dst, int64_t bytes, int num_ctas,
+                              cudaStream_t s);
+
+}  // namespace hs

@@ -1,0 +1,253 @@
+"""Thin ctypes binding of libhisparse.so (include/hisparse.h).
+
+Argument marshalling only: every step of the swap-in path runs in the CUDA
+library.  Device arrays may be passed as torch CUDA tensors or raw integer
+addresses; streams as torch streams, raw ``cudaStream_t`` integers or None
+(torch's current stream).  There is no CPU fallback: if the library is not
+built, loading it raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libhisparse.so")
+
+OK = 0
+ERR_INVALID_ARG, ERR_LAYOUT, ERR_CAPACITY, ERR_LAYER = -1, -2, -3, -4
+ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT = -5, -6, -7, -8
+STATUS_OK, STATUS_BAD_INDEX, STATUS_DUPLICATE, STATUS_BAD_SEQ_LEN, STATUS_BAD_POSITION = 0, 1, 2, 3, 4
+COPY_FUSED, COPY_SPLIT = 1, 2
+
+
+class HiSparseError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {error_string(code)} ({code})")
+        self.code = code
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("num_requests", ctypes.c_int32), ("num_layers", ctypes.c_int32),
+                ("row_bytes", ctypes.c_int64), ("top_k", ctypes.c_int32),
+                ("device_buffer_size", ctypes.c_int32),
+                ("host_to_device_ratio", ctypes.c_int32),
+                ("swap_in_block_size", ctypes.c_int32),
+                ("anchor_of_layer", ctypes.c_void_p), ("host_capacity", ctypes.c_void_p)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_void_p), ("counts", ctypes.c_void_p)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libhisparse.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(p)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "hisparse_create": [P, P],
+        "hisparse_destroy": [P],
+        "hisparse_host_rows": [P, I32, I32, P],
+        "hisparse_device_buffer": [P, I32, P],
+        "hisparse_prefill": [P, P, P],
+        "hisparse_swap_in": [P, I32, P, P, P, P, P],
+        "hisparse_replay_plan": [P, P, I32, I32, P],
+        "hisparse_backup": [P, I32, P, P, P],
+        "hisparse_status": [P, P],
+        "hisparse_read_state": [P, I32, P, P, P, P, P, P],
+        "hisparse_set_copy_mode": [P, I32],
+        "hisparse_version": [],
+        "hisparse_synthetic_compute": [P, I64, I32, I32, P],
+        "hisparse_link_probe": [P, P, I64, I32, P],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.hisparse_error_string.argtypes = [ctypes.c_int]
+    lib.hisparse_error_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    try:
+        return load_library().hisparse_error_string(code).decode()
+    except RuntimeError:
+        return "unknown"
+
+
+def _addr(x) -> Optional[int]:
+    """Device/host address of a torch tensor, numpy array or raw integer."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != OK:
+        raise HiSparseError(rc, what)
+
+
+class HiSparse:
+    """One handle of the swap-in resolver (see include/hisparse.h)."""
+
+    def __init__(self, num_requests: int, num_layers: int, row_bytes: int, top_k: int,
+                 device_buffer_size: int, host_to_device_ratio: int,
+                 host_capacity: Sequence[int], anchor_of_layer: Optional[Sequence[int]] = None,
+                 swap_in_block_size: int = 960):
+        self.lib = load_library()
+        self.R, self.L, self.B = num_requests, num_layers, row_bytes
+        self.k, self.D = top_k, device_buffer_size
+        self.cap = np.ascontiguousarray(host_capacity, dtype=np.int64)
+        self.anchor = np.ascontiguousarray(
+            anchor_of_layer if anchor_of_layer is not None else [-1] * num_layers, dtype=np.int32)
+        self.total_cap = int(self.cap.sum())
+        lay = Layout(num_requests, num_layers, row_bytes, top_k, device_buffer_size,
+                     host_to_device_ratio, swap_in_block_size,
+                     self.anchor.ctypes.data, self.cap.ctypes.data)
+        h = ctypes.c_void_p()
+        _check(self.lib.hisparse_create(ctypes.byref(lay), ctypes.byref(h)), "hisparse_create")
+        self.h = h
+
+    @classmethod
+    def for_workload(cls, w) -> "HiSparse":
+        return cls(w.num_requests, w.num_layers, w.row_bytes, w.top_k, w.device_buffer_size,
+                   w.host_to_device_ratio, w.host_capacity, w.anchor_of_layer)
+
+    def close(self) -> None:
+        if getattr(self, "h", None) and self.h.value:
+            self.lib.hisparse_destroy(self.h)
+            self.h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- storage ------------------------------------------------------------
+    def host_rows_ptr(self, layer: int, request: int) -> int:
+        p = ctypes.c_void_p()
+        _check(self.lib.hisparse_host_rows(self.h, layer, request, ctypes.byref(p)),
+               "hisparse_host_rows")
+        return p.value
+
+    def host_rows(self, layer: int, request: int) -> np.ndarray:
+        """Writable numpy view [host_capacity[request]][B] of pinned host rows."""
+        n = int(self.cap[request]) * self.B
+        buf = (ctypes.c_uint8 * n).from_address(self.host_rows_ptr(layer, request))
+        return np.frombuffer(buf, dtype=np.uint8).reshape(int(self.cap[request]), self.B)
+
+    def device_buffer_ptr(self, layer: int) -> int:
+        p = ctypes.c_void_p()
+        _check(self.lib.hisparse_device_buffer(self.h, layer, ctypes.byref(p)),
+               "hisparse_device_buffer")
+        return p.value
+
+    def device_buffer(self, layer: int):
+        """torch uint8 CUDA tensor [R][D][B] aliasing the layer's hot buffer."""
+        import torch
+
+        class _View:
+            __cuda_array_interface__ = {
+                "shape": (self.R, self.D, self.B), "typestr": "|u1",
+                "data": (self.device_buffer_ptr(layer), False), "version": 3,
+                "strides": None}
+        return torch.as_tensor(_View(), device="cuda")
+
+    def status_ptr(self) -> int:
+        p = ctypes.c_void_p()
+        _check(self.lib.hisparse_status(self.h, ctypes.byref(p)), "hisparse_status")
+        return p.value
+
+    def status(self):
+        """torch int32 CUDA tensor [R] aliasing the status array."""
+        import torch
+
+        class _View:
+            __cuda_array_interface__ = {
+                "shape": (self.R,), "typestr": "<i4", "data": (self.status_ptr(), False),
+                "version": 3, "strides": None}
+        return torch.as_tensor(_View(), device="cuda")
+
+    # -- decode path --------------------------------------------------------
+    def prefill(self, seq_lens, stream=None) -> None:
+        _check(self.lib.hisparse_prefill(self.h, _addr(seq_lens), _stream(stream)),
+               "hisparse_prefill")
+
+    def swap_in(self, layer: int, topk, seq_lens, out_slot_ids, plan_rows=None,
+                plan_counts=None, stream=None) -> None:
+        plan = None
+        if plan_rows is not None or plan_counts is not None:
+            plan = ctypes.byref(Plan(_addr(plan_rows), _addr(plan_counts)))
+        _check(self.lib.hisparse_swap_in(self.h, layer, _addr(topk), _addr(seq_lens),
+                                         _addr(out_slot_ids), plan, _stream(stream)),
+               "hisparse_swap_in")
+
+    def replay_plan(self, plan_rows, plan_counts, layer: int, num_ctas: int = 0,
+                    stream=None) -> None:
+        plan = Plan(_addr(plan_rows), _addr(plan_counts))
+        _check(self.lib.hisparse_replay_plan(self.h, ctypes.byref(plan), layer, num_ctas,
+                                             _stream(stream)), "hisparse_replay_plan")
+
+    def backup(self, layer: int, rows, positions, stream=None) -> None:
+        _check(self.lib.hisparse_backup(self.h, layer, _addr(rows), _addr(positions),
+                                        _stream(stream)), "hisparse_backup")
+
+    def set_copy_mode(self, mode: int) -> None:
+        _check(self.lib.hisparse_set_copy_mode(self.h, mode), "hisparse_set_copy_mode")
+
+    def read_state(self, layer: int, stream=None):
+        """(slot2tok [R][D], last_used [R][D], tok2slot [total_cap], lru [R][D], ticks [R])."""
+        s2t = np.empty((self.R, self.D), dtype=np.int32)
+        lu = np.empty((self.R, self.D), dtype=np.uint32)
+        t2s = np.empty(self.total_cap, dtype=np.int32)
+        lru = np.empty((self.R, self.D), dtype=np.int32)
+        ticks = np.empty(self.R, dtype=np.uint32)
+        _check(self.lib.hisparse_read_state(self.h, layer, s2t.ctypes.data, lu.ctypes.data,
+                                            t2s.ctypes.data, lru.ctypes.data, ticks.ctypes.data,
+                                            _stream(stream)), "hisparse_read_state")
+        return s2t, lu, t2s, lru, ticks
+
+
+# -- measurement kernels (include/hisparse_measure.h) -----------------------
+
+def synthetic_compute(buf, num_threads: int, iters: int, stream=None) -> None:
+    lib = load_library()
+    _check(lib.hisparse_synthetic_compute(_addr(buf), buf.numel(), num_threads, iters,
+                                          _stream(stream)), "hisparse_synthetic_compute")
+
+
+def link_probe(src, dst, nbytes: int, num_ctas: int = 0, stream=None) -> None:
+    lib = load_library()
+    _check(lib.hisparse_link_probe(_addr(src), _addr(dst), nbytes, num_ctas, _stream(stream)),
+           "hisparse_link_probe")

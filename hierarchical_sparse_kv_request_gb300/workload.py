@@ -101,6 +101,7 @@ class Workload:
     backup: bool                    # one backup row per request per layer per step
     seq_lens0: np.ndarray           # int32 [R], lengths before step 0
     seed: int
+    capacity: Optional[np.ndarray] = None  # explicit host capacity per request
 
     @property
     def growth(self) -> int:
@@ -109,6 +110,8 @@ class Workload:
     @property
     def host_capacity(self) -> np.ndarray:
         """Tokens of host storage per request: the context plus growth."""
+        if self.capacity is not None:
+            return np.asarray(self.capacity, dtype=np.int64)
         return (self.seq_lens0.astype(np.int64) + self.growth).astype(np.int64)
 
     def seq_lens_at(self, step: int) -> np.ndarray:
@@ -123,6 +126,16 @@ class Workload:
 
 def _seed(config_no: int) -> int:
     return 0x48530000 + config_no
+
+
+def custom(R: int, k: int, D: int, seq_lens, row_bytes: int = 16, layers: int = 1,
+           anchor_of_layer: Optional[List[int]] = None, capacity=None, seed: int = 7,
+           ratio: int = 1000) -> Workload:
+    """A small ad-hoc workload (bf16 rows) for edge-case tests."""
+    lens = np.asarray(seq_lens, dtype=np.int32)
+    return Workload("custom", 0, R, layers, anchor_of_layer or [-1] * layers, 1, 1, k, D,
+                    row_bytes, "bf16", ratio, 0, "uniform", False, lens, seed,
+                    None if capacity is None else np.asarray(capacity, dtype=np.int64))
 
 
 def make_config(config_no: int, *, steps: Optional[int] = None,
@@ -275,15 +288,10 @@ def topk_schedule(w: Workload) -> Dict[int, np.ndarray]:
 # KV row bytes
 # --------------------------------------------------------------------------
 
-def _row_words(w: Workload, layer: int, request: int, tokens: np.ndarray,
-               nwords: int) -> np.ndarray:
-    """uint64 [len(tokens)][nwords], a pure function of (layer, request, token)."""
-    key = np.uint64(stream_key(w.seed, 0x52, layer, request))
-    t = np.asarray(tokens, dtype=np.uint64)[:, None]
-    i = np.arange(nwords, dtype=np.uint64)[None, :]
-    with np.errstate(over="ignore"):
-        ctr = t * np.uint64(nwords) + i + np.uint64(1)
-        return _mix(key + ctr * _GOLDEN)
+def _pool_words(seed: int, n: int, nwords: int) -> np.ndarray:
+    """uint64 [n][nwords] of seeded random words."""
+    st = Stream(stream_key(seed, 0x50))
+    return st.u64(n * nwords).reshape(n, nwords)
 
 
 def _to_bf16_bits(f: np.ndarray) -> np.ndarray:
@@ -293,34 +301,81 @@ def _to_bf16_bits(f: np.ndarray) -> np.ndarray:
     return b.astype(np.uint16)
 
 
-def kv_rows(w: Workload, layer: int, request: int, tokens) -> np.ndarray:
-    """uint8 [len(tokens)][row_bytes]: the KV rows of these token positions.
+_POOL_ROWS = 4096
+_pools: Dict[tuple, np.ndarray] = {}
+
+
+def _row_pool(w: Workload) -> np.ndarray:
+    """uint8 [4096][row_bytes] of random rows in the workload's row format.
 
     "mla_fp8" (656 B): 512 fp8 e4m3 latent bytes (random, never the NaN
     codes 0x7F/0xFF) + 4 fp32 scales uniform in [2^-8, 1] + 64 bf16 rope
-    values uniform in [-1, 1].  "bf16": row_bytes/2 bf16 values in [-1, 1].
+    values uniform in [-1, 1] (rounded to nearest even).  "bf16":
+    row_bytes/2 bf16 values uniform in [-1, 1].
     """
-    tokens = np.atleast_1d(np.asarray(tokens, dtype=np.int64))
-    n = tokens.size
-    B = w.row_bytes
+    key = (w.seed, w.row_kind, w.row_bytes)
+    if key in _pools:
+        return _pools[key]
+    n, B = _POOL_ROWS, w.row_bytes
     if w.row_kind == "mla_fp8":
         assert B == 656
-        words = _row_words(w, layer, request, tokens, 64 + 2 + 32)
+        words = _pool_words(w.seed, n, 64 + 34)
         latent = words[:, :64].copy().view(np.uint8).reshape(n, 512)
         latent[latent == 0x7F] = 0x7E
         latent[latent == 0xFF] = 0xFE
         u32 = words[:, 64:].copy().view(np.uint32).reshape(n, 68)
         sc = (2.0 ** -8 + (1.0 - 2.0 ** -8) * (u32[:, :4] >> 8) * (2.0 ** -24)).astype(np.float32)
         rope = _to_bf16_bits((u32[:, 4:] >> 8).astype(np.float64) * (2.0 ** -23) - 1.0)
-        return np.concatenate([latent, sc.view(np.uint8).reshape(n, 16),
+        pool = np.concatenate([latent, sc.view(np.uint8).reshape(n, 16),
                                rope.view(np.uint8).reshape(n, 128)], axis=1)
-    if w.row_kind == "bf16":
+    elif w.row_kind == "bf16":
         nv = B // 2
-        words = _row_words(w, layer, request, tokens, (nv + 1) // 2)
+        words = _pool_words(w.seed, n, (nv + 1) // 2)
         u32 = words.copy().view(np.uint32).reshape(n, -1)[:, :nv]
-        vals = _to_bf16_bits((u32 >> 8).astype(np.float64) * (2.0 ** -23) - 1.0)
-        return vals.view(np.uint8).reshape(n, B)
-    raise ValueError(w.row_kind)
+        pool = _to_bf16_bits((u32 >> 8).astype(np.float64) * (2.0 ** -23) - 1.0) \
+            .view(np.uint8).reshape(n, B)
+    else:
+        raise ValueError(w.row_kind)
+    _pools[key] = np.ascontiguousarray(pool)
+    return _pools[key]
+
+
+def kv_rows(w: Workload, layer: int, request: int, tokens) -> np.ndarray:
+    """uint8 [len(tokens)][row_bytes]: the KV rows of these token positions.
+
+    Each row is a random row of the workload's format (drawn from a seeded
+    pool by a hash of its coordinates) that also carries its own identity
+    in fields whose values stay in the format's ranges, so no two
+    (layer, request, token) rows are equal:
+      "mla_fp8": the 4 fp32 scales become 0.5 * (1 + f / 2^23) with f =
+                 token, request, layer and hash bits (values in [0.5, 1));
+      "bf16":    the first 6 values become +-0.5 * (1 + m / 128), carrying
+                 8 bits of (token | request << 20 | layer << 36) each.
+    """
+    tokens = np.atleast_1d(np.asarray(tokens, dtype=np.int64))
+    pool = _row_pool(w)
+    key = np.uint64(stream_key(w.seed, 0x52, layer, request))
+    with np.errstate(over="ignore"):
+        hsh = _mix(key + (tokens.astype(np.uint64) + np.uint64(1)) * _GOLDEN)
+    rows = pool[(hsh % np.uint64(_POOL_ROWS)).astype(np.int64)]
+    n = tokens.size
+    if w.row_kind == "mla_fp8":
+        f = np.empty((n, 4), dtype=np.uint32)
+        f[:, 0] = tokens.astype(np.uint32) & 0x7FFFFF
+        f[:, 1] = request & 0x7FFFFF
+        f[:, 2] = layer & 0x7FFFFF
+        f[:, 3] = (hsh >> np.uint64(41)).astype(np.uint32) & 0x7FFFFF
+        bits = (np.uint32(126) << np.uint32(23)) | f          # 0.5 * (1 + f/2^23)
+        rows[:, 512:528] = bits.view(np.uint8).reshape(n, 16)
+    else:
+        ident = (tokens.astype(np.uint64) | (np.uint64(request) << np.uint64(20))
+                 | (np.uint64(layer) << np.uint64(36)))
+        vals = np.empty((n, 6), dtype=np.uint16)
+        for q in range(6):
+            byte = ((ident >> np.uint64(8 * q)) & np.uint64(0xFF)).astype(np.uint16)
+            vals[:, q] = ((byte >> 7) << 15) | (np.uint16(126) << 7) | (byte & 0x7F)
+        rows[:, :12] = vals.view(np.uint8).reshape(n, 12)
+    return rows
 
 
 def fill_host_rows(w: Workload, layer: int, request: int, dst: np.ndarray,

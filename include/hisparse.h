@@ -1,0 +1,266 @@
+/*
+ * hisparse.h -- C ABI of the HiSparse decode-time swap-in resolver for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Each decode step, for every request and every sparse layer that owns an
+ * indexer, the resolver takes the top-k token positions chosen by the
+ * indexer and turns them into physical row IDs of a small per-request
+ * device ("hot") buffer, copying the rows that are not hot from pinned host
+ * memory, where the full KV of every request lives.
+ *
+ * Sources (cited by page title and section):
+ *   [Guide] "HiSparse: Hierarchical Sparse Attention" (SGLang user guide):
+ *           Decode Workflow; HiSparse Config Parameters; Shared-index
+ *           prefetch.
+ *   [Arch]  "HiSparse local KV offload architecture" (vLLM design doc):
+ *           Ownership; Resident device pages; Hot lookup and LRU;
+ *           Performance invariants.
+ *
+ * Conventions for every entry point:
+ *   - Return value: HISPARSE_OK (0) or a negative HISPARSE_ERR_* code.  Host
+ *     checks run before any GPU work; on error nothing is enqueued.
+ *   - Pointers documented as "device" must be device memory (cudaMalloc or
+ *     torch CUDA tensors) of the handle's device; "host" means ordinary host
+ *     memory.  No entry point keeps a caller pointer after it returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls that take a stream are asynchronous and stream-ordered:
+ *     they never synchronise, never read device data back to the host and
+ *     launch exactly one kernel ([Arch] Performance invariants: no device
+ *     scalar readback, no CPU/device metadata round trip, no extra launch),
+ *     so they can be captured in a CUDA graph.
+ *   - Problems in the *data* (a bad top-k index, a duplicate, a bad
+ *     position) are reported per request in a device status array (see
+ *     hisparse_status); the affected request's state is left untouched.
+ *   - A handle is not thread-safe; calls on one handle must be ordered by
+ *     the caller (one stream, or events between streams).
+ */
+#ifndef HISPARSE_H
+#define HISPARSE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes (host) ---------------------------------------------- */
+#define HISPARSE_OK 0
+#define HISPARSE_ERR_INVALID_ARG (-1)  /* null pointer, bad index, bad handle */
+#define HISPARSE_ERR_LAYOUT (-2)       /* inconsistent layout                 */
+#define HISPARSE_ERR_CAPACITY (-3)     /* host capacity beyond the ratio      */
+#define HISPARSE_ERR_LAYER (-4)        /* layer out of range / has no state   */
+#define HISPARSE_ERR_CUDA (-5)         /* a CUDA runtime call failed          */
+#define HISPARSE_ERR_NO_MEMORY (-6)    /* pinned or device allocation failed  */
+#define HISPARSE_ERR_UNSUPPORTED (-7)  /* beyond this library's size limits   */
+#define HISPARSE_ERR_ALIGNMENT (-8)    /* pointer not 16-byte aligned         */
+
+/* ---- per-request status codes (device array, see hisparse_status) ----- */
+#define HISPARSE_STATUS_OK 0
+#define HISPARSE_STATUS_BAD_INDEX 1    /* entry outside {-1} U [0, seq_len)   */
+#define HISPARSE_STATUS_DUPLICATE 2    /* a position selected twice           */
+#define HISPARSE_STATUS_BAD_SEQ_LEN 3  /* seq_len outside [0, host_capacity]  */
+#define HISPARSE_STATUS_BAD_POSITION 4 /* backup position outside [0, cap)    */
+
+/* ---- size limits ------------------------------------------------------- */
+#define HISPARSE_MAX_TOP_K 8192
+#define HISPARSE_MAX_DEVICE_BUFFER 32768
+#define HISPARSE_MAX_HOST_CAPACITY (1 << 20) /* tokens per request          */
+#define HISPARSE_MAX_REQUESTS 8192
+
+/* Copy strategy of hisparse_swap_in (see hisparse_set_copy_mode). */
+#define HISPARSE_COPY_FUSED 1  /* the resolving CTA copies its own misses     */
+#define HISPARSE_COPY_SPLIT 2  /* a second, wide grid copies all misses       */
+
+typedef struct hisparse_handle *hisparse_t;
+
+/*
+ * Layout of one handle ([Guide] HiSparse Config Parameters; [Arch] Resident
+ * device pages, Ownership).
+ *   num_requests          R: request rows of the batch (the attention
+ *                         metadata's graph-stable request index; row r of
+ *                         every per-request array below).
+ *   num_layers            L: sparse layers sharing this handle.
+ *   row_bytes             B: bytes of one token's KV row in one layer, a
+ *                         multiple of 16 (656 for fp8 MLA rows, 1152 for bf16).
+ *   top_k                 k: indices per request per call, 1 <= k <= D.
+ *   device_buffer_size    D: hot slots per request per layer.
+ *   host_to_device_ratio  host token capacity, summed over requests, may not
+ *                         exceed ratio * R * D ("host_to_device_ratio").
+ *   swap_in_block_size    accepted for compatibility with the guide's
+ *                         config ("swap_in_block_size", default 960); a hint
+ *                         only, the kernels pick their own block shapes.
+ *   anchor_of_layer       host [L] or NULL: -1 = the layer has its own
+ *                         indexer and hot state (maps + LRU); a value a >= 0
+ *                         marks a "skip" layer that reuses layer a's top-k
+ *                         and owns KV storage only ([Guide] Shared-index
+ *                         prefetch; [Arch] Performance invariants: index-
+ *                         sharing followers drop their private LRU state).
+ *                         NULL = every layer owns its state.
+ *   host_capacity         host [R]: token rows of host storage per request,
+ *                         at least its longest seq_len including growth by
+ *                         backups.
+ * The arrays are copied by hisparse_create.
+ */
+typedef struct hisparse_layout {
+    int32_t num_requests;
+    int32_t num_layers;
+    int64_t row_bytes;
+    int32_t top_k;
+    int32_t device_buffer_size;
+    int32_t host_to_device_ratio;
+    int32_t swap_in_block_size;
+    const int32_t *anchor_of_layer;
+    const int64_t *host_capacity;
+} hisparse_layout;
+
+/*
+ * A miss plan ([Guide] Shared-index prefetch: the anchor's swap-in records
+ * which host slot goes to which device buffer slot).  Caller-owned device
+ * memory:
+ *   rows    device int32 [R][k][2]: (token position, device slot) pairs of
+ *           request r, ascending by token; only the first counts[r] pairs
+ *           are written.
+ *   counts  device int32 [R]: misses of request r in the recording call.
+ * Speculative verification ([Arch] Resident device pages: every
+ * verification step gets its own replayable plan row) uses one plan per
+ * sub-step.
+ */
+typedef struct hisparse_plan {
+    int32_t *rows;
+    int32_t *counts;
+} hisparse_plan;
+
+/*
+ * hisparse_create: validate `layout`, allocate the pinned host pool
+ * ([L][sum of host_capacity][B] bytes, mapped into the device address
+ * space), the device hot buffers ([L][R][D][B] bytes), and, for every layer
+ * that owns state, the token->slot map (int32 per host token), slot->token
+ * map and LRU stamps (int32/uint32 [R][D]), the LRU order ([R][D] slots)
+ * and one LRU tick per request ([Arch] Ownership: the per-cache runtime owns
+ * the host/hot storage, the hot-row map and the LRU).  The handle belongs to
+ * the device current at the call.  Pinned memory is zeroed; the hot state
+ * starts empty until hisparse_prefill.
+ * Errors: INVALID_ARG (null), LAYOUT (a field out of range, top_k > D,
+ * row_bytes % 16, an anchor that owns no state), CAPACITY (ratio exceeded),
+ * UNSUPPORTED (limits above), NO_MEMORY, CUDA.  *out is NULL on error.
+ */
+int hisparse_create(const hisparse_layout *layout, hisparse_t *out);
+
+/* Free everything the handle owns.  The caller must have synchronised all
+ * streams that used it.  NULL is accepted. */
+int hisparse_destroy(hisparse_t h);
+
+/*
+ * hisparse_host_rows: host pointer to token row 0 of (layer, request) in the
+ * pinned pool; rows are contiguous, B bytes each, host_capacity[request] of
+ * them.  The caller writes the request's prefix KV there (the role of the
+ * direct-to-host import in [Guide] PD Disaggregation Integration) before
+ * hisparse_prefill.  Valid until hisparse_destroy.
+ */
+int hisparse_host_rows(hisparse_t h, int32_t layer, int32_t request, void **host_ptr);
+
+/*
+ * hisparse_device_buffer: device pointer to layer `layer`'s hot buffer,
+ * [R][D][B] bytes, request-major; slot s of request r is the row at byte
+ * offset (r * D + s) * B.  This is what sparse attention reads with the
+ * slot IDs from hisparse_swap_in ([Arch] Ownership: the attention backend
+ * consumes the device cache and physical row IDs).
+ */
+int hisparse_device_buffer(hisparse_t h, int32_t layer, void **dev_ptr);
+
+/*
+ * hisparse_prefill: (re)start requests.  seq_lens: device int32 [R]; an
+ * entry of -1 leaves that request untouched, any other value must lie in
+ * [0, host_capacity[r]] (else status BAD_SEQ_LEN).  For every layer, the
+ * newest n = min(S, D) token rows are copied from the host pool into slots
+ * 0..n-1 (slot i <- token S-n+i), and for state-owning layers the maps are
+ * set to match, every stamp and the tick are reset to 0 and the LRU order
+ * becomes slot order.  A request with S <= D therefore holds every token at
+ * slot = token ([Guide] Decode Workflow, fast path).  One launch.
+ */
+int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream);
+
+/*
+ * hisparse_swap_in: resolve one call's top-k for every request on a layer
+ * that owns state ([Guide] Decode Workflow, swap-in; [Arch] Hot lookup and
+ * LRU), in one launch.
+ *   topk_idx      device int32 [R][k]: token positions; -1 = padding.
+ *   seq_lens      device int32 [R]: current length S of each request.
+ *   out_slot_ids  device int32 [R][k]: output, the hot slot holding each
+ *                 input position (-1 for padding), in input order.
+ *   out_plan      NULL, or a plan (both pointers non-NULL) to record the
+ *                 misses into.
+ * Per request: the tick advances by one.  If S <= D the fast path applies:
+ * out = topk, nothing else changes.  Otherwise each position is looked up
+ * in the token->slot map; hits keep their slot; misses, in ascending token
+ * order, take the non-hit slots with the smallest (last_used, slot) in that
+ * order, the evicted tokens are unmapped, and each miss's row is copied from
+ * the pinned host pool into its slot; every selected slot is stamped with
+ * the tick.  A malformed row (see status codes) leaves the request's state
+ * untouched and writes -1 to its outputs and 0 to its plan count.
+ * Errors: INVALID_ARG, LAYER (skip layer or out of range), ALIGNMENT.
+ */
+int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx,
+                     const int32_t *seq_lens, int32_t *out_slot_ids,
+                     const hisparse_plan *out_plan, void *stream);
+
+/*
+ * hisparse_replay_plan: copy-only replay of a recorded plan onto another
+ * layer's storage ([Guide] Shared-index prefetch: skip layers replay the
+ * anchor's plan as copy-only kernels pre-issued on a side stream, with a
+ * small fixed grid to keep their SM footprint low).  For every request r and
+ * i < counts[r]: layer `layer`'s device slot rows[r][i][1] <- its host row
+ * rows[r][i][0].  No map or LRU changes.  `num_ctas` sets the grid (0 = 16).
+ * The caller orders it after the recording swap-in (an event on `stream`).
+ */
+int hisparse_replay_plan(hisparse_t h, const hisparse_plan *plan, int32_t layer,
+                         int32_t num_ctas, void *stream);
+
+/*
+ * hisparse_backup: eager backup of each request's newest KV row to host
+ * ([Guide] Decode Workflow, eager backup).
+ *   rows       device [R][B] bytes, 16-byte aligned.
+ *   positions  device int32 [R]: the row's token position, normally the
+ *              request's current seq_len; -1 skips the request; outside
+ *              [0, host_capacity[r]) sets status BAD_POSITION.
+ * Host row p <- rows[r].  If p < D (a short request, whose buffer holds
+ * every token at slot = token) device slot p is written too and, on a layer
+ * with state, the maps pair slot p with token p.  Stamps are unchanged.
+ */
+int hisparse_backup(hisparse_t h, int32_t layer, const void *rows,
+                    const int32_t *positions, void *stream);
+
+/*
+ * hisparse_status: device pointer to the int32 [R] status array.  Every
+ * hisparse_swap_in and hisparse_prefill writes each request's entry;
+ * hisparse_backup writes an entry only on error.  Read it stream-ordered.
+ */
+int hisparse_status(hisparse_t h, int32_t **dev_status);
+
+/*
+ * hisparse_read_state: synchronous copy of a state-owning layer's hot state
+ * to host memory, for checking (not on the decode path).  Any pointer may be
+ * NULL.  slot2tok int32 [R][D], last_used uint32 [R][D], tok2slot int32
+ * [sum of host_capacity] (request-major), lru_order int32 [R][D] (slots from
+ * least to most recently used), ticks uint32 [R].  `stream` is synchronised
+ * first.
+ */
+int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok,
+                        uint32_t *last_used, int32_t *tok2slot, int32_t *lru_order,
+                        uint32_t *ticks, void *stream);
+
+/* hisparse_set_copy_mode: HISPARSE_COPY_FUSED (default) or
+ * HISPARSE_COPY_SPLIT for hisparse_swap_in's miss copies.  Results are
+ * identical; only the launch shape differs. */
+int hisparse_set_copy_mode(hisparse_t h, int32_t mode);
+
+/* Text of a return code (static storage). */
+const char *hisparse_error_string(int code);
+
+/* ABI version: 100 * major + minor. */
+int hisparse_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HISPARSE_H */

@@ -1,0 +1,127 @@
+"""Run a workload through the CUDA library (via its C ABI) and the CPU oracle
+side by side, and compare everything they produce bit for bit."""
+
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+import oracle as O
+from hierarchical_sparse_kv_request_gb300 import workload as W
+from hierarchical_sparse_kv_request_gb300.hisparse import HiSparse
+
+
+class Pair:
+    """One workload on the GPU library and on the oracle."""
+
+    def __init__(self, w: W.Workload, track_bytes: bool, copy_mode: Optional[int] = None):
+        self.w = w
+        self.track = track_bytes
+        self.gpu = HiSparse.for_workload(w)
+        if copy_mode is not None:
+            self.gpu.set_copy_mode(copy_mode)
+        self.orc = O.Oracle.for_workload(w, track_bytes=track_bytes)
+        R, k = w.num_requests, w.top_k
+        for l in range(w.num_layers):
+            for r in range(R):
+                n = int(w.seq_lens0[r])
+                dst = self.gpu.host_rows(l, r)
+                W.fill_host_rows(w, l, r, dst, n)
+                if track_bytes:
+                    self.orc.host_rows(l, r)[:n] = dst[:n]
+        self.seq = w.seq_lens0.astype(np.int32).copy()
+        self.seq_d = torch.from_numpy(self.seq).cuda()
+        self.gpu.prefill(self.seq_d)
+        self.orc.prefill(self.seq)
+        self.out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+        self.plan = torch.empty((R, k, 2), dtype=torch.int32, device="cuda")
+        self.cnt = torch.empty(R, dtype=torch.int32, device="cuda")
+        self.last = None
+
+    def close(self):
+        self.gpu.close()
+        self.orc.close()
+
+    def swap_in(self, layer: int, topk: np.ndarray, plan=None, cnt=None):
+        """One call on both sides; returns (gpu results, oracle results)."""
+        plan = self.plan if plan is None else plan
+        cnt = self.cnt if cnt is None else cnt
+        t = torch.from_numpy(np.ascontiguousarray(topk, dtype=np.int32)).cuda()
+        self.gpu.swap_in(layer, t, self.seq_d, self.out, plan, cnt)
+        o = self.orc.swap_in(layer, topk, self.seq)
+        torch.cuda.synchronize()
+        g = (self.out.cpu().numpy(), plan.cpu().numpy(), cnt.cpu().numpy(),
+             self.gpu.status().cpu().numpy())
+        self.last = (g, o)
+        return g, o
+
+    def backup(self, layer: int, positions: np.ndarray):
+        """Back up each request's row at `positions` (generator rows)."""
+        w = self.w
+        rows = np.zeros((w.num_requests, w.row_bytes), dtype=np.uint8)
+        for r in range(w.num_requests):
+            if positions[r] >= 0:
+                rows[r] = W.kv_rows(w, layer, r, [int(positions[r])])[0]
+        rows_d = torch.from_numpy(rows).cuda()
+        pos_d = torch.from_numpy(np.ascontiguousarray(positions, dtype=np.int32)).cuda()
+        self.gpu.backup(layer, rows_d, pos_d)
+        st = self.orc.backup(layer, rows, positions)
+        torch.cuda.synchronize()
+        return st
+
+    def advance(self, delta: int = 1):
+        self.seq += delta
+        self.seq_d.copy_(torch.from_numpy(self.seq))
+
+
+def assert_call_equal(g, o, ctx=""):
+    out, plan, cnt, st = g
+    o_out, o_plan, o_cnt, o_st = o
+    assert np.array_equal(st, o_st), f"{ctx}: status {st} != {o_st}"
+    assert np.array_equal(cnt, o_cnt), f"{ctx}: miss counts differ"
+    assert np.array_equal(out, o_out), f"{ctx}: slot ids differ"
+    for r in range(out.shape[0]):
+        n = int(o_cnt[r])
+        assert np.array_equal(plan[r, :n], o_plan[r, :n]), f"{ctx}: plan of request {r} differs"
+
+
+def assert_state_equal(p: Pair, layer: int, ctx=""):
+    s2t, lu, t2s, lru, ticks = p.gpu.read_state(layer)
+    o_s2t, o_lu, o_t2s, o_tick = p.orc.state(layer)
+    assert np.array_equal(s2t, o_s2t), f"{ctx}: slot->token maps differ"
+    assert np.array_equal(lu, o_lu), f"{ctx}: LRU stamps differ"
+    assert np.array_equal(t2s, o_t2s), f"{ctx}: token->slot maps differ"
+    assert (ticks == o_tick).all(), f"{ctx}: ticks {set(ticks.tolist())} != {o_tick}"
+    # the kernel's LRU list must be the slots sorted by the oracle's (last_used, slot)
+    D = p.w.device_buffer_size
+    key = o_lu.astype(np.int64) * (D + 1) + np.arange(D)[None, :]
+    want = np.argsort(key, axis=1, kind="stable")
+    assert np.array_equal(lru, want), f"{ctx}: LRU order differs"
+    return o_s2t
+
+
+def assert_device_rows(p: Pair, layer: int, slot2tok: np.ndarray, sample: Optional[int] = None,
+                       seed: int = 0, ctx=""):
+    """Device slots hold the generator's row of the token the oracle maps
+    there (every filled slot, or a random sample of them)."""
+    w = p.w
+    dev = p.gpu.device_buffer(layer)
+    rng = np.random.default_rng(seed)
+    for r in range(w.num_requests):
+        filled = np.nonzero(slot2tok[r] >= 0)[0]
+        if sample is not None and filled.size > sample:
+            filled = np.sort(rng.choice(filled, sample, replace=False))
+        if filled.size == 0:
+            continue
+        got = dev[r][torch.from_numpy(filled).cuda()].cpu().numpy()
+        want = W.kv_rows(w, layer, r, slot2tok[r][filled])
+        bad = np.nonzero((got != want).any(axis=1))[0]
+        assert bad.size == 0, f"{ctx}: request {r} slot {filled[bad[0]]} holds wrong bytes"
+
+
+def assert_device_bytes_equal_oracle(p: Pair, layer: int, ctx=""):
+    dev = p.gpu.device_buffer(layer).cpu().numpy()
+    for r in range(p.w.num_requests):
+        assert np.array_equal(dev[r], p.orc.dev_rows(layer, r)), f"{ctx}: device bytes of request {r}"

@@ -1,0 +1,103 @@
+"""The C ABI library loads and exports every declared entry point; its
+host-side checks return the documented codes (CPU only, no GPU calls)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+from hierarchical_sparse_kv_request_gb300 import build as B
+from hierarchical_sparse_kv_request_gb300 import hisparse as H
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build_library()
+    return H.load_library()
+
+
+def declared_functions():
+    names = set()
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(hdr).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(hisparse_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_headers_declare_the_entry_points():
+    names = declared_functions()
+    for n in ["hisparse_create", "hisparse_swap_in", "hisparse_replay_plan", "hisparse_backup",
+              "hisparse_prefill", "hisparse_destroy", "hisparse_link_probe"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_error_strings(lib):
+    assert lib.hisparse_version() == 100
+    for code in range(0, -9, -1):
+        assert lib.hisparse_error_string(code) not in (None, b"unknown error")
+    assert lib.hisparse_error_string(-99) == b"unknown error"
+
+
+def _create(lib, R=2, L=1, B_=16, k=8, D=16, ratio=10, caps=(50, 50), anchors=None):
+    caps = np.ascontiguousarray(caps, dtype=np.int64)
+    anc = None if anchors is None else np.ascontiguousarray(anchors, dtype=np.int32)
+    lay = H.Layout(R, L, B_, k, D, ratio, 960, None if anc is None else anc.ctypes.data,
+                   caps.ctypes.data)
+    h = ctypes.c_void_p(1234)
+    rc = lib.hisparse_create(ctypes.byref(lay), ctypes.byref(h))
+    return rc, h
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=17, D=16), H.ERR_LAYOUT),                     # top_k > device_buffer_size
+    (dict(B_=24), H.ERR_LAYOUT),                          # row_bytes not a multiple of 16
+    (dict(B_=0), H.ERR_LAYOUT),
+    (dict(R=0, caps=()), H.ERR_LAYOUT),
+    (dict(ratio=0), H.ERR_LAYOUT),
+    (dict(caps=(200, 200), ratio=10), H.ERR_CAPACITY),   # 400 > 10 * 2 * 16
+    (dict(caps=(-1, 5)), H.ERR_LAYOUT),
+    (dict(caps=(0, 0)), H.ERR_LAYOUT),
+    (dict(L=2, anchors=(0, 0)), H.ERR_LAYOUT),            # a layer anchored on itself
+    (dict(L=3, anchors=(-1, 0, 1)), H.ERR_LAYOUT),        # an anchor that owns no state
+    (dict(L=2, anchors=(1, 0)), H.ERR_LAYOUT),            # no layer owns state
+    (dict(L=2, anchors=(-1, 5)), H.ERR_LAYOUT),
+    (dict(k=9000, D=9000, caps=(1, 1), ratio=1), H.ERR_UNSUPPORTED),
+    (dict(D=40000, caps=(1, 1)), H.ERR_UNSUPPORTED),
+    (dict(caps=((1 << 20) + 1, 1), ratio=100000), H.ERR_UNSUPPORTED),
+])
+def test_create_rejects_bad_layouts_before_any_gpu_work(lib, kw, code):
+    rc, h = _create(lib, **kw)
+    assert rc == code
+    assert h.value is None                      # *out cleared on error
+
+
+def test_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.hisparse_create(None, ctypes.byref(h)) == H.ERR_INVALID_ARG
+    assert lib.hisparse_create(None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_destroy(None) == H.OK
+    assert lib.hisparse_swap_in(None, 0, None, None, None, None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_replay_plan(None, None, 0, 0, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_backup(None, 0, None, None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_prefill(None, None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_status(None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_read_state(None, 0, None, None, None, None, None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_set_copy_mode(None, 1) == H.ERR_INVALID_ARG
+    assert lib.hisparse_link_probe(None, None, 16, 0, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_synthetic_compute(None, 0, 1, 1, None) == H.ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        H.load_library(str(tmp_path / "libhisparse.so"))

@@ -1,0 +1,279 @@
+"""Parity of the CUDA library (called through its C ABI) with the CPU oracle.
+
+Every comparison is exact (tolerance 0): slot IDs, statuses, miss plans,
+slot<->token maps, LRU stamps and order, ticks and device buffer bytes.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from golden_trace import load, names
+from harness import (Pair, assert_call_equal, assert_device_bytes_equal_oracle,
+                     assert_device_rows, assert_state_equal)
+from hierarchical_sparse_kv_request_gb300 import hisparse as H
+from hierarchical_sparse_kv_request_gb300 import workload as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+
+
+# ----------------------------------------------------------------------------
+# hand-derived golden traces, on the GPU
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", names())
+def test_golden_trace_gpu(name):
+    layout, ops = load(name)
+    S0 = ops[0][1]["S"]
+    w = W.custom(1, layout["k"], layout["D"], [S0], capacity=[layout["cap"]])
+    p = Pair(w, track_bytes=True)
+    for i, (op, a) in enumerate(ops[1:]):
+        if op == "backup":
+            st = p.backup(0, np.array([a["pos"]], dtype=np.int32))
+            assert st[0] == 0
+            continue
+        if a["S"] != p.seq[0]:                # grown by backups since the last call
+            p.advance(a["S"] - int(p.seq[0]))
+        g, o = p.swap_in(0, np.array([a["topk"]], dtype=np.int32))
+        assert_call_equal(g, o, f"{name} op {i}")
+        e = a["expect"]
+        out, plan, cnt, st = g
+        assert out[0].tolist() == e["out"]
+        assert int(st[0]) == e["status"]
+        assert [tuple(x) for x in plan[0, : cnt[0]].tolist()] == e["plan"]
+        s2t = assert_state_equal(p, 0, f"{name} op {i}")
+        assert s2t[0].tolist() == e["slot2tok"]
+        lu = p.gpu.read_state(0)[1]
+        assert lu[0].tolist() == e["last_used"]
+        assert_device_bytes_equal_oracle(p, 0, f"{name} op {i}")
+    p.close()
+
+
+# ----------------------------------------------------------------------------
+# the tiny workload, every byte every call
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", [H.COPY_FUSED, H.COPY_SPLIT])
+def test_tiny_workload_full_parity(mode):
+    w = W.make_config(1)
+    sched = W.topk_schedule(w)[0]
+    p = Pair(w, track_bytes=True, copy_mode=mode)
+    for c in range(w.steps):
+        g, o = p.swap_in(0, sched[c])
+        assert_call_equal(g, o, f"call {c}")
+        assert_state_equal(p, 0, f"call {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"call {c}")
+    assert g[2][0] == 0                  # the short request never misses
+    assert g[2][1:].sum() > 0
+    p.close()
+
+
+# ----------------------------------------------------------------------------
+# edge cases
+# ----------------------------------------------------------------------------
+
+def _random_rows(rng, R, k, lens, pad=0.0):
+    rows = np.empty((R, k), dtype=np.int32)
+    for r in range(R):
+        rows[r] = rng.choice(int(lens[r]), k, replace=False)
+        if pad:
+            rows[r][rng.random(k) < pad] = -1
+    return rows
+
+
+def _reuse_rows(rng, prev, lens, keep=0.6, pad=0.0):
+    """Keep a fraction of each previous row's tokens, draw the rest anew."""
+    R, k = prev.shape
+    rows = np.empty_like(prev)
+    for r in range(R):
+        old = prev[r][prev[r] >= 0]
+        kept = rng.choice(old, min(old.size, int(keep * k)), replace=False)
+        pool = np.setdiff1d(np.arange(int(lens[r])), kept)
+        rows[r] = rng.permutation(np.concatenate([kept, rng.choice(pool, k - kept.size, replace=False)]))
+        if pad:
+            rows[r][rng.random(k) < pad] = -1
+    return rows
+
+
+@pytest.mark.parametrize("R,k,D,lens,pad", [
+    (3, 1500, 2000, [2500, 2000, 2001], 0.1),     # ragged k, S == D and D + 1
+    (2, 64, 64, [64, 65], 0.0),                   # top_k == D at both sides of the edge
+    (5, 1, 7, [8, 9, 100, 7, 3], 0.0),            # k = 1, odd D, tiny S
+    (4, 300, 999, [5000, 1000, 999, 4321], 0.3),  # odd D, heavy padding
+    (1, 4096, 8192, [200000], 0.0),               # KT = 4, long context
+    (2, 8192, 8192, [9000, 8192], 0.0),           # maximum top_k, KT = 8
+])
+def test_edge_shapes(R, k, D, lens, pad):
+    rng = np.random.default_rng(R * 7919 + k)
+    w = W.custom(R, k, D, lens, row_bytes=32)
+    p = Pair(w, track_bytes=True)
+    topk = _random_rows(rng, R, k, lens, pad)
+    for c in range(6):
+        g, o = p.swap_in(0, topk)
+        assert_call_equal(g, o, f"call {c}")
+        assert_state_equal(p, 0, f"call {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"call {c}")
+        topk = _reuse_rows(rng, topk, lens, keep=0.5, pad=pad)
+    p.close()
+
+
+def test_all_hits_then_all_misses():
+    R, k, D, S = 4, 256, 512, 5000
+    w = W.custom(R, k, D, [S] * R, row_bytes=64)
+    p = Pair(w, track_bytes=True)
+    # all hits: the newest k tokens are in the buffer after prefill
+    topk = np.tile(np.arange(S - k, S, dtype=np.int32)[::-1], (R, 1))
+    g, o = p.swap_in(0, topk)
+    assert_call_equal(g, o)
+    assert (g[2] == 0).all()
+    # all misses: k tokens never resident
+    topk = np.tile(np.arange(0, k, dtype=np.int32), (R, 1))
+    g, o = p.swap_in(0, topk)
+    assert_call_equal(g, o)
+    assert (g[2] == k).all()
+    assert_state_equal(p, 0)
+    assert_device_bytes_equal_oracle(p, 0)
+    # empty rows: all padding
+    g, o = p.swap_in(0, np.full((R, k), -1, dtype=np.int32))
+    assert_call_equal(g, o)
+    assert (g[0] == -1).all() and (g[2] == 0).all()
+    assert_state_equal(p, 0)
+    p.close()
+
+
+def test_malformed_rows_set_status_and_leave_state():
+    R, k, D = 6, 8, 16
+    lens = [100, 100, 100, 100, 10, 100]
+    w = W.custom(R, k, D, lens, row_bytes=16, capacity=[120] * R)
+    p = Pair(w, track_bytes=True)
+    good = np.array([np.arange(8) * 3 + 1] * R, dtype=np.int32)
+    good[4] = np.arange(8)   # request 4 is short (S = 10)
+    g, o = p.swap_in(0, good)
+    before = p.gpu.read_state(0)
+    bad = good.copy()
+    bad[0, 3] = 100          # == S: out of range
+    bad[1, 5] = bad[1, 2]    # duplicate
+    bad[2, 0] = -5           # negative, not padding
+    bad[3, 1] = 7; bad[3, 2] = 7; bad[3, 7] = 500   # both: out of range wins
+    bad[4, 4] = 10           # fast path, out of range (S = 10)
+    g, o = p.swap_in(0, bad)
+    assert_call_equal(g, o)
+    assert g[3].tolist() == [O.BAD_INDEX, O.DUPLICATE, O.BAD_INDEX, O.BAD_INDEX, O.BAD_INDEX, 0]
+    assert (g[0][:5] == -1).all()
+    after = p.gpu.read_state(0)
+    # requests 0..4 untouched: their slot maps, stamps and LRU order
+    for a, b in ((before[0], after[0]), (before[1], after[1]), (before[3], after[3])):
+        assert np.array_equal(a[:5], b[:5])
+    assert np.array_equal(before[2][: 5 * 120], after[2][: 5 * 120])
+    assert (after[4][:5] == 1).all() and after[4][5] == 2   # ticks still advance
+    assert_state_equal(p, 0)
+    # seq_len beyond the host capacity
+    p.seq[5] = 121
+    p.seq_d.copy_(torch.from_numpy(p.seq))
+    g, o = p.swap_in(0, good)
+    assert_call_equal(g, o)
+    assert g[3][5] == O.BAD_SEQ_LEN
+    assert_state_equal(p, 0)
+    p.close()
+
+
+def test_fast_path_grows_into_slow_path_with_backups():
+    R, k, D = 3, 16, 40
+    lens = [30, 38, 70]
+    steps = 12
+    w = W.custom(R, k, D, lens, row_bytes=48, capacity=[l + steps for l in lens])
+    p = Pair(w, track_bytes=True)
+    rng = np.random.default_rng(11)
+    for c in range(steps):
+        topk = _random_rows(rng, R, k, p.seq)
+        g, o = p.swap_in(0, topk)
+        assert_call_equal(g, o, f"call {c}")
+        st = p.backup(0, p.seq.copy())
+        assert (st == 0).all()
+        p.advance()
+        assert_state_equal(p, 0, f"call {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"call {c}")
+    assert (p.seq > D).all()
+    # a position outside the host capacity is reported, nothing written
+    pos = np.array([-1, 10_000, -1], dtype=np.int32)
+    st = p.backup(0, pos)
+    assert st.tolist() == [0, O.BAD_POSITION, 0]
+    assert p.gpu.status().cpu().numpy()[1] == O.BAD_POSITION
+    p.close()
+
+
+def test_replay_on_skip_layers_side_stream():
+    R, k, D = 4, 128, 256
+    lens = [3000, 256, 5000, 4000]
+    w = W.custom(R, k, D, lens, row_bytes=656, layers=4,
+                 anchor_of_layer=[-1, 0, 0, 0])
+    p = Pair(w, track_bytes=True)
+    rng = np.random.default_rng(3)
+    side = torch.cuda.Stream()
+    for c in range(6):
+        topk = _random_rows(rng, R, k, lens)
+        t = torch.from_numpy(topk).cuda()
+        p.gpu.swap_in(0, t, p.seq_d, p.out, p.plan, p.cnt)
+        ev = torch.cuda.Event()
+        ev.record()
+        side.wait_event(ev)
+        for l, ctas in ((1, 1), (2, 16), (3, 152)):
+            p.gpu.replay_plan(p.plan, p.cnt, l, num_ctas=ctas, stream=side)
+        done = torch.cuda.Event()
+        done.record(side)
+        torch.cuda.current_stream().wait_event(done)
+        o_out, o_plan, o_cnt, _ = p.orc.swap_in(0, topk, p.seq)
+        for l in (1, 2, 3):
+            p.orc.replay(o_plan, o_cnt, l)
+        torch.cuda.synchronize()
+        assert np.array_equal(p.out.cpu().numpy(), o_out)
+        for l in range(4):
+            assert_device_bytes_equal_oracle(p, l, f"call {c} layer {l}")
+    with pytest.raises(H.HiSparseError):
+        p.gpu.swap_in(1, t, p.seq_d, p.out, p.plan, p.cnt)   # skip layers own no state
+    p.close()
+
+
+def test_largest_supported_shapes():
+    # the biggest top-k / buffer / context the kernels accept
+    R, k, D, S = 2, 8192, 32768, 700_000
+    w = W.custom(R, k, D, [S, D], row_bytes=16)
+    p = Pair(w, track_bytes=True)
+    rng = np.random.default_rng(5)
+    for c in range(3):
+        topk = _random_rows(rng, R, k, [S, D])
+        g, o = p.swap_in(0, topk)
+        assert_call_equal(g, o, f"call {c}")
+        assert_state_equal(p, 0, f"call {c}")
+    assert_device_bytes_equal_oracle(p, 0)
+    p.close()
+    # 2^20 tokens with the guide's top_k / buffer
+    w = W.custom(1, 2048, 6144, [1 << 20], row_bytes=16)
+    p = Pair(w, track_bytes=False)
+    for c in range(3):
+        g, o = p.swap_in(0, _random_rows(rng, 1, 2048, [1 << 20]))
+        assert_call_equal(g, o)
+    s2t = assert_state_equal(p, 0)
+    assert_device_rows(p, 0, s2t)
+    p.close()
+
+
+def test_layout_errors_through_abi():
+    with pytest.raises(H.HiSparseError) as e:
+        H.HiSparse(2, 1, 16, 64, 32, 10, [100, 100])            # top_k > D
+    assert e.value.code == H.ERR_LAYOUT
+    with pytest.raises(H.HiSparseError) as e:
+        H.HiSparse(2, 1, 16, 16, 32, 1, [100, 100])             # ratio exceeded
+    assert e.value.code == H.ERR_CAPACITY
+    with pytest.raises(H.HiSparseError) as e:
+        H.HiSparse(1, 1, 16, 8192, 32768, 1000, [1 << 20])      # shared memory
+    assert e.value.code == H.ERR_UNSUPPORTED
