@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="warm-up and timed steps only (for ncu): no link probe, e2e, "
+                         "CPU baseline or clock sampling")
     return ap.parse_args()
 
 
@@ -56,6 +59,28 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Each rank runs an independent replica of the workload (requests are
+    independent units; no data crosses ranks)."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The slowest rank's time (the job's time); identity on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world_size: int, job_seconds: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank * world_size / job_seconds
 
 
 # ----------------------------------------------------------------------------
@@ -72,7 +97,9 @@ class Clocks:
         self.proc = None
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
 
-    def start(self):
+    def start(self, settle_s: float = 3.0):
+        """Start sampling and wait for the first sample, so the sampler's own
+        start-up is over before the timed region begins."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
@@ -80,6 +107,14 @@ class Clocks:
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < settle_s:
+            self.f.flush()
+            if os.path.getsize(self.f.name) > 0:
+                break
+            time.sleep(0.05)
+        time.sleep(0.3)
 
     def stop(self):
         if not self.proc:
@@ -120,8 +155,7 @@ class Setup:
         w = W.make_config(cfg)
         steps = -(-calls_needed // w.substeps)
         w.steps = steps
-        if rank:
-            w.seed += 1000 * rank          # an independent replica per rank
+        w.seed = replica_seed(w.seed, rank)
         self.w = w
         self.torch = torch
         self.H = H
@@ -255,6 +289,9 @@ def run_gpu(args):
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    clocks = Clocks(local)
+    if not args.profile:
+        clocks.start()
     for s in range(Wm):
         st.step(s)
     torch.cuda.synchronize()
@@ -262,11 +299,9 @@ def run_gpu(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     miss = torch.zeros(K, dtype=torch.int64, device="cuda")
-    clocks = Clocks(local)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks.start()
     wall0 = time.perf_counter()
     for i in range(K):
         flush.zero_()                       # L2 flush between timed steps (untimed)
@@ -277,21 +312,22 @@ def run_gpu(args):
             miss[i] += c.sum()              # untimed bookkeeping after the step
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    clk = clocks.stop()
+    clk = clocks.stop() if not args.profile else None
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_s = sum(step_ms) * 1e-3
-    if ws > 1:
-        t = torch.tensor([total_s], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(sum(step_ms) * 1e-3, "cuda")
     calls_per_step = len(w.anchors) * w.substeps
     rows_per_step = st.valid_per_call * calls_per_step
-    value = rows_per_step * K * ws / total_s
+    value = job_throughput(rows_per_step * K, ws, total_s)
     misses = int(miss.sum().item())
     miss_bytes = misses * w.row_bytes
     miss_gbs = miss_bytes / total_s / 1e9
 
     result = None
+    if args.profile:
+        if rank == 0:
+            result = {"profile_run": True, "ms_per_step": round(total_s / K * 1e3, 4),
+                      "miss_rows_per_step": round(int(miss.sum().item()) / K, 1)}
+        return result
     if rank == 0:
         link = measure_link_peak(torch, H)
         peak_hbm, hbm_src = hbm_peak()
@@ -326,6 +362,8 @@ def run_gpu(args):
                        "substeps": w.substeps, "backup": w.backup, "copy_mode": args.copy_mode,
                        "l2": "flushed between timed steps (512 MB write)"},
             "us_per_decode_step": round(total_s / K * 1e6, 2),
+            "step_ms_min_median_max": [round(min(step_ms), 4), round(statistics.median(step_ms), 4),
+                                       round(max(step_ms), 4)],
             "miss_h2d_gbs": round(miss_gbs, 1),
             "miss_rows_per_step": round(misses / K, 1),
             "link_peak": link,
@@ -402,11 +440,8 @@ def run_e2e(st, torch, K, Wm, rank, ws):
             calls += ncalls
             h2d += ncalls * R * k * 4
             d2h += R * k * 4
-    if ws > 1:
-        t = torch.tensor([total], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total = float(t.item())
-    return {"value": round(st.valid_per_call * calls * ws / total, 1), "unit": "rows/s",
+    total = max_over_ranks(total, "cuda")
+    return {"value": round(job_throughput(st.valid_per_call * calls, ws, total), 1), "unit": "rows/s",
             "h2d_bytes_per_step": h2d // K, "d2h_bytes_per_step": d2h // K,
             "ms_per_step": round(total / K * 1e3, 4)}
 
