@@ -168,9 +168,6 @@ size_t replay_smem_bytes(int R) { return (size_t)(R + 1) * 4; }
 cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s)
 {
     const size_t smem = replay_smem_bytes(a.g.R);
-    cudaError_t e = cudaFuncSetAttribute(replay_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_ctas);
     cfg.blockDim = dim3(REPLAY_NT);

@@ -36,6 +36,7 @@ struct hisparse_handle {
     hs::LayerDescDev *d_layers = nullptr;
     int32_t *d_plan_rows = nullptr, *d_plan_counts = nullptr;  // split-copy plan
     int32_t copy_mode = HISPARSE_COPY_FUSED;
+    bool stage_s2t = false;   // resolve kernel stages the slot->token row
 };
 
 namespace {
@@ -183,10 +184,16 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
     }
     int max_smem = 0;
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
-    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap) > (size_t)max_smem ||
+    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, false) > (size_t)max_smem ||
         hs::replay_smem_bytes(h->R) > (size_t)max_smem) {
         release(h);
         return HISPARSE_ERR_UNSUPPORTED;
+    }
+    // the slot->token row rides in shared memory when it fits
+    h->stage_s2t = hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, true) <= (size_t)max_smem;
+    if (hs::resolve_prepare((size_t)max_smem) != cudaSuccess) {
+        release(h);
+        return HISPARSE_ERR_CUDA;
     }
 
     // Pinned host pool, mapped into the device address space.  A test hook
@@ -306,6 +313,7 @@ int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx, const
     a.max_cap = (int32_t)h->max_cap;
     const bool split = h->copy_mode == HISPARSE_COPY_SPLIT;
     a.fused_copy = !split;
+    a.stage_s2t = h->stage_s2t;
     a.plan_rows = out_plan ? out_plan->rows : (split ? h->d_plan_rows : nullptr);
     a.plan_counts = out_plan ? out_plan->counts : (split ? h->d_plan_counts : nullptr);
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));

@@ -123,12 +123,16 @@ struct ResolveLaunch {
     LayerStore store;
     Geometry g;
     int32_t max_cap;       // largest host capacity (sizes the miss bitmap)
-    bool fused_copy;
+    bool fused_copy;       // copy the misses in this kernel
+    bool stage_s2t;        // stage the slot->token row in shared memory
 };
 
 // Shared-memory bytes the resolve kernel needs for this geometry.
-size_t resolve_smem_bytes(int k, int D, int max_cap);
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t);
 int resolve_threads();
+// Allow every instantiation of the resolve kernel up to `smem` bytes of
+// dynamic shared memory (called at handle creation, outside any capture).
+cudaError_t resolve_prepare(size_t smem);
 cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s);
 
 struct ReplayLaunch {
@@ -139,7 +143,7 @@ struct ReplayLaunch {
     int num_ctas;
     bool programmatic;  // launched right after a resolve (programmatic dependency)
 };
-size_t replay_smem_bytes(int R);
+size_t replay_smem_bytes(int R);  // below the 48 KB default for R <= 8192
 cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s);
 
 struct BackupLaunch {

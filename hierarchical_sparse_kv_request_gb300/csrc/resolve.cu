@@ -1,11 +1,24 @@
 // resolve.cu -- the swap-in resolver kernel.
 //
-// One CTA resolves one request's top-k for one call ([Guide] "HiSparse:
-// Hierarchical Sparse Attention", Decode Workflow: fast path for short
-// sequences; otherwise hit detection -> LRU reorder -> miss handling with a
-// host-to-device copy; [Arch] "HiSparse local KV offload architecture", Hot
-// lookup and LRU: a hot row is used in place and refreshes the GPU LRU, a
-// miss takes the LRU victim and copies the pinned host row into it).
+// One CTA of 1024 threads resolves one request's top-k for one call
+// ([Guide] "HiSparse: Hierarchical Sparse Attention", Decode Workflow: fast
+// path for short sequences; otherwise hit detection -> LRU reorder -> miss
+// handling with a host-to-device copy; [Arch] "HiSparse local KV offload
+// architecture", Hot lookup and LRU: a hot row is used in place and
+// refreshes the GPU LRU, a miss takes the LRU victim and copies the pinned
+// host row into it).
+//
+// The miss copies cross the host link and dominate the call, so everything
+// else is arranged around starting them early and keeping them going:
+//   1. the LRU list is staged into shared memory with asynchronous copies
+//      issued at kernel start, under the first global round trips;
+//   2. once the sorted miss list exists, every thread loads its first host
+//      chunks into registers, and those loads are in flight while the
+//      victims are chosen;
+//   3. the slot->token row is staged too, so once the victims are known all
+//      state writes are plain stores that never wait behind the host loads;
+//      they are issued before the prefetched rows are consumed, then every
+//      thread streams the rest of the rows.
 //
 // Exact LRU without sorting.  The request's slots are kept in a list `lru`
 // ordered by (last_used, slot).  One call stamps every selected slot (hits and
@@ -17,43 +30,34 @@
 // non-hit flags of the list, plus a popcount prefix over the selected-slot
 // bitmap.  Misses are ranked by token with a bitmap over [0, seq_len) and a
 // popcount prefix, which yields ascending token order without a sort.
-//
-// Every global access below is a coalesced row/array access or a single
-// gather of the token->slot map; there are no loops over keys.
 #include "hs_common.cuh"
 
 namespace hs {
 namespace {
 
 constexpr int NT = 1024;       // threads per CTA
-constexpr int COPY_UNROLL = 8;  // 16-byte host loads in flight per thread
-
-struct Smem {
-    uint32_t *warp_tot;  // [32]
-    uint32_t *hitbits;   // [DW]  slots hit by this call
-    uint32_t *selbits;   // [DW]  slots chosen as victims
-    uint32_t *missbits;  // [MW]  miss tokens (and, on the fast path, all tokens)
-    uint16_t *lru_s;     // [D]   staged LRU list
-    uint16_t *chunk_pre; // [NT]  misses before each thread's chunk of missbits
-    uint16_t *victims;   // [k]   victim slot of miss rank i
-    int32_t *misstok;    // [k]   token of miss rank i
-};
+constexpr int PREFETCH = 4;    // host chunks per thread loaded before the victims
+constexpr int COPY_UNROLL = 8; // host chunks in flight per thread in the copy loop
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct SmemPlan {
-    size_t hit, sel, miss, lru, chunk, vict, mtok, total;
+    size_t hit, sel, miss, lru, s2t, chunk, vict, mtok, total;
 };
 
-__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap)
+// Shared memory of the CTA: bitmaps over slots and tokens, the staged LRU
+// list, optionally the staged slot->token row, and miss tokens and victims
+// by miss rank.
+__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t)
 {
     SmemPlan p;
     const size_t DW = (size_t)(D + 31) / 32, MW = (size_t)(max_cap + 31) / 32;
-    size_t o = 32 * 4;
+    size_t o = 32 * 4;             // warp totals
     p.hit = o;   o += DW * 4;
     p.sel = o;   o += DW * 4;
     p.miss = o;  o += MW * 4;
-    p.lru = o;   o = align_up(o + (size_t)D * 2, 4);
+    p.lru = align_up(o, 16); o = p.lru + align_up((size_t)D * 2, 16);
+    p.s2t = o;   o += stage_s2t ? align_up((size_t)D * 4, 16) : 0;
     p.chunk = o; o = align_up(o + (size_t)NT * 2, 4);
     p.vict = o;  o = align_up(o + (size_t)k * 2, 4);
     p.mtok = o;  o += (size_t)k * 4;
@@ -61,10 +65,30 @@ __host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap)
     return p;
 }
 
+struct Smem {
+    uint32_t *warp_tot;  // [32]
+    uint32_t *hitbits;   // [DW]  slots hit by this call
+    uint32_t *selbits;   // [DW]  slots chosen as victims
+    uint32_t *missbits;  // [MW]  miss tokens (and, on the fast path, all tokens)
+    uint16_t *lru_s;     // [D]   staged LRU list
+    int32_t *s2t_s;      // [D]   staged slot->token row (null when not staged)
+    uint16_t *chunk_pre; // [NT]  misses before each thread's chunk of missbits
+    uint16_t *victims;   // [k]   victim slot of miss rank i
+    int32_t *misstok;    // [k]   token of miss rank i
+};
+
 __device__ __forceinline__ bool test_bit(const uint32_t *bits, int i)
 {
     return (bits[i >> 5] >> (i & 31)) & 1u;
 }
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Final writes of a request whose call ends without touching its state.
 template <int KT>
@@ -73,6 +97,7 @@ __device__ __forceinline__ void finish_untouched(const ResolveLaunch &a, int r,
                                                  uint32_t tick)
 {
     const int k = a.g.k;
+    cp_async_wait_all();  // staged rows may still be landing in shared memory
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int j = threadIdx.x + i * NT;
@@ -94,13 +119,14 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int k = a.g.k, D = a.g.D;
     const int DW = (D + 31) >> 5;
 
-    const SmemPlan sp = plan_smem(k, D, a.max_cap);
+    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t);
     Smem sm;
     sm.warp_tot = reinterpret_cast<uint32_t *>(smem_raw);
     sm.hitbits = reinterpret_cast<uint32_t *>(smem_raw + sp.hit);
     sm.selbits = reinterpret_cast<uint32_t *>(smem_raw + sp.sel);
     sm.missbits = reinterpret_cast<uint32_t *>(smem_raw + sp.miss);
     sm.lru_s = reinterpret_cast<uint16_t *>(smem_raw + sp.lru);
+    sm.s2t_s = a.stage_s2t ? reinterpret_cast<int32_t *>(smem_raw + sp.s2t) : nullptr;
     sm.chunk_pre = reinterpret_cast<uint16_t *>(smem_raw + sp.chunk);
     sm.victims = reinterpret_cast<uint16_t *>(smem_raw + sp.vict);
     sm.misstok = reinterpret_cast<int32_t *>(smem_raw + sp.mtok);
@@ -120,6 +146,17 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         const int j = tid + i * NT;
         t[i] = j < k ? a.topk[(int64_t)r * k + j] : -1;
     }
+    // Stage the LRU list and the slot->token row with asynchronous copies;
+    // they land under the round trips above.  (16-byte rows need D % 8 == 0.)
+    const uint16_t *lru = a.st.lru + (int64_t)r * D;
+    int32_t *slot2tok = a.st.slot2tok + (int64_t)r * D;
+    const bool staged_async = (D & 7) == 0;
+    if (staged_async) {
+        for (int i = tid; i < (D >> 3); i += NT) cp_async16(sm.lru_s + i * 8, lru + i * 8);
+        if (sm.s2t_s)
+            for (int i = tid; i < (D >> 2); i += NT) cp_async16(sm.s2t_s + i * 4, slot2tok + i * 4);
+    }
+    cp_async_commit();
 
     if (S < 0 || (int64_t)S > cap) {  // uniform across the CTA
         finish_untouched<KT>(a, r, t, kStatusBadSeqLen, tick);
@@ -147,32 +184,23 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         return;
     }
 
-    // ---- slow path --------------------------------------------------------
+    // ---- slow path: hit detection ----------------------------------------
     int32_t *tok2slot = a.st.tok2slot + off;
-    int32_t *slot2tok = a.st.slot2tok + (int64_t)r * D;
-    uint32_t *last_used = a.st.last_used + (int64_t)r * D;
-    uint16_t *lru = a.st.lru + (int64_t)r * D;
-
-    // Hit detection: gather the token->slot map (issued before the barrier
-    // so its latency overlaps the shared-memory clears and the list staging).
     int32_t s[KT];
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         s[i] = (t[i] >= 0 && t[i] < S) ? tok2slot[t[i]] : -1;
         if (s[i] >= D) s[i] = -1;  // never true for state this library wrote
     }
-
     const int mw = (S + 31) >> 5;
     for (int w = tid; w < mw; w += NT) sm.missbits[w] = 0u;
     for (int w = tid; w < DW; w += NT) { sm.hitbits[w] = 0u; sm.selbits[w] = 0u; }
-    // stage the LRU list (pairs of slots when D is even, so rows stay 4-byte aligned)
-    if ((D & 1) == 0) {
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(lru);
-        uint32_t *dst = reinterpret_cast<uint32_t *>(sm.lru_s);
-        for (int i = tid; i < (D >> 1); i += NT) dst[i] = src[i];
-    } else {
+    if (!staged_async) {
         for (int i = tid; i < D; i += NT) sm.lru_s[i] = lru[i];
+        if (sm.s2t_s)
+            for (int i = tid; i < D; i += NT) sm.s2t_s[i] = slot2tok[i];
     }
+    cp_async_wait_all();
     __syncthreads();
 
     bool bad = false, dup = false;
@@ -195,13 +223,20 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         finish_untouched<KT>(a, r, t, bad ? kStatusBadIndex : kStatusDuplicate, tick);
         return;
     }
+    // hits and padding resolve now
+    int32_t *out = a.out + (int64_t)r * k;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        const int j = tid + i * NT;
+        if (j < k && (t[i] < 0 || s[i] >= 0)) out[j] = t[i] < 0 ? -1 : s[i];
+    }
 
-    // One prefix sum gives both (a) the number of misses before each
-    // thread's chunk of miss-bitmap words and (b) the number of non-hit list
-    // entries before each thread's chunk of the LRU list.
-    const int C = (D + NT - 1) / NT;   // list entries per thread
+    // One prefix sum gives both (a) the misses before each thread's chunk of
+    // miss-bitmap words and (b) the non-hit list entries before each
+    // thread's chunk of the LRU list.
+    const int C = (D + NT - 1) / NT;
     const int e0 = min(tid * C, D), e1 = min(e0 + C, D);
-    const int WC = (mw + NT - 1) / NT; // miss-bitmap words per thread
+    const int WC = (mw + NT - 1) / NT;
     const int w0 = min(tid * WC, mw), w1 = min(w0 + WC, mw);
     uint32_t nh = 0, mc = 0;
     for (int e = e0; e < e1; ++e) nh += !test_bit(sm.hitbits, sm.lru_s[e]);
@@ -209,12 +244,40 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     uint32_t tot;
     const uint32_t pre = block_exclusive_scan<NT>((mc << 16) | nh, sm.warp_tot, tot);
     const int m = (int)(tot >> 16);
-    const int nonhit = (int)(tot & 0xFFFFu);
-    const int h = D - nonhit;
+    const int h = D - (int)(tot & 0xFFFFu);
     sm.chunk_pre[tid] = (uint16_t)(pre >> 16);
+    {   // the sorted miss list: enumerate this thread's words in order
+        uint32_t rank = pre >> 16;
+        for (int w = w0; w < w1; ++w) {
+            uint32_t bits = sm.missbits[w];
+            while (bits) {
+                const int b = __ffs(bits) - 1;
+                bits &= bits - 1u;
+                sm.misstok[rank++] = w * 32 + b;
+            }
+        }
+    }
+    __syncthreads();
+
+    // First host chunks: loaded now, stored after the state writes below.
+    const int64_t B = a.g.B;
+    const int CH = a.g.chunks;
+    const int total = a.fused_copy ? m * CH : 0;
+    const uint8_t *hrow0 = a.store.host + off * B;
+    uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
+    uint4 pv[PREFETCH];
+#pragma unroll
+    for (int u = 0; u < PREFETCH; ++u) {
+        const int e = tid + u * NT;
+        if (e < total) {
+            const int i = e / CH, c = e - i * CH;
+            pv[u] = ld_host_v4(hrow0 + (int64_t)sm.misstok[i] * B + c * 16);
+        }
+    }
 
     // Victims = the first m non-hit list entries; the rest keep their order
     // at the front of the new list.
+    uint16_t *lru_w = a.st.lru + (int64_t)r * D;
     {
         uint32_t q = pre & 0xFFFFu;
         for (int e = e0; e < e1; ++e) {
@@ -224,16 +287,41 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
                 sm.victims[q] = (uint16_t)sl;
                 atomicOr(&sm.selbits[sl >> 5], 1u << (sl & 31));
             } else {
-                lru[q - m] = (uint16_t)sl;
+                lru_w[q - m] = (uint16_t)sl;
             }
             ++q;
         }
     }
     __syncthreads();
 
+    // State writes (stores only, so nothing here waits behind the host
+    // loads in flight).  Misses take victims by ascending token rank.
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        const int j = tid + i * NT;
+        const int32_t x = t[i];
+        if (j >= k || x < 0 || s[i] >= 0) continue;
+        const int w = x >> 5;
+        const int owner = w / WC;
+        uint32_t rank = sm.chunk_pre[owner];
+        for (int q = owner * WC; q < w; ++q) rank += __popc(sm.missbits[q]);
+        rank += __popc(sm.missbits[w] & ((1u << (x & 31)) - 1u));
+        const int v = sm.victims[rank];
+        const int32_t old = sm.s2t_s ? sm.s2t_s[v] : slot2tok[v];
+        if (old >= 0 && (int64_t)old < cap) tok2slot[old] = -1;
+        slot2tok[v] = x;
+        tok2slot[x] = v;
+        out[j] = v;
+        if (a.plan_rows) {
+            int32_t *pr = a.plan_rows + ((int64_t)r * k + rank) * 2;
+            pr[0] = x;
+            pr[1] = v;
+        }
+    }
     // Selected slots (hits and victims) go to the back of the list in slot
     // order and are stamped with the tick.
     {
+        uint32_t *last_used = a.st.last_used + (int64_t)r * D;
         const uint32_t w = tid < DW ? (sm.hitbits[tid] | sm.selbits[tid]) : 0u;
         uint32_t tot2;
         uint32_t pos = (uint32_t)(D - h - m) + block_exclusive_scan<NT>(__popc(w), sm.warp_tot, tot2);
@@ -242,36 +330,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
             const int b = __ffs(bits) - 1;
             bits &= bits - 1u;
             const int sl = tid * 32 + b;
-            lru[pos++] = (uint16_t)sl;
+            lru_w[pos++] = (uint16_t)sl;
             last_used[sl] = tick;
-        }
-    }
-
-    // Outputs in input order; misses take victims by ascending token rank.
-    int32_t *out = a.out + (int64_t)r * k;
-#pragma unroll
-    for (int i = 0; i < KT; ++i) {
-        const int j = tid + i * NT;
-        if (j >= k) continue;
-        const int32_t x = t[i];
-        if (x < 0) { out[j] = -1; continue; }
-        if (s[i] >= 0) { out[j] = s[i]; continue; }
-        const int w = x >> 5;
-        const int owner = w / WC;
-        uint32_t rank = sm.chunk_pre[owner];
-        for (int q = owner * WC; q < w; ++q) rank += __popc(sm.missbits[q]);
-        rank += __popc(sm.missbits[w] & ((1u << (x & 31)) - 1u));
-        const int v = sm.victims[rank];
-        const int32_t old = slot2tok[v];
-        if (old >= 0 && (int64_t)old < cap) tok2slot[old] = -1;
-        slot2tok[v] = x;
-        tok2slot[x] = v;
-        out[j] = v;
-        sm.misstok[rank] = x;
-        if (a.plan_rows) {
-            int32_t *pr = a.plan_rows + ((int64_t)r * k + rank) * 2;
-            pr[0] = x;
-            pr[1] = v;
         }
     }
     if (tid == 0) {
@@ -279,16 +339,17 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (a.plan_counts) a.plan_counts[r] = m;
         a.st.tick[r] = tick;
     }
-    if (!a.fused_copy || m == 0) return;
 
-    // ---- fused miss copy: pinned host rows -> freed device slots ---------
-    __syncthreads();
-    const int64_t B = a.g.B;
-    const int CH = a.g.chunks;
-    const int total = m * CH;
-    const uint8_t *hrow0 = a.store.host + off * B;
-    uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
-    for (int e = tid; e < total; e += NT * COPY_UNROLL) {
+    // ---- miss copies: pinned host rows -> victim slots ---------------------
+#pragma unroll
+    for (int u = 0; u < PREFETCH; ++u) {
+        const int e = tid + u * NT;
+        if (e < total) {
+            const int i = e / CH, c = e - i * CH;
+            st_v4(drow0 + (int64_t)sm.victims[i] * B + c * 16, pv[u]);
+        }
+    }
+    for (int e = PREFETCH * NT + tid; e < total; e += NT * COPY_UNROLL) {
         uint4 v[COPY_UNROLL];
         uint8_t *dst[COPY_UNROLL];
 #pragma unroll
@@ -310,21 +371,38 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
 template <int KT>
 cudaError_t launch_kt(const ResolveLaunch &a, cudaStream_t s, size_t smem)
 {
-    cudaError_t e = cudaFuncSetAttribute(resolve_kernel<KT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     resolve_kernel<KT><<<a.g.R, NT, smem, s>>>(a);
     return cudaGetLastError();
 }
 
+template <int KT>
+cudaError_t prepare_kt(size_t smem)
+{
+    return cudaFuncSetAttribute(resolve_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem);
+}
+
 }  // namespace
 
-size_t resolve_smem_bytes(int k, int D, int max_cap) { return plan_smem(k, D, max_cap).total; }
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t)
+{
+    return plan_smem(k, D, max_cap, stage_s2t).total;
+}
+
 int resolve_threads() { return NT; }
+
+cudaError_t resolve_prepare(size_t smem)
+{
+    cudaError_t e = prepare_kt<1>(smem);
+    if (e == cudaSuccess) e = prepare_kt<2>(smem);
+    if (e == cudaSuccess) e = prepare_kt<4>(smem);
+    if (e == cudaSuccess) e = prepare_kt<8>(smem);
+    return e;
+}
 
 cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s)
 {
-    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap);
+    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t);
     const int kt = (a.g.k + NT - 1) / NT;
     if (kt <= 1) return launch_kt<1>(a, s, smem);
     if (kt <= 2) return launch_kt<2>(a, s, smem);
