@@ -44,16 +44,24 @@ class Pair:
         self.gpu.close()
         self.orc.close()
 
-    def swap_in(self, layer: int, topk: np.ndarray, plan=None, cnt=None):
-        """One call on both sides; returns (gpu results, oracle results)."""
+    def swap_in(self, layer: int, topk: np.ndarray, plan=None, cnt=None, record_plan=True):
+        """One call on both sides; returns (gpu results, oracle results).
+        With record_plan=False the library gets no plan to fill; the GPU
+        plan/count results are then the oracle's (nothing to compare)."""
         plan = self.plan if plan is None else plan
         cnt = self.cnt if cnt is None else cnt
         t = torch.from_numpy(np.ascontiguousarray(topk, dtype=np.int32)).cuda()
-        self.gpu.swap_in(layer, t, self.seq_d, self.out, plan, cnt)
+        if record_plan:
+            self.gpu.swap_in(layer, t, self.seq_d, self.out, plan, cnt)
+        else:
+            self.gpu.swap_in(layer, t, self.seq_d, self.out)
         o = self.orc.swap_in(layer, topk, self.seq)
         torch.cuda.synchronize()
-        g = (self.out.cpu().numpy(), plan.cpu().numpy(), cnt.cpu().numpy(),
-             self.gpu.status().cpu().numpy())
+        if record_plan:
+            g = (self.out.cpu().numpy(), plan.cpu().numpy(), cnt.cpu().numpy(),
+                 self.gpu.status().cpu().numpy())
+        else:
+            g = (self.out.cpu().numpy(), o[1], o[2], self.gpu.status().cpu().numpy())
         self.last = (g, o)
         return g, o
 

@@ -77,6 +77,20 @@ def test_tiny_workload_full_parity(mode):
     p.close()
 
 
+def test_split_copy_with_the_librarys_own_plan():
+    """Split copy mode without a caller plan: the resolve grid records the
+    misses in the handle's internal plan and the copy grid reads them."""
+    w = W.make_config(1)
+    sched = W.topk_schedule(w)[0]
+    p = Pair(w, track_bytes=True, copy_mode=H.COPY_SPLIT)
+    for c in range(w.steps):
+        g, o = p.swap_in(0, sched[c], record_plan=False)
+        assert_call_equal(g, o, f"call {c}")
+        assert_state_equal(p, 0, f"call {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"call {c}")
+    p.close()
+
+
 # ----------------------------------------------------------------------------
 # edge cases
 # ----------------------------------------------------------------------------

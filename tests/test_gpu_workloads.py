@@ -1,0 +1,137 @@
+"""Full-size parity of the four larger workloads, in the launch configuration
+the benchmark times (fused resolve + copy; 16-CTA replays on a side stream
+next to the stand-in compute kernel; separate plans per verification
+sub-step; eager backups).
+
+Every call's slot IDs, statuses, miss counts and plans are compared with the
+oracle in full.  The hot state (maps, stamps, LRU order, ticks) is compared
+in full at checkpoints, and device rows against the generator's rows of the
+tokens the oracle maps there: a sample during the run, every slot at the end.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from harness import Pair, assert_call_equal, assert_device_rows, assert_state_equal
+from hierarchical_sparse_kv_request_gb300 import hisparse as H
+from hierarchical_sparse_kv_request_gb300 import workload as W
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+
+
+def test_decode_40k_all_steps():
+    """32 x 40000 tokens, k 2048, D 6144, 656 B rows, 64 decode steps."""
+    w = W.make_config(2)
+    sched = W.topk_schedule(w)[0]
+    p = Pair(w, track_bytes=False)
+    misses = 0
+    for c in range(w.steps):
+        g, o = p.swap_in(0, sched[c])
+        assert_call_equal(g, o, f"call {c}")
+        misses += int(g[2].sum())
+        if c % 16 == 15:
+            s2t = assert_state_equal(p, 0, f"call {c}")
+            assert_device_rows(p, 0, s2t, sample=256, seed=c, ctx=f"call {c}")
+    assert_device_rows(p, 0, s2t, ctx="end")
+    assert misses > 0
+    p.close()
+
+
+def test_mixed_lengths_four_layers_with_backups():
+    """128 requests of U[2048, 81920] tokens, 4 layers, backups every step."""
+    w = W.make_config(3)
+    sched = W.topk_schedule(w)
+    p = Pair(w, track_bytes=False)
+    assert (w.seq_lens0 <= w.device_buffer_size).any()      # some take the fast path
+    for step in range(w.steps):
+        for l in range(w.num_layers):
+            g, o = p.swap_in(l, sched[l][step])
+            assert_call_equal(g, o, f"step {step} layer {l}")
+        for l in range(w.num_layers):
+            st = p.backup(l, p.seq.copy())
+            assert (st == 0).all()
+        p.advance()
+        if step % 8 == 7:
+            for l in range(w.num_layers):
+                s2t = assert_state_equal(p, l, f"step {step} layer {l}")
+                assert_device_rows(p, l, s2t, sample=64, seed=step, ctx=f"step {step} layer {l}")
+    for l in range(w.num_layers):
+        s2t = assert_state_equal(p, l, f"end layer {l}")
+        assert_device_rows(p, l, s2t, ctx=f"end layer {l}")
+    p.close()
+
+
+def test_shared_index_replay_beside_compute():
+    """1 anchor + 3 skip layers, 64 x 65536 tokens: each skip layer replays
+    the anchor's plan with 16 CTAs on a side stream while the stand-in
+    compute kernel runs on the main stream."""
+    w = W.make_config(4)
+    sched = W.topk_schedule(w)[0]
+    p = Pair(w, track_bytes=False)
+    side = torch.cuda.Stream(priority=-1)
+    nthreads = 152 * 256
+    buf = torch.zeros(nthreads, dtype=torch.float32, device="cuda")
+    for c in range(w.steps):
+        t = torch.from_numpy(sched[c]).cuda()
+        p.gpu.swap_in(0, t, p.seq_d, p.out, p.plan, p.cnt)
+        ev = torch.cuda.Event()
+        ev.record()
+        side.wait_event(ev)
+        for l in (1, 2, 3):
+            p.gpu.replay_plan(p.plan, p.cnt, l, num_ctas=16, stream=side)
+        done = torch.cuda.Event()
+        done.record(side)
+        H.synthetic_compute(buf, nthreads, 20000)
+        torch.cuda.current_stream().wait_event(done)
+        o = p.orc.swap_in(0, sched[c], p.seq)
+        torch.cuda.synchronize()
+        g = (p.out.cpu().numpy(), p.plan.cpu().numpy(), p.cnt.cpu().numpy(),
+             p.gpu.status().cpu().numpy())
+        assert_call_equal(g, o, f"call {c}")
+        if c % 8 == 7:
+            s2t = assert_state_equal(p, 0, f"call {c}")
+            for l in range(4):
+                assert_device_rows(p, l, s2t, sample=64, seed=c, ctx=f"call {c} layer {l}")
+    s2t = assert_state_equal(p, 0, "end")
+    for l in range(4):
+        assert_device_rows(p, l, s2t, ctx=f"end layer {l}")
+    p.close()
+
+
+def test_speculative_substeps_with_backups():
+    """256 x 32768 tokens, D 4096, 1152 B rows: 3 verification sub-steps per
+    decode step, each with its own plan, then one backup per step."""
+    w = W.make_config(5)
+    sched = W.topk_schedule(w)[0]
+    p = Pair(w, track_bytes=False)
+    R, k = w.num_requests, w.top_k
+    plans = [torch.empty((R, k, 2), dtype=torch.int32, device="cuda") for _ in range(3)]
+    cnts = [torch.empty(R, dtype=torch.int32, device="cuda") for _ in range(3)]
+    for step in range(w.steps):
+        oracle_calls = []
+        for sub in range(w.substeps):
+            g, o = p.swap_in(0, sched[step * w.substeps + sub], plan=plans[sub], cnt=cnts[sub])
+            assert_call_equal(g, o, f"step {step} sub {sub}")
+            oracle_calls.append(o)
+        # each sub-step's plan row is still intact after the later sub-steps
+        for sub, o in enumerate(oracle_calls):
+            g = (o[0], plans[sub].cpu().numpy(), cnts[sub].cpu().numpy(), o[3])
+            assert_call_equal(g, o, f"step {step} plan {sub} after the step")
+        st = p.backup(0, p.seq.copy())
+        assert (st == 0).all()
+        p.advance()
+        if step % 4 == 3:
+            s2t = assert_state_equal(p, 0, f"step {step}")
+            assert_device_rows(p, 0, s2t, sample=64, seed=step, ctx=f"step {step}")
+    s2t = assert_state_equal(p, 0, "end")
+    assert_device_rows(p, 0, s2t, ctx="end")
+    p.close()
