@@ -10,6 +10,7 @@
 // device_buffer_size, host_to_device_ratio, swap_in_block_size.
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -394,6 +395,87 @@ int hisparse_set_copy_mode(hisparse_t h, int32_t mode)
     if (!h || (mode != HISPARSE_COPY_FUSED && mode != HISPARSE_COPY_SPLIT)) return HISPARSE_ERR_INVALID_ARG;
     h->copy_mode = mode;
     return HISPARSE_OK;
+}
+
+}  // extern "C"
+
+// ---- allocation-free split copy --------------------------------------------
+//
+// The miss plan that the resolve grid hands to the copy grid lives in this
+// fixed array instead of device memory obtained from cudaMalloc.  Each GPU
+// that loads the library holds its own copy (HISPARSE_NOALLOC_SCRATCH_BYTES)
+// until the process exits.  Layout: (token, slot) pairs of request r at
+// [r * k * 2, ...), then R miss counts after the pairs region.
+static __device__ __align__(256) int32_t g_noalloc_scratch[HISPARSE_NOALLOC_SCRATCH_BYTES / 4];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t *g_noalloc_addr[kNoallocMaxDevices] = {};
+
+// Device address of this device's copy of the array.  Host code only holds a
+// stand-in for the symbol, so the address is looked up once per device, with
+// that device current, and cached.
+int noalloc_scratch(int32_t **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HISPARSE_ERR_CUDA;
+    if (dev < 0 || dev >= kNoallocMaxDevices) return HISPARSE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return HISPARSE_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = static_cast<int32_t *>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return HISPARSE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_idx,
+                             const int32_t *seq_lens, int32_t *out_slot_ids, void *stream)
+{
+    if (!h || !topk_idx || !seq_lens || !out_slot_ids) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L || h->anchor[layer] >= 0) return HISPARSE_ERR_LAYER;
+    // the pairs of all requests plus one count per request must fit the array
+    const int64_t need = ((int64_t)h->R * h->k * 2 + h->R) * 4;
+    if (need > HISPARSE_NOALLOC_SCRATCH_BYTES) return HISPARSE_ERR_UNSUPPORTED;
+    int32_t *scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != HISPARSE_OK) return rc;
+    // Nothing needs clearing between calls: the resolve grid writes every
+    // request's count, and the copy grid reads only the pairs those counts
+    // cover.
+    hs::ResolveLaunch a;
+    a.topk = topk_idx;
+    a.seq_lens = seq_lens;
+    a.out = out_slot_ids;
+    a.status = h->d_status;
+    a.st = h->state[layer];
+    a.store = layer_store(h, layer);
+    a.g = geometry(h);
+    a.max_cap = (int32_t)h->max_cap;
+    a.fused_copy = false;
+    a.stage_s2t = h->stage_s2t;
+    a.plan_rows = scratch;
+    a.plan_counts = scratch + (int64_t)h->R * h->k * 2;
+    cudaError_t e = hs::launch_resolve(a, as_stream(stream));
+    if (e != cudaSuccess) return HISPARSE_ERR_CUDA;
+    hs::ReplayLaunch c;
+    c.plan_rows = a.plan_rows;
+    c.plan_counts = a.plan_counts;
+    c.store = a.store;
+    c.g = a.g;
+    c.num_ctas = h->num_sms;
+    c.programmatic = true;
+    return cuda_status(hs::launch_replay(c, as_stream(stream)));
 }
 
 // ---- measurement kernels ---------------------------------------------------

@@ -65,6 +65,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_device_buffer": [P, I32, P],
         "hisparse_prefill": [P, P, P],
         "hisparse_swap_in": [P, I32, P, P, P, P, P],
+        "hisparse_swap_in_noalloc": [P, I32, P, P, P, P],
         "hisparse_replay_plan": [P, P, I32, I32, P],
         "hisparse_backup": [P, I32, P, P, P],
         "hisparse_status": [P, P],
@@ -212,6 +213,14 @@ class HiSparse:
         _check(self.lib.hisparse_swap_in(self.h, layer, _addr(topk), _addr(seq_lens),
                                          _addr(out_slot_ids), plan, _stream(stream)),
                "hisparse_swap_in")
+
+    def swap_in_noalloc(self, layer: int, topk, seq_lens, out_slot_ids, stream=None) -> None:
+        """hisparse_swap_in_noalloc: the split-copy swap-in whose internal
+        miss plan lives in the library's fixed per-GPU array, so the call
+        causes no device allocation (for callers that may not allocate)."""
+        _check(self.lib.hisparse_swap_in_noalloc(self.h, layer, _addr(topk), _addr(seq_lens),
+                                                 _addr(out_slot_ids), _stream(stream)),
+               "hisparse_swap_in_noalloc")
 
     def replay_plan(self, plan_rows, plan_counts, layer: int, num_ctas: int = 0,
                     stream=None) -> None:

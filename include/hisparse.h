@@ -254,6 +254,32 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok,
  * identical; only the launch shape differs. */
 int hisparse_set_copy_mode(hisparse_t h, int32_t mode);
 
+/*
+ * hisparse_swap_in_noalloc: hisparse_swap_in in the split copy shape (a
+ * resolve grid, then a full-GPU copy grid), for callers that must not cause
+ * any device allocation -- for example a serving process whose device memory
+ * is owned up front by one pool, or a call site that runs where allocation
+ * is forbidden.  The miss plan handed from the resolve grid to the copy grid
+ * lives in a fixed array of HISPARSE_NOALLOC_SCRATCH_BYTES inside the library
+ * (one per GPU, held from the library's loading until the process exits)
+ * instead of memory from cudaMalloc; this call allocates nothing, and no plan
+ * is returned to the caller.  Arguments, results and status codes are those
+ * of hisparse_swap_in with out_plan = NULL.
+ *   - The array must hold (2 * top_k + 1) * num_requests int32 values; a
+ *     larger handle gets HISPARSE_ERR_UNSUPPORTED and nothing is launched.
+ *   - The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call outside any stream capture.
+ *   - Every call on a device shares the one array and leaves the last call's
+ *     contents in it.  Each call writes everything it later reads, so nothing
+ *     needs clearing, but calls whose work overlaps on the GPU (two streams,
+ *     two handles) race on it: order them.
+ * The pages this library follows have no counterpart to this call.
+ */
+#define HISPARSE_NOALLOC_SCRATCH_BYTES (4 << 20)
+int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_idx,
+                             const int32_t *seq_lens, int32_t *out_slot_ids, void *stream);
+
 /* Text of a return code (static storage). */
 const char *hisparse_error_string(int code);
 
