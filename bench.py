@@ -148,12 +148,11 @@ class Clocks:
 # ----------------------------------------------------------------------------
 
 class Setup:
-    def __init__(self, cfg: int, calls_needed: int, rank: int, copy_mode: str):
+    def __init__(self, cfg: int, steps: int, rank: int, copy_mode: str):
         import torch
         from hierarchical_sparse_kv_request_gb300 import hisparse as H
 
         w = W.make_config(cfg)
-        steps = -(-calls_needed // w.substeps)
         w.steps = steps
         w.seed = replica_seed(w.seed, rank)
         self.w = w
@@ -254,6 +253,24 @@ def measure_link_peak(torch, H):
             "h2d_sm_loads_gbs": round(best_sm, 1)}
 
 
+def profiled_traffic(kernel_src: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    source is unchanged since that capture (else None)."""
+    import hashlib
+    import re
+    try:
+        with open(os.path.join(ROOT, kernel_src), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        text = open(os.path.join(ROOT, "profiles", summary)).read()
+    except OSError:
+        return None
+    h = re.search(r"source sha256 \(first 16 hex\): ([0-9a-f]{16})", text)
+    t = re.search(r"traffic \(DRAM read \+ write\) per launch: (\d+) bytes", text)
+    if not h or not t or h.group(1) != digest:
+        return None
+    return int(t.group(1))
+
+
 def hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -281,7 +298,7 @@ def run_gpu(args):
         return run_config4(args, ws, rank, H)
 
     K, Wm = args.steps, args.warmup
-    st = Setup(args.config, (K + Wm) * 1, rank, args.copy_mode)
+    st = Setup(args.config, K + Wm, rank, args.copy_mode)
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -347,10 +364,14 @@ def run_gpu(args):
         res_bytes = (slow * (16 * w.top_k + 4 * w.device_buffer_size + 8) + fast * 8 * w.top_k) \
             * calls_per_step * K + 24 * misses
         kernel_ms = statistics.mean(call_ms)
+        traffic = None
+        if w.config_no == 2 and not st.split:
+            traffic = profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/resolve.cu",
+                                       "resolve_kernel_decode_40k.md")
         roof = {"bound": "host_link", "achieved": round(miss_gbs, 1),
                 "peak": link["h2d_copy_engine_gbs"], "unit": "GB/s",
                 "frac": round(miss_gbs / link["h2d_copy_engine_gbs"], 4),
-                "traffic": None, "kernel": "resolve_kernel (fused resolve + miss copy)",
+                "traffic": traffic, "kernel": "resolve_kernel (fused resolve + miss copy)",
                 "peak_source": "measured in this run: 1 GiB pinned cudaMemcpyAsync H2D"}
         roof_hbm = {"bound": "hbm", "achieved": round(res_bytes / total_s / 1e9, 1),
                     "peak": peak_hbm, "unit": "GB/s",
@@ -456,62 +477,84 @@ def run_config4(args, ws, rank, H):
     plan = torch.empty((R, k, 2), dtype=torch.int32, device="cuda")
     cnt = torch.zeros(R, dtype=torch.int32, device="cuda")
     side = torch.cuda.Stream(priority=-1)
-    # stand-in compute: 152 SMs x 256 threads, calibrated to ~2 ms per step
-    nthreads = 152 * 256
-    buf = torch.zeros(nthreads, dtype=torch.float32, device="cuda")
+    # Stand-in for the compute of the layers between the anchor and its skip
+    # layers: a memory-bound bf16 elementwise stream (decode-step layer work
+    # is HBM-bound) over a 1 GiB buffer, 2 CTAs of 256 threads per SM, with
+    # the number of passes calibrated to ~2 ms.
+    buf = torch.zeros(512 << 20, dtype=torch.bfloat16, device="cuda")
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    iters = 100000
+    one = []
     for _ in range(3):
         s.record()
-        H.synthetic_compute(buf, nthreads, iters)
+        H.synthetic_compute(buf, 1)
         e.record()
         e.synchronize()
-        ms = s.elapsed_time(e)
-        iters = max(1000, int(iters * 2.0 / ms))
+        one.append(s.elapsed_time(e))
+    passes = max(1, round(2.0 / statistics.median(one)))
     comp_ms = []
     for _ in range(5):
         s.record()
-        H.synthetic_compute(buf, nthreads, iters)
+        H.synthetic_compute(buf, passes)
         e.record()
         e.synchronize()
         comp_ms.append(s.elapsed_time(e))
     compute_ms = statistics.median(comp_ms)
-
-    def step(c, prefetch=True):
+    def step(c, prefetch=True, marks=None):
+        """Anchor swap-in, three skip-layer replays, stand-in compute.
+        marks, if given: events after the anchor, the replays, the compute."""
         gpu.swap_in(0, sched[c], seq, out, plan, cnt)
+        if marks:
+            marks[0].record()
         if prefetch:
             ev = torch.cuda.Event()
             ev.record()
             side.wait_event(ev)
-            for l in (1, 2, 3):
-                gpu.replay_plan(plan, cnt, l, num_ctas=16, stream=side)
+            gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=16, stream=side)
+            if marks:
+                marks[1].record(side)
             done = torch.cuda.Event()
             done.record(side)
-            H.synthetic_compute(buf, nthreads, iters)
+            H.synthetic_compute(buf, passes)
+            if marks:
+                marks[2].record()
             torch.cuda.current_stream().wait_event(done)
         else:
-            for l in (1, 2, 3):
-                gpu.replay_plan(plan, cnt, l, num_ctas=16)
-            H.synthetic_compute(buf, nthreads, iters)
+            gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=16)
+            if marks:
+                marks[1].record()
+            H.synthetic_compute(buf, passes)
+            if marks:
+                marks[2].record()
 
     prefetch = not args.no_prefetch
     for c in range(Wm):
         step(c, prefetch)
     torch.cuda.synchronize()
+    # the replay of the last warm-up plan onto the three skip layers, alone
+    rep_ms = []
+    for _ in range(3):
+        s.record()
+        gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=16)
+        e.record()
+        e.synchronize()
+        rep_ms.append(s.elapsed_time(e))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     clocks = Clocks(dist_env()[2])
     clocks.start()
     times, anchor_ms = [], []
     miss = torch.zeros(K, dtype=torch.int64, device="cuda")
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    phases = []
     for i in range(K):
         flush.zero_()
         torch.cuda.synchronize()
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         s.record()
-        step(Wm + i, prefetch)
+        step(Wm + i, prefetch, marks)
         e.record()
         e.synchronize()
         times.append(s.elapsed_time(e))
+        phases.append([s.elapsed_time(m) for m in marks])
         miss[i] = cnt.sum()
     clk = clocks.stop()
     # the anchor swap-in alone, for the exposed-time arithmetic
@@ -524,8 +567,9 @@ def run_config4(args, ws, rank, H):
         a1.synchronize()
         anchor_ms.append(a0.elapsed_time(a1))
     step_ms = statistics.mean(times)
-    anchor = statistics.mean(anchor_ms)
-    exposed = step_ms - compute_ms - anchor
+    anchor = statistics.median(anchor_ms)
+    # exposed copy time from medians (a single slow step should not decide it)
+    exposed = statistics.median(times) - compute_ms - anchor
     misses = int(miss.sum().item())
     replay_bytes = misses * w.row_bytes * 3
     return {
@@ -536,12 +580,19 @@ def run_config4(args, ws, rank, H):
         "config": {"workload": w.name, "requests": R, "seq_len": int(w.seq_lens0[0]),
                    "layers": "1 anchor + 3 skip", "top_k": k,
                    "device_buffer_size": w.device_buffer_size, "row_bytes": w.row_bytes,
-                   "prefetch": prefetch, "replay_ctas": 16,
+                   "prefetch": prefetch, "replay_ctas": 16, "replay_launches_per_step": 1,
                    "l2": "flushed between timed steps (512 MB write)"},
         "compute_ms": round(compute_ms, 4), "anchor_swap_in_ms": round(anchor, 4),
+        "replays_alone_ms": round(statistics.median(rep_ms), 4),
+        "phase_ends_ms_median": {"anchor": round(statistics.median(p[0] for p in phases), 4),
+                                 "replays": round(statistics.median(p[1] for p in phases), 4),
+                                 "compute": round(statistics.median(p[2] for p in phases), 4)},
         "exposed_copy_ms": round(exposed, 4),
         "replay_bytes_per_step": replay_bytes // K,
-        "gpu_launches": (1 + 3 + 1) * K, "clocks": clk,
+        "gpu_launches": (1 + 1 + 1) * K, "clocks": clk,
+        "compute_stand_in": f"bf16 elementwise stream, 1 GiB x {passes} passes, 2 x 256-thread CTAs per SM",
+        "step_ms_min_median_max": [round(min(times), 4), round(statistics.median(times), 4),
+                                   round(max(times), 4)],
     }
 
 

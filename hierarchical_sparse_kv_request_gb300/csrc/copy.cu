@@ -12,12 +12,15 @@ namespace {
 constexpr int REPLAY_NT = 512;
 constexpr int REPLAY_UNROLL = 8;
 
-// Copy every (token -> slot) pair of a plan, host row -> device slot, for one
-// layer.  Work items are 16-byte chunks of the rows, numbered over the
-// concatenation of all requests' plan rows; each CTA first builds the prefix
-// sum of plan counts in shared memory (clamped to [0, k]), then walks its
-// items with COPY_UNROLL host loads in flight per thread.  Pairs whose token
-// or slot is out of range are skipped.
+// Copy every (token -> slot) pair of a plan, host row -> device slot, for
+// each of a list of layers.  Work items are 16-byte chunks of the rows,
+// numbered layer by layer over the concatenation of all requests' plan rows;
+// each CTA first builds the prefix sum of plan counts in shared memory
+// (clamped to [0, k]), then walks its items with REPLAY_UNROLL host loads in
+// flight per thread.  One launch covers all the skip layers of an anchor, so
+// its few CTAs are placed once, ahead of the compute they overlap, and stay
+// until every layer is copied.  Pairs whose token or slot is out of range are
+// skipped.
 __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
 {
     extern __shared__ __align__(16) uint32_t rows_before[];  // [R + 1]
@@ -45,7 +48,8 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
 
     const int CH = a.g.chunks;
     const int64_t B = a.g.B;
-    const uint64_t total = (uint64_t)total_rows * CH;
+    const uint64_t per_layer = (uint64_t)total_rows * CH;
+    const uint64_t total = per_layer * (uint64_t)a.num_layers;
     const uint64_t stride = (uint64_t)gridDim.x * REPLAY_NT;
     for (uint64_t e = (uint64_t)blockIdx.x * REPLAY_NT + tid; e < total;
          e += stride * REPLAY_UNROLL) {
@@ -57,8 +61,10 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
             dst[u] = nullptr;
             const uint64_t ee = e + u * stride;
             if (ee >= total) continue;
-            const uint32_t row = (uint32_t)(ee / CH);
-            const int c = (int)(ee - (uint64_t)row * CH);
+            const int layer = (int)(ee / per_layer);
+            const uint64_t el = ee - (uint64_t)layer * per_layer;
+            const uint32_t row = (uint32_t)(el / CH);
+            const int c = (int)(el - (uint64_t)row * CH);
             int lo = 0, hi = R;  // last r with rows_before[r] <= row
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
@@ -69,8 +75,8 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
             const int32_t *pr = a.plan_rows + ((int64_t)r * k + i) * 2;
             const int32_t tok = pr[0], slot = pr[1];
             if (tok < 0 || (int64_t)tok >= a.g.host_cap[r] || slot < 0 || slot >= D) continue;
-            src[u] = a.store.host + (a.g.host_off[r] + tok) * B + c * 16;
-            dst[u] = a.store.dev + ((int64_t)r * D + slot) * B + c * 16;
+            src[u] = a.store[layer].host + (a.g.host_off[r] + tok) * B + c * 16;
+            dst[u] = a.store[layer].dev + ((int64_t)r * D + slot) * B + c * 16;
         }
         uint4 v[REPLAY_UNROLL];
 #pragma unroll

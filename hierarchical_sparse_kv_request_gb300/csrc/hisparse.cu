@@ -322,26 +322,38 @@ int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx, const
     hs::ReplayLaunch c;
     c.plan_rows = a.plan_rows;
     c.plan_counts = a.plan_counts;
-    c.store = a.store;
+    c.store[0] = a.store;
+    c.num_layers = 1;
     c.g = a.g;
     c.num_ctas = h->num_sms;
     c.programmatic = true;
     return cuda_status(hs::launch_replay(c, as_stream(stream)));
 }
 
-int hisparse_replay_plan(hisparse_t h, const hisparse_plan *plan, int32_t layer, int32_t num_ctas,
-                         void *stream)
+int hisparse_replay_plan_layers(hisparse_t h, const hisparse_plan *plan, const int32_t *layers,
+                                int32_t num_layers, int32_t num_ctas, void *stream)
 {
-    if (!h || !plan || !plan->rows || !plan->counts || num_ctas < 0) return HISPARSE_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
+    if (!h || !plan || !plan->rows || !plan->counts || !layers || num_ctas < 0)
+        return HISPARSE_ERR_INVALID_ARG;
+    if (num_layers < 1 || num_layers > hs::kMaxReplayLayers) return HISPARSE_ERR_INVALID_ARG;
     hs::ReplayLaunch c;
+    for (int i = 0; i < num_layers; ++i) {
+        if (layers[i] < 0 || layers[i] >= h->L) return HISPARSE_ERR_LAYER;
+        c.store[i] = layer_store(h, layers[i]);
+    }
+    c.num_layers = num_layers;
     c.plan_rows = plan->rows;
     c.plan_counts = plan->counts;
-    c.store = layer_store(h, layer);
     c.g = geometry(h);
     c.num_ctas = num_ctas ? num_ctas : 16;
     c.programmatic = false;
     return cuda_status(hs::launch_replay(c, as_stream(stream)));
+}
+
+int hisparse_replay_plan(hisparse_t h, const hisparse_plan *plan, int32_t layer, int32_t num_ctas,
+                         void *stream)
+{
+    return hisparse_replay_plan_layers(h, plan, &layer, 1, num_ctas, stream);
 }
 
 int hisparse_backup(hisparse_t h, int32_t layer, const void *rows, const int32_t *positions,
@@ -471,7 +483,8 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     hs::ReplayLaunch c;
     c.plan_rows = a.plan_rows;
     c.plan_counts = a.plan_counts;
-    c.store = a.store;
+    c.store[0] = a.store;
+    c.num_layers = 1;
     c.g = a.g;
     c.num_ctas = h->num_sms;
     c.programmatic = true;
@@ -480,10 +493,18 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
 
 // ---- measurement kernels ---------------------------------------------------
 
-int hisparse_synthetic_compute(float *buf, int64_t n, int32_t num_threads, int32_t iters, void *stream)
+int hisparse_synthetic_compute(void *buf, int64_t bytes, int32_t passes, int32_t ctas_per_sm,
+                               void *stream)
 {
-    if (!buf || num_threads < 1 || iters < 0 || n < num_threads) return HISPARSE_ERR_INVALID_ARG;
-    return cuda_status(hs::launch_synthetic_compute(buf, num_threads, iters, as_stream(stream)));
+    if (!buf || bytes <= 0 || bytes % 16 != 0 || passes < 0 || ctas_per_sm < 1)
+        return HISPARSE_ERR_INVALID_ARG;
+    if (!aligned16(buf)) return HISPARSE_ERR_ALIGNMENT;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return HISPARSE_ERR_CUDA;
+    return cuda_status(hs::launch_synthetic_compute(buf, bytes, passes, sms * ctas_per_sm,
+                                                    as_stream(stream)));
 }
 
 int hisparse_link_probe(const void *src, void *dst, int64_t bytes, int32_t num_ctas, void *stream)

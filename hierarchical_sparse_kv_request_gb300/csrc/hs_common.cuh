@@ -135,10 +135,13 @@ int resolve_threads();
 cudaError_t resolve_prepare(size_t smem);
 cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s);
 
+constexpr int kMaxReplayLayers = 16;  // layers one replay launch copies for
+
 struct ReplayLaunch {
     const int32_t *plan_rows;
     const int32_t *plan_counts;
-    LayerStore store;
+    LayerStore store[kMaxReplayLayers];  // the layers to copy into, in order
+    int num_layers;
     Geometry g;
     int num_ctas;
     bool programmatic;  // launched right after a resolve (programmatic dependency)
@@ -167,7 +170,7 @@ struct LayerDescDev {
 cudaError_t launch_prefill(const int32_t *seq_lens, const LayerDescDev *layers, int num_layers,
                            const Geometry &g, int32_t *status, cudaStream_t s);
 
-cudaError_t launch_synthetic_compute(float *buf, int32_t num_threads, int32_t iters,
+cudaError_t launch_synthetic_compute(void *buf, int64_t bytes, int32_t passes, int32_t ctas,
                                      cudaStream_t s);
 cudaError_t launch_link_probe(const void *src, void *dst, int64_t bytes, int num_ctas,
                               cudaStream_t s);

@@ -3,30 +3,48 @@
 //
 // [Guide] "HiSparse: Hierarchical Sparse Attention", Shared-index prefetch:
 // the skip layers' copies overlap the compute of the layers in between; the
-// stand-in compute kernel plays that compute.  [Arch] "HiSparse local KV
+// stand-in compute kernel plays that compute (a memory-bound bf16 stream,
+// as decode-step layer work is).  [Arch] "HiSparse local KV
 // offload architecture", Performance invariants: misses copy directly from
 // pinned host memory; the probe measures what SM loads over the host link
 // can move.
+#include <cuda_bf16.h>
+
 #include "hs_common.cuh"
 
 namespace hs {
 namespace {
 
-__global__ void __launch_bounds__(256) synthetic_compute_kernel(float *buf, int32_t n,
-                                                                int32_t iters)
+// y <- 0.999 y + 0.001 over a bf16 buffer, `passes` times: an HBM-bound
+// elementwise stream like the memory-bound layer work of a decode step.  Each
+// thread moves 16-byte vectors with 4 in flight; fp32 math, bf16 in and out
+// (round to nearest even through the cuda_bf16 conversions).
+__global__ void __launch_bounds__(256) synthetic_compute_kernel(uint4 *buf, int64_t vecs,
+                                                                int32_t passes)
 {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    float x = buf[i], y = 1.0f + 1e-7f * (float)(i & 1023);
-    // four independent chains keep the FMA pipe busy without memory traffic
-    float a0 = x, a1 = x + 1.f, a2 = x + 2.f, a3 = x + 3.f;
-    for (int it = 0; it < iters; ++it) {
-        a0 = fmaf(a0, y, 1e-6f);
-        a1 = fmaf(a1, y, -1e-6f);
-        a2 = fmaf(a2, y, 2e-6f);
-        a3 = fmaf(a3, y, -2e-6f);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int p = 0; p < passes; ++p) {
+        for (int64_t v0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v0 < vecs;
+             v0 += stride * 4) {
+            uint4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v0 + u * stride < vecs) x[u] = buf[v0 + u * stride];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (v0 + u * stride >= vecs) continue;
+                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&x[u]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float2 f = __bfloat1622float2(h[q]);
+                    f.x = fmaf(f.x, 0.999f, 0.001f);
+                    f.y = fmaf(f.y, 0.999f, 0.001f);
+                    h[q] = __float22bfloat162_rn(f);
+                }
+                buf[v0 + u * stride] = x[u];
+            }
+        }
     }
-    buf[i] = a0 + a1 + a2 + a3;
 }
 
 constexpr int PROBE_NT = 1024;
@@ -54,11 +72,10 @@ __global__ void __launch_bounds__(PROBE_NT) link_probe_kernel(const uint8_t *src
 
 }  // namespace
 
-cudaError_t launch_synthetic_compute(float *buf, int32_t num_threads, int32_t iters,
+cudaError_t launch_synthetic_compute(void *buf, int64_t bytes, int32_t passes, int32_t ctas,
                                      cudaStream_t s)
 {
-    const int blocks = (num_threads + 255) / 256;
-    synthetic_compute_kernel<<<blocks, 256, 0, s>>>(buf, num_threads, iters);
+    synthetic_compute_kernel<<<ctas, 256, 0, s>>>(static_cast<uint4 *>(buf), bytes / 16, passes);
     return cudaGetLastError();
 }
 

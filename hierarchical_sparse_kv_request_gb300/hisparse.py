@@ -67,6 +67,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_swap_in": [P, I32, P, P, P, P, P],
         "hisparse_swap_in_noalloc": [P, I32, P, P, P, P],
         "hisparse_replay_plan": [P, P, I32, I32, P],
+        "hisparse_replay_plan_layers": [P, P, P, I32, I32, P],
         "hisparse_backup": [P, I32, P, P, P],
         "hisparse_status": [P, P],
         "hisparse_read_state": [P, I32, P, P, P, P, P, P],
@@ -228,6 +229,14 @@ class HiSparse:
         _check(self.lib.hisparse_replay_plan(self.h, ctypes.byref(plan), layer, num_ctas,
                                              _stream(stream)), "hisparse_replay_plan")
 
+    def replay_plan_layers(self, plan_rows, plan_counts, layers, num_ctas: int = 0,
+                           stream=None) -> None:
+        plan = Plan(_addr(plan_rows), _addr(plan_counts))
+        lay = np.ascontiguousarray(layers, dtype=np.int32)
+        _check(self.lib.hisparse_replay_plan_layers(self.h, ctypes.byref(plan), lay.ctypes.data,
+                                                    len(lay), num_ctas, _stream(stream)),
+               "hisparse_replay_plan_layers")
+
     def backup(self, layer: int, rows, positions, stream=None) -> None:
         _check(self.lib.hisparse_backup(self.h, layer, _addr(rows), _addr(positions),
                                         _stream(stream)), "hisparse_backup")
@@ -250,10 +259,12 @@ class HiSparse:
 
 # -- measurement kernels (include/hisparse_measure.h) -----------------------
 
-def synthetic_compute(buf, num_threads: int, iters: int, stream=None) -> None:
+def synthetic_compute(buf, passes: int, ctas_per_sm: int = 2, stream=None) -> None:
+    """The memory-bound bf16 stand-in compute over torch tensor `buf`."""
     lib = load_library()
-    _check(lib.hisparse_synthetic_compute(_addr(buf), buf.numel(), num_threads, iters,
-                                          _stream(stream)), "hisparse_synthetic_compute")
+    _check(lib.hisparse_synthetic_compute(_addr(buf), buf.numel() * buf.element_size(), passes,
+                                          ctas_per_sm, _stream(stream)),
+           "hisparse_synthetic_compute")
 
 
 def link_probe(src, dst, nbytes: int, num_ctas: int = 0, stream=None) -> None:

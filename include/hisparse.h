@@ -211,10 +211,22 @@ int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx,
  * small fixed grid to keep their SM footprint low).  For every request r and
  * i < counts[r]: layer `layer`'s device slot rows[r][i][1] <- its host row
  * rows[r][i][0].  No map or LRU changes.  `num_ctas` sets the grid (0 = 16).
- * The caller orders it after the recording swap-in (an event on `stream`).
+ * Pairs whose token or slot is out of range are skipped.  The caller orders
+ * it after the recording swap-in (an event on `stream`).
  */
 int hisparse_replay_plan(hisparse_t h, const hisparse_plan *plan, int32_t layer,
                          int32_t num_ctas, void *stream);
+
+/*
+ * hisparse_replay_plan_layers: hisparse_replay_plan for several layers in
+ * one launch: layers (host int32 [num_layers], 1 <= num_layers <= 16) are
+ * copied in order by the same `num_ctas` CTAs.  Pre-issued ahead of the
+ * compute it overlaps, the grid is placed once and keeps its SMs until every
+ * layer is done; separate launches per layer each have to find free SMs
+ * again while the compute occupies them.
+ */
+int hisparse_replay_plan_layers(hisparse_t h, const hisparse_plan *plan, const int32_t *layers,
+                                int32_t num_layers, int32_t num_ctas, void *stream);
 
 /*
  * hisparse_backup: eager backup of each request's newest KV row to host

@@ -24,15 +24,17 @@ extern "C" {
 /*
  * hisparse_synthetic_compute: a stand-in for the compute of the layers
  * between an anchor and its skip layers ([Guide] Shared-index prefetch).
- * Each of `num_threads` threads (rounded up to whole 256-thread CTAs) runs
- * `iters` dependent fp32 fused multiply-adds on one element of `buf` (device
- * float [n], n >= num_threads) and writes it back; no tensor cores, no
- * memory traffic to speak of.  The grid is ceil(num_threads / 256) CTAs of
- * 256 threads, so a caller can leave room on every SM for other kernels.
- * Errors: INVALID_ARG.
+ * Decode-step layer work is memory-bound, so the stand-in is a bf16
+ * elementwise stream: `passes` times over `buf` (device, `bytes` bytes of
+ * bf16, a multiple of 16, 16-byte aligned) it sets y <- 0.999 y + 0.001
+ * (fp32 math, bf16 storage), moving 2 * bytes through HBM per pass.  No
+ * tensor cores, no host-link traffic.  Grid: ctas_per_sm CTAs of 256
+ * threads per SM, each looping over the buffer, so a caller can leave
+ * thread slots and issue bandwidth for other kernels on every SM.
+ * Errors: INVALID_ARG, ALIGNMENT, CUDA.
  */
-int hisparse_synthetic_compute(float *buf, int64_t n, int32_t num_threads,
-                               int32_t iters, void *stream);
+int hisparse_synthetic_compute(void *buf, int64_t bytes, int32_t passes, int32_t ctas_per_sm,
+                               void *stream);
 
 /*
  * hisparse_link_probe: measure what SM loads and stores over the host link

@@ -240,8 +240,11 @@ def test_replay_on_skip_layers_side_stream():
         ev = torch.cuda.Event()
         ev.record()
         side.wait_event(ev)
-        for l, ctas in ((1, 1), (2, 16), (3, 152)):
-            p.gpu.replay_plan(p.plan, p.cnt, l, num_ctas=ctas, stream=side)
+        if c % 2 == 0:
+            for l, ctas in ((1, 1), (2, 16), (3, 152)):
+                p.gpu.replay_plan(p.plan, p.cnt, l, num_ctas=ctas, stream=side)
+        else:
+            p.gpu.replay_plan_layers(p.plan, p.cnt, [3, 1, 2], num_ctas=3 + c, stream=side)
         done = torch.cuda.Event()
         done.record(side)
         torch.cuda.current_stream().wait_event(done)

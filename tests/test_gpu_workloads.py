@@ -71,26 +71,24 @@ def test_mixed_lengths_four_layers_with_backups():
 
 
 def test_shared_index_replay_beside_compute():
-    """1 anchor + 3 skip layers, 64 x 65536 tokens: each skip layer replays
-    the anchor's plan with 16 CTAs on a side stream while the stand-in
-    compute kernel runs on the main stream."""
+    """1 anchor + 3 skip layers, 64 x 65536 tokens: the skip layers replay
+    the anchor's plan in one 16-CTA launch on a side stream while the
+    stand-in compute kernel (many short CTAs) runs on the main stream."""
     w = W.make_config(4)
     sched = W.topk_schedule(w)[0]
     p = Pair(w, track_bytes=False)
     side = torch.cuda.Stream(priority=-1)
-    nthreads = 152 * 256
-    buf = torch.zeros(nthreads, dtype=torch.float32, device="cuda")
+    buf = torch.zeros(64 << 20, dtype=torch.bfloat16, device="cuda")
     for c in range(w.steps):
         t = torch.from_numpy(sched[c]).cuda()
         p.gpu.swap_in(0, t, p.seq_d, p.out, p.plan, p.cnt)
         ev = torch.cuda.Event()
         ev.record()
         side.wait_event(ev)
-        for l in (1, 2, 3):
-            p.gpu.replay_plan(p.plan, p.cnt, l, num_ctas=16, stream=side)
+        p.gpu.replay_plan_layers(p.plan, p.cnt, [1, 2, 3], num_ctas=16, stream=side)
         done = torch.cuda.Event()
         done.record(side)
-        H.synthetic_compute(buf, nthreads, 20000)
+        H.synthetic_compute(buf, 4)
         torch.cuda.current_stream().wait_event(done)
         o = p.orc.swap_in(0, sched[c], p.seq)
         torch.cuda.synchronize()
