@@ -91,6 +91,52 @@ def test_split_copy_with_the_librarys_own_plan():
     p.close()
 
 
+def test_swap_in_replayed_from_a_cuda_graph():
+    """A swap-in (plus a skip-layer replay and a backup) captured once in a
+    CUDA graph and replayed with new inputs written into the captured
+    buffers gives, call after call, what the oracle gives: the tick lives on
+    the device, so every replay advances the LRU ([Arch] Performance
+    invariants: top-k resolution stays graph-capturable)."""
+    w = W.make_config(1, steps=8)
+    w.num_layers, w.anchor_of_layer = 2, [-1, 0]
+    w.capacity = w.seq_lens0.astype(np.int64) + w.steps
+    sched = W.topk_schedule(w)[0]
+    p = Pair(w, track_bytes=True)
+    R, k, B = w.num_requests, w.top_k, w.row_bytes
+    topk_d = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    rows_d = torch.empty((R, B), dtype=torch.uint8, device="cuda")
+    pos_d = torch.empty(R, dtype=torch.int32, device="cuda")
+    one_d = torch.ones(R, dtype=torch.int32, device="cuda")
+    topk_d.copy_(torch.from_numpy(sched[0]))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        p.gpu.swap_in(0, topk_d, p.seq_d, p.out, p.plan, p.cnt)
+        p.gpu.replay_plan(p.plan, p.cnt, 1, num_ctas=4)
+        p.gpu.backup(0, rows_d, pos_d)
+        p.gpu.backup(1, rows_d, pos_d)
+        p.seq_d.add_(one_d)
+    for c in range(w.steps):
+        topk_d.copy_(torch.from_numpy(sched[c]))
+        pos = p.seq.copy()
+        rows = np.stack([W.kv_rows(w, 0, r, [int(pos[r])])[0] for r in range(R)])
+        rows_d.copy_(torch.from_numpy(rows))
+        pos_d.copy_(torch.from_numpy(pos))
+        graph.replay()
+        o = p.orc.swap_in(0, sched[c], p.seq)
+        p.orc.replay(o[1], o[2], 1)
+        p.orc.backup(0, rows, pos)
+        p.orc.backup(1, rows, pos)      # the skip layer backs up the same rows here
+        p.seq += 1
+        torch.cuda.synchronize()
+        g = (p.out.cpu().numpy(), p.plan.cpu().numpy(), p.cnt.cpu().numpy(),
+             p.gpu.status().cpu().numpy())
+        assert_call_equal(g, o, f"graph replay {c}")
+        assert_state_equal(p, 0, f"graph replay {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"graph replay {c}")
+        assert_device_bytes_equal_oracle(p, 1, f"graph replay {c}")
+    p.close()
+
+
 # ----------------------------------------------------------------------------
 # edge cases
 # ----------------------------------------------------------------------------
