@@ -38,7 +38,7 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--steps", type=int, default=128)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
@@ -305,14 +305,15 @@ def run_gpu(args):
     clocks = Clocks(local)
     if not args.profile:
         clocks.start()
-    for s in range(Wm):
+    for s in range(Wm - 1):
         st.step(s)
     torch.cuda.synchronize()
 
-    # The K timed steps (each preceded by an untimed L2 flush) are captured
-    # in one CUDA graph and replayed once, so host launch gaps cannot leak
-    # into the per-step event times.  Event pairs bracket every swap-in call
-    # (the dominant kernel) and every whole step.
+    # The last warm-up step and the K timed steps (each preceded by an
+    # untimed L2 flush) are captured in one CUDA graph and replayed once, so
+    # host launch gaps cannot leak into the per-step event times and the
+    # graph's first-replay cost falls on the warm-up step.  Event pairs
+    # bracket every swap-in call (the dominant kernel) and every whole step.
     ev = [(torch.cuda.Event(enable_timing=True, external=True),
            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(K)]
     ncalls = len(st.calls_of_step(0))
@@ -322,6 +323,9 @@ def run_gpu(args):
     miss = torch.zeros(K, dtype=torch.int64, device="cuda")
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
+        if Wm >= 1:
+            flush.zero_()
+            st.step(Wm - 1)
         for i in range(K):
             flush.zero_()
             ev[i][0].record()

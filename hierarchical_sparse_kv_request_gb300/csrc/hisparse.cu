@@ -65,6 +65,13 @@ hs::LayerStore layer_store(const hisparse_handle *h, int layer)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launching calls must run with the handle's device current.
+bool on_own_device(const hisparse_handle *h)
+{
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev == h->device;
+}
+
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HISPARSE_OK : HISPARSE_ERR_CUDA; }
@@ -293,6 +300,7 @@ int hisparse_device_buffer(hisparse_t h, int32_t layer, void **dev_ptr)
 int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream)
 {
     if (!h || !seq_lens) return HISPARSE_ERR_INVALID_ARG;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
     return cuda_status(hs::launch_prefill(seq_lens, h->d_layers, h->L, geometry(h), h->d_status,
                                           as_stream(stream)));
 }
@@ -303,6 +311,7 @@ int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx, const
     if (!h || !topk_idx || !seq_lens || !out_slot_ids) return HISPARSE_ERR_INVALID_ARG;
     if (out_plan && (!out_plan->rows || !out_plan->counts)) return HISPARSE_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->L || h->anchor[layer] >= 0) return HISPARSE_ERR_LAYER;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
     hs::ResolveLaunch a;
     a.topk = topk_idx;
     a.seq_lens = seq_lens;
@@ -336,6 +345,7 @@ int hisparse_replay_plan_layers(hisparse_t h, const hisparse_plan *plan, const i
     if (!h || !plan || !plan->rows || !plan->counts || !layers || num_ctas < 0)
         return HISPARSE_ERR_INVALID_ARG;
     if (num_layers < 1 || num_layers > hs::kMaxReplayLayers) return HISPARSE_ERR_INVALID_ARG;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
     hs::ReplayLaunch c;
     for (int i = 0; i < num_layers; ++i) {
         if (layers[i] < 0 || layers[i] >= h->L) return HISPARSE_ERR_LAYER;
@@ -362,6 +372,7 @@ int hisparse_backup(hisparse_t h, int32_t layer, const void *rows, const int32_t
     if (!h || !rows || !positions) return HISPARSE_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
     if (!aligned16(rows)) return HISPARSE_ERR_ALIGNMENT;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
     hs::BackupLaunch b;
     b.rows = static_cast<const uint8_t *>(rows);
     b.positions = positions;
@@ -456,6 +467,7 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
 {
     if (!h || !topk_idx || !seq_lens || !out_slot_ids) return HISPARSE_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->L || h->anchor[layer] >= 0) return HISPARSE_ERR_LAYER;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
     // the pairs of all requests plus one count per request must fit the array
     const int64_t need = ((int64_t)h->R * h->k * 2 + h->R) * 4;
     if (need > HISPARSE_NOALLOC_SCRATCH_BYTES) return HISPARSE_ERR_UNSUPPORTED;

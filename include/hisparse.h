@@ -33,6 +33,9 @@
  *     hisparse_status); the affected request's state is left untouched.
  *   - A handle is not thread-safe; calls on one handle must be ordered by
  *     the caller (one stream, or events between streams).
+ *   - A handle belongs to the device current at hisparse_create; calls that
+ *     launch work return HISPARSE_ERR_INVALID_ARG unless that device is
+ *     current.
  */
 #ifndef HISPARSE_H
 #define HISPARSE_H
