@@ -18,7 +18,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "hisparse_oracle.c")
 _LIB = os.path.join(_HERE, "libhisparse_oracle.so")
 
-OK, BAD_INDEX, DUPLICATE, BAD_SEQ_LEN, BAD_POSITION = 0, 1, 2, 3, 4
+OK, BAD_INDEX, DUPLICATE, BAD_SEQ_LEN, BAD_POSITION, BAD_RESIDENT = 0, 1, 2, 3, 4, 5
+RESIDENT_FLAG = 1 << 30
 
 
 def build(force: bool = False, extra_flags: Sequence[str] = ()) -> str:
@@ -54,6 +55,7 @@ def _load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.hso_dev_row.argtypes = [P, I, I, I64]
     lib.hso_prefill.argtypes = [P, P]
     lib.hso_swap_in.argtypes = [P, I, P, P, P, P, P, P]
+    lib.hso_swap_in_resident.argtypes = [P, I, P, P, P, I, I, P, P, P, P]
     lib.hso_replay.argtypes = [P, P, P, I]
     lib.hso_backup.argtypes = [P, I, P, P, P]
     lib.hso_state.argtypes = [P, I, P, P, P, P]
@@ -131,16 +133,23 @@ class Oracle:
         if self.lib.hso_prefill(self.h, _ptr(s)) != 0:
             raise ValueError("bad seq_lens for prefill")
 
-    def swap_in(self, layer: int, topk, seq_lens):
-        """Returns (out [R][k], plan [R][k][2], count [R], status [R])."""
+    def swap_in(self, layer: int, topk, seq_lens, resident_blocks=None, block_size: int = 0):
+        """Returns (out [R][k], plan [R][k][2], count [R], status [R]).
+        resident_blocks: optional int32 [R][max_blocks] resident block table."""
         t = np.ascontiguousarray(topk, dtype=np.int32).reshape(self.R, self.k)
         s = np.ascontiguousarray(seq_lens, dtype=np.int32)
         out = np.full((self.R, self.k), -7, dtype=np.int32)
         plan = np.full((self.R, self.k, 2), -7, dtype=np.int32)
         cnt = np.zeros(self.R, dtype=np.int32)
         st = np.zeros(self.R, dtype=np.int32)
-        rc = self.lib.hso_swap_in(self.h, layer, _ptr(t), _ptr(s), _ptr(out),
-                                  _ptr(plan), _ptr(cnt), _ptr(st))
+        if resident_blocks is None:
+            rc = self.lib.hso_swap_in(self.h, layer, _ptr(t), _ptr(s), _ptr(out),
+                                      _ptr(plan), _ptr(cnt), _ptr(st))
+        else:
+            rb = np.ascontiguousarray(resident_blocks, dtype=np.int32).reshape(self.R, -1)
+            rc = self.lib.hso_swap_in_resident(self.h, layer, _ptr(t), _ptr(s), _ptr(rb),
+                                               rb.shape[1], block_size, _ptr(out), _ptr(plan),
+                                               _ptr(cnt), _ptr(st))
         if rc != 0:
             raise ValueError("layer holds no hot state")
         return out, plan, cnt, st

@@ -25,7 +25,11 @@
  *     (hit or refilled) gets last_used = tick;
  *   - top-k entries are -1 (padding, resolves to -1) or distinct positions in
  *     [0, seq_len); anything else sets a per-request status, leaves that
- *     request's state untouched and writes -1 to all its outputs.
+ *     request's state untouched and writes -1 to all its outputs;
+ *   - resident pages come first ([Arch] Resident device pages; Hot lookup and
+ *     LRU): with a resident block table, a position whose block is resident
+ *     resolves to RESIDENT_FLAG | (block * block_size + position % block_size)
+ *     and touches no hot state -- no stamp, no map, no plan entry, no miss.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -36,6 +40,10 @@
 #define HSO_DUPLICATE 2     /* a position selected twice            */
 #define HSO_BAD_SEQ_LEN 3   /* seq_len outside [0, host capacity]   */
 #define HSO_BAD_POSITION 4  /* backup position outside [0, capacity) */
+#define HSO_BAD_RESIDENT 5  /* a resident block id outside [-1, 2^30 / block_size) */
+
+/* A resident hit resolves to this flag OR'd with its row in the resident pool. */
+#define HSO_RESIDENT_FLAG 0x40000000
 
 typedef struct hs_oracle {
     int R, L, k, D;
@@ -211,26 +219,74 @@ static int32_t validate(const int32_t *topk, int k, int32_t S)
     return st;
 }
 
+/* Resident block table of one request ([Arch] Resident device pages: the
+ * attention-facing handle's block table).  NULL blocks = no resident tier. */
+typedef struct {
+    const int32_t *blocks;  /* [max_blocks]: resident block id or -1 */
+    int32_t max_blocks;
+    int32_t block_size;
+} resident_table;
+
+/* Row of token t in the resident pool, or -1 when its block is not resident
+ * (a block past the end of the table is not resident). */
+static int64_t resident_row(const resident_table *rt, int32_t t)
+{
+    if (!rt->blocks) return -1;
+    int32_t b = t / rt->block_size;
+    if (b >= rt->max_blocks || rt->blocks[b] < 0) return -1;
+    return (int64_t)rt->blocks[b] * rt->block_size + t % rt->block_size;
+}
+
+/* Every looked-up block id must be -1 or name rows below the flag bit. */
+static int32_t validate_resident(const resident_table *rt, const int32_t *topk, int k)
+{
+    if (!rt->blocks) return HSO_OK;
+    for (int j = 0; j < k; ++j) {
+        if (topk[j] < 0) continue;
+        int32_t b = topk[j] / rt->block_size;
+        if (b >= rt->max_blocks) continue;
+        int32_t id = rt->blocks[b];
+        if (id < -1 || (int64_t)id * rt->block_size + rt->block_size > HSO_RESIDENT_FLAG)
+            return HSO_BAD_RESIDENT;
+    }
+    return HSO_OK;
+}
+
 /*
  * One request of one swap-in call on hot-state layer `a`
  * ([Guide] Decode Workflow, swap-in step; [Arch] Hot lookup and LRU).
  */
 static void swap_in_request(hs_oracle *o, int a, int r, const int32_t *topk,
-                            int32_t S, uint32_t tick, int32_t *out,
-                            int32_t *plan, int32_t *count, int32_t *status)
+                            int32_t S, uint32_t tick, const resident_table *rt,
+                            int32_t *out, int32_t *plan, int32_t *count, int32_t *status)
 {
     const int k = o->k, D = o->D;
     *count = 0;
     if (S < 0 || S > o->cap[r]) *status = HSO_BAD_SEQ_LEN;
     else *status = validate(topk, k, S);
+    if (*status == HSO_OK) *status = validate_resident(rt, topk, k);
     if (*status != HSO_OK) {
         for (int j = 0; j < k; ++j) out[j] = -1;
         return;
     }
 
+    /* Resident pages first: a resident position resolves to its resident row
+     * and is done. */
+    char *done = (char *)calloc((size_t)k, 1);
+    for (int j = 0; j < k; ++j) {
+        if (topk[j] < 0) continue;
+        int64_t row = resident_row(rt, topk[j]);
+        if (row >= 0) {
+            out[j] = (int32_t)(HSO_RESIDENT_FLAG | row);
+            done[j] = 1;
+        }
+    }
+
     /* Short sequence: every KV row is already in the buffer, slot = token. */
     if (S <= D) {
-        for (int j = 0; j < k; ++j) out[j] = topk[j];
+        for (int j = 0; j < k; ++j)
+            if (!done[j]) out[j] = topk[j];
+        free(done);
         return;
     }
 
@@ -244,7 +300,7 @@ static void swap_in_request(hs_oracle *o, int a, int r, const int32_t *topk,
     int m = 0;
     for (int j = 0; j < k; ++j) {
         int32_t t = topk[j];
-        if (t < 0) continue;
+        if (t < 0 || done[j]) continue;
         if (t2s[t] >= 0) is_hit_slot[t2s[t]] = 1;
         else miss[m++] = t;
     }
@@ -274,11 +330,12 @@ static void swap_in_request(hs_oracle *o, int a, int r, const int32_t *topk,
     /* Outputs in input order; every selected slot is stamped with the tick. */
     for (int j = 0; j < k; ++j) {
         int32_t t = topk[j];
+        if (done[j]) continue;
         if (t < 0) { out[j] = -1; continue; }
         out[j] = t2s[t];
         lu[t2s[t]] = tick;
     }
-    free(is_hit_slot); free(miss); free(cand);
+    free(done); free(is_hit_slot); free(miss); free(cand);
 }
 
 /*
@@ -288,16 +345,29 @@ static void swap_in_request(hs_oracle *o, int a, int r, const int32_t *topk,
  *   count  [R] int32        status [R] int32
  * Returns -1 if `layer` holds no hot state of its own.
  */
+int hso_swap_in_resident(hs_oracle *o, int layer, const int32_t *topk, const int32_t *seq_lens,
+                         const int32_t *resident_blocks, int32_t max_blocks, int32_t block_size,
+                         int32_t *out, int32_t *plan, int32_t *count, int32_t *status)
+{
+    if (layer < 0 || layer >= o->L || o->anchor[layer] >= 0) return -1;
+    if (resident_blocks && (max_blocks < 1 || block_size < 1)) return -1;
+    uint32_t tick = ++o->tick[layer];
+    for (int r = 0; r < o->R; ++r) {
+        resident_table rt;
+        rt.blocks = resident_blocks ? resident_blocks + (int64_t)r * max_blocks : NULL;
+        rt.max_blocks = max_blocks;
+        rt.block_size = block_size;
+        swap_in_request(o, layer, r, topk + (int64_t)r * o->k, seq_lens[r], tick, &rt,
+                        out + (int64_t)r * o->k, plan + (int64_t)r * o->k * 2,
+                        count + r, status + r);
+    }
+    return 0;
+}
+
 int hso_swap_in(hs_oracle *o, int layer, const int32_t *topk, const int32_t *seq_lens,
                 int32_t *out, int32_t *plan, int32_t *count, int32_t *status)
 {
-    if (layer < 0 || layer >= o->L || o->anchor[layer] >= 0) return -1;
-    uint32_t tick = ++o->tick[layer];
-    for (int r = 0; r < o->R; ++r)
-        swap_in_request(o, layer, r, topk + (int64_t)r * o->k, seq_lens[r], tick,
-                        out + (int64_t)r * o->k, plan + (int64_t)r * o->k * 2,
-                        count + r, status + r);
-    return 0;
+    return hso_swap_in_resident(o, layer, topk, seq_lens, NULL, 0, 0, out, plan, count, status);
 }
 
 /*

@@ -8,8 +8,16 @@ from typing import Dict, List, Tuple
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
+RESIDENT = 1 << 30
+
+
+def _val(x: str) -> int:
+    """An integer; 'R<n>' is the resident row n (flagged)."""
+    return RESIDENT | int(x[1:]) if x.startswith("R") else int(x)
+
+
 def _ints(s: str) -> List[int]:
-    return [int(x) for x in s.split(",")] if s and s != "-" else []
+    return [_val(x) for x in s.split(",")] if s and s != "-" else []
 
 
 def _kv(tokens: List[str]) -> Dict[str, str]:
@@ -40,6 +48,8 @@ def load(name: str) -> Tuple[Dict[str, int], List[Tuple[str, dict]]]:
                     "slot2tok": _ints(kv["slot2tok"]), "last_used": _ints(kv["last_used"])}
             elif head == "backup":
                 ops.append(("backup", {"pos": int(kv["pos"])}))
+            elif head == "resident":
+                ops.append(("resident", {"ids": _ints(kv["ids"])}))
             else:
                 raise ValueError(head)
     return layout, ops

@@ -7,12 +7,16 @@ explicit recency list, least recently used first, the textbook form of LRU
 updates the GPU LRU, a miss takes the LRU victim).  Slots used in the same
 call are equally recent; they move to the back of the list in slot order,
 which is the tie-break this library specifies.  Misses are served in
-ascending token order.  Pure Python, for tiny cases only.
+ascending token order.  Positions held in resident pages are answered from
+there first and never reach the list ([Arch] Resident device pages: a
+resident hit exits before the hot lookup).  Pure Python, tiny cases only.
 """
 
 from __future__ import annotations
 
 from typing import Dict, List, Optional, Sequence, Tuple
+
+RESIDENT = 1 << 30   # flag of a position resolved from resident pages
 
 
 class ListLRU:
@@ -27,11 +31,17 @@ class ListLRU:
             self.slot_of[seq_len - n + i] = i
         self.recency: List[int] = list(range(D))   # least recently used first
 
-    def call(self, topk: Sequence[int], seq_len: int) -> Tuple[List[int], List[Tuple[int, int]]]:
-        """Resolve one top-k row; returns (slots in input order, plan)."""
+    def call(self, topk: Sequence[int], seq_len: int, resident: Optional[Dict[int, int]] = None
+             ) -> Tuple[List[int], List[Tuple[int, int]]]:
+        """Resolve one top-k row; returns (slots in input order, plan).
+
+        `resident` maps positions held in resident pages to their resident
+        rows; those resolve to RESIDENT | row before anything else and leave
+        the hot buffer alone."""
+        resident = resident or {}
         if seq_len <= self.D:                       # short: slot = token
-            return list(topk), []
-        wanted = [t for t in topk if t >= 0]
+            return [RESIDENT | resident[t] if t in resident else t for t in topk], []
+        wanted = [t for t in topk if t >= 0 and t not in resident]
         hit_slots = {self.slot_of[t] for t in wanted if t in self.slot_of}
         misses = sorted(t for t in wanted if t not in self.slot_of)
         victims = [s for s in self.recency if s not in hit_slots][: len(misses)]
@@ -46,7 +56,8 @@ class ListLRU:
             plan.append((t, v))
         used = hit_slots | set(victims)
         self.recency = [s for s in self.recency if s not in used] + sorted(used)
-        out = [self.slot_of[t] if t >= 0 else -1 for t in topk]
+        out = [RESIDENT | resident[t] if t in resident else (self.slot_of[t] if t >= 0 else -1)
+               for t in topk]
         return out, plan
 
     def backup(self, pos: int) -> None:

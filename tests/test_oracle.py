@@ -27,8 +27,11 @@ def run_trace_on_oracle(name, lib_path=None):
     D, k, cap = layout["D"], layout["k"], layout["cap"]
     orc = O.Oracle(1, 1, 16, k, D, [-1], [cap], track_bytes=True, lib_path=lib_path)
     S = None
+    resident = None
     for op, a in ops:
-        if op == "prefill":
+        if op == "resident":
+            resident = np.array([a["ids"]], dtype=np.int32)
+        elif op == "prefill":
             S = a["S"]
             orc.host_rows(0, 0)[:] = np.arange(cap, dtype=np.uint8)[:, None]
             orc.prefill([S])
@@ -37,7 +40,8 @@ def run_trace_on_oracle(name, lib_path=None):
             st = orc.backup(0, row, [a["pos"]])
             assert st[0] == 0
         else:
-            out, plan, cnt, st = orc.swap_in(0, np.array([a["topk"]]), [a["S"]])
+            out, plan, cnt, st = orc.swap_in(0, np.array([a["topk"]]), [a["S"]],
+                                             resident, layout.get("bs", 0))
             e = a["expect"]
             s2t, lu, _, _ = orc.state(0)
             got = {"out": out[0].tolist(), "status": int(st[0]),
@@ -147,6 +151,47 @@ def test_random_vs_list_model(seed):
     for S in lens:
         progs += _random_programs(rng, 1, D, k, S, 10)
     assert compare_with_model(D, k, lens, progs) is None
+
+
+def compare_resident_with_model(D, k, S, bs, programs, tables, lib_path=None):
+    """Like compare_with_model, with a resident block table per call."""
+    R = len(programs)
+    orc = O.Oracle(R, 1, 16, k, D, [-1], [S] * R, track_bytes=False, lib_path=lib_path)
+    orc.prefill([S] * R)
+    models = [ListLRU(D, S) for _ in range(R)]
+    for c in range(len(programs[0])):
+        topk = np.array([programs[r][c] for r in range(R)], dtype=np.int32)
+        tab = np.array([tables[r][c] for r in range(R)], dtype=np.int32)
+        out, plan, cnt, st = orc.swap_in(0, topk, [S] * R, tab, bs)
+        s2t, lu, _, _ = orc.state(0)
+        for r in range(R):
+            res = {t: int(tab[r][t // bs]) * bs + t % bs for t in range(S)
+                   if t // bs < tab.shape[1] and tab[r][t // bs] >= 0}
+            mo, mp = models[r].call(programs[r][c], S, res)
+            if st[r] != 0 or out[r].tolist() != mo or \
+                    [tuple(p) for p in plan[r, :cnt[r]].tolist()] != mp or \
+                    s2t[r].tolist() != models[r].slot2tok():
+                return f"r{r} c{c}: {out[r].tolist()} vs {mo}"
+            if S > D:
+                order = sorted(range(D), key=lambda s_: (int(lu[r, s_]), s_))
+                if order != models[r].recency:
+                    return f"r{r} c{c}: LRU order"
+    return None
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_random_resident_tables_vs_list_model(seed, lib_path=None):
+    rng = np.random.default_rng(500 + seed)
+    D, k, bs = 8, 5, 3
+    S = 40 if seed < 2 else 7          # the last seed runs the fast path
+    nb = -(-S // bs) - (1 if seed == 1 else 0)   # seed 1: table shorter than S
+    R, ncalls = 60, 8
+    progs, tabs = [], []
+    for _ in range(R):
+        progs.append([rng.choice(S, k, replace=False).tolist() for _ in range(ncalls)])
+        tabs.append([np.where(rng.random(nb) < 0.3, rng.integers(0, 50, nb), -1).tolist()
+                     for _ in range(ncalls)])
+    assert compare_resident_with_model(D, k, S, bs, progs, tabs, lib_path) is None
 
 
 def test_random_biased_reuse_vs_list_model():

@@ -40,8 +40,8 @@ MUTANTS = [
      "if (!is_hit_slot[s]) { cand[nc]",
      "if (1) { cand[nc]"),
     ("fast_path_strict",
-     "if (S <= D) {\n        for (int j = 0; j < k; ++j) out[j] = topk[j];",
-     "if (S < D) {\n        for (int j = 0; j < k; ++j) out[j] = topk[j];"),
+     "if (S <= D) {\n        for (int j = 0; j < k; ++j)\n            if (!done[j]) out[j] = topk[j];",
+     "if (S < D) {\n        for (int j = 0; j < k; ++j)\n            if (!done[j]) out[j] = topk[j];"),
     ("prefill_oldest_tokens",
      "s2t[i] = S - n + i;\n                    t2s[S - n + i] = i;",
      "s2t[i] = i;\n                    t2s[i] = i;"),
@@ -66,6 +66,20 @@ MUTANTS = [
     ("replay_wrong_layer",
      "copy_row(o, layer, r, plan[((int64_t)r * o->k + i) * 2],",
      "copy_row(o, 0, r, plan[((int64_t)r * o->k + i) * 2],"),
+    ("resident_after_hot",
+     "        if (row >= 0) {\n            out[j] = (int32_t)(HSO_RESIDENT_FLAG | row);",
+     "        if (row >= 0 && (S <= D || o->tok2slot[a][o->host_off[r] + topk[j]] < 0)) {\n"
+     "            out[j] = (int32_t)(HSO_RESIDENT_FLAG | row);"),
+    ("resident_hits_stamped",
+     "        if (done[j]) continue;\n        if (t < 0) { out[j] = -1; continue; }",
+     "        if (done[j]) { if (t2s[t] >= 0) lu[t2s[t]] = tick; continue; }\n"
+     "        if (t < 0) { out[j] = -1; continue; }"),
+    ("resident_counted_as_miss",
+     "        if (t < 0 || done[j]) continue;",
+     "        if (t < 0) continue;"),
+    ("resident_row_offset_dropped",
+     "return (int64_t)rt->blocks[b] * rt->block_size + t % rt->block_size;",
+     "return (int64_t)rt->blocks[b] * rt->block_size;"),
 ]
 
 
@@ -90,6 +104,11 @@ def run_all_pins(lib_path):
             pin(lib_path)
         except Exception:
             failed.append(pin.__name__)
+    for seed in range(3):
+        try:
+            T.test_random_resident_tables_vs_list_model(seed, lib_path)
+        except Exception:
+            failed.append(f"resident_random:{seed}")
     return failed
 
 
