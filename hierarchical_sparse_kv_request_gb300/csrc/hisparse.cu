@@ -305,11 +305,17 @@ int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream)
                                           as_stream(stream)));
 }
 
-int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int32_t *seq_lens,
-                     int32_t *out_slot_ids, const hisparse_plan *out_plan, void *stream)
+}  // extern "C"
+
+namespace {
+
+int swap_in_impl(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int32_t *seq_lens,
+                 const int32_t *resident_blocks, int32_t max_blocks, int32_t block_size,
+                 int32_t *out_slot_ids, const hisparse_plan *out_plan, void *stream)
 {
     if (!h || !topk_idx || !seq_lens || !out_slot_ids) return HISPARSE_ERR_INVALID_ARG;
     if (out_plan && (!out_plan->rows || !out_plan->counts)) return HISPARSE_ERR_INVALID_ARG;
+    if (resident_blocks && (max_blocks < 1 || block_size < 1)) return HISPARSE_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->L || h->anchor[layer] >= 0) return HISPARSE_ERR_LAYER;
     if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
     hs::ResolveLaunch a;
@@ -324,6 +330,9 @@ int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx, const
     const bool split = h->copy_mode == HISPARSE_COPY_SPLIT;
     a.fused_copy = !split;
     a.stage_s2t = h->stage_s2t;
+    a.resident = resident_blocks;
+    a.res_max_blocks = resident_blocks ? max_blocks : 0;
+    a.res_block_size = resident_blocks ? block_size : 0;
     a.plan_rows = out_plan ? out_plan->rows : (split ? h->d_plan_rows : nullptr);
     a.plan_counts = out_plan ? out_plan->counts : (split ? h->d_plan_counts : nullptr);
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));
@@ -337,6 +346,26 @@ int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx, const
     c.num_ctas = h->num_sms;
     c.programmatic = true;
     return cuda_status(hs::launch_replay(c, as_stream(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int32_t *seq_lens,
+                     int32_t *out_slot_ids, const hisparse_plan *out_plan, void *stream)
+{
+    return swap_in_impl(h, layer, topk_idx, seq_lens, nullptr, 0, 0, out_slot_ids, out_plan, stream);
+}
+
+int hisparse_swap_in_resident(hisparse_t h, int32_t layer, const int32_t *topk_idx,
+                              const int32_t *seq_lens, const int32_t *resident_blocks,
+                              int32_t max_blocks, int32_t block_size, int32_t *out_slot_ids,
+                              const hisparse_plan *out_plan, void *stream)
+{
+    if (!resident_blocks) return HISPARSE_ERR_INVALID_ARG;
+    return swap_in_impl(h, layer, topk_idx, seq_lens, resident_blocks, max_blocks, block_size,
+                        out_slot_ids, out_plan, stream);
 }
 
 int hisparse_replay_plan_layers(hisparse_t h, const hisparse_plan *plan, const int32_t *layers,
@@ -488,6 +517,9 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     a.max_cap = (int32_t)h->max_cap;
     a.fused_copy = false;
     a.stage_s2t = h->stage_s2t;
+    a.resident = nullptr;
+    a.res_max_blocks = 0;
+    a.res_block_size = 0;
     a.plan_rows = scratch;
     a.plan_counts = scratch + (int64_t)h->R * h->k * 2;
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));

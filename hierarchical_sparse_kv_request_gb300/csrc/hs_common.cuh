@@ -17,6 +17,8 @@ constexpr int kStatusBadIndex = 1;
 constexpr int kStatusDuplicate = 2;
 constexpr int kStatusBadSeqLen = 3;
 constexpr int kStatusBadPosition = 4;
+constexpr int kStatusBadResident = 5;
+constexpr int32_t kResidentFlag = 1 << 30;  // marks a row of the resident pool
 
 // Hot state of one state-owning layer.  Per request r:
 //   tok2slot[host_off[r] + t]  slot holding token t, or -1   (host_cap[r] ints)
@@ -125,6 +127,9 @@ struct ResolveLaunch {
     int32_t max_cap;       // largest host capacity (sizes the miss bitmap)
     bool fused_copy;       // copy the misses in this kernel
     bool stage_s2t;        // stage the slot->token row in shared memory
+    const int32_t *resident;  // [R][res_max_blocks] resident block ids, or null
+    int32_t res_max_blocks;
+    int32_t res_block_size;
 };
 
 // Shared-memory bytes the resolve kernel needs for this geometry.

@@ -90,18 +90,35 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Final writes of a request whose call ends without touching its state.
+// Resident row of position t from its block id `id` (-1: not resident), or
+// -2 when the id is malformed (below -1, or rows reaching the flag bit).
+__device__ __forceinline__ int32_t resident_row(int32_t id, int32_t t, int32_t bs)
+{
+    if (id == -1) return -1;
+    if (id < -1 || (int64_t)id * bs + bs > kResidentFlag) return -2;
+    return id * bs + t % bs;
+}
+
+// Final writes of a request whose call ends without touching its state; on
+// success (the fast path) each position resolves to its resident row or to
+// slot = position.
 template <int KT>
 __device__ __forceinline__ void finish_untouched(const ResolveLaunch &a, int r,
-                                                 const int32_t (&t)[KT], int status,
-                                                 uint32_t tick)
+                                                 const int32_t (&t)[KT], const int32_t (&rid)[KT],
+                                                 int status, uint32_t tick)
 {
     const int k = a.g.k;
     cp_async_wait_all();  // staged rows may still be landing in shared memory
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int j = threadIdx.x + i * NT;
-        if (j < k) a.out[(int64_t)r * k + j] = status == kStatusOk ? t[i] : -1;
+        if (j >= k) continue;
+        int32_t v = -1;
+        if (status == kStatusOk) {
+            const int32_t row = t[i] >= 0 ? resident_row(rid[i], t[i], a.res_block_size) : -1;
+            v = row >= 0 ? (kResidentFlag | row) : t[i];
+        }
+        a.out[(int64_t)r * k + j] = v;
     }
     if (threadIdx.x == 0) {
         a.status[r] = status;
@@ -157,9 +174,21 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
             for (int i = tid; i < (D >> 2); i += NT) cp_async16(sm.s2t_s + i * 4, slot2tok + i * 4);
     }
     cp_async_commit();
+    // Resident pages first ([Arch] Resident device pages; Hot lookup and
+    // LRU): gather the block id of every position's block (-1 when there is
+    // no table or the block lies past its end).
+    int32_t rid[KT];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        rid[i] = -1;
+        if (a.resident && t[i] >= 0 && t[i] < S && t[i] <= cap) {
+            const int32_t b = t[i] / a.res_block_size;
+            if (b < a.res_max_blocks) rid[i] = a.resident[(int64_t)r * a.res_max_blocks + b];
+        }
+    }
 
     if (S < 0 || (int64_t)S > cap) {  // uniform across the CTA
-        finish_untouched<KT>(a, r, t, kStatusBadSeqLen, tick);
+        finish_untouched<KT>(a, r, t, rid, kStatusBadSeqLen, tick);
         return;
     }
 
@@ -168,19 +197,23 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         const int mw = (S + 31) >> 5;
         for (int w = tid; w < mw; w += NT) sm.missbits[w] = 0u;
         __syncthreads();
-        bool bad = false, dup = false;
+        bool bad = false, dup = false, badres = false;
 #pragma unroll
         for (int i = 0; i < KT; ++i) {
             const int32_t x = t[i];
             if (x == -1) continue;
             if (x < 0 || x >= S) { bad = true; continue; }
+            badres |= resident_row(rid[i], x, a.res_block_size) == -2;
             const uint32_t bit = 1u << (x & 31);
             dup |= (atomicOr(&sm.missbits[x >> 5], bit) & bit) != 0u;
         }
         bad = __syncthreads_or(bad);
         dup = __syncthreads_or(dup);
-        finish_untouched<KT>(a, r, t,
-                             bad ? kStatusBadIndex : (dup ? kStatusDuplicate : kStatusOk), tick);
+        badres = __syncthreads_or(badres);
+        finish_untouched<KT>(a, r, t, rid,
+                             bad ? kStatusBadIndex
+                                 : (dup ? kStatusDuplicate : (badres ? kStatusBadResident : kStatusOk)),
+                             tick);
         return;
     }
 
@@ -203,13 +236,18 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     cp_async_wait_all();
     __syncthreads();
 
-    bool bad = false, dup = false;
+    // Classify.  A resident position is marked in the token bitmap only to
+    // catch duplicates; its bit is cleared again before the misses are
+    // ranked, and it never touches the hot state.
+    bool bad = false, dup = false, badres = false;
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int32_t x = t[i];
         if (x == -1) continue;
         if (x < 0 || x >= S) { bad = true; continue; }
-        if (s[i] >= 0) {
+        rid[i] = resident_row(rid[i], x, a.res_block_size);   // now the row
+        badres |= rid[i] == -2;
+        if (rid[i] < 0 && s[i] >= 0) {
             const uint32_t bit = 1u << (s[i] & 31);
             dup |= (atomicOr(&sm.hitbits[s[i] >> 5], bit) & bit) != 0u;
         } else {
@@ -219,16 +257,30 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     }
     bad = __syncthreads_or(bad);
     dup = __syncthreads_or(dup);
-    if (bad || dup) {
-        finish_untouched<KT>(a, r, t, bad ? kStatusBadIndex : kStatusDuplicate, tick);
+    badres = __syncthreads_or(badres);
+    if (bad || dup || badres) {
+#pragma unroll
+        for (int i = 0; i < KT; ++i) rid[i] = -1;
+        finish_untouched<KT>(a, r, t, rid,
+                             bad ? kStatusBadIndex : (dup ? kStatusDuplicate : kStatusBadResident),
+                             tick);
         return;
     }
-    // hits and padding resolve now
+    if (a.resident) {
+#pragma unroll
+        for (int i = 0; i < KT; ++i)
+            if (t[i] >= 0 && rid[i] >= 0) atomicAnd(&sm.missbits[t[i] >> 5], ~(1u << (t[i] & 31)));
+        __syncthreads();
+    }
+    // resident positions, hits and padding resolve now
     int32_t *out = a.out + (int64_t)r * k;
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int j = tid + i * NT;
-        if (j < k && (t[i] < 0 || s[i] >= 0)) out[j] = t[i] < 0 ? -1 : s[i];
+        if (j >= k) continue;
+        if (t[i] < 0) out[j] = -1;
+        else if (rid[i] >= 0) out[j] = kResidentFlag | rid[i];
+        else if (s[i] >= 0) out[j] = s[i];
     }
 
     // One prefix sum gives both (a) the misses before each thread's chunk of
@@ -300,7 +352,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     for (int i = 0; i < KT; ++i) {
         const int j = tid + i * NT;
         const int32_t x = t[i];
-        if (j >= k || x < 0 || s[i] >= 0) continue;
+        if (j >= k || x < 0 || rid[i] >= 0 || s[i] >= 0) continue;
         const int w = x >> 5;
         const int owner = w / WC;
         uint32_t rank = sm.chunk_pre[owner];

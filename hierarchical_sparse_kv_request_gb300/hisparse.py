@@ -22,6 +22,8 @@ OK = 0
 ERR_INVALID_ARG, ERR_LAYOUT, ERR_CAPACITY, ERR_LAYER = -1, -2, -3, -4
 ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT = -5, -6, -7, -8
 STATUS_OK, STATUS_BAD_INDEX, STATUS_DUPLICATE, STATUS_BAD_SEQ_LEN, STATUS_BAD_POSITION = 0, 1, 2, 3, 4
+STATUS_BAD_RESIDENT = 5
+RESIDENT_FLAG = 1 << 30
 COPY_FUSED, COPY_SPLIT = 1, 2
 
 
@@ -66,6 +68,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_prefill": [P, P, P],
         "hisparse_swap_in": [P, I32, P, P, P, P, P],
         "hisparse_swap_in_noalloc": [P, I32, P, P, P, P],
+        "hisparse_swap_in_resident": [P, I32, P, P, P, I32, I32, P, P, P],
         "hisparse_replay_plan": [P, P, I32, I32, P],
         "hisparse_replay_plan_layers": [P, P, P, I32, I32, P],
         "hisparse_backup": [P, I32, P, P, P],
@@ -214,6 +217,19 @@ class HiSparse:
         _check(self.lib.hisparse_swap_in(self.h, layer, _addr(topk), _addr(seq_lens),
                                          _addr(out_slot_ids), plan, _stream(stream)),
                "hisparse_swap_in")
+
+    def swap_in_resident(self, layer: int, topk, seq_lens, resident_blocks, block_size: int,
+                         out_slot_ids, plan_rows=None, plan_counts=None, stream=None) -> None:
+        """hisparse_swap_in_resident; resident_blocks is a [R][max_blocks]
+        int32 device tensor of resident page ids (-1 = not resident)."""
+        plan = None
+        if plan_rows is not None or plan_counts is not None:
+            plan = ctypes.byref(Plan(_addr(plan_rows), _addr(plan_counts)))
+        max_blocks = int(resident_blocks.shape[1])
+        _check(self.lib.hisparse_swap_in_resident(self.h, layer, _addr(topk), _addr(seq_lens),
+                                                  _addr(resident_blocks), max_blocks, block_size,
+                                                  _addr(out_slot_ids), plan, _stream(stream)),
+               "hisparse_swap_in_resident")
 
     def swap_in_noalloc(self, layer: int, topk, seq_lens, out_slot_ids, stream=None) -> None:
         """hisparse_swap_in_noalloc: the split-copy swap-in whose internal

@@ -63,6 +63,11 @@ extern "C" {
 #define HISPARSE_STATUS_DUPLICATE 2    /* a position selected twice           */
 #define HISPARSE_STATUS_BAD_SEQ_LEN 3  /* seq_len outside [0, host_capacity]  */
 #define HISPARSE_STATUS_BAD_POSITION 4 /* backup position outside [0, cap)    */
+#define HISPARSE_STATUS_BAD_RESIDENT 5 /* resident block id < -1 or too large */
+
+/* A slot ID with this bit set names a row of the caller's resident pool
+ * (see hisparse_swap_in_resident); hot slots are below D. */
+#define HISPARSE_RESIDENT_FLAG (1 << 30)
 
 /* ---- size limits ------------------------------------------------------- */
 #define HISPARSE_MAX_TOP_K 8192
@@ -206,6 +211,31 @@ int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream);
 int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx,
                      const int32_t *seq_lens, int32_t *out_slot_ids,
                      const hisparse_plan *out_plan, void *stream);
+
+/*
+ * hisparse_swap_in_resident: hisparse_swap_in with the resident-page tier in
+ * front of the hot buffer ([Arch] Resident device pages: one fused resolver
+ * checks resident pages first, then hot rows, then pinned host memory, and a
+ * resident hit exits before the hot-LRU lookup or a host copy; [Arch]
+ * Performance invariants).
+ *   resident_blocks  device int32 [R][max_blocks]: for request r, entry b is
+ *                    the id of the resident page holding its tokens
+ *                    [b * block_size, (b + 1) * block_size) in the caller's
+ *                    paged pool, or -1 if that block is not resident.
+ *   block_size       tokens per resident page (>= 1); max_blocks >= 1.
+ * A position t with id = resident_blocks[r][t / block_size] >= 0 (blocks at
+ * or past max_blocks are not resident) resolves to
+ *     HISPARSE_RESIDENT_FLAG | (id * block_size + t % block_size)
+ * and touches no hot state: no stamp, no map change, no plan entry, not a
+ * miss -- also on the fast path.  Every other position is resolved as by
+ * hisparse_swap_in.  A looked-up id below -1, or one whose rows reach the
+ * flag bit, sets status BAD_RESIDENT (after BAD_INDEX and DUPLICATE) and
+ * leaves the request untouched.  Errors: as hisparse_swap_in.
+ */
+int hisparse_swap_in_resident(hisparse_t h, int32_t layer, const int32_t *topk_idx,
+                              const int32_t *seq_lens, const int32_t *resident_blocks,
+                              int32_t max_blocks, int32_t block_size, int32_t *out_slot_ids,
+                              const hisparse_plan *out_plan, void *stream);
 
 /*
  * hisparse_replay_plan: copy-only replay of a recorded plan onto another

@@ -44,18 +44,24 @@ class Pair:
         self.gpu.close()
         self.orc.close()
 
-    def swap_in(self, layer: int, topk: np.ndarray, plan=None, cnt=None, record_plan=True):
+    def swap_in(self, layer: int, topk: np.ndarray, plan=None, cnt=None, record_plan=True,
+                resident=None, block_size: int = 0):
         """One call on both sides; returns (gpu results, oracle results).
         With record_plan=False the library gets no plan to fill; the GPU
-        plan/count results are then the oracle's (nothing to compare)."""
+        plan/count results are then the oracle's (nothing to compare).
+        resident: optional int32 [R][max_blocks] resident block table."""
         plan = self.plan if plan is None else plan
         cnt = self.cnt if cnt is None else cnt
         t = torch.from_numpy(np.ascontiguousarray(topk, dtype=np.int32)).cuda()
-        if record_plan:
+        if resident is not None:
+            rb = torch.from_numpy(np.ascontiguousarray(resident, dtype=np.int32)).cuda()
+            self.gpu.swap_in_resident(layer, t, self.seq_d, rb, block_size, self.out,
+                                      plan if record_plan else None, cnt if record_plan else None)
+        elif record_plan:
             self.gpu.swap_in(layer, t, self.seq_d, self.out, plan, cnt)
         else:
             self.gpu.swap_in(layer, t, self.seq_d, self.out)
-        o = self.orc.swap_in(layer, topk, self.seq)
+        o = self.orc.swap_in(layer, topk, self.seq, resident, block_size)
         torch.cuda.synchronize()
         if record_plan:
             g = (self.out.cpu().numpy(), plan.cpu().numpy(), cnt.cpu().numpy(),

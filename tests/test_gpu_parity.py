@@ -36,14 +36,19 @@ def test_golden_trace_gpu(name):
     S0 = ops[0][1]["S"]
     w = W.custom(1, layout["k"], layout["D"], [S0], capacity=[layout["cap"]])
     p = Pair(w, track_bytes=True)
+    resident = None
     for i, (op, a) in enumerate(ops[1:]):
+        if op == "resident":
+            resident = np.array([a["ids"]], dtype=np.int32)
+            continue
         if op == "backup":
             st = p.backup(0, np.array([a["pos"]], dtype=np.int32))
             assert st[0] == 0
             continue
         if a["S"] != p.seq[0]:                # grown by backups since the last call
             p.advance(a["S"] - int(p.seq[0]))
-        g, o = p.swap_in(0, np.array([a["topk"]], dtype=np.int32))
+        g, o = p.swap_in(0, np.array([a["topk"]], dtype=np.int32), resident=resident,
+                         block_size=layout.get("bs", 0))
         assert_call_equal(g, o, f"{name} op {i}")
         e = a["expect"]
         out, plan, cnt, st = g
@@ -134,6 +139,40 @@ def test_swap_in_replayed_from_a_cuda_graph():
         assert_state_equal(p, 0, f"graph replay {c}")
         assert_device_bytes_equal_oracle(p, 0, f"graph replay {c}")
         assert_device_bytes_equal_oracle(p, 1, f"graph replay {c}")
+    p.close()
+
+
+@pytest.mark.parametrize("bs,frac,lens", [
+    (16, 0.3, [3000, 400, 5000, 2100]),       # mixed fast and slow requests
+    (1, 0.5, [2000, 2000, 2000, 2000]),       # one-token pages
+    (64, 0.0, [3000, 3000, 3000, 3000]),      # a table with nothing resident
+    (64, 1.0, [3000, 9000, 3000, 512]),       # everything resident
+])
+def test_resident_tier_parity(bs, frac, lens):
+    """Resident pages first: random block tables per call, reuse between calls."""
+    rng = np.random.default_rng(int(bs * 100 + frac * 10))
+    R, k, D = 4, 256, 512
+    w = W.custom(R, k, D, lens, row_bytes=48)
+    p = Pair(w, track_bytes=True)
+    nb = -(-max(lens) // bs) - 3                 # a table a little shorter than S
+    topk = _random_rows(rng, R, k, lens)
+    for c in range(6):
+        tab = np.where(rng.random((R, nb)) < frac, rng.integers(0, 3000, (R, nb)), -1)
+        g, o = p.swap_in(0, topk, resident=tab.astype(np.int32), block_size=bs)
+        assert_call_equal(g, o, f"call {c}")
+        assert_state_equal(p, 0, f"call {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"call {c}")
+        topk = _reuse_rows(rng, topk, lens, keep=0.6)
+    # a malformed id in a looked-up block sets BAD_RESIDENT and touches nothing
+    before = p.gpu.read_state(0)
+    tab = np.full((R, nb), -1, dtype=np.int32)
+    inside = topk[1][topk[1] // bs < nb]          # a position whose block is in the table
+    tab[1, inside[0] // bs] = -3
+    g, o = p.swap_in(0, topk, resident=tab, block_size=bs)
+    assert_call_equal(g, o, "malformed")
+    assert g[3][1] == H.STATUS_BAD_RESIDENT and (g[0][1] == -1).all()
+    after = p.gpu.read_state(0)
+    assert np.array_equal(before[0][1], after[0][1]) and np.array_equal(before[1][1], after[1][1])
     p.close()
 
 

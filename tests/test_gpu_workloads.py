@@ -46,6 +46,31 @@ def test_decode_40k_all_steps():
     p.close()
 
 
+def test_decode_40k_with_resident_recent_pages():
+    """decode_40k with the newest 4096 tokens of every request still in
+    resident pages of 64 tokens (ids scattered over a shared pool)."""
+    w = W.make_config(2, steps=16)
+    sched = W.topk_schedule(w)[0]
+    p = Pair(w, track_bytes=False)
+    R, bs = w.num_requests, 64
+    nb = 40000 // bs + 1
+    rng = np.random.default_rng(9)
+    tab = np.full((R, nb), -1, dtype=np.int32)
+    first = (40000 - 4096) // bs
+    ids = rng.permutation(R * (nb - first)).reshape(R, nb - first)
+    tab[:, first:] = ids
+    resident_hits = 0
+    for c in range(w.steps):
+        g, o = p.swap_in(0, sched[c], resident=tab, block_size=bs)
+        assert_call_equal(g, o, f"call {c}")
+        resident_hits += int((g[0] >= H.RESIDENT_FLAG).sum())
+        if c % 8 == 7:
+            s2t = assert_state_equal(p, 0, f"call {c}")
+            assert_device_rows(p, 0, s2t, sample=128, seed=c, ctx=f"call {c}")
+    assert resident_hits > 0
+    p.close()
+
+
 def test_mixed_lengths_four_layers_with_backups():
     """128 requests of U[2048, 81920] tokens, 4 layers, backups every step."""
     w = W.make_config(3)
