@@ -35,13 +35,17 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
     // exclusive prefix of counts over requests (R <= 8192: 16 per thread)
     const int per = (R + REPLAY_NT - 1) / REPLAY_NT;
     const int r0 = min(tid * per, R), r1 = min(r0 + per, R);
+    auto rows_of = [&](int r) -> uint32_t {
+        if (a.only_if && a.only_if[r] == 0) return 0u;
+        return (uint32_t)min(max(a.plan_counts[r], 0), k);
+    };
     uint32_t local = 0;
-    for (int r = r0; r < r1; ++r) local += (uint32_t)min(max(a.plan_counts[r], 0), k);
+    for (int r = r0; r < r1; ++r) local += rows_of(r);
     uint32_t total_rows;
     uint32_t run = block_exclusive_scan<REPLAY_NT>(local, warp_tot, total_rows);
     for (int r = r0; r < r1; ++r) {
         rows_before[r] = run;
-        run += (uint32_t)min(max(a.plan_counts[r], 0), k);
+        run += rows_of(r);
     }
     if (tid == 0) rows_before[R] = total_rows;
     __syncthreads();

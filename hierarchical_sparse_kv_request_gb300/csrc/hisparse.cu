@@ -36,11 +36,21 @@ struct hisparse_handle {
     std::vector<hs::HotState> state;   // per layer; tok2slot null for skip layers
     hs::LayerDescDev *d_layers = nullptr;
     int32_t *d_plan_rows = nullptr, *d_plan_counts = nullptr;  // split-copy plan
+    int32_t *d_deferred = nullptr;     // [R] requests left to the copy grid (auto mode)
     int32_t copy_mode = HISPARSE_COPY_FUSED;
     bool stage_s2t = false;   // resolve kernel stages the slot->token row
 };
 
 namespace {
+
+// Auto copy mode: in batches of fewer than kAutoDeferBelowRequests requests,
+// a request whose misses exceed kAutoDeferBytes leaves them to the full-GPU
+// copy grid (one SM moves such a volume several times slower).  From that
+// batch size on, the CTAs of the batch already keep the host link busy, and
+// deferring only moves every copy behind the resolve grid (measured on
+// GB300: a cold call of 1 request 76 -> 29 us, of 32 requests 170 -> 191 us).
+constexpr int64_t kAutoDeferBytes = 256 << 10;
+constexpr int kAutoDeferBelowRequests = 8;
 
 hs::Geometry geometry(const hisparse_handle *h)
 {
@@ -95,6 +105,7 @@ void release(hisparse_handle *h)
     cudaFree(h->d_layers);
     cudaFree(h->d_plan_rows);
     cudaFree(h->d_plan_counts);
+    cudaFree(h->d_deferred);
     cudaFree(h->d_status);
     cudaFree(h->d_zero);
     cudaFree(h->d_off);
@@ -232,7 +243,8 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
               dev_alloc(&h->d_zero, (size_t)h->R) == cudaSuccess &&
               dev_alloc(&h->d_layers, (size_t)h->L) == cudaSuccess &&
               dev_alloc(&h->d_plan_rows, (size_t)h->R * h->k * 2) == cudaSuccess &&
-              dev_alloc(&h->d_plan_counts, (size_t)h->R) == cudaSuccess;
+              dev_alloc(&h->d_plan_counts, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(&h->d_deferred, (size_t)h->R) == cudaSuccess;
     h->state.assign(h->L, hs::HotState{nullptr, nullptr, nullptr, nullptr, nullptr});
     for (int l = 0; ok && l < h->L; ++l) {
         if (h->anchor[l] >= 0) continue;
@@ -263,6 +275,7 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
     if (e == cudaSuccess) e = cudaMemset(h->d_zero, 0, sizeof(int32_t) * h->R);
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t) * h->R);
     if (e == cudaSuccess) e = cudaMemset(h->d_plan_counts, 0, sizeof(int32_t) * h->R);
+    if (e == cudaSuccess) e = cudaMemset(h->d_deferred, 0, sizeof(int32_t) * h->R);
     // empty hot state: seq_len 0 everywhere (maps -1, LRU in slot order, ticks 0)
     if (e == cudaSuccess) e = hs::launch_prefill(h->d_zero, h->d_layers, h->L, geometry(h), h->d_status, nullptr);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -328,15 +341,19 @@ int swap_in_impl(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int
     a.g = geometry(h);
     a.max_cap = (int32_t)h->max_cap;
     const bool split = h->copy_mode == HISPARSE_COPY_SPLIT;
+    const bool autom = h->copy_mode == HISPARSE_COPY_AUTO && h->R < kAutoDeferBelowRequests;
     a.fused_copy = !split;
     a.stage_s2t = h->stage_s2t;
     a.resident = resident_blocks;
     a.res_max_blocks = resident_blocks ? max_blocks : 0;
     a.res_block_size = resident_blocks ? block_size : 0;
-    a.plan_rows = out_plan ? out_plan->rows : (split ? h->d_plan_rows : nullptr);
-    a.plan_counts = out_plan ? out_plan->counts : (split ? h->d_plan_counts : nullptr);
+    a.deferred = autom ? h->d_deferred : nullptr;
+    a.defer_bytes = kAutoDeferBytes;
+    const bool wide_copy = split || autom;
+    a.plan_rows = out_plan ? out_plan->rows : (wide_copy ? h->d_plan_rows : nullptr);
+    a.plan_counts = out_plan ? out_plan->counts : (wide_copy ? h->d_plan_counts : nullptr);
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));
-    if (e != cudaSuccess || !split) return cuda_status(e);
+    if (e != cudaSuccess || !wide_copy) return cuda_status(e);
     hs::ReplayLaunch c;
     c.plan_rows = a.plan_rows;
     c.plan_counts = a.plan_counts;
@@ -345,6 +362,7 @@ int swap_in_impl(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int
     c.g = a.g;
     c.num_ctas = h->num_sms;
     c.programmatic = true;
+    c.only_if = autom ? h->d_deferred : nullptr;
     return cuda_status(hs::launch_replay(c, as_stream(stream)));
 }
 
@@ -386,6 +404,7 @@ int hisparse_replay_plan_layers(hisparse_t h, const hisparse_plan *plan, const i
     c.g = geometry(h);
     c.num_ctas = num_ctas ? num_ctas : 16;
     c.programmatic = false;
+    c.only_if = nullptr;
     return cuda_status(hs::launch_replay(c, as_stream(stream)));
 }
 
@@ -444,7 +463,8 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok, uint32_t
 
 int hisparse_set_copy_mode(hisparse_t h, int32_t mode)
 {
-    if (!h || (mode != HISPARSE_COPY_FUSED && mode != HISPARSE_COPY_SPLIT)) return HISPARSE_ERR_INVALID_ARG;
+    if (!h || (mode != HISPARSE_COPY_FUSED && mode != HISPARSE_COPY_SPLIT && mode != HISPARSE_COPY_AUTO))
+        return HISPARSE_ERR_INVALID_ARG;
     h->copy_mode = mode;
     return HISPARSE_OK;
 }
@@ -520,6 +540,8 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     a.resident = nullptr;
     a.res_max_blocks = 0;
     a.res_block_size = 0;
+    a.deferred = nullptr;
+    a.defer_bytes = 0;
     a.plan_rows = scratch;
     a.plan_counts = scratch + (int64_t)h->R * h->k * 2;
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));
@@ -532,6 +554,7 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     c.g = a.g;
     c.num_ctas = h->num_sms;
     c.programmatic = true;
+    c.only_if = nullptr;
     return cuda_status(hs::launch_replay(c, as_stream(stream)));
 }
 

@@ -130,6 +130,8 @@ struct ResolveLaunch {
     const int32_t *resident;  // [R][res_max_blocks] resident block ids, or null
     int32_t res_max_blocks;
     int32_t res_block_size;
+    int32_t *deferred;        // [R]: 1 = misses left to the copy grid; null = never defer
+    int64_t defer_bytes;      // defer a request whose misses exceed this many bytes
 };
 
 // Shared-memory bytes the resolve kernel needs for this geometry.
@@ -150,6 +152,7 @@ struct ReplayLaunch {
     Geometry g;
     int num_ctas;
     bool programmatic;  // launched right after a resolve (programmatic dependency)
+    const int32_t *only_if;  // [R] or null: copy only requests whose entry is nonzero
 };
 size_t replay_smem_bytes(int R);  // below the 48 KB default for R <= 8192
 cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s);

@@ -123,6 +123,7 @@ __device__ __forceinline__ void finish_untouched(const ResolveLaunch &a, int r,
     if (threadIdx.x == 0) {
         a.status[r] = status;
         if (a.plan_counts) a.plan_counts[r] = 0;
+        if (a.deferred) a.deferred[r] = 0;
         a.st.tick[r] = tick;
     }
 }
@@ -314,7 +315,10 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     // First host chunks: loaded now, stored after the state writes below.
     const int64_t B = a.g.B;
     const int CH = a.g.chunks;
-    const int total = a.fused_copy ? m * CH : 0;
+    // A request with many misses can leave its copies to a full-GPU copy
+    // grid launched behind this kernel: one SM alone moves them slowly.
+    const bool defer = a.deferred && (int64_t)m * B > a.defer_bytes;
+    const int total = (a.fused_copy && !defer) ? m * CH : 0;
     const uint8_t *hrow0 = a.store.host + off * B;
     uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
     uint4 pv[PREFETCH];
@@ -389,6 +393,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     if (tid == 0) {
         a.status[r] = kStatusOk;
         if (a.plan_counts) a.plan_counts[r] = m;
+        if (a.deferred) a.deferred[r] = defer ? 1 : 0;
         a.st.tick[r] = tick;
     }
 

@@ -24,7 +24,7 @@ ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT = -5, -6, -7, -8
 STATUS_OK, STATUS_BAD_INDEX, STATUS_DUPLICATE, STATUS_BAD_SEQ_LEN, STATUS_BAD_POSITION = 0, 1, 2, 3, 4
 STATUS_BAD_RESIDENT = 5
 RESIDENT_FLAG = 1 << 30
-COPY_FUSED, COPY_SPLIT = 1, 2
+COPY_FUSED, COPY_SPLIT, COPY_AUTO = 1, 2, 3
 
 
 class HiSparseError(RuntimeError):

@@ -24,10 +24,11 @@
  *     memory.  No entry point keeps a caller pointer after it returns.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls that take a stream are asynchronous and stream-ordered:
- *     they never synchronise, never read device data back to the host and
- *     launch exactly one kernel ([Arch] Performance invariants: no device
- *     scalar readback, no CPU/device metadata round trip, no extra launch),
- *     so they can be captured in a CUDA graph.
+ *     they never synchronise and never read device data back to the host
+ *     ([Arch] Performance invariants: no device scalar readback, no
+ *     CPU/device metadata round trip), and they launch one kernel ([Arch]:
+ *     no extra launch) -- two for hisparse_swap_in in the split and auto
+ *     copy modes -- so they can be captured in a CUDA graph.
  *   - Problems in the *data* (a bad top-k index, a duplicate, a bad
  *     position) are reported per request in a device status array (see
  *     hisparse_status); the affected request's state is left untouched.
@@ -78,6 +79,9 @@ extern "C" {
 /* Copy strategy of hisparse_swap_in (see hisparse_set_copy_mode). */
 #define HISPARSE_COPY_FUSED 1  /* the resolving CTA copies its own misses     */
 #define HISPARSE_COPY_SPLIT 2  /* a second, wide grid copies all misses       */
+#define HISPARSE_COPY_AUTO 3   /* fused; in batches below 8 requests, requests
+                                  with > 256 KB of misses leave them to a
+                                  second, wide grid                          */
 
 typedef struct hisparse_handle *hisparse_t;
 
@@ -294,9 +298,20 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok,
                         uint32_t *last_used, int32_t *tok2slot, int32_t *lru_order,
                         uint32_t *ticks, void *stream);
 
-/* hisparse_set_copy_mode: HISPARSE_COPY_FUSED (default) or
- * HISPARSE_COPY_SPLIT for hisparse_swap_in's miss copies.  Results are
- * identical; only the launch shape differs. */
+/* hisparse_set_copy_mode: how hisparse_swap_in (and _resident) copy the
+ * misses; results are identical, only the launch shape differs.
+ *   HISPARSE_COPY_FUSED (default)  each request's CTA copies its own rows:
+ *                                  one launch per call.
+ *   HISPARSE_COPY_SPLIT            the resolve grid records the plan and a
+ *                                  full-GPU copy grid, launched behind it
+ *                                  with a programmatic dependency, copies.
+ *   HISPARSE_COPY_AUTO             with fewer than 8 requests: fused, except
+ *                                  that a request whose misses exceed 256 KB
+ *                                  is flagged on the device and left to the
+ *                                  full-GPU copy grid that follows (two
+ *                                  launches per call; no readback) -- one SM
+ *                                  alone copies such a volume slowly; with
+ *                                  8 or more requests: the same as FUSED. */
 int hisparse_set_copy_mode(hisparse_t h, int32_t mode);
 
 /*

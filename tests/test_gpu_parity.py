@@ -67,7 +67,7 @@ def test_golden_trace_gpu(name):
 # the tiny workload, every byte every call
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("mode", [H.COPY_FUSED, H.COPY_SPLIT])
+@pytest.mark.parametrize("mode", [H.COPY_FUSED, H.COPY_SPLIT, H.COPY_AUTO])
 def test_tiny_workload_full_parity(mode):
     w = W.make_config(1)
     sched = W.topk_schedule(w)[0]
@@ -79,6 +79,29 @@ def test_tiny_workload_full_parity(mode):
         assert_device_bytes_equal_oracle(p, 0, f"call {c}")
     assert g[2][0] == 0                  # the short request never misses
     assert g[2][1:].sum() > 0
+    p.close()
+
+
+@pytest.mark.parametrize("record_plan", [True, False])
+def test_auto_copy_defers_requests_with_many_misses(record_plan):
+    """Auto copy mode: requests whose misses exceed 256 KB leave them to the
+    full-GPU copy grid, the others copy their own; results are unchanged.
+    (Deferral applies to batches of fewer than 8 requests.)"""
+    R, k, D = 4, 512, 1024
+    lens = [600, 20000, 20000, 5000]           # short / cold / cold / cold
+    w = W.custom(R, k, D, lens, row_bytes=1152)
+    p = Pair(w, track_bytes=True, copy_mode=H.COPY_AUTO)
+    rng = np.random.default_rng(21)
+    topk = _random_rows(rng, R, k, lens)
+    topk[3] = np.arange(5000 - k, 5000)        # request 3 hits everything
+    for c in range(4):
+        g, o = p.swap_in(0, topk, record_plan=record_plan)
+        assert_call_equal(g, o, f"call {c}")
+        assert_state_equal(p, 0, f"call {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"call {c}")
+        if c == 0:   # requests 1 and 2 missed > 256 KB and were deferred
+            assert (o[2][1:3] * w.row_bytes > 256 << 10).all() and o[2][3] == 0
+        topk = _reuse_rows(rng, topk, lens, keep=0.9 if c else 0.5)
     p.close()
 
 
