@@ -41,8 +41,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=128)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5, 6])
     ap.add_argument("--copy-mode", default="fused", choices=["fused", "split"])
+    ap.add_argument("--replay-ctas", type=int, default=None,
+                    help="configs 4 and 6: CTAs of the skip-layer replay launch "
+                         "(default 16 for config 4, 48 for config 6)")
     ap.add_argument("--no-prefetch", action="store_true",
                     help="config 4: replay skip layers in-line on the main stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -296,6 +299,8 @@ def run_gpu(args):
 
     if args.config == 4:
         return run_config4(args, ws, rank, H)
+    if args.config == 6:
+        return run_pipelined(args, ws, rank, H)
 
     K, Wm = args.steps, args.warmup
     st = Setup(args.config, K + Wm, rank, args.copy_mode)
@@ -513,7 +518,7 @@ def run_config4(args, ws, rank, H):
             ev = torch.cuda.Event()
             ev.record()
             side.wait_event(ev)
-            gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=16, stream=side)
+            gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=args.replay_ctas, stream=side)
             if marks:
                 marks[1].record(side)
             done = torch.cuda.Event()
@@ -523,7 +528,7 @@ def run_config4(args, ws, rank, H):
                 marks[2].record()
             torch.cuda.current_stream().wait_event(done)
         else:
-            gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=16)
+            gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=args.replay_ctas)
             if marks:
                 marks[1].record()
             H.synthetic_compute(buf, passes)
@@ -538,7 +543,7 @@ def run_config4(args, ws, rank, H):
     rep_ms = []
     for _ in range(3):
         s.record()
-        gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=16)
+        gpu.replay_plan_layers(plan, cnt, [1, 2, 3], num_ctas=args.replay_ctas)
         e.record()
         e.synchronize()
         rep_ms.append(s.elapsed_time(e))
@@ -584,7 +589,8 @@ def run_config4(args, ws, rank, H):
         "config": {"workload": w.name, "requests": R, "seq_len": int(w.seq_lens0[0]),
                    "layers": "1 anchor + 3 skip", "top_k": k,
                    "device_buffer_size": w.device_buffer_size, "row_bytes": w.row_bytes,
-                   "prefetch": prefetch, "replay_ctas": 16, "replay_launches_per_step": 1,
+                   "prefetch": prefetch, "replay_ctas": args.replay_ctas,
+                   "replay_launches_per_step": 1,
                    "l2": "flushed between timed steps (512 MB write)"},
         "compute_ms": round(compute_ms, 4), "anchor_swap_in_ms": round(anchor, 4),
         "replays_alone_ms": round(statistics.median(rep_ms), 4),
@@ -597,6 +603,103 @@ def run_config4(args, ws, rank, H):
         "compute_stand_in": f"bf16 elementwise stream, 1 GiB x {passes} passes, 2 x 256-thread CTAs per SM",
         "step_ms_min_median_max": [round(min(times), 4), round(statistics.median(times), 4),
                                    round(max(times), 4)],
+    }
+
+
+# ----------------------------------------------------------------------------
+# config 6: pipelined index sharing over a 16-layer slice
+# ----------------------------------------------------------------------------
+
+def run_pipelined(args, ws, rank, H):
+    """4 groups of (anchor + 3 skip layers) per decode step, each step one
+    CUDA graph.  Per group: the anchor's swap-in records its plan into buffer
+    g mod 2 (double-buffered: the next anchor may write while this plan is
+    still replayed); the replay of the group's 3 skip layers is pre-issued on
+    a side stream; one layer of stand-in compute (the anchor layer's own
+    work) runs on the main stream, which then waits for the replay (the skip
+    layers read their rows) and runs three more layers.  The same steps run
+    three ways from the same state: pre-issued replays, replays in-line after
+    the anchor layer, and no replays (compute-only reference)."""
+    import torch
+    K, Wm = args.steps, args.warmup
+    w = W.make_config(6, steps=K + Wm)
+    w.seed = replica_seed(w.seed, rank)
+    gpu = H.HiSparse.for_workload(w)
+    for l in range(w.num_layers):
+        for r in range(w.num_requests):
+            W.fill_host_rows(w, l, r, gpu.host_rows(l, r), int(w.seq_lens0[r]))
+    sched = {a: torch.from_numpy(x).cuda() for a, x in W.topk_schedule(w).items()}
+    R, k = w.num_requests, w.top_k
+    seq = torch.from_numpy(w.seq_lens0.astype(np.int32)).cuda()
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    plans = [torch.empty((R, k, 2), dtype=torch.int32, device="cuda") for _ in range(2)]
+    cnts = [torch.zeros(R, dtype=torch.int32, device="cuda") for _ in range(2)]
+    groups = [(a, [a + 1, a + 2, a + 3]) for a in w.anchors]
+    side = torch.cuda.Stream(priority=-1)
+    # one "layer" of stand-in compute: a bf16 stream over 320 MB (~0.1 ms)
+    buf = torch.zeros(160 << 20, dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def step(si, mode):
+        for gi, (a, skips) in enumerate(groups):
+            P, C = plans[gi % 2], cnts[gi % 2]
+            gpu.swap_in(a, sched[a][si], seq, out, P, C)
+            if mode == "prefetch":
+                ev = torch.cuda.Event()
+                ev.record()
+                side.wait_event(ev)
+                gpu.replay_plan_layers(P, C, skips, num_ctas=args.replay_ctas, stream=side)
+                done = torch.cuda.Event()
+                done.record(side)
+                H.synthetic_compute(buf, 1)
+                torch.cuda.current_stream().wait_event(done)
+            else:
+                H.synthetic_compute(buf, 1)
+                if mode == "inline":
+                    gpu.replay_plan_layers(P, C, skips, num_ctas=args.replay_ctas)
+            H.synthetic_compute(buf, 3)
+
+    results = {}
+    for mode in ("prefetch", "inline", "none"):
+        gpu.prefill(seq)
+        for si in range(Wm):
+            step(si, mode)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(K)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(K):
+                flush.zero_()
+                ev[i][0].record()
+                step(Wm + i, mode)
+                ev[i][1].record()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        t = [a.elapsed_time(b) for a, b in ev]
+        results[mode] = (statistics.median(t), sum(t) * 1e-3)
+        del graph
+    med = {m: v[0] for m, v in results.items()}
+    total_s = max_over_ranks(results["prefetch"][1], "cuda")
+    rows = R * k * len(groups) * K
+    return {
+        "metric": "resolved top-k rows/s", "value": round(job_throughput(rows, ws, total_s), 1),
+        "unit": "rows/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+        "ms_per_step": round(total_s / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32+u8", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "requests": R, "seq_len": int(w.seq_lens0[0]),
+                   "layers": "4 x (1 anchor + 3 skip)", "top_k": k,
+                   "device_buffer_size": w.device_buffer_size, "row_bytes": w.row_bytes,
+                   "plans": "double-buffered", "replay_ctas": args.replay_ctas,
+                   "graph": "one per timed run",
+                   "compute_stand_in": "bf16 stream over 320 MB per layer",
+                   "l2": "flushed between timed steps (512 MB write)"},
+        "step_ms_median": {m: round(v, 4) for m, v in med.items()},
+        "exposed_copy_ms_prefetch": round(med["prefetch"] - med["none"], 4),
+        "exposed_copy_ms_inline": round(med["inline"] - med["none"], 4),
+        # per group: swap-in, replay, two stand-in compute launches
+        "gpu_launches": 4 * len(groups) * K,
     }
 
 
@@ -671,6 +774,8 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.replay_ctas is None:
+        args.replay_ctas = 48 if args.config == 6 else 16
     if args.impl == "reference":
         res = run_reference(args)
     else:

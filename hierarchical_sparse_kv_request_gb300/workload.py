@@ -140,7 +140,8 @@ def custom(R: int, k: int, D: int, seq_lens, row_bytes: int = 16, layers: int = 
 
 def make_config(config_no: int, *, steps: Optional[int] = None,
                 num_requests: Optional[int] = None) -> Workload:
-    """The five workloads; ``steps``/``num_requests`` shrink a config for tests."""
+    """The workloads (1-5, and 6: a pipelined 16-layer index-sharing slice);
+    ``steps``/``num_requests`` shrink a config for tests."""
     seed = _seed(config_no)
     if config_no == 1:
         # Tiny check: 4 requests, seq_len {400,3000,5000,8000}, k 256, D 512,
@@ -179,6 +180,16 @@ def make_config(config_no: int, *, steps: Optional[int] = None,
         w = Workload("spec_verify", 5, R, 1, [-1], 16, 3, 2048, 4096, 1152,
                      "bf16", 10, 1024, "mixture", True,
                      np.full(R, 32768, dtype=np.int32), seed)
+    elif config_no == 6:
+        # Pipelined index sharing over a 16-layer slice: 4 anchors, each
+        # followed by 3 skip layers reusing its top-k, decode_40k shapes.
+        R = 32
+        anchors = []
+        for g in range(4):
+            anchors += [-1, 4 * g, 4 * g, 4 * g]
+        w = Workload("index_share_16", 6, R, 16, anchors, 32, 1, 2048, 6144, 656,
+                     "mla_fp8", 10, int(round(0.8 * 2048)), "mixture", False,
+                     np.full(R, 40000, dtype=np.int32), seed)
     else:
         raise ValueError(f"unknown config {config_no}")
     if steps is not None:

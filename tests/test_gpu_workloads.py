@@ -130,6 +130,52 @@ def test_shared_index_replay_beside_compute():
     p.close()
 
 
+def test_pipelined_index_share_graph_double_buffered_plans():
+    """The 16-layer pipelined index-sharing schedule (4 anchors x 3 skip
+    layers) with double-buffered plans, each decode step captured once in a
+    CUDA graph: replays pre-issued on a side stream between stand-in compute
+    launches.  After every step the anchors' outputs, hot state and all 16
+    layers' device rows match the oracle."""
+    w = W.make_config(6, steps=5, num_requests=6)
+    sched = W.topk_schedule(w)
+    p = Pair(w, track_bytes=False)
+    R, k = w.num_requests, w.top_k
+    plans = [torch.empty((R, k, 2), dtype=torch.int32, device="cuda") for _ in range(2)]
+    cnts = [torch.zeros(R, dtype=torch.int32, device="cuda") for _ in range(2)]
+    outs = {a: torch.empty((R, k), dtype=torch.int32, device="cuda") for a in w.anchors}
+    tk = {a: torch.empty((R, k), dtype=torch.int32, device="cuda") for a in w.anchors}
+    side = torch.cuda.Stream(priority=-1)
+    buf = torch.zeros(8 << 20, dtype=torch.bfloat16, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for gi, a in enumerate(w.anchors):
+            P, C = plans[gi % 2], cnts[gi % 2]
+            p.gpu.swap_in(a, tk[a], p.seq_d, outs[a], P, C)
+            ev = torch.cuda.Event()
+            ev.record()
+            side.wait_event(ev)
+            p.gpu.replay_plan_layers(P, C, [a + 1, a + 2, a + 3], num_ctas=16, stream=side)
+            done = torch.cuda.Event()
+            done.record(side)
+            H.synthetic_compute(buf, 1)
+            torch.cuda.current_stream().wait_event(done)
+            H.synthetic_compute(buf, 3)
+    for step in range(w.steps):
+        for a in w.anchors:
+            tk[a].copy_(torch.from_numpy(sched[a][step]))
+        graph.replay()
+        torch.cuda.synchronize()
+        for a in w.anchors:
+            o = p.orc.swap_in(a, sched[a][step], p.seq)
+            g = (outs[a].cpu().numpy(), o[1], o[2], p.gpu.status().cpu().numpy())
+            assert_call_equal(g, o, f"step {step} anchor {a}")
+            s2t = assert_state_equal(p, a, f"step {step} anchor {a}")
+            for l in (a, a + 1, a + 2, a + 3):
+                assert_device_rows(p, l, s2t, sample=None if step == w.steps - 1 else 48,
+                                   seed=step, ctx=f"step {step} layer {l}")
+    p.close()
+
+
 def test_speculative_substeps_with_backups():
     """256 x 32768 tokens, D 4096, 1152 B rows: 3 verification sub-steps per
     decode step, each with its own plan, then one backup per step."""
