@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "hisparse_oracle.c")
 _LIB = os.path.join(_HERE, "libhisparse_oracle.so")
 
-OK, BAD_INDEX, DUPLICATE, BAD_SEQ_LEN, BAD_POSITION, BAD_RESIDENT = 0, 1, 2, 3, 4, 5
+OK, BAD_INDEX, DUPLICATE, BAD_SEQ_LEN, BAD_POSITION, BAD_RESIDENT, NO_HOST_ROW = 0, 1, 2, 3, 4, 5, 6
 RESIDENT_FLAG = 1 << 30
 
 
@@ -48,12 +48,24 @@ def _load(path: Optional[str] = None) -> ctypes.CDLL:
     P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     lib.hso_create.restype = P
     lib.hso_create.argtypes = [I, I, I64, I, I, P, P, I]
+    lib.hso_create_paged.restype = P
+    lib.hso_create_paged.argtypes = [I, I, I64, I, I, P, P, I, I, I]
+    lib.hso_pool_blocks.restype = I
+    lib.hso_pool_blocks.argtypes = [P]
+    lib.hso_free_blocks.restype = I
+    lib.hso_free_blocks.argtypes = [P]
+    lib.hso_reserve.argtypes = [P, I, P, P]
+    lib.hso_release.argtypes = [P, I, P]
+    lib.hso_block_table.restype = I
+    lib.hso_block_table.argtypes = [P, I, P]
+    lib.hso_block_rows.restype = P
+    lib.hso_block_rows.argtypes = [P, I, I]
     lib.hso_destroy.argtypes = [P]
     lib.hso_host_row.restype = P
     lib.hso_host_row.argtypes = [P, I, I, I64]
     lib.hso_dev_row.restype = P
     lib.hso_dev_row.argtypes = [P, I, I, I64]
-    lib.hso_prefill.argtypes = [P, P]
+    lib.hso_prefill.argtypes = [P, P, P]
     lib.hso_swap_in.argtypes = [P, I, P, P, P, P, P, P]
     lib.hso_swap_in_resident.argtypes = [P, I, P, P, P, I, I, P, P, P, P]
     lib.hso_replay.argtypes = [P, P, P, I]
@@ -71,31 +83,43 @@ def _ptr(a: np.ndarray) -> int:
 
 
 class Oracle:
-    """Numpy-facing wrapper of the C oracle state for one layout."""
+    """Numpy-facing wrapper of the C oracle state for one layout.
+
+    host_block_tokens > 0 selects the paged host pool: floor(ratio * R * D /
+    host_block_tokens) blocks per layer, handed to requests by reserve()."""
 
     def __init__(self, num_requests: int, num_layers: int, row_bytes: int,
                  top_k: int, device_buffer_size: int,
                  anchor_of_layer: Sequence[int], host_capacity: Sequence[int],
-                 track_bytes: bool = True, lib_path: Optional[str] = None):
+                 track_bytes: bool = True, lib_path: Optional[str] = None,
+                 host_block_tokens: int = 0, ratio: int = 0):
         self.lib = _load(lib_path)
         self.R, self.L, self.B = num_requests, num_layers, row_bytes
         self.k, self.D = top_k, device_buffer_size
         self.anchor = np.ascontiguousarray(anchor_of_layer, dtype=np.int32)
         self.cap = np.ascontiguousarray(host_capacity, dtype=np.int64)
         self.track_bytes = track_bytes
-        self.h = self.lib.hso_create(self.R, self.L, self.B, self.k, self.D,
-                                     _ptr(self.anchor), _ptr(self.cap),
-                                     1 if track_bytes else 0)
+        self.hb = int(host_block_tokens)
+        if self.hb > 0:
+            self.h = self.lib.hso_create_paged(self.R, self.L, self.B, self.k, self.D,
+                                               _ptr(self.anchor), _ptr(self.cap), int(ratio),
+                                               self.hb, 1 if track_bytes else 0)
+        else:
+            self.h = self.lib.hso_create(self.R, self.L, self.B, self.k, self.D,
+                                         _ptr(self.anchor), _ptr(self.cap),
+                                         1 if track_bytes else 0)
         if not self.h:
             raise ValueError("oracle rejected the layout")
         self.total_cap = int(self.lib.hso_total_capacity(self.h))
         self.host_off = np.concatenate([[0], np.cumsum(self.cap)[:-1]]).astype(np.int64)
+        self.pool_blocks = int(self.lib.hso_pool_blocks(self.h))
 
     @classmethod
-    def for_workload(cls, w, track_bytes: bool = True, lib_path: Optional[str] = None):
+    def for_workload(cls, w, track_bytes: bool = True, lib_path: Optional[str] = None,
+                     host_block_tokens: int = 0):
         return cls(w.num_requests, w.num_layers, w.row_bytes, w.top_k,
                    w.device_buffer_size, w.anchor_of_layer, w.host_capacity,
-                   track_bytes, lib_path)
+                   track_bytes, lib_path, host_block_tokens, w.host_to_device_ratio)
 
     def close(self):
         if self.h:
@@ -110,7 +134,10 @@ class Oracle:
 
     # -- bytes ------------------------------------------------------------
     def host_rows(self, layer: int, r: int) -> np.ndarray:
-        """Writable view [cap_r][B] of the oracle's host rows of (layer, r)."""
+        """Writable view [cap_r][B] of the oracle's host rows of (layer, r)
+        (contiguous host regions only)."""
+        if self.hb:
+            raise RuntimeError("a paged pool has no per-request region; use block_rows")
         p = self.lib.hso_host_row(self.h, layer, r, 0)
         if not p:
             raise RuntimeError("oracle built without byte tracking")
@@ -127,11 +154,46 @@ class Oracle:
         buf = (ctypes.c_uint8 * n).from_address(p)
         return np.frombuffer(buf, dtype=np.uint8).reshape(self.D, self.B)
 
+    def block_rows(self, layer: int, block: int) -> np.ndarray:
+        """Writable view [hb][B] of host block `block` of a layer's paged pool."""
+        p = self.lib.hso_block_rows(self.h, layer, block)
+        if not p:
+            raise RuntimeError("no such block, or byte tracking off")
+        n = self.hb * self.B
+        buf = (ctypes.c_uint8 * n).from_address(p)
+        return np.frombuffer(buf, dtype=np.uint8).reshape(self.hb, self.B)
+
+    # -- paged host pool ----------------------------------------------------
+    def reserve(self, requests, num_tokens) -> int:
+        """0, -1 (bad argument) or -2 (pool exhausted); nothing changes on error."""
+        q = np.ascontiguousarray(requests, dtype=np.int32)
+        n = np.ascontiguousarray(num_tokens, dtype=np.int64)
+        assert q.shape == n.shape
+        return int(self.lib.hso_reserve(self.h, q.size, _ptr(q), _ptr(n)))
+
+    def release(self, requests) -> int:
+        q = np.ascontiguousarray(requests, dtype=np.int32)
+        return int(self.lib.hso_release(self.h, q.size, _ptr(q)))
+
+    def block_table(self, r: int) -> np.ndarray:
+        n = int(self.lib.hso_block_table(self.h, r, None))
+        if n < 0:
+            raise ValueError("no paged pool, or bad request")
+        ids = np.empty(max(n, 1), dtype=np.int32)
+        self.lib.hso_block_table(self.h, r, _ptr(ids))
+        return ids[:n].copy()
+
+    def free_blocks(self) -> int:
+        return int(self.lib.hso_free_blocks(self.h))
+
     # -- calls ------------------------------------------------------------
-    def prefill(self, seq_lens) -> None:
+    def prefill(self, seq_lens) -> np.ndarray:
+        """Restart requests (S = -1 leaves one alone); returns the status
+        array (entries of skipped requests are 0)."""
         s = np.ascontiguousarray(seq_lens, dtype=np.int32)
-        if self.lib.hso_prefill(self.h, _ptr(s)) != 0:
-            raise ValueError("bad seq_lens for prefill")
+        st = np.zeros(self.R, dtype=np.int32)
+        self.lib.hso_prefill(self.h, _ptr(s), _ptr(st))
+        return st
 
     def swap_in(self, layer: int, topk, seq_lens, resident_blocks=None, block_size: int = 0):
         """Returns (out [R][k], plan [R][k][2], count [R], status [R]).
@@ -169,12 +231,11 @@ class Oracle:
         return st
 
     def state(self, layer: int):
-        """(slot2tok [R][D], last_used [R][D], tok2slot [total_cap], tick)."""
+        """(slot2tok [R][D], last_used [R][D], tok2slot [total_cap], ticks [R])."""
         s2t = np.empty((self.R, self.D), dtype=np.int32)
         lu = np.empty((self.R, self.D), dtype=np.uint32)
-        t2s = np.empty(self.total_cap, dtype=np.int32)
-        tick = ctypes.c_uint32(0)
-        if self.lib.hso_state(self.h, layer, _ptr(s2t), _ptr(lu), _ptr(t2s),
-                              ctypes.addressof(tick)) != 0:
+        t2s = np.empty(max(self.total_cap, 1), dtype=np.int32)
+        ticks = np.empty(self.R, dtype=np.uint32)
+        if self.lib.hso_state(self.h, layer, _ptr(s2t), _ptr(lu), _ptr(t2s), _ptr(ticks)) != 0:
             raise ValueError("layer holds no hot state")
-        return s2t, lu, t2s, int(tick.value)
+        return s2t, lu, t2s[: self.total_cap], ticks

@@ -29,7 +29,18 @@
  *   - resident pages come first ([Arch] Resident device pages; Hot lookup and
  *     LRU): with a resident block table, a position whose block is resident
  *     resolves to RESIDENT_FLAG | (block * block_size + position % block_size)
- *     and touches no hot state -- no stamp, no map, no plan entry, no miss.
+ *     and touches no hot state -- no stamp, no map, no plan entry, no miss;
+ *   - the tick is kept per request (a prefill restarts one request's clock);
+ *   - paged host pool ([Arch] Ownership: the coordinator maps tokens to
+ *     logical host blocks and owns their allocation; the pool budget is
+ *     rounded down to whole host blocks): each layer's pool holds
+ *     floor(ratio * R * D / hb) blocks of hb token rows; a request's tokens
+ *     [b*hb, (b+1)*hb) live in the block its table names at entry b.
+ *     Reservation hands out the lowest free block ids, one at a time, in the
+ *     order asked.  A miss, a backup or a prefill that needs a row of a block
+ *     not reserved sets status NO_HOST_ROW and leaves the request untouched.
+ *     A plan then records the host row in the layer's pool (block * hb +
+ *     token % hb), the "host slot" a replay reads.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -41,6 +52,7 @@
 #define HSO_BAD_SEQ_LEN 3   /* seq_len outside [0, host capacity]   */
 #define HSO_BAD_POSITION 4  /* backup position outside [0, capacity) */
 #define HSO_BAD_RESIDENT 5  /* a resident block id outside [-1, 2^30 / block_size) */
+#define HSO_NO_HOST_ROW 6   /* a needed host row lies in a block not reserved */
 
 /* A resident hit resolves to this flag OR'd with its row in the resident pool. */
 #define HSO_RESIDENT_FLAG 0x40000000
@@ -57,9 +69,17 @@ typedef struct hs_oracle {
     int32_t **tok2slot;   /* [L] -> [total_cap]  token -> slot or -1        */
     int32_t **slot2tok;   /* [L] -> [R*D]        slot -> token or -1        */
     uint32_t **last_used; /* [L] -> [R*D]        LRU stamp of each slot     */
-    uint32_t *tick;       /* [L]                 stamp of the latest call   */
+    uint32_t **tick;      /* [L] -> [R]          stamp of the latest call   */
+    /* paged host pool (hb > 0); hb == 0: request r owns host rows
+     * [host_off[r], host_off[r] + cap[r]) of each layer */
+    int32_t hb;           /* token rows per host block                       */
+    int32_t pool_blocks;  /* host blocks per layer                           */
+    int32_t **blocks;     /* [R] -> [ceil(cap[r] / hb)] block id or -1       */
+    int32_t *nblocks;     /* [R] reserved blocks, always a prefix of the table */
+    char *in_use;         /* [pool_blocks]                                    */
+    int64_t host_rows;    /* rows of one layer's pool                        */
     /* bytes (only with track_bytes) */
-    uint8_t **host;       /* [L] -> [total_cap * B]  pinned host pool       */
+    uint8_t **host;       /* [L] -> [host_rows * B]  pinned host pool       */
     uint8_t **dev;        /* [L] -> [R * D * B]      device hot buffer      */
 } hs_oracle;
 
@@ -70,20 +90,24 @@ static void hso_free(hs_oracle *o)
         if (o->tok2slot) free(o->tok2slot[l]);
         if (o->slot2tok) free(o->slot2tok[l]);
         if (o->last_used) free(o->last_used[l]);
+        if (o->tick) free(o->tick[l]);
         if (o->host) free(o->host[l]);
         if (o->dev) free(o->dev[l]);
     }
+    if (o->blocks)
+        for (int r = 0; r < o->R; ++r) free(o->blocks[r]);
     free(o->tok2slot); free(o->slot2tok); free(o->last_used); free(o->tick);
     free(o->host); free(o->dev);
+    free(o->blocks); free(o->nblocks); free(o->in_use);
     free(o->anchor); free(o->cap); free(o->host_off);
     free(o);
 }
 
 void hso_destroy(hs_oracle *o) { hso_free(o); }
 
-hs_oracle *hso_create(int R, int L, int64_t B, int k, int D,
-                      const int *anchor_of_layer, const int64_t *host_capacity,
-                      int track_bytes)
+static hs_oracle *create(int R, int L, int64_t B, int k, int D,
+                         const int *anchor_of_layer, const int64_t *host_capacity,
+                         int32_t hb, int64_t pool_blocks, int track_bytes)
 {
     if (R <= 0 || L <= 0 || B <= 0 || k <= 0 || D <= 0 || k > D) return NULL;
     hs_oracle *o = (hs_oracle *)calloc(1, sizeof(hs_oracle));
@@ -96,18 +120,38 @@ hs_oracle *hso_create(int R, int L, int64_t B, int k, int D,
     o->tok2slot = (int32_t **)calloc((size_t)L, sizeof(int32_t *));
     o->slot2tok = (int32_t **)calloc((size_t)L, sizeof(int32_t *));
     o->last_used = (uint32_t **)calloc((size_t)L, sizeof(uint32_t *));
-    o->tick = (uint32_t *)calloc((size_t)L, sizeof(uint32_t));
+    o->tick = (uint32_t **)calloc((size_t)L, sizeof(uint32_t *));
     o->host = (uint8_t **)calloc((size_t)L, sizeof(uint8_t *));
     o->dev = (uint8_t **)calloc((size_t)L, sizeof(uint8_t *));
     if (!o->anchor || !o->cap || !o->host_off || !o->tok2slot || !o->slot2tok ||
         !o->last_used || !o->tick || !o->host || !o->dev) { hso_free(o); return NULL; }
     int64_t off = 0;
     for (int r = 0; r < R; ++r) {
+        if (host_capacity[r] < 0) { hso_free(o); return NULL; }
         o->cap[r] = host_capacity[r];
         o->host_off[r] = off;
         off += host_capacity[r];
     }
     o->total_cap = off;
+    o->hb = hb;
+    o->host_rows = off;
+    if (hb > 0) {
+        /* [Arch] Ownership: a pool of whole host blocks, and one block table
+         * per request naming the block of each hb tokens. */
+        if (pool_blocks < 1 || pool_blocks * hb > INT32_MAX) { hso_free(o); return NULL; }
+        o->pool_blocks = (int32_t)pool_blocks;
+        o->host_rows = pool_blocks * hb;
+        o->blocks = (int32_t **)calloc((size_t)R, sizeof(int32_t *));
+        o->nblocks = (int32_t *)calloc((size_t)R, sizeof(int32_t));
+        o->in_use = (char *)calloc((size_t)pool_blocks, 1);
+        if (!o->blocks || !o->nblocks || !o->in_use) { hso_free(o); return NULL; }
+        for (int r = 0; r < R; ++r) {
+            int64_t nb = (o->cap[r] + hb - 1) / hb;
+            o->blocks[r] = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nb > 0 ? nb : 1));
+            if (!o->blocks[r]) { hso_free(o); return NULL; }
+            for (int64_t b = 0; b < nb; ++b) o->blocks[r][b] = -1;
+        }
+    }
     for (int l = 0; l < L; ++l) {
         o->anchor[l] = anchor_of_layer ? anchor_of_layer[l] : -1;
         if (o->anchor[l] >= L || o->anchor[l] == l) { hso_free(o); return NULL; }
@@ -115,15 +159,19 @@ hs_oracle *hso_create(int R, int L, int64_t B, int k, int D,
             /* [Arch] Ownership: the hot-row map and LRU belong to the
              * per-cache runtime; index-sharing followers hold none
              * ([Arch] Performance invariants). */
-            o->tok2slot[l] = (int32_t *)malloc(sizeof(int32_t) * (size_t)o->total_cap);
+            o->tok2slot[l] = (int32_t *)malloc(sizeof(int32_t) * (size_t)(o->total_cap > 0 ? o->total_cap : 1));
             o->slot2tok[l] = (int32_t *)malloc(sizeof(int32_t) * (size_t)R * D);
             o->last_used[l] = (uint32_t *)calloc((size_t)R * D, sizeof(uint32_t));
-            if (!o->tok2slot[l] || !o->slot2tok[l] || !o->last_used[l]) { hso_free(o); return NULL; }
+            o->tick[l] = (uint32_t *)calloc((size_t)R, sizeof(uint32_t));
+            if (!o->tok2slot[l] || !o->slot2tok[l] || !o->last_used[l] || !o->tick[l]) {
+                hso_free(o);
+                return NULL;
+            }
             for (int64_t i = 0; i < o->total_cap; ++i) o->tok2slot[l][i] = -1;
             for (int64_t i = 0; i < (int64_t)R * D; ++i) o->slot2tok[l][i] = -1;
         }
         if (track_bytes) {
-            o->host[l] = (uint8_t *)calloc((size_t)(o->total_cap * B), 1);
+            o->host[l] = (uint8_t *)calloc((size_t)(o->host_rows * B), 1);
             o->dev[l] = (uint8_t *)calloc((size_t)((int64_t)R * D * B), 1);
             if (!o->host[l] || !o->dev[l]) { hso_free(o); return NULL; }
         }
@@ -131,10 +179,135 @@ hs_oracle *hso_create(int R, int L, int64_t B, int k, int D,
     return o;
 }
 
+/* Every request owns host_capacity[r] contiguous token rows of each layer. */
+hs_oracle *hso_create(int R, int L, int64_t B, int k, int D,
+                      const int *anchor_of_layer, const int64_t *host_capacity,
+                      int track_bytes)
+{
+    return create(R, L, B, k, D, anchor_of_layer, host_capacity, 0, 0, track_bytes);
+}
+
+/*
+ * Paged host pool: host_capacity[r] is only the longest request r may grow
+ * to; the rows themselves come from a pool of floor(ratio * R * D / hb)
+ * blocks of hb rows per layer ([Guide] HiSparse Config Parameters: the
+ * host_to_device_ratio sizes the logical pool against the device pool;
+ * [Arch] the budget is rounded down to whole host blocks).
+ */
+hs_oracle *hso_create_paged(int R, int L, int64_t B, int k, int D,
+                            const int *anchor_of_layer, const int64_t *host_capacity,
+                            int ratio, int32_t hb, int track_bytes)
+{
+    if (ratio < 1 || hb < 1) return NULL;
+    int64_t pool_blocks = (int64_t)ratio * R * D / hb;
+    return create(R, L, B, k, D, anchor_of_layer, host_capacity, hb, pool_blocks, track_bytes);
+}
+
+int32_t hso_pool_blocks(const hs_oracle *o) { return o->pool_blocks; }
+
+int32_t hso_free_blocks(const hs_oracle *o)
+{
+    int32_t n = 0;
+    for (int32_t b = 0; b < o->pool_blocks; ++b) n += !o->in_use[b];
+    return n;
+}
+
+/* Host row (in the layer's pool) of token t of request r; -1 when the
+ * token's block is not reserved. */
+static int64_t host_row_of(const hs_oracle *o, int r, int64_t t)
+{
+    if (o->hb == 0) return o->host_off[r] + t;
+    int32_t id = o->blocks[r][t / o->hb];
+    if (id < 0) return -1;
+    return (int64_t)id * o->hb + t % o->hb;
+}
+
+/* The plan's "host slot" of token t: its position within the request's
+ * region, or, with a paged pool, its row in the layer's pool. */
+static int32_t plan_host_slot(const hs_oracle *o, int r, int32_t t)
+{
+    return o->hb == 0 ? t : (int32_t)host_row_of(o, r, t);
+}
+
+/*
+ * Reserve host blocks ([Arch] Ownership: logical host block allocation
+ * belongs to the coordinator): for each i in order, request reqs[i] gets
+ * blocks until its table covers tokens [0, ntok[i]); each new table entry,
+ * in block order, takes the lowest-numbered free block.  All or nothing:
+ * returns -1 (bad request or length, nothing changed), -2 (too few free
+ * blocks, nothing changed) or 0.
+ */
+int hso_reserve(hs_oracle *o, int n, const int32_t *reqs, const int64_t *ntok)
+{
+    if (o->hb == 0 || n < 0) return -1;
+    int64_t *want = (int64_t *)calloc((size_t)o->R, sizeof(int64_t));
+    for (int r = 0; r < o->R; ++r) want[r] = o->nblocks[r];
+    for (int i = 0; i < n; ++i) {
+        if (reqs[i] < 0 || reqs[i] >= o->R || ntok[i] < 0 || ntok[i] > o->cap[reqs[i]]) {
+            free(want);
+            return -1;
+        }
+        int64_t nb = (ntok[i] + o->hb - 1) / o->hb;
+        if (nb > want[reqs[i]]) want[reqs[i]] = nb;
+    }
+    int64_t need = 0;
+    for (int r = 0; r < o->R; ++r) need += want[r] - o->nblocks[r];
+    free(want);
+    if (need > hso_free_blocks(o)) return -2;
+    for (int i = 0; i < n; ++i) {
+        int r = reqs[i];
+        int64_t nb = (ntok[i] + o->hb - 1) / o->hb;
+        while (o->nblocks[r] < nb) {
+            int32_t id = 0;
+            while (o->in_use[id]) ++id;
+            o->in_use[id] = 1;
+            o->blocks[r][o->nblocks[r]++] = id;
+        }
+    }
+    return 0;
+}
+
+/* Release every host block of each listed request; their table entries
+ * become -1.  The request's hot state is left as it is.  Returns -1 (bad
+ * request, nothing changed) or 0. */
+int hso_release(hs_oracle *o, int n, const int32_t *reqs)
+{
+    if (o->hb == 0 || n < 0) return -1;
+    for (int i = 0; i < n; ++i)
+        if (reqs[i] < 0 || reqs[i] >= o->R) return -1;
+    for (int i = 0; i < n; ++i) {
+        int r = reqs[i];
+        for (int32_t b = 0; b < o->nblocks[r]; ++b) {
+            o->in_use[o->blocks[r][b]] = 0;
+            o->blocks[r][b] = -1;
+        }
+        o->nblocks[r] = 0;
+    }
+    return 0;
+}
+
+/* Copy out request r's reserved block ids; returns how many there are. */
+int32_t hso_block_table(const hs_oracle *o, int r, int32_t *ids)
+{
+    if (o->hb == 0 || r < 0 || r >= o->R) return -1;
+    if (ids) memcpy(ids, o->blocks[r], sizeof(int32_t) * (size_t)o->nblocks[r]);
+    return o->nblocks[r];
+}
+
+/* Rows [hb][B] of host block `id` of a layer's paged pool. */
+uint8_t *hso_block_rows(hs_oracle *o, int layer, int32_t id)
+{
+    if (!o->track_bytes || o->hb == 0 || id < 0 || id >= o->pool_blocks) return NULL;
+    return o->host[layer] + (int64_t)id * o->hb * o->B;
+}
+
+/* Host row of token t of request r in a layer's pool (NULL when not
+ * tracking bytes, or when the token's host block is not reserved). */
 uint8_t *hso_host_row(hs_oracle *o, int layer, int r, int64_t t)
 {
     if (!o->track_bytes) return NULL;
-    return o->host[layer] + (o->host_off[r] + t) * o->B;
+    int64_t row = host_row_of(o, r, t);
+    return row < 0 ? NULL : o->host[layer] + row * o->B;
 }
 
 uint8_t *hso_dev_row(hs_oracle *o, int layer, int r, int64_t s)
@@ -152,18 +325,27 @@ static void copy_row(hs_oracle *o, int layer, int r, int32_t t, int32_t s)
 
 /*
  * Prefill: the hot buffer of every request starts with the most recent
- * n = min(S, D) tokens, slot i holding token S - n + i, all stamped 0.
- * ([Guide] Decode Workflow: for S <= D "all KV is already in the buffer",
- * which fixes slot = token in that case.)
+ * n = min(S, D) tokens, slot i holding token S - n + i, all stamped 0, and
+ * the request's tick restarts at 0.  ([Guide] Decode Workflow: for S <= D
+ * "all KV is already in the buffer", which fixes slot = token in that
+ * case.)  S = -1 leaves request r alone; S outside [0, capacity] sets
+ * BAD_SEQ_LEN and a row of the newest n tokens in a host block not reserved
+ * sets NO_HOST_ROW, both leaving the request untouched.  status may be NULL.
  */
-int hso_prefill(hs_oracle *o, const int32_t *seq_lens)
+int hso_prefill(hs_oracle *o, const int32_t *seq_lens, int32_t *status)
 {
-    for (int r = 0; r < o->R; ++r)
-        if (seq_lens[r] < 0 || seq_lens[r] > o->cap[r]) return -1;
-    for (int l = 0; l < o->L; ++l) {
-        for (int r = 0; r < o->R; ++r) {
-            int32_t S = seq_lens[r];
-            int32_t n = S < o->D ? S : o->D;
+    for (int r = 0; r < o->R; ++r) {
+        int32_t S = seq_lens[r];
+        if (S == -1) continue;
+        int32_t st = HSO_OK;
+        int32_t n = S < o->D ? S : o->D;
+        if (S < 0 || S > o->cap[r]) st = HSO_BAD_SEQ_LEN;
+        else
+            for (int32_t i = 0; i < n; ++i)
+                if (host_row_of(o, r, S - n + i) < 0) { st = HSO_NO_HOST_ROW; break; }
+        if (status) status[r] = st;
+        if (st != HSO_OK) continue;
+        for (int l = 0; l < o->L; ++l) {
             if (o->anchor[l] < 0) {
                 int32_t *t2s = o->tok2slot[l] + o->host_off[r];
                 int32_t *s2t = o->slot2tok[l] + (int64_t)r * o->D;
@@ -174,10 +356,10 @@ int hso_prefill(hs_oracle *o, const int32_t *seq_lens)
                     s2t[i] = S - n + i;
                     t2s[S - n + i] = i;
                 }
+                o->tick[l][r] = 0;
             }
             for (int32_t i = 0; i < n; ++i) copy_row(o, l, r, S - n + i, i);
         }
-        o->tick[l] = 0;
     }
     return 0;
 }
@@ -304,6 +486,15 @@ static void swap_in_request(hs_oracle *o, int a, int r, const int32_t *topk,
         if (t2s[t] >= 0) is_hit_slot[t2s[t]] = 1;
         else miss[m++] = t;
     }
+    /* Every miss needs its host row; with a paged pool its block must be
+     * reserved, else the request is left untouched. */
+    for (int i = 0; i < m; ++i)
+        if (host_row_of(o, r, miss[i]) < 0) {
+            *status = HSO_NO_HOST_ROW;
+            for (int j = 0; j < k; ++j) out[j] = -1;
+            free(done); free(is_hit_slot); free(miss);
+            return;
+        }
     /* Misses are handled in ascending token order. */
     qsort(miss, (size_t)m, sizeof(int32_t), cmp_i32);
 
@@ -321,7 +512,7 @@ static void swap_in_request(hs_oracle *o, int a, int r, const int32_t *topk,
         if (s2t[v] >= 0) t2s[s2t[v]] = -1;
         s2t[v] = t;
         t2s[t] = v;
-        plan[2 * i] = t;
+        plan[2 * i] = plan_host_slot(o, r, t);
         plan[2 * i + 1] = v;
         copy_row(o, a, r, t, v);
     }
@@ -351,8 +542,8 @@ int hso_swap_in_resident(hs_oracle *o, int layer, const int32_t *topk, const int
 {
     if (layer < 0 || layer >= o->L || o->anchor[layer] >= 0) return -1;
     if (resident_blocks && (max_blocks < 1 || block_size < 1)) return -1;
-    uint32_t tick = ++o->tick[layer];
     for (int r = 0; r < o->R; ++r) {
+        uint32_t tick = ++o->tick[layer][r];
         resident_table rt;
         rt.blocks = resident_blocks ? resident_blocks + (int64_t)r * max_blocks : NULL;
         rt.max_blocks = max_blocks;
@@ -372,16 +563,25 @@ int hso_swap_in(hs_oracle *o, int layer, const int32_t *topk, const int32_t *seq
 
 /*
  * Replay a recorded miss plan on another layer's KV storage
- * ([Guide] Shared-index prefetch): for every (token, slot) pair, copy that
- * layer's host row into that layer's device slot.  No map or LRU changes.
+ * ([Guide] Shared-index prefetch): for every (host slot, device slot) pair,
+ * copy that layer's host row into that layer's device slot.  No map or LRU
+ * changes.  A pair naming a row or slot out of range is skipped.
  */
 int hso_replay(hs_oracle *o, const int32_t *plan, const int32_t *count, int layer)
 {
     if (layer < 0 || layer >= o->L) return -1;
-    for (int r = 0; r < o->R; ++r)
-        for (int i = 0; i < count[r]; ++i)
-            copy_row(o, layer, r, plan[((int64_t)r * o->k + i) * 2],
-                     plan[((int64_t)r * o->k + i) * 2 + 1]);
+    if (!o->track_bytes) return 0;
+    for (int r = 0; r < o->R; ++r) {
+        int32_t c = count[r] < 0 ? 0 : (count[r] > o->k ? o->k : count[r]);
+        for (int i = 0; i < c; ++i) {
+            int32_t h = plan[((int64_t)r * o->k + i) * 2];
+            int32_t v = plan[((int64_t)r * o->k + i) * 2 + 1];
+            int64_t limit = o->hb == 0 ? o->cap[r] : o->host_rows;
+            if (h < 0 || h >= limit || v < 0 || v >= o->D) continue;
+            int64_t row = o->hb == 0 ? o->host_off[r] + h : h;
+            memcpy(hso_dev_row(o, layer, r, v), o->host[layer] + row * o->B, (size_t)o->B);
+        }
+    }
     return 0;
 }
 
@@ -403,6 +603,7 @@ int hso_backup(hs_oracle *o, int layer, const uint8_t *rows, const int32_t *posi
         status[r] = HSO_OK;
         if (p == -1) continue;
         if (p < 0 || p >= o->cap[r]) { status[r] = HSO_BAD_POSITION; continue; }
+        if (host_row_of(o, r, p) < 0) { status[r] = HSO_NO_HOST_ROW; continue; }
         if (o->track_bytes)
             memcpy(hso_host_row(o, layer, r, p), rows + (int64_t)r * o->B, (size_t)o->B);
         if (p < o->D) {
@@ -422,7 +623,7 @@ int hso_backup(hs_oracle *o, int layer, const uint8_t *rows, const int32_t *posi
     return 0;
 }
 
-/* Copy out a hot-state layer's maps, LRU stamps and tick. */
+/* Copy out a hot-state layer's maps, LRU stamps and per-request ticks. */
 int hso_state(hs_oracle *o, int layer, int32_t *slot2tok, uint32_t *last_used,
               int32_t *tok2slot, uint32_t *tick)
 {
@@ -431,7 +632,7 @@ int hso_state(hs_oracle *o, int layer, int32_t *slot2tok, uint32_t *last_used,
     if (slot2tok) memcpy(slot2tok, o->slot2tok[layer], nd * sizeof(int32_t));
     if (last_used) memcpy(last_used, o->last_used[layer], nd * sizeof(uint32_t));
     if (tok2slot) memcpy(tok2slot, o->tok2slot[layer], (size_t)o->total_cap * sizeof(int32_t));
-    if (tick) *tick = o->tick[layer];
+    if (tick) memcpy(tick, o->tick[layer], (size_t)o->R * sizeof(uint32_t));
     return 0;
 }
 

@@ -16,6 +16,7 @@ import pytest
 import oracle as O
 from golden_trace import names
 import test_oracle as T
+import test_oracle_paged as TP
 
 SRC = os.path.join(os.path.dirname(O.__file__), "hisparse_oracle.c")
 
@@ -46,14 +47,14 @@ MUTANTS = [
      "s2t[i] = S - n + i;\n                    t2s[S - n + i] = i;",
      "s2t[i] = i;\n                    t2s[i] = i;"),
     ("tick_not_advanced",
-     "uint32_t tick = ++o->tick[layer];",
-     "uint32_t tick = o->tick[layer] + 1;"),
+     "uint32_t tick = ++o->tick[layer][r];",
+     "uint32_t tick = o->tick[layer][r] + 1;"),
     ("copy_transposed",
      "copy_row(o, a, r, t, v);",
      "copy_row(o, a, r, v, t);"),
     ("plan_transposed",
-     "plan[2 * i] = t;\n        plan[2 * i + 1] = v;",
-     "plan[2 * i] = v;\n        plan[2 * i + 1] = t;"),
+     "plan[2 * i] = plan_host_slot(o, r, t);\n        plan[2 * i + 1] = v;",
+     "plan[2 * i] = v;\n        plan[2 * i + 1] = plan_host_slot(o, r, t);"),
     ("duplicates_accepted",
      "if (v[i] == v[i - 1]) { st = HSO_DUPLICATE; break; }",
      ";"),
@@ -64,8 +65,8 @@ MUTANTS = [
      "memcpy(hso_dev_row(o, layer, r, p), rows + (int64_t)r * o->B, (size_t)o->B);",
      ";"),
     ("replay_wrong_layer",
-     "copy_row(o, layer, r, plan[((int64_t)r * o->k + i) * 2],",
-     "copy_row(o, 0, r, plan[((int64_t)r * o->k + i) * 2],"),
+     "memcpy(hso_dev_row(o, layer, r, v), o->host[layer] + row * o->B, (size_t)o->B);",
+     "memcpy(hso_dev_row(o, 0, r, v), o->host[layer] + row * o->B, (size_t)o->B);"),
     ("resident_after_hot",
      "        if (row >= 0) {\n            out[j] = (int32_t)(HSO_RESIDENT_FLAG | row);",
      "        if (row >= 0 && (S <= D || o->tok2slot[a][o->host_off[r] + topk[j]] < 0)) {\n"
@@ -80,6 +81,36 @@ MUTANTS = [
     ("resident_row_offset_dropped",
      "return (int64_t)rt->blocks[b] * rt->block_size + t % rt->block_size;",
      "return (int64_t)rt->blocks[b] * rt->block_size;"),
+    ("paged_row_offset_dropped",
+     "return (int64_t)id * o->hb + t % o->hb;",
+     "return (int64_t)id * o->hb;"),
+    ("paged_highest_free_first",
+     "int32_t id = 0;\n            while (o->in_use[id]) ++id;",
+     "int32_t id = o->pool_blocks - 1;\n            while (o->in_use[id]) --id;"),
+    ("paged_partial_reservation",
+     "    if (need > hso_free_blocks(o)) return -2;\n",
+     ""),
+    ("paged_release_keeps_blocks",
+     "            o->in_use[o->blocks[r][b]] = 0;\n",
+     ""),
+    ("paged_plan_records_token",
+     "return o->hb == 0 ? t : (int32_t)host_row_of(o, r, t);",
+     "return t;"),
+    ("paged_pool_rounds_up",
+     "int64_t pool_blocks = (int64_t)ratio * R * D / hb;",
+     "int64_t pool_blocks = ((int64_t)ratio * R * D + hb - 1) / hb;"),
+    ("paged_missing_row_not_reported",
+     "            *status = HSO_NO_HOST_ROW;\n            for (int j = 0; j < k; ++j) out[j] = -1;\n            free(done); free(is_hit_slot); free(miss);\n            return;",
+     "            break;"),
+    ("paged_backup_without_block",
+     "        if (host_row_of(o, r, p) < 0) { status[r] = HSO_NO_HOST_ROW; continue; }\n",
+     ""),
+    ("prefill_without_rows",
+     "                if (host_row_of(o, r, S - n + i) < 0) { st = HSO_NO_HOST_ROW; break; }",
+     "                ;"),
+    ("prefill_resets_other_requests",
+     "        if (S == -1) continue;",
+     "        if (S == -1) S = 0;"),
 ]
 
 
@@ -109,6 +140,11 @@ def run_all_pins(lib_path):
             T.test_random_resident_tables_vs_list_model(seed, lib_path)
         except Exception:
             failed.append(f"resident_random:{seed}")
+    for pin in TP.PAGED_PINS:
+        try:
+            pin(lib_path)
+        except Exception:
+            failed.append(pin.__name__)
     return failed
 
 
