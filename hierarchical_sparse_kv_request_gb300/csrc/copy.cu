@@ -12,15 +12,17 @@ namespace {
 constexpr int REPLAY_NT = 512;
 constexpr int REPLAY_UNROLL = 8;
 
-// Copy every (token -> slot) pair of a plan, host row -> device slot, for
-// each of a list of layers.  Work items are 16-byte chunks of the rows,
-// numbered layer by layer over the concatenation of all requests' plan rows;
+// Copy every (host slot -> device slot) pair of a plan, host row -> device
+// slot, for each of a list of layers.  A host slot is a token position in the
+// request's region, or, with a paged host pool, a row of the layer's pool.
+// Work items are 16-byte chunks of the rows, numbered layer by layer over
+// the concatenation of all requests' plan rows;
 // each CTA first builds the prefix sum of plan counts in shared memory
 // (clamped to [0, k]), then walks its items with REPLAY_UNROLL host loads in
 // flight per thread.  One launch covers all the skip layers of an anchor, so
 // its few CTAs are placed once, ahead of the compute they overlap, and stay
-// until every layer is copied.  Pairs whose token or slot is out of range are
-// skipped.
+// until every layer is copied.  Pairs whose host slot or device slot is out of
+// range are skipped.
 __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
 {
     extern __shared__ __align__(16) uint32_t rows_before[];  // [R + 1]
@@ -77,9 +79,11 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
             const int r = lo;
             const uint32_t i = row - rows_before[r];
             const int32_t *pr = a.plan_rows + ((int64_t)r * k + i) * 2;
-            const int32_t tok = pr[0], slot = pr[1];
-            if (tok < 0 || (int64_t)tok >= a.g.host_cap[r] || slot < 0 || slot >= D) continue;
-            src[u] = a.store[layer].host + (a.g.host_off[r] + tok) * B + c * 16;
+            const int32_t hslot = pr[0], slot = pr[1];
+            const int64_t limit = a.g.hb ? a.g.pool_rows : a.g.host_cap[r];
+            if (hslot < 0 || (int64_t)hslot >= limit || slot < 0 || slot >= D) continue;
+            const int64_t hrow = a.g.hb ? (int64_t)hslot : a.g.host_off[r] + hslot;
+            src[u] = a.store[layer].host + hrow * B + c * 16;
             dst[u] = a.store[layer].dev + ((int64_t)r * D + slot) * B + c * 16;
         }
         uint4 v[REPLAY_UNROLL];
@@ -106,10 +110,16 @@ __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
         if (c == 0) a.status[r] = kStatusBadPosition;
         return;
     }
+    // with a paged host pool the position's block must be reserved
+    const int64_t row = host_row_of(a.g, r, p);
+    if (row < 0) {
+        if (c == 0) a.status[r] = kStatusNoHostRow;
+        return;
+    }
     const int64_t B = a.g.B;
     const int D = a.g.D;
     const uint4 v = ld_dev_v4(a.rows + (int64_t)r * B + c * 16);
-    st_v4(a.host + (a.g.host_off[r] + p) * B + c * 16, v);
+    st_v4(a.host + row * B + c * 16, v);
     if (p < D) {
         st_v4(a.dev + ((int64_t)r * D + p) * B + c * 16, v);
         if (c == 0 && a.st.tok2slot) {
@@ -126,7 +136,9 @@ __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
 
 // Prefill: grid (blocks per request, R, L).  For request r, n = min(S, D):
 // slot i <- token S-n+i.  Every map entry is written with its final value,
-// so blocks never race.
+// so blocks never race.  With a paged host pool every block of tokens
+// [S-n, S) must be reserved; each CTA checks that itself, so either all of a
+// request's CTAs write or none does.
 __global__ void __launch_bounds__(256) prefill_kernel(const int32_t *seq_lens,
                                                       const LayerDescDev *layers, Geometry g,
                                                       int32_t *status)
@@ -139,10 +151,22 @@ __global__ void __launch_bounds__(256) prefill_kernel(const int32_t *seq_lens,
         if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusBadSeqLen;
         return;
     }
-    if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusOk;
-    const LayerDescDev L = layers[l];
     const int D = g.D;
     const int32_t n = S < D ? S : D;
+    if (g.hb) {
+        bool missing = false;
+        if (n > 0) {
+            const int32_t b0 = (S - n) / g.hb, b1 = (S - 1) / g.hb;
+            for (int32_t b = b0 + (int32_t)threadIdx.x; b <= b1; b += blockDim.x)
+                missing |= g.host_tbl[(int64_t)r * g.tbl_stride + b] < 0;
+        }
+        if (__syncthreads_or(missing)) {
+            if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusNoHostRow;
+            return;
+        }
+    }
+    if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusOk;
+    const LayerDescDev L = layers[l];
     const int64_t off = g.host_off[r];
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t gs = (int64_t)gridDim.x * blockDim.x;
@@ -166,14 +190,31 @@ __global__ void __launch_bounds__(256) prefill_kernel(const int32_t *seq_lens,
     for (int64_t e = gt; e < total; e += gs) {
         const int64_t i = e / CH;
         const int c = (int)(e - i * CH);
-        const uint4 v = ld_host_v4(L.host + (off + S - n + i) * B + c * 16);
+        const uint4 v = ld_host_v4(L.host + host_row_of(g, r, S - n + i) * B + c * 16);
         st_v4(L.dev + ((int64_t)r * D + i) * B + c * 16, v);
     }
+}
+
+// Host block table edits: one CTA per run.
+__global__ void __launch_bounds__(128) table_runs_kernel(int32_t *table, TableRuns runs)
+{
+    const int i = blockIdx.x;
+    if (i >= runs.n) return;
+    const int32_t first = runs.first[i], value = runs.value[i], len = runs.len[i];
+    for (int32_t j = threadIdx.x; j < len; j += blockDim.x)
+        table[first + j] = value < 0 ? -1 : value + j;
 }
 
 }  // namespace
 
 size_t replay_smem_bytes(int R) { return (size_t)(R + 1) * 4; }
+
+cudaError_t launch_table_runs(int32_t *table, const TableRuns &runs, cudaStream_t s)
+{
+    if (runs.n <= 0) return cudaSuccess;
+    table_runs_kernel<<<runs.n, 128, 0, s>>>(table, runs);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s)
 {

@@ -8,6 +8,7 @@
 // invariants: no device readback, one kernel per call.  [Guide] "HiSparse:
 // Hierarchical Sparse Attention", HiSparse Config Parameters: top_k,
 // device_buffer_size, host_to_device_ratio, swap_in_block_size.
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -27,7 +28,7 @@ struct hisparse_handle {
     std::vector<int32_t> anchor;
     std::vector<int64_t> cap, off;
     int64_t total_cap = 0, max_cap = 0;
-    uint8_t *host_pool = nullptr;      // pinned [L][total_cap][B]
+    uint8_t *host_pool = nullptr;      // pinned [L][layer_rows()][B]
     uint8_t *host_pool_dev = nullptr;  // the same memory, device address
     uint8_t *dev_buf = nullptr;        // [L][R][D][B]
     int64_t *d_off = nullptr, *d_cap = nullptr;
@@ -39,6 +40,24 @@ struct hisparse_handle {
     int32_t *d_deferred = nullptr;     // [R] requests left to the copy grid (auto mode)
     int32_t copy_mode = HISPARSE_COPY_FUSED;
     bool stage_s2t = false;   // resolve kernel stages the slot->token row
+
+    // Paged host pool (hb > 0): pool_blocks blocks of hb rows per layer,
+    // handed to requests by hisparse_host_reserve.  `tbl` is the host copy of
+    // the block table [R][tbl_stride] (the device copy, d_tbl, follows it in
+    // stream order); a request's reserved blocks are the first nblocks[r]
+    // entries of its row.
+    int32_t hb = 0;
+    int32_t pool_blocks = 0;
+    int32_t tbl_stride = 0;
+    int64_t pool_rows = 0;
+    std::vector<int32_t> tbl;
+    std::vector<int32_t> nblocks;
+    std::vector<uint64_t> used;        // one bit per block; bits past the pool are set
+    int32_t free_blocks = 0;
+    int32_t lowest_free = 0;           // no block below this id is free
+    int32_t *d_tbl = nullptr;
+
+    int64_t layer_rows() const { return hb ? pool_rows : total_cap; }
 };
 
 namespace {
@@ -62,13 +81,17 @@ hs::Geometry geometry(const hisparse_handle *h)
     g.chunks = h->chunks;
     g.host_off = h->d_off;
     g.host_cap = h->d_cap;
+    g.host_tbl = h->d_tbl;
+    g.hb = h->hb;
+    g.tbl_stride = h->tbl_stride;
+    g.pool_rows = h->pool_rows;
     return g;
 }
 
 hs::LayerStore layer_store(const hisparse_handle *h, int layer)
 {
     hs::LayerStore s;
-    s.host = h->host_pool_dev + (int64_t)layer * h->total_cap * h->B;
+    s.host = h->host_pool_dev + (int64_t)layer * h->layer_rows() * h->B;
     s.dev = h->dev_buf + (int64_t)layer * h->R * h->D * h->B;
     return s;
 }
@@ -110,12 +133,15 @@ void release(hisparse_handle *h)
     cudaFree(h->d_zero);
     cudaFree(h->d_off);
     cudaFree(h->d_cap);
+    cudaFree(h->d_tbl);
     cudaFree(h->dev_buf);
     if (h->host_pool) cudaFreeHost(h->host_pool);
     delete h;
 }
 
-int validate_layout(const hisparse_layout *l)
+// Checks of a layout; `paged` drops the bound on summed capacities (a paged
+// pool bounds the rows themselves).
+int validate_layout(const hisparse_layout *l, bool paged)
 {
     if (l->num_requests < 1 || l->num_layers < 1 || l->row_bytes <= 0 || l->top_k < 1 ||
         l->device_buffer_size < 1 || l->host_to_device_ratio < 1 || l->swap_in_block_size < 0)
@@ -143,9 +169,66 @@ int validate_layout(const hisparse_layout *l)
     }
     if (total < 1) return HISPARSE_ERR_LAYOUT;
     const int64_t limit = (int64_t)l->host_to_device_ratio * l->num_requests * l->device_buffer_size;
-    if (total > limit) return HISPARSE_ERR_CAPACITY;
+    if (!paged && total > limit) return HISPARSE_ERR_CAPACITY;
     return HISPARSE_OK;
 }
+
+// Lowest free block of the pool (the caller checked free_blocks > 0).
+int32_t take_lowest_free(hisparse_handle *h)
+{
+    size_t w = (size_t)h->lowest_free / 64;
+    while (h->used[w] == ~0ull) ++w;
+    const int32_t id = (int32_t)(w * 64 + __builtin_ctzll(~h->used[w]));
+    h->used[w] |= 1ull << (id % 64);
+    --h->free_blocks;
+    h->lowest_free = id + 1;
+    return id;
+}
+
+void give_back(hisparse_handle *h, int32_t id)
+{
+    h->used[id / 64] &= ~(1ull << (id % 64));
+    ++h->free_blocks;
+    h->lowest_free = std::min(h->lowest_free, id);
+}
+
+// Table edits, merged into runs and applied on the stream, 128 runs a launch.
+struct RunList {
+    std::vector<int32_t> first, value, len;
+    void add(int32_t idx, int32_t id)
+    {
+        const size_t n = first.size();
+        if (n && value[n - 1] >= 0 && first[n - 1] + len[n - 1] == idx &&
+            value[n - 1] + len[n - 1] == id) {
+            ++len[n - 1];
+            return;
+        }
+        first.push_back(idx);
+        value.push_back(id);
+        len.push_back(1);
+    }
+    void clear_range(int32_t idx, int32_t count)
+    {
+        first.push_back(idx);
+        value.push_back(-1);
+        len.push_back(count);
+    }
+    cudaError_t apply(int32_t *table, cudaStream_t s) const
+    {
+        for (size_t i0 = 0; i0 < first.size(); i0 += hs::kTableRuns) {
+            hs::TableRuns tr;
+            tr.n = (int32_t)std::min(first.size() - i0, (size_t)hs::kTableRuns);
+            for (int32_t i = 0; i < tr.n; ++i) {
+                tr.first[i] = first[i0 + i];
+                tr.value[i] = value[i0 + i];
+                tr.len[i] = len[i0 + i];
+            }
+            const cudaError_t e = hs::launch_table_runs(table, tr, s);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+};
 
 }  // namespace
 
@@ -159,7 +242,8 @@ const char *hisparse_error_string(int code)
     case HISPARSE_OK: return "ok";
     case HISPARSE_ERR_INVALID_ARG: return "invalid argument";
     case HISPARSE_ERR_LAYOUT: return "inconsistent layout";
-    case HISPARSE_ERR_CAPACITY: return "host capacity exceeds host_to_device_ratio * R * D";
+    case HISPARSE_ERR_CAPACITY:
+        return "host capacity exceeds host_to_device_ratio * R * D (or too few free host blocks)";
     case HISPARSE_ERR_LAYER: return "layer out of range or without hot state";
     case HISPARSE_ERR_CUDA: return "CUDA runtime error";
     case HISPARSE_ERR_NO_MEMORY: return "out of pinned or device memory";
@@ -169,13 +253,28 @@ const char *hisparse_error_string(int code)
     }
 }
 
-int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
+}  // extern "C"
+
+namespace {
+
+int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hisparse_t *out)
 {
     if (!out) return HISPARSE_ERR_INVALID_ARG;
     *out = nullptr;
     if (!layout) return HISPARSE_ERR_INVALID_ARG;
-    int rc = validate_layout(layout);
+    const bool paged = host_block_tokens != 0;
+    int rc = validate_layout(layout, paged);
     if (rc != HISPARSE_OK) return rc;
+    int64_t pool_blocks = 0;
+    if (paged) {
+        if (host_block_tokens < 1) return HISPARSE_ERR_LAYOUT;
+        if (host_block_tokens > HISPARSE_MAX_HOST_BLOCK_TOKENS) return HISPARSE_ERR_UNSUPPORTED;
+        // [Arch] Ownership: the budget is rounded down to whole host blocks
+        pool_blocks = (int64_t)layout->host_to_device_ratio * layout->num_requests *
+                      layout->device_buffer_size / host_block_tokens;
+        if (pool_blocks < 1) return HISPARSE_ERR_CAPACITY;
+        if (pool_blocks * host_block_tokens > INT32_MAX) return HISPARSE_ERR_UNSUPPORTED;
+    }
 
     hisparse_handle *h = new (std::nothrow) hisparse_handle;
     if (!h) return HISPARSE_ERR_NO_MEMORY;
@@ -195,6 +294,19 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
         h->total_cap += h->cap[r];
         if (h->cap[r] > h->max_cap) h->max_cap = h->cap[r];
     }
+    if (paged) {
+        h->hb = host_block_tokens;
+        h->pool_blocks = (int32_t)pool_blocks;
+        h->pool_rows = pool_blocks * host_block_tokens;
+        const int64_t per_req = (h->max_cap + h->hb - 1) / h->hb;
+        h->tbl_stride = (int32_t)std::max<int64_t>(4, (per_req + 3) / 4 * 4);
+        h->tbl.assign((size_t)h->R * h->tbl_stride, -1);
+        h->nblocks.assign(h->R, 0);
+        h->used.assign((size_t)(pool_blocks + 63) / 64, 0ull);
+        for (int64_t b = pool_blocks; b < (int64_t)h->used.size() * 64; ++b)
+            h->used[b / 64] |= 1ull << (b % 64);
+        h->free_blocks = h->pool_blocks;
+    }
 
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -203,13 +315,14 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
     }
     int max_smem = 0;
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
-    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, false) > (size_t)max_smem ||
+    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, false, h->tbl_stride) > (size_t)max_smem ||
         hs::replay_smem_bytes(h->R) > (size_t)max_smem) {
         release(h);
         return HISPARSE_ERR_UNSUPPORTED;
     }
     // the slot->token row rides in shared memory when it fits
-    h->stage_s2t = hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, true) <= (size_t)max_smem;
+    h->stage_s2t = hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, true, h->tbl_stride) <=
+                   (size_t)max_smem;
     if (hs::resolve_prepare((size_t)max_smem) != cudaSuccess) {
         release(h);
         return HISPARSE_ERR_CUDA;
@@ -217,7 +330,7 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
 
     // Pinned host pool, mapped into the device address space.  A test hook
     // makes this allocation fail on request so the failure path is exercised.
-    const size_t pool_bytes = (size_t)h->L * h->total_cap * h->B;
+    const size_t pool_bytes = (size_t)h->L * h->layer_rows() * h->B;
     const char *fail = std::getenv("HISPARSE_TEST_FAIL_PINNED_ALLOC");
     if ((fail && fail[0] == '1') ||
         cudaHostAlloc(reinterpret_cast<void **>(&h->host_pool), pool_bytes,
@@ -244,7 +357,8 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
               dev_alloc(&h->d_layers, (size_t)h->L) == cudaSuccess &&
               dev_alloc(&h->d_plan_rows, (size_t)h->R * h->k * 2) == cudaSuccess &&
               dev_alloc(&h->d_plan_counts, (size_t)h->R) == cudaSuccess &&
-              dev_alloc(&h->d_deferred, (size_t)h->R) == cudaSuccess;
+              dev_alloc(&h->d_deferred, (size_t)h->R) == cudaSuccess &&
+              (!paged || dev_alloc(&h->d_tbl, h->tbl.size()) == cudaSuccess);
     h->state.assign(h->L, hs::HotState{nullptr, nullptr, nullptr, nullptr, nullptr});
     for (int l = 0; ok && l < h->L; ++l) {
         if (h->anchor[l] >= 0) continue;
@@ -276,6 +390,7 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t) * h->R);
     if (e == cudaSuccess) e = cudaMemset(h->d_plan_counts, 0, sizeof(int32_t) * h->R);
     if (e == cudaSuccess) e = cudaMemset(h->d_deferred, 0, sizeof(int32_t) * h->R);
+    if (e == cudaSuccess && paged) e = cudaMemset(h->d_tbl, 0xFF, sizeof(int32_t) * h->tbl.size());
     // empty hot state: seq_len 0 everywhere (maps -1, LRU in slot order, ticks 0)
     if (e == cudaSuccess) e = hs::launch_prefill(h->d_zero, h->d_layers, h->L, geometry(h), h->d_status, nullptr);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -287,6 +402,104 @@ int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
     return HISPARSE_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int hisparse_create(const hisparse_layout *layout, hisparse_t *out)
+{
+    return create_impl(layout, 0, out);
+}
+
+int hisparse_create_paged(const hisparse_layout *layout, int32_t host_block_tokens, hisparse_t *out)
+{
+    if (out) *out = nullptr;
+    if (host_block_tokens < 1) return out ? HISPARSE_ERR_LAYOUT : HISPARSE_ERR_INVALID_ARG;
+    return create_impl(layout, host_block_tokens, out);
+}
+
+int hisparse_host_reserve(hisparse_t h, int32_t n, const int32_t *requests,
+                          const int64_t *num_tokens, void *stream)
+{
+    if (!h || !h->hb || n < 0 || (n > 0 && (!requests || !num_tokens)))
+        return HISPARSE_ERR_INVALID_ARG;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
+    std::vector<int32_t> want(h->nblocks);
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t r = requests[i];
+        if (r < 0 || r >= h->R || num_tokens[i] < 0 || num_tokens[i] > h->cap[r])
+            return HISPARSE_ERR_INVALID_ARG;
+        const int64_t nb = (num_tokens[i] + h->hb - 1) / h->hb;
+        want[r] = (int32_t)std::max<int64_t>(want[r], nb);
+    }
+    int64_t need = 0;
+    for (int32_t r = 0; r < h->R; ++r) need += want[r] - h->nblocks[r];
+    if (need > h->free_blocks) return HISPARSE_ERR_CAPACITY;
+    // [Arch] Ownership: logical host block allocation; the lowest free block
+    // goes to each new table entry, in the order asked
+    RunList runs;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t r = requests[i];
+        const int64_t nb = (num_tokens[i] + h->hb - 1) / h->hb;
+        while (h->nblocks[r] < nb) {
+            const int32_t idx = r * h->tbl_stride + h->nblocks[r]++;
+            h->tbl[idx] = take_lowest_free(h);
+            runs.add(idx, h->tbl[idx]);
+        }
+    }
+    return cuda_status(runs.apply(h->d_tbl, as_stream(stream)));
+}
+
+int hisparse_host_release(hisparse_t h, int32_t n, const int32_t *requests, void *stream)
+{
+    if (!h || !h->hb || n < 0 || (n > 0 && !requests)) return HISPARSE_ERR_INVALID_ARG;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        if (requests[i] < 0 || requests[i] >= h->R) return HISPARSE_ERR_INVALID_ARG;
+    RunList runs;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t r = requests[i];
+        if (h->nblocks[r] == 0) continue;
+        for (int32_t b = 0; b < h->nblocks[r]; ++b) {
+            give_back(h, h->tbl[r * h->tbl_stride + b]);
+            h->tbl[r * h->tbl_stride + b] = -1;
+        }
+        runs.clear_range(r * h->tbl_stride, h->nblocks[r]);
+        h->nblocks[r] = 0;
+    }
+    return cuda_status(runs.apply(h->d_tbl, as_stream(stream)));
+}
+
+int hisparse_host_block_table(hisparse_t h, int32_t request, int32_t *ids, int32_t max_ids,
+                              int32_t *count)
+{
+    if (!h || !h->hb || !count || max_ids < 0 || (max_ids > 0 && !ids)) return HISPARSE_ERR_INVALID_ARG;
+    if (request < 0 || request >= h->R) return HISPARSE_ERR_INVALID_ARG;
+    *count = h->nblocks[request];
+    const int32_t n = std::min(max_ids, h->nblocks[request]);
+    if (n > 0) std::memcpy(ids, &h->tbl[(size_t)request * h->tbl_stride], sizeof(int32_t) * n);
+    return HISPARSE_OK;
+}
+
+int hisparse_host_pool_info(hisparse_t h, int32_t *block_tokens, int32_t *pool_blocks,
+                            int32_t *free_blocks)
+{
+    if (!h) return HISPARSE_ERR_INVALID_ARG;
+    if (block_tokens) *block_tokens = h->hb;
+    if (pool_blocks) *pool_blocks = h->pool_blocks;
+    if (free_blocks) *free_blocks = h->free_blocks;
+    return HISPARSE_OK;
+}
+
+int hisparse_host_block_rows(hisparse_t h, int32_t layer, int32_t block, void **host_ptr)
+{
+    if (!h || !h->hb || !host_ptr) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
+    if (block < 0 || block >= h->pool_blocks) return HISPARSE_ERR_INVALID_ARG;
+    *host_ptr = h->host_pool + ((int64_t)layer * h->pool_rows + (int64_t)block * h->hb) * h->B;
+    return HISPARSE_OK;
+}
+
 int hisparse_destroy(hisparse_t h)
 {
     release(h);
@@ -295,7 +508,7 @@ int hisparse_destroy(hisparse_t h)
 
 int hisparse_host_rows(hisparse_t h, int32_t layer, int32_t request, void **host_ptr)
 {
-    if (!h || !host_ptr) return HISPARSE_ERR_INVALID_ARG;
+    if (!h || !host_ptr || h->hb) return HISPARSE_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
     if (request < 0 || request >= h->R) return HISPARSE_ERR_INVALID_ARG;
     *host_ptr = h->host_pool + ((int64_t)layer * h->total_cap + h->off[request]) * h->B;

@@ -18,6 +18,7 @@ constexpr int kStatusDuplicate = 2;
 constexpr int kStatusBadSeqLen = 3;
 constexpr int kStatusBadPosition = 4;
 constexpr int kStatusBadResident = 5;
+constexpr int kStatusNoHostRow = 6;
 constexpr int32_t kResidentFlag = 1 << 30;  // marks a row of the resident pool
 
 // Hot state of one state-owning layer.  Per request r:
@@ -38,17 +39,35 @@ struct HotState {
 // Storage of one layer: the pinned host pool as seen from the device and
 // the device hot buffer.
 struct LayerStore {
-    const uint8_t *host;  // [total_cap][B] (device-visible pinned memory)
+    const uint8_t *host;  // [host rows][B] (device-visible pinned memory)
     uint8_t *dev;         // [R][D][B]
 };
 
+// host_off[r] is request r's first token->slot entry.  Without a paged pool
+// (hb == 0) it is also the first host row of the request's contiguous region
+// of host_cap[r] rows.  With a paged pool (hb > 0), token t of request r is
+// pool row host_tbl[r * tbl_stride + t / hb] * hb + t % hb, or has no host
+// row when that entry is -1; a pool holds pool_rows rows per layer.
 struct Geometry {
     int32_t R, k, D;
     int64_t B;             // multiple of 16
     int32_t chunks;        // B / 16
     const int64_t *host_off;  // device [R]
     const int64_t *host_cap;  // device [R]
+    const int32_t *host_tbl;  // device [R][tbl_stride] host block ids, or null
+    int32_t hb;               // token rows per host block; 0 = no paged pool
+    int32_t tbl_stride;       // multiple of 4 (16-byte rows)
+    int64_t pool_rows;
 };
+
+// Host row of token t of request r (see Geometry), or -1 when its block is
+// not reserved.
+__device__ __forceinline__ int64_t host_row_of(const Geometry &g, int r, int64_t t)
+{
+    if (g.hb == 0) return g.host_off[r] + t;
+    const int32_t id = g.host_tbl[(int64_t)r * g.tbl_stride + t / g.hb];
+    return id < 0 ? -1 : (int64_t)id * g.hb + t % g.hb;
+}
 
 // ---------------------------------------------------------------------------
 // Memory access helpers.
@@ -134,8 +153,9 @@ struct ResolveLaunch {
     int64_t defer_bytes;      // defer a request whose misses exceed this many bytes
 };
 
-// Shared-memory bytes the resolve kernel needs for this geometry.
-size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t);
+// Shared-memory bytes the resolve kernel needs for this geometry
+// (tbl_stride: the host block table row staged per request, 0 = none).
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int tbl_stride);
 int resolve_threads();
 // Allow every instantiation of the resolve kernel up to `smem` bytes of
 // dynamic shared memory (called at handle creation, outside any capture).
@@ -177,6 +197,18 @@ struct LayerDescDev {
 };
 cudaError_t launch_prefill(const int32_t *seq_lens, const LayerDescDev *layers, int num_layers,
                            const Geometry &g, int32_t *status, cudaStream_t s);
+
+// Runs of host block table entries to set: entry first[i] + j becomes
+// value[i] + j for j < len[i], or -1 for every j when value[i] < 0.  Passed
+// by value, so a launch needs no host buffer that outlives the call.
+constexpr int kTableRuns = 128;
+struct TableRuns {
+    int32_t n;
+    int32_t first[kTableRuns];
+    int32_t value[kTableRuns];
+    int32_t len[kTableRuns];
+};
+cudaError_t launch_table_runs(int32_t *table, const TableRuns &runs, cudaStream_t s);
 
 cudaError_t launch_synthetic_compute(void *buf, int64_t bytes, int32_t passes, int32_t ctas,
                                      cudaStream_t s);

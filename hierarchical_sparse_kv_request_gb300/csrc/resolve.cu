@@ -20,6 +20,12 @@
 //      they are issued before the prefetched rows are consumed, then every
 //      thread streams the rest of the rows.
 //
+// With a paged host pool ([Arch] Ownership: tokens map to logical host
+// blocks), the request's host block table row is staged as well, under the
+// token->slot round trip; a miss whose block is not reserved stops the call
+// for that request (status NO_HOST_ROW), and miss rows are addressed, and
+// recorded in the plan, by their row in the layer's pool.
+//
 // Exact LRU without sorting.  The request's slots are kept in a list `lru`
 // ordered by (last_used, slot).  One call stamps every selected slot (hits and
 // refilled victims) with a new, larger tick, so afterwards the list is
@@ -42,13 +48,14 @@ constexpr int COPY_UNROLL = 8; // host chunks in flight per thread in the copy l
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct SmemPlan {
-    size_t hit, sel, miss, lru, s2t, chunk, vict, mtok, total;
+    size_t hit, sel, miss, lru, s2t, tbl, chunk, vict, mtok, total;
 };
 
 // Shared memory of the CTA: bitmaps over slots and tokens, the staged LRU
-// list, optionally the staged slot->token row, and miss tokens and victims
-// by miss rank.
-__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t)
+// list, optionally the staged slot->token row and host block table row, and
+// miss rows and victims by miss rank.
+__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t,
+                                              int tbl_stride)
 {
     SmemPlan p;
     const size_t DW = (size_t)(D + 31) / 32, MW = (size_t)(max_cap + 31) / 32;
@@ -58,6 +65,7 @@ __host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool st
     p.miss = o;  o += MW * 4;
     p.lru = align_up(o, 16); o = p.lru + align_up((size_t)D * 2, 16);
     p.s2t = o;   o += stage_s2t ? align_up((size_t)D * 4, 16) : 0;
+    p.tbl = o;   o += (size_t)tbl_stride * 4;   // a multiple of 16
     p.chunk = o; o = align_up(o + (size_t)NT * 2, 4);
     p.vict = o;  o = align_up(o + (size_t)k * 2, 4);
     p.mtok = o;  o += (size_t)k * 4;
@@ -72,9 +80,10 @@ struct Smem {
     uint32_t *missbits;  // [MW]  miss tokens (and, on the fast path, all tokens)
     uint16_t *lru_s;     // [D]   staged LRU list
     int32_t *s2t_s;      // [D]   staged slot->token row (null when not staged)
+    int32_t *tbl_s;      // [tbl_stride] staged host block table row (null: no paged pool)
     uint16_t *chunk_pre; // [NT]  misses before each thread's chunk of missbits
     uint16_t *victims;   // [k]   victim slot of miss rank i
-    int32_t *misstok;    // [k]   token of miss rank i
+    int32_t *misstok;    // [k]   host row of miss rank i (token, or pool row when paged)
 };
 
 __device__ __forceinline__ bool test_bit(const uint32_t *bits, int i)
@@ -137,7 +146,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int k = a.g.k, D = a.g.D;
     const int DW = (D + 31) >> 5;
 
-    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t);
+    const int32_t hb = a.g.hb;
+    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t, hb ? a.g.tbl_stride : 0);
     Smem sm;
     sm.warp_tot = reinterpret_cast<uint32_t *>(smem_raw);
     sm.hitbits = reinterpret_cast<uint32_t *>(smem_raw + sp.hit);
@@ -145,6 +155,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     sm.missbits = reinterpret_cast<uint32_t *>(smem_raw + sp.miss);
     sm.lru_s = reinterpret_cast<uint16_t *>(smem_raw + sp.lru);
     sm.s2t_s = a.stage_s2t ? reinterpret_cast<int32_t *>(smem_raw + sp.s2t) : nullptr;
+    sm.tbl_s = hb ? reinterpret_cast<int32_t *>(smem_raw + sp.tbl) : nullptr;
     sm.chunk_pre = reinterpret_cast<uint16_t *>(smem_raw + sp.chunk);
     sm.victims = reinterpret_cast<uint16_t *>(smem_raw + sp.vict);
     sm.misstok = reinterpret_cast<int32_t *>(smem_raw + sp.mtok);
@@ -219,6 +230,19 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     }
 
     // ---- slow path: hit detection ----------------------------------------
+    if (hb) {
+        // the host block ids of tokens [0, S): 16-byte rows of the table
+        // (the stride is a multiple of 4 entries and covers the capacity)
+        const int32_t *tbl = a.g.host_tbl + (int64_t)r * a.g.tbl_stride;
+        const int nq = (int)(((int64_t)S + 4LL * hb - 1) / (4LL * hb));
+        for (int i = tid; i < nq; i += NT) cp_async16(sm.tbl_s + i * 4, tbl + i * 4);
+        cp_async_commit();
+    }
+    // host row of token x: its position in the request's region, or its row
+    // in the layer's pool
+    auto host_slot = [&](int32_t x) -> int32_t {
+        return hb ? sm.tbl_s[x / hb] * hb + x % hb : x;
+    };
     int32_t *tok2slot = a.st.tok2slot + off;
     int32_t s[KT];
 #pragma unroll
@@ -240,7 +264,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     // Classify.  A resident position is marked in the token bitmap only to
     // catch duplicates; its bit is cleared again before the misses are
     // ranked, and it never touches the hot state.
-    bool bad = false, dup = false, badres = false;
+    bool bad = false, dup = false, badres = false, nohost = false;
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int32_t x = t[i];
@@ -248,6 +272,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (x < 0 || x >= S) { bad = true; continue; }
         rid[i] = resident_row(rid[i], x, a.res_block_size);   // now the row
         badres |= rid[i] == -2;
+        if (rid[i] == -1 && s[i] < 0 && hb) nohost |= sm.tbl_s[x / hb] < 0;
         if (rid[i] < 0 && s[i] >= 0) {
             const uint32_t bit = 1u << (s[i] & 31);
             dup |= (atomicOr(&sm.hitbits[s[i] >> 5], bit) & bit) != 0u;
@@ -259,11 +284,14 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     bad = __syncthreads_or(bad);
     dup = __syncthreads_or(dup);
     badres = __syncthreads_or(badres);
-    if (bad || dup || badres) {
+    nohost = __syncthreads_or(nohost);
+    if (bad || dup || badres || nohost) {
 #pragma unroll
         for (int i = 0; i < KT; ++i) rid[i] = -1;
         finish_untouched<KT>(a, r, t, rid,
-                             bad ? kStatusBadIndex : (dup ? kStatusDuplicate : kStatusBadResident),
+                             bad ? kStatusBadIndex
+                                 : (dup ? kStatusDuplicate
+                                        : (badres ? kStatusBadResident : kStatusNoHostRow)),
                              tick);
         return;
     }
@@ -306,7 +334,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
             while (bits) {
                 const int b = __ffs(bits) - 1;
                 bits &= bits - 1u;
-                sm.misstok[rank++] = w * 32 + b;
+                sm.misstok[rank++] = host_slot(w * 32 + b);
             }
         }
     }
@@ -319,7 +347,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     // grid launched behind this kernel: one SM alone moves them slowly.
     const bool defer = a.deferred && (int64_t)m * B > a.defer_bytes;
     const int total = (a.fused_copy && !defer) ? m * CH : 0;
-    const uint8_t *hrow0 = a.store.host + off * B;
+    const uint8_t *hrow0 = a.store.host + (hb ? 0 : off) * B;
     uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
     uint4 pv[PREFETCH];
 #pragma unroll
@@ -370,7 +398,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         out[j] = v;
         if (a.plan_rows) {
             int32_t *pr = a.plan_rows + ((int64_t)r * k + rank) * 2;
-            pr[0] = x;
+            pr[0] = host_slot(x);
             pr[1] = v;
         }
     }
@@ -441,9 +469,9 @@ cudaError_t prepare_kt(size_t smem)
 
 }  // namespace
 
-size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t)
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int tbl_stride)
 {
-    return plan_smem(k, D, max_cap, stage_s2t).total;
+    return plan_smem(k, D, max_cap, stage_s2t, tbl_stride).total;
 }
 
 int resolve_threads() { return NT; }
@@ -459,7 +487,8 @@ cudaError_t resolve_prepare(size_t smem)
 
 cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s)
 {
-    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t);
+    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t,
+                                           a.g.hb ? a.g.tbl_stride : 0);
     const int kt = (a.g.k + NT - 1) / NT;
     if (kt <= 1) return launch_kt<1>(a, s, smem);
     if (kt <= 2) return launch_kt<2>(a, s, smem);

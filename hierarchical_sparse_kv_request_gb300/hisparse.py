@@ -22,7 +22,7 @@ OK = 0
 ERR_INVALID_ARG, ERR_LAYOUT, ERR_CAPACITY, ERR_LAYER = -1, -2, -3, -4
 ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT = -5, -6, -7, -8
 STATUS_OK, STATUS_BAD_INDEX, STATUS_DUPLICATE, STATUS_BAD_SEQ_LEN, STATUS_BAD_POSITION = 0, 1, 2, 3, 4
-STATUS_BAD_RESIDENT = 5
+STATUS_BAD_RESIDENT, STATUS_NO_HOST_ROW = 5, 6
 RESIDENT_FLAG = 1 << 30
 COPY_FUSED, COPY_SPLIT, COPY_AUTO = 1, 2, 3
 
@@ -62,6 +62,12 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     sig = {
         "hisparse_create": [P, P],
+        "hisparse_create_paged": [P, I32, P],
+        "hisparse_host_reserve": [P, I32, P, P, P],
+        "hisparse_host_release": [P, I32, P, P],
+        "hisparse_host_block_table": [P, I32, P, I32, P],
+        "hisparse_host_pool_info": [P, P, P, P],
+        "hisparse_host_block_rows": [P, I32, I32, P],
         "hisparse_destroy": [P],
         "hisparse_host_rows": [P, I32, I32, P],
         "hisparse_device_buffer": [P, I32, P],
@@ -123,12 +129,16 @@ def _check(rc: int, what: str) -> None:
 
 
 class HiSparse:
-    """One handle of the swap-in resolver (see include/hisparse.h)."""
+    """One handle of the swap-in resolver (see include/hisparse.h).
+
+    host_block_tokens > 0 creates a paged host pool (hisparse_create_paged):
+    host_capacity then only bounds each request's length, and rows come from
+    blocks that host_reserve hands out."""
 
     def __init__(self, num_requests: int, num_layers: int, row_bytes: int, top_k: int,
                  device_buffer_size: int, host_to_device_ratio: int,
                  host_capacity: Sequence[int], anchor_of_layer: Optional[Sequence[int]] = None,
-                 swap_in_block_size: int = 960):
+                 swap_in_block_size: int = 960, host_block_tokens: int = 0):
         self.lib = load_library()
         self.R, self.L, self.B = num_requests, num_layers, row_bytes
         self.k, self.D = top_k, device_buffer_size
@@ -140,13 +150,19 @@ class HiSparse:
                      host_to_device_ratio, swap_in_block_size,
                      self.anchor.ctypes.data, self.cap.ctypes.data)
         h = ctypes.c_void_p()
-        _check(self.lib.hisparse_create(ctypes.byref(lay), ctypes.byref(h)), "hisparse_create")
+        self.hb = int(host_block_tokens)
+        if self.hb:
+            _check(self.lib.hisparse_create_paged(ctypes.byref(lay), self.hb, ctypes.byref(h)),
+                   "hisparse_create_paged")
+        else:
+            _check(self.lib.hisparse_create(ctypes.byref(lay), ctypes.byref(h)), "hisparse_create")
         self.h = h
 
     @classmethod
-    def for_workload(cls, w) -> "HiSparse":
+    def for_workload(cls, w, host_block_tokens: int = 0) -> "HiSparse":
         return cls(w.num_requests, w.num_layers, w.row_bytes, w.top_k, w.device_buffer_size,
-                   w.host_to_device_ratio, w.host_capacity, w.anchor_of_layer)
+                   w.host_to_device_ratio, w.host_capacity, w.anchor_of_layer,
+                   host_block_tokens=host_block_tokens)
 
     def close(self) -> None:
         if getattr(self, "h", None) and self.h.value:
@@ -171,6 +187,47 @@ class HiSparse:
         n = int(self.cap[request]) * self.B
         buf = (ctypes.c_uint8 * n).from_address(self.host_rows_ptr(layer, request))
         return np.frombuffer(buf, dtype=np.uint8).reshape(int(self.cap[request]), self.B)
+
+    # -- paged host pool ----------------------------------------------------
+    def host_reserve(self, requests, num_tokens, stream=None) -> None:
+        """Grow the block tables so request requests[i] covers tokens
+        [0, num_tokens[i]); raises HiSparseError (code ERR_CAPACITY when the
+        pool is short, nothing reserved)."""
+        q = np.ascontiguousarray(requests, dtype=np.int32)
+        n = np.ascontiguousarray(num_tokens, dtype=np.int64)
+        if q.shape != n.shape:
+            raise ValueError("requests and num_tokens differ in length")
+        _check(self.lib.hisparse_host_reserve(self.h, q.size, q.ctypes.data, n.ctypes.data,
+                                              _stream(stream)), "hisparse_host_reserve")
+
+    def host_release(self, requests, stream=None) -> None:
+        q = np.ascontiguousarray(requests, dtype=np.int32)
+        _check(self.lib.hisparse_host_release(self.h, q.size, q.ctypes.data, _stream(stream)),
+               "hisparse_host_release")
+
+    def host_block_table(self, request: int) -> np.ndarray:
+        cnt = ctypes.c_int32()
+        _check(self.lib.hisparse_host_block_table(self.h, request, None, 0, ctypes.byref(cnt)),
+               "hisparse_host_block_table")
+        ids = np.empty(max(cnt.value, 1), dtype=np.int32)
+        _check(self.lib.hisparse_host_block_table(self.h, request, ids.ctypes.data, cnt.value,
+                                                  ctypes.byref(cnt)), "hisparse_host_block_table")
+        return ids[: cnt.value].copy()
+
+    def host_pool_info(self):
+        """(host_block_tokens, pool_blocks, free_blocks)."""
+        v = [ctypes.c_int32() for _ in range(3)]
+        _check(self.lib.hisparse_host_pool_info(self.h, *[ctypes.byref(x) for x in v]),
+               "hisparse_host_pool_info")
+        return tuple(x.value for x in v)
+
+    def host_block_rows(self, layer: int, block: int) -> np.ndarray:
+        """Writable numpy view [host_block_tokens][B] of a pinned pool block."""
+        p = ctypes.c_void_p()
+        _check(self.lib.hisparse_host_block_rows(self.h, layer, block, ctypes.byref(p)),
+               "hisparse_host_block_rows")
+        buf = (ctypes.c_uint8 * (self.hb * self.B)).from_address(p.value)
+        return np.frombuffer(buf, dtype=np.uint8).reshape(self.hb, self.B)
 
     def device_buffer_ptr(self, layer: int) -> int:
         p = ctypes.c_void_p()

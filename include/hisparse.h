@@ -51,7 +51,8 @@ extern "C" {
 #define HISPARSE_OK 0
 #define HISPARSE_ERR_INVALID_ARG (-1)  /* null pointer, bad index, bad handle */
 #define HISPARSE_ERR_LAYOUT (-2)       /* inconsistent layout                 */
-#define HISPARSE_ERR_CAPACITY (-3)     /* host capacity beyond the ratio      */
+#define HISPARSE_ERR_CAPACITY (-3)     /* host capacity beyond the ratio, or
+                                          too few free host blocks           */
 #define HISPARSE_ERR_LAYER (-4)        /* layer out of range / has no state   */
 #define HISPARSE_ERR_CUDA (-5)         /* a CUDA runtime call failed          */
 #define HISPARSE_ERR_NO_MEMORY (-6)    /* pinned or device allocation failed  */
@@ -65,6 +66,8 @@ extern "C" {
 #define HISPARSE_STATUS_BAD_SEQ_LEN 3  /* seq_len outside [0, host_capacity]  */
 #define HISPARSE_STATUS_BAD_POSITION 4 /* backup position outside [0, cap)    */
 #define HISPARSE_STATUS_BAD_RESIDENT 5 /* resident block id < -1 or too large */
+#define HISPARSE_STATUS_NO_HOST_ROW 6  /* paged pool: a needed host row lies in
+                                          a block the request has not reserved */
 
 /* A slot ID with this bit set names a row of the caller's resident pool
  * (see hisparse_swap_in_resident); hot slots are below D. */
@@ -75,6 +78,7 @@ extern "C" {
 #define HISPARSE_MAX_DEVICE_BUFFER 32768
 #define HISPARSE_MAX_HOST_CAPACITY (1 << 20) /* tokens per request          */
 #define HISPARSE_MAX_REQUESTS 8192
+#define HISPARSE_MAX_HOST_BLOCK_TOKENS 65536
 
 /* Copy strategy of hisparse_swap_in (see hisparse_set_copy_mode). */
 #define HISPARSE_COPY_FUSED 1  /* the resolving CTA copies its own misses     */
@@ -129,9 +133,12 @@ typedef struct hisparse_layout {
  * A miss plan ([Guide] Shared-index prefetch: the anchor's swap-in records
  * which host slot goes to which device buffer slot).  Caller-owned device
  * memory:
- *   rows    device int32 [R][k][2]: (token position, device slot) pairs of
+ *   rows    device int32 [R][k][2]: (host slot, device slot) pairs of
  *           request r, ascending by token; only the first counts[r] pairs
- *           are written.
+ *           are written.  The host slot is the token position within the
+ *           request's host region, or, with a paged host pool, the token's
+ *           row in the layer's pool (block id * host_block_tokens + token %
+ *           host_block_tokens).
  *   counts  device int32 [R]: misses of request r in the recording call.
  * Speculative verification ([Arch] Resident device pages: every
  * verification step gets its own replayable plan row) uses one plan per
@@ -158,6 +165,72 @@ typedef struct hisparse_plan {
  */
 int hisparse_create(const hisparse_layout *layout, hisparse_t *out);
 
+/*
+ * hisparse_create_paged: hisparse_create with a paged host pool ([Arch]
+ * Ownership: the coordinator maps each request's tokens to logical host
+ * blocks and owns their allocation, from a CPU block pool with its own
+ * lifecycle; the configured budget is rounded down to whole host blocks.
+ * [Guide] HiSparse Config Parameters: host_to_device_ratio sizes the logical
+ * pool against the device pool).
+ *   host_block_tokens  hb >= 1: token rows per host block.
+ * Each layer's pinned pool holds floor(ratio * R * D / hb) blocks of hb
+ * rows, [pool_blocks * hb][B] bytes; block ids are the same in every layer.
+ * host_capacity[r] is now only the longest request r may grow to (it sizes
+ * the token->slot map and the block table; the sum may exceed the pool).
+ * Request r's token t lives in row  table[r][t / hb] * hb + t % hb  of the
+ * layer's pool; its table starts empty (see hisparse_host_reserve).
+ * Errors: as hisparse_create, plus LAYOUT (hb < 1), CAPACITY (the budget is
+ * less than one block), UNSUPPORTED (hb > HISPARSE_MAX_HOST_BLOCK_TOKENS,
+ * more than 2^31 - 1 rows per layer, or a block table row that does not fit
+ * in the resolve kernel's shared memory).
+ */
+int hisparse_create_paged(const hisparse_layout *layout, int32_t host_block_tokens,
+                          hisparse_t *out);
+
+/*
+ * hisparse_host_reserve: grow requests' host block tables.  For each i in
+ * order, request requests[i] (host int32 [n]) gets blocks until its table
+ * covers tokens [0, num_tokens[i]) (host int64 [n], 0 <= num_tokens[i] <=
+ * host_capacity); each new entry, in block order, takes the lowest-numbered
+ * free block.  All or nothing: too few free blocks for the whole batch
+ * returns CAPACITY and changes nothing; a bad request or length returns
+ * INVALID_ARG.  The host copy of the tables (hisparse_host_block_table) is
+ * updated at once; the device copy that the kernels read is updated by
+ * stream-ordered launches on `stream` (one per 128 runs of consecutive
+ * ids), so order the calls that use the new blocks after it.  Capturable.
+ * The caller writes the rows of new blocks (hisparse_host_block_rows) before
+ * the swap-in, backup or prefill that reads them.
+ */
+int hisparse_host_reserve(hisparse_t h, int32_t n, const int32_t *requests,
+                          const int64_t *num_tokens, void *stream);
+
+/*
+ * hisparse_host_release: return every host block of each listed request
+ * (host int32 [n]) to the pool; their table entries become -1 (device copy:
+ * stream-ordered on `stream`).  The requests' hot state is left as it is:
+ * restart a request with hisparse_prefill before its next swap-in.  A
+ * released block may be handed out by the next reservation: the caller
+ * must not write its rows for a new owner until the GPU work that reads the
+ * old owner's rows has completed ([Arch] Spill transaction: host pages are
+ * republished only after the copy event is observed).  INVALID_ARG for a
+ * bad request, nothing released.
+ */
+int hisparse_host_release(hisparse_t h, int32_t n, const int32_t *requests, void *stream);
+
+/* Host copy of request `request`'s block table: *count = reserved blocks;
+ * the first min(max_ids, count) ids go to `ids` (host).  No GPU work. */
+int hisparse_host_block_table(hisparse_t h, int32_t request, int32_t *ids, int32_t max_ids,
+                              int32_t *count);
+
+/* Host block size, pool size and free blocks (all 0 without a paged pool);
+ * any pointer may be NULL.  No GPU work. */
+int hisparse_host_pool_info(hisparse_t h, int32_t *block_tokens, int32_t *pool_blocks,
+                            int32_t *free_blocks);
+
+/* Host pointer to the hb rows (B bytes each, contiguous) of pool block
+ * `block` of layer `layer`.  Valid until hisparse_destroy. */
+int hisparse_host_block_rows(hisparse_t h, int32_t layer, int32_t block, void **host_ptr);
+
 /* Free everything the handle owns.  The caller must have synchronised all
  * streams that used it.  NULL is accepted. */
 int hisparse_destroy(hisparse_t h);
@@ -167,7 +240,9 @@ int hisparse_destroy(hisparse_t h);
  * pinned pool; rows are contiguous, B bytes each, host_capacity[request] of
  * them.  The caller writes the request's prefix KV there (the role of the
  * direct-to-host import in [Guide] PD Disaggregation Integration) before
- * hisparse_prefill.  Valid until hisparse_destroy.
+ * hisparse_prefill.  Valid until hisparse_destroy.  A handle with a paged
+ * host pool has no per-request region: INVALID_ARG (use
+ * hisparse_host_block_rows).
  */
 int hisparse_host_rows(hisparse_t h, int32_t layer, int32_t request, void **host_ptr);
 
@@ -188,7 +263,9 @@ int hisparse_device_buffer(hisparse_t h, int32_t layer, void **dev_ptr);
  * 0..n-1 (slot i <- token S-n+i), and for state-owning layers the maps are
  * set to match, every stamp and the tick are reset to 0 and the LRU order
  * becomes slot order.  A request with S <= D therefore holds every token at
- * slot = token ([Guide] Decode Workflow, fast path).  One launch.
+ * slot = token ([Guide] Decode Workflow, fast path).  With a paged host pool
+ * the blocks of tokens [S-n, S) must be reserved, else status NO_HOST_ROW
+ * and the request is left untouched.  One launch.
  */
 int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream);
 
@@ -209,7 +286,9 @@ int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream);
  * order, the evicted tokens are unmapped, and each miss's row is copied from
  * the pinned host pool into its slot; every selected slot is stamped with
  * the tick.  A malformed row (see status codes) leaves the request's state
- * untouched and writes -1 to its outputs and 0 to its plan count.
+ * untouched and writes -1 to its outputs and 0 to its plan count; so does,
+ * with a paged host pool, a miss whose host block the request has not
+ * reserved (status NO_HOST_ROW, checked last).
  * Errors: INVALID_ARG, LAYER (skip layer or out of range), ALIGNMENT.
  */
 int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx,
@@ -248,7 +327,7 @@ int hisparse_swap_in_resident(hisparse_t h, int32_t layer, const int32_t *topk_i
  * small fixed grid to keep their SM footprint low).  For every request r and
  * i < counts[r]: layer `layer`'s device slot rows[r][i][1] <- its host row
  * rows[r][i][0].  No map or LRU changes.  `num_ctas` sets the grid (0 = 16).
- * Pairs whose token or slot is out of range are skipped.  The caller orders
+ * Pairs whose host slot or device slot is out of range are skipped.  The caller orders
  * it after the recording swap-in (an event on `stream`).
  */
 int hisparse_replay_plan(hisparse_t h, const hisparse_plan *plan, int32_t layer,
@@ -271,7 +350,9 @@ int hisparse_replay_plan_layers(hisparse_t h, const hisparse_plan *plan, const i
  *   rows       device [R][B] bytes, 16-byte aligned.
  *   positions  device int32 [R]: the row's token position, normally the
  *              request's current seq_len; -1 skips the request; outside
- *              [0, host_capacity[r]) sets status BAD_POSITION.
+ *              [0, host_capacity[r]) sets status BAD_POSITION; with a paged
+ *              host pool, a position whose block the request has not
+ *              reserved sets status NO_HOST_ROW and writes nothing.
  * Host row p <- rows[r].  If p < D (a short request, whose buffer holds
  * every token at slot = token) device slot p is written too and, on a layer
  * with state, the maps pair slot p with token p.  Stamps are unchanged.

@@ -13,20 +13,64 @@ from hierarchical_sparse_kv_request_gb300 import workload as W
 from hierarchical_sparse_kv_request_gb300.hisparse import HiSparse
 
 
-class Pair:
-    """One workload on the GPU library and on the oracle."""
+def reserve_interleaved(gpu, orc, caps, hb: int, blocks_per_round: int = 8, seed: int = 0):
+    """Reserve every request's whole capacity on both sides in rounds of a
+    few blocks per request, requests in a seeded random order each round, so
+    each request's blocks are scattered over the pool."""
+    rng = np.random.default_rng(seed)
+    caps = [int(c) for c in caps]
+    done = [0] * len(caps)
+    while any(d < c for d, c in zip(done, caps)):
+        reqs = [int(r) for r in rng.permutation(len(caps)) if done[r] < caps[r]]
+        ntok = [min(caps[r], done[r] + blocks_per_round * hb) for r in reqs]
+        gpu.host_reserve(reqs, ntok)
+        assert orc.reserve(reqs, ntok) == 0
+        for r, n in zip(reqs, ntok):
+            done[r] = n
 
-    def __init__(self, w: W.Workload, track_bytes: bool, copy_mode: Optional[int] = None):
+
+def fill_paged_rows(w: W.Workload, gpu, orc, layer: int, r: int, upto: int,
+                    track_bytes: bool, chunk: int = 8192):
+    """Generator rows of tokens [0, upto) of (layer, r) into the pool blocks
+    the request holds, on both sides."""
+    hb = gpu.hb
+    table = gpu.host_block_table(r)
+    for t0 in range(0, upto, chunk):
+        t1 = min(upto, t0 + chunk)
+        rows = W.kv_rows(w, layer, r, np.arange(t0, t1))
+        for b in range(t0 // hb, (t1 + hb - 1) // hb):
+            a, e = max(b * hb, t0), min((b + 1) * hb, t1)
+            gpu.host_block_rows(layer, int(table[b]))[a - b * hb:e - b * hb] = rows[a - t0:e - t0]
+            if track_bytes:
+                orc.block_rows(layer, int(table[b]))[a - b * hb:e - b * hb] = rows[a - t0:e - t0]
+
+
+class Pair:
+    """One workload on the GPU library and on the oracle.  host_block_tokens
+    > 0 runs both with a paged host pool, each request's whole capacity
+    reserved up front in interleaved rounds."""
+
+    def __init__(self, w: W.Workload, track_bytes: bool, copy_mode: Optional[int] = None,
+                 host_block_tokens: int = 0):
         self.w = w
         self.track = track_bytes
-        self.gpu = HiSparse.for_workload(w)
+        self.hb = host_block_tokens
+        self.gpu = HiSparse.for_workload(w, host_block_tokens=host_block_tokens)
         if copy_mode is not None:
             self.gpu.set_copy_mode(copy_mode)
-        self.orc = O.Oracle.for_workload(w, track_bytes=track_bytes)
+        self.orc = O.Oracle.for_workload(w, track_bytes=track_bytes,
+                                         host_block_tokens=host_block_tokens)
         R, k = w.num_requests, w.top_k
+        if self.hb:
+            reserve_interleaved(self.gpu, self.orc, w.host_capacity, self.hb)
+            for r in range(R):
+                assert np.array_equal(self.gpu.host_block_table(r), self.orc.block_table(r))
         for l in range(w.num_layers):
             for r in range(R):
                 n = int(w.seq_lens0[r])
+                if self.hb:
+                    fill_paged_rows(w, self.gpu, self.orc, l, r, n, track_bytes)
+                    continue
                 dst = self.gpu.host_rows(l, r)
                 W.fill_host_rows(w, l, r, dst, n)
                 if track_bytes:

@@ -82,6 +82,28 @@ def test_create_rejects_bad_layouts_before_any_gpu_work(lib, kw, code):
     assert h.value is None                      # *out cleared on error
 
 
+def _create_paged(lib, hb, R=2, D=16, ratio=10, caps=(500, 500)):
+    caps = np.ascontiguousarray(caps, dtype=np.int64)
+    lay = H.Layout(R, 1, 16, 8, D, ratio, 960, None, caps.ctypes.data)
+    h = ctypes.c_void_p(1234)
+    rc = lib.hisparse_create_paged(ctypes.byref(lay), hb, ctypes.byref(h))
+    return rc, h
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hb=0), H.ERR_LAYOUT),
+    (dict(hb=-4), H.ERR_LAYOUT),
+    (dict(hb=64, ratio=1), H.ERR_CAPACITY),               # 1 * 2 * 16 rows: no whole block of 64
+    (dict(hb=(1 << 16) + 1), H.ERR_UNSUPPORTED),
+    (dict(hb=16, ratio=0), H.ERR_LAYOUT),
+    (dict(hb=4, caps=((1 << 20) + 1, 1)), H.ERR_UNSUPPORTED),
+])
+def test_create_paged_rejects_bad_layouts_before_any_gpu_work(lib, kw, code):
+    rc, h = _create_paged(lib, **kw)
+    assert rc == code
+    assert h.value is None
+
+
 def test_null_arguments(lib):
     h = ctypes.c_void_p()
     assert lib.hisparse_create(None, ctypes.byref(h)) == H.ERR_INVALID_ARG
@@ -96,6 +118,13 @@ def test_null_arguments(lib):
     assert lib.hisparse_set_copy_mode(None, 1) == H.ERR_INVALID_ARG
     assert lib.hisparse_link_probe(None, None, 16, 0, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_synthetic_compute(None, 0, 1, 1, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_create_paged(None, 16, ctypes.byref(h)) == H.ERR_INVALID_ARG
+    assert lib.hisparse_create_paged(None, 16, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_host_reserve(None, 0, None, None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_host_release(None, 0, None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_host_block_table(None, 0, None, 0, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_host_pool_info(None, None, None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_host_block_rows(None, 0, 0, None) == H.ERR_INVALID_ARG
 
 
 def test_missing_library_fails_loudly(tmp_path):
