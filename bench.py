@@ -48,6 +48,9 @@ def parse():
                          "(default 16 for config 4, 48 for config 6)")
     ap.add_argument("--no-prefetch", action="store_true",
                     help="config 4: replay skip layers in-line on the main stream")
+    ap.add_argument("--host-block-tokens", type=int, default=0,
+                    help="paged host pool with blocks of this many tokens, each request's "
+                         "blocks scattered over the pool (0: one contiguous region per request)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -150,8 +153,23 @@ class Clocks:
 # workload set-up (inputs resident in HBM before the timed region)
 # ----------------------------------------------------------------------------
 
+def reserve_scattered(gpu, caps, hb: int, seed: int, blocks_per_round: int = 8):
+    """Reserve every request's capacity in rounds of a few blocks, requests
+    in a seeded random order each round: each request's host blocks end up
+    scattered over the pool, as after a long run of admissions and exits."""
+    rng = np.random.default_rng(seed)
+    caps = [int(c) for c in caps]
+    done = [0] * len(caps)
+    while any(d < c for d, c in zip(done, caps)):
+        reqs = [int(r) for r in rng.permutation(len(caps)) if done[r] < caps[r]]
+        ntok = [min(caps[r], done[r] + blocks_per_round * hb) for r in reqs]
+        gpu.host_reserve(reqs, ntok)
+        for r, n in zip(reqs, ntok):
+            done[r] = n
+
+
 class Setup:
-    def __init__(self, cfg: int, steps: int, rank: int, copy_mode: str):
+    def __init__(self, cfg: int, steps: int, rank: int, copy_mode: str, host_block_tokens: int = 0):
         import torch
         from hierarchical_sparse_kv_request_gb300 import hisparse as H
 
@@ -161,11 +179,17 @@ class Setup:
         self.w = w
         self.torch = torch
         self.H = H
-        self.gpu = H.HiSparse.for_workload(w)
+        self.hb = host_block_tokens
+        self.gpu = H.HiSparse.for_workload(w, host_block_tokens=host_block_tokens)
         self.gpu.set_copy_mode(H.COPY_SPLIT if copy_mode == "split" else H.COPY_FUSED)
+        if self.hb:
+            reserve_scattered(self.gpu, w.host_capacity, self.hb, w.seed)
         for l in range(w.num_layers):
             for r in range(w.num_requests):
-                W.fill_host_rows(w, l, r, self.gpu.host_rows(l, r), int(w.seq_lens0[r]))
+                n = int(w.seq_lens0[r])
+                for t0 in range(0, n, 8192):
+                    t1 = min(n, t0 + 8192)
+                    self.gpu.write_host_rows(l, r, t0, W.kv_rows(w, l, r, np.arange(t0, t1)))
         sched = W.topk_schedule(w)
         self.sched = {l: torch.from_numpy(a).cuda() for l, a in sched.items()}
         self.sched_np = sched
@@ -303,7 +327,7 @@ def run_gpu(args):
         return run_pipelined(args, ws, rank, H)
 
     K, Wm = args.steps, args.warmup
-    st = Setup(args.config, K + Wm, rank, args.copy_mode)
+    st = Setup(args.config, K + Wm, rank, args.copy_mode, args.host_block_tokens)
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -374,7 +398,7 @@ def run_gpu(args):
             * calls_per_step * K + 24 * misses
         kernel_ms = statistics.mean(call_ms)
         traffic = None
-        if w.config_no == 2 and not st.split:
+        if w.config_no == 2 and not st.split and not st.hb:
             traffic = profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/resolve.cu",
                                        "resolve_kernel_decode_40k.md")
         roof = {"bound": "host_link", "achieved": round(miss_gbs, 1),
@@ -398,6 +422,8 @@ def run_gpu(args):
                        "top_k": w.top_k, "device_buffer_size": w.device_buffer_size,
                        "row_bytes": w.row_bytes, "host_to_device_ratio": w.host_to_device_ratio,
                        "substeps": w.substeps, "backup": w.backup, "copy_mode": args.copy_mode,
+                       "host_pool": (f"paged: {st.hb}-token blocks scattered over the pool"
+                                     if st.hb else "one contiguous region per request"),
                        "l2": "flushed between timed steps (512 MB write)"},
             "us_per_decode_step": round(total_s / K * 1e6, 2),
             "step_ms_min_median_max": [round(min(step_ms), 4), round(statistics.median(step_ms), 4),

@@ -229,6 +229,23 @@ class HiSparse:
         buf = (ctypes.c_uint8 * (self.hb * self.B)).from_address(p.value)
         return np.frombuffer(buf, dtype=np.uint8).reshape(self.hb, self.B)
 
+    def write_host_rows(self, layer: int, request: int, t0: int, rows: np.ndarray) -> None:
+        """Copy rows ([n][B] uint8) into the pinned host rows of tokens
+        [t0, t0 + n) of (layer, request): the request's region, or, with a
+        paged pool, the blocks its table names (which must be reserved)."""
+        n = rows.shape[0]
+        if not self.hb:
+            self.host_rows(layer, request)[t0:t0 + n] = rows
+            return
+        hb = self.hb
+        table = self.host_block_table(request)
+        t1 = t0 + n
+        if n and (t1 - 1) // hb >= table.size:
+            raise ValueError("rows beyond the request's reserved host blocks")
+        for b in range(t0 // hb, (t1 + hb - 1) // hb):
+            a, e = max(b * hb, t0), min((b + 1) * hb, t1)
+            self.host_block_rows(layer, int(table[b]))[a - b * hb:e - b * hb] = rows[a - t0:e - t0]
+
     def device_buffer_ptr(self, layer: int) -> int:
         p = ctypes.c_void_p()
         _check(self.lib.hisparse_device_buffer(self.h, layer, ctypes.byref(p)),
