@@ -441,9 +441,11 @@ def run_gpu(args):
             "clocks": clk, "wall_s_timed_loop": round(wall, 3),
         }
     if not args.no_e2e:
-        e2e = run_e2e(st, torch, K, Wm, rank, ws)
+        e2e = run_e2e(st, torch, K, Wm, rank, ws, zero_copy=True)
+        e2e_ce = run_e2e(st, torch, K, Wm, rank, ws, zero_copy=False)
         if rank == 0:
             result["e2e"] = e2e
+            result["e2e_copy_engine"] = e2e_ce
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         result["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
     if ws > 1:
@@ -452,15 +454,19 @@ def run_gpu(args):
     return result
 
 
-def run_e2e(st, torch, K, Wm, rank, ws):
+def run_e2e(st, torch, K, Wm, rank, ws, zero_copy=True):
     """The same decode steps through the public API with host buffers, the
-    way a serving loop drives it: one CUDA graph per step, captured once,
-    holds the host->device copies of the step's top-k rows from pinned
-    staging buffers, the step's swap-in calls (and backups), and the
-    device->host copy of the slot IDs into a pinned buffer.  Before each
-    step the host writes that step's top-k rows into the staging buffers
-    (the producer's part, untimed); the timed region is the graph's replay:
-    copies in, swap-ins, copy out."""
+    way a serving loop drives them: one CUDA graph per step, captured once,
+    replayed every step.  Before each step the host writes that step's top-k
+    rows into pinned staging buffers (the producer's part, untimed); the
+    timed region is the graph's replay, which moves the top-k rows host ->
+    device and the slot IDs device -> host:
+      zero_copy=True   the swap-in kernels read the top-k rows straight from
+                       the pinned buffers and write the slot IDs straight
+                       into a pinned buffer, over the host link (GB300's
+                       NVLink-C2C makes pinned host memory device-addressable);
+      zero_copy=False  copy-engine transfers: pinned -> device copies before
+                       the swap-ins, a device -> pinned copy after them."""
     w, g = st.w, st.gpu
     R, k = w.num_requests, w.top_k
     calls0 = st.calls_of_step(0)
@@ -478,15 +484,21 @@ def run_e2e(st, torch, K, Wm, rank, ws):
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        for i in range(len(calls0)):
-            dtopk[i].copy_(stage[i], non_blocking=True)
+        if not zero_copy:
+            for i in range(len(calls0)):
+                dtopk[i].copy_(stage[i], non_blocking=True)
         for i, (l, _) in enumerate(calls0):
-            g.swap_in(l, dtopk[i], st.seq, st.out, st.plans[i], st.cnts[i])
+            if zero_copy:
+                g.swap_in(l, stage[i].data_ptr(), st.seq, host_out.data_ptr(), st.plans[i],
+                          st.cnts[i])
+            else:
+                g.swap_in(l, dtopk[i], st.seq, st.out, st.plans[i], st.cnts[i])
         if w.backup:
             for l in range(w.num_layers):
                 g.backup(l, dback[l], st.seq)
             st.seq += 1
-        host_out.copy_(st.out, non_blocking=True)
+        if not zero_copy:
+            host_out.copy_(st.out, non_blocking=True)
     total = 0.0
     h2d = d2h = 0
     calls = 0
@@ -507,12 +519,14 @@ def run_e2e(st, torch, K, Wm, rank, ws):
             ncalls = len(calls0)
             calls += ncalls
             h2d += ncalls * R * k * 4
-            d2h += R * k * 4
+            d2h += (ncalls if zero_copy else 1) * R * k * 4
     total = max_over_ranks(total, "cuda")
+    how = ("one CUDA graph per step; the swap-ins read the top-k rows from pinned host memory and "
+           "write the slot IDs into pinned host memory (zero-copy over NVLink-C2C)" if zero_copy else
+           "one CUDA graph per step: pinned top-k -> device copies, swap-ins, slot IDs -> pinned copy")
     return {"value": round(job_throughput(st.valid_per_call * calls, ws, total), 1), "unit": "rows/s",
             "h2d_bytes_per_step": h2d // K, "d2h_bytes_per_step": d2h // K,
-            "ms_per_step": round(total / K * 1e3, 4),
-            "how": "one CUDA graph per step: pinned top-k -> device, swap-ins, slot IDs -> pinned"}
+            "ms_per_step": round(total / K * 1e3, 4), "how": how}
 
 
 # ----------------------------------------------------------------------------

@@ -21,7 +21,12 @@
  *     checks run before any GPU work; on error nothing is enqueued.
  *   - Pointers documented as "device" must be device memory (cudaMalloc or
  *     torch CUDA tensors) of the handle's device; "host" means ordinary host
- *     memory.  No entry point keeps a caller pointer after it returns.
+ *     memory.  "Device-addressable" accepts both device memory and pinned
+ *     host memory the device can address (cudaHostAlloc, cudaHostRegister;
+ *     with unified addressing, as on GB300, the host pointer itself): the
+ *     kernels then read or write it over the host link directly (zero-copy,
+ *     NVLink-C2C on GB300).  No entry point keeps a caller pointer after it
+ *     returns.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls that take a stream are asynchronous and stream-ordered:
  *     they never synchronise and never read device data back to the host
@@ -133,13 +138,14 @@ typedef struct hisparse_layout {
  * A miss plan ([Guide] Shared-index prefetch: the anchor's swap-in records
  * which host slot goes to which device buffer slot).  Caller-owned device
  * memory:
- *   rows    device int32 [R][k][2]: (host slot, device slot) pairs of
+ *   rows    device-addressable int32 [R][k][2]: (host slot, device slot) pairs of
  *           request r, ascending by token; only the first counts[r] pairs
  *           are written.  The host slot is the token position within the
  *           request's host region, or, with a paged host pool, the token's
  *           row in the layer's pool (block id * host_block_tokens + token %
  *           host_block_tokens).
- *   counts  device int32 [R]: misses of request r in the recording call.
+ *   counts  device-addressable int32 [R]: misses of request r in the
+ *           recording call.
  * Speculative verification ([Arch] Resident device pages: every
  * verification step gets its own replayable plan row) uses one plan per
  * sub-step.
@@ -273,10 +279,13 @@ int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream);
  * hisparse_swap_in: resolve one call's top-k for every request on a layer
  * that owns state ([Guide] Decode Workflow, swap-in; [Arch] Hot lookup and
  * LRU), in one launch.
- *   topk_idx      device int32 [R][k]: token positions; -1 = padding.
- *   seq_lens      device int32 [R]: current length S of each request.
- *   out_slot_ids  device int32 [R][k]: output, the hot slot holding each
- *                 input position (-1 for padding), in input order.
+ *   topk_idx      device-addressable int32 [R][k]: token positions; -1 =
+ *                 padding.
+ *   seq_lens      device-addressable int32 [R]: current length S of each
+ *                 request.
+ *   out_slot_ids  device-addressable int32 [R][k]: output, the hot slot
+ *                 holding each input position (-1 for padding), in input
+ *                 order.
  *   out_plan      NULL, or a plan (both pointers non-NULL) to record the
  *                 misses into.
  * Per request: the tick advances by one.  If S <= D the fast path applies:

@@ -82,6 +82,48 @@ def test_tiny_workload_full_parity(mode):
     p.close()
 
 
+@pytest.mark.parametrize("mode", [H.COPY_FUSED, H.COPY_SPLIT])
+def test_arguments_in_pinned_host_memory(mode):
+    """Top-k rows, sequence lengths, slot IDs and plans may live in pinned
+    host memory: the kernels read and write them over the host link.  Eager
+    calls and calls replayed from a CUDA graph both match the oracle."""
+    w = W.make_config(1)
+    sched = W.topk_schedule(w)[0]
+    p = Pair(w, track_bytes=True, copy_mode=mode)
+    R, k = w.num_requests, w.top_k
+    topk_h = torch.empty((R, k), dtype=torch.int32).pin_memory()
+    seq_h = torch.from_numpy(p.seq.copy()).pin_memory()
+    out_h = torch.empty((R, k), dtype=torch.int32).pin_memory()
+    plan_h = torch.empty((R, k, 2), dtype=torch.int32).pin_memory()
+    cnt_h = torch.empty(R, dtype=torch.int32).pin_memory()
+
+    def check(c):
+        o = p.orc.swap_in(0, sched[c], p.seq)
+        torch.cuda.synchronize()
+        g = (out_h.numpy().copy(), plan_h.numpy().copy(), cnt_h.numpy().copy(),
+             p.gpu.status().cpu().numpy())
+        assert_call_equal(g, o, f"call {c}")
+
+    half = w.steps // 2
+    for c in range(half):
+        topk_h.numpy()[:] = sched[c]
+        p.gpu.swap_in(0, topk_h.data_ptr(), seq_h.data_ptr(), out_h.data_ptr(),
+                      plan_h.data_ptr(), cnt_h.data_ptr())
+        check(c)
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        p.gpu.swap_in(0, topk_h.data_ptr(), seq_h.data_ptr(), out_h.data_ptr(),
+                      plan_h.data_ptr(), cnt_h.data_ptr())
+    for c in range(half, w.steps):
+        topk_h.numpy()[:] = sched[c]
+        graph.replay()
+        check(c)
+    assert_state_equal(p, 0, "end")
+    assert_device_bytes_equal_oracle(p, 0, "end")
+    p.close()
+
+
 @pytest.mark.parametrize("record_plan", [True, False])
 def test_auto_copy_defers_requests_with_many_misses(record_plan):
     """Auto copy mode: requests whose misses exceed 256 KB leave them to the
