@@ -33,6 +33,11 @@ sys.path.insert(0, ROOT)
 from hierarchical_sparse_kv_request_gb300 import workload as W  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2
+# Untimed steps of the workload run before the W warm-up steps.  After
+# set-up, the first decode steps sometimes run 2-25x slower for ~14 steps
+# (pinned pages the CPU has just filled, read by the GPU for the first time);
+# these steps absorb that transient whatever W is asked for.
+SETTLE_STEPS = 16
 
 
 def parse():
@@ -153,6 +158,25 @@ class Clocks:
 # workload set-up (inputs resident in HBM before the timed region)
 # ----------------------------------------------------------------------------
 
+def settle_host_pool(torch, H, gpu, w, chunk: int = 256 << 20):
+    """Set-up: read every pinned pool row once from the GPU after the host
+    has written them.  The first GPU reads of pinned pages the CPU has just
+    filled are much slower (measured on GB300: the first ~10 decode steps
+    after set-up took 2-25x the steady step), a transient of set-up that a
+    long-running decode loop does not see."""
+    hb, pool_blocks, _ = gpu.host_pool_info()
+    rows = pool_blocks * hb if hb else int(w.host_capacity.sum())
+    nbytes = rows * w.row_bytes
+    tmp = torch.empty(min(chunk, nbytes), dtype=torch.uint8, device="cuda")
+    for l in range(w.num_layers):
+        base = gpu.host_block_rows(l, 0).ctypes.data if hb else gpu.host_rows_ptr(l, 0)
+        for off in range(0, nbytes, chunk):
+            n = min(chunk, nbytes - off)
+            H.link_probe(base + off, tmp, n)
+    torch.cuda.synchronize()
+    del tmp
+
+
 def reserve_scattered(gpu, caps, hb: int, seed: int, blocks_per_round: int = 8):
     """Reserve every request's capacity in rounds of a few blocks, requests
     in a seeded random order each round: each request's host blocks end up
@@ -210,9 +234,10 @@ class Setup:
         self.valid_per_call = R * k        # the schedule never pads
         self.launches_per_step = 0
 
-    def step(self, s: int, call_events=None):
+    def step(self, s: int, call_events=None, backup_events=None):
         """One decode step: every swap-in call of step s, then the backups.
-        call_events[i], if given, brackets the i-th swap-in launch."""
+        call_events[i], if given, brackets the i-th swap-in launch;
+        backup_events, if given, brackets the step's backup launches."""
         w, g = self.w, self.gpu
         for i, (l, c) in enumerate(self.calls_of_step(s)):
             if call_events:
@@ -221,8 +246,12 @@ class Setup:
             if call_events:
                 call_events[i][1].record()
         if w.backup:
+            if backup_events:
+                backup_events[0].record()
             for l in range(w.num_layers):
                 g.backup(l, self.backup_rows[s, l], self.seq)
+            if backup_events:
+                backup_events[1].record()
             self.seq += 1
 
     def calls_of_step(self, s: int):
@@ -240,6 +269,22 @@ class Setup:
         if w.backup:
             n += w.num_layers
         return n
+
+
+def backup_report(w, bev, link):
+    """Eager-backup D2H rate: the step's R x L rows over the time of its
+    backup launches (one event pair around them), against the D2H copy peak.
+    The rows are small (R x B per layer), so the launches are latency-bound."""
+    if not bev:
+        return {}
+    ms = statistics.median([a.elapsed_time(b) for a, b in bev])
+    nbytes = w.num_requests * w.num_layers * w.row_bytes
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"backup": {"bytes_per_step": nbytes, "launches_per_step": w.num_layers,
+                       "median_ms": round(ms, 5), "d2h_gbs": round(gbs, 2),
+                       "frac_of_d2h_peak": round(gbs / link["d2h_copy_engine_gbs"], 4),
+                       "note": "one event pair around the step's backup launches; "
+                               "includes the ~5 us cost of the pair itself"}}
 
 
 def measure_link_peak(torch, H):
@@ -327,14 +372,16 @@ def run_gpu(args):
         return run_pipelined(args, ws, rank, H)
 
     K, Wm = args.steps, args.warmup
-    st = Setup(args.config, K + Wm, rank, args.copy_mode, args.host_block_tokens)
+    S0 = SETTLE_STEPS
+    st = Setup(args.config, S0 + K + Wm, rank, args.copy_mode, args.host_block_tokens)
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     clocks = Clocks(local)
     if not args.profile:
         clocks.start()
-    for s in range(Wm - 1):
+    settle_host_pool(torch, H, st.gpu, w)
+    for s in range(S0 + Wm - 1):
         st.step(s)
     torch.cuda.synchronize()
 
@@ -349,16 +396,23 @@ def run_gpu(args):
     kev = [[(torch.cuda.Event(enable_timing=True, external=True),
              torch.cuda.Event(enable_timing=True, external=True)) for _ in range(ncalls)]
            for _ in range(K)]
+    # An event pair costs ~5 us of GPU time on GB300, so a step that is a
+    # single swap-in launch is not bracketed twice: its step events time the
+    # launch itself.
+    inner = ncalls > 1 or w.backup
+    bev = [(torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(K)] if w.backup else None
     miss = torch.zeros(K, dtype=torch.int64, device="cuda")
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        if Wm >= 1:
+        if S0 + Wm >= 1:
             flush.zero_()
-            st.step(Wm - 1)
+            st.step(S0 + Wm - 1)
         for i in range(K):
             flush.zero_()
             ev[i][0].record()
-            st.step(Wm + i, call_events=kev[i])
+            st.step(S0 + Wm + i, call_events=kev[i] if inner else None,
+                    backup_events=bev[i] if bev else None)
             ev[i][1].record()
             for c in st.cnts:
                 miss[i] += c.sum()
@@ -371,7 +425,7 @@ def run_gpu(args):
     wall = time.perf_counter() - wall0
     clk = clocks.stop() if not args.profile else None
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    call_ms = [a.elapsed_time(b) for row in kev for a, b in row]
+    call_ms = [a.elapsed_time(b) for row in kev for a, b in row] if inner else list(step_ms)
     total_s = max_over_ranks(sum(step_ms) * 1e-3, "cuda")
     calls_per_step = len(w.anchors) * w.substeps
     rows_per_step = st.valid_per_call * calls_per_step
@@ -413,7 +467,7 @@ def run_gpu(args):
                             f"peak {hbm_src}"}
         result = {
             "metric": "resolved top-k rows/s", "value": round(value, 1), "unit": "rows/s",
-            "n_gpus": ws, "steps": K, "warmup": Wm,
+            "n_gpus": ws, "steps": K, "warmup": Wm, "settle_steps": S0,
             "ms_per_step": round(total_s / K * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int32+u8",
             "data": "synthetic (seeded splitmix64; shapes of the guide's decode setting)",
@@ -428,6 +482,8 @@ def run_gpu(args):
             "us_per_decode_step": round(total_s / K * 1e6, 2),
             "step_ms_min_median_max": [round(min(step_ms), 4), round(statistics.median(step_ms), 4),
                                        round(max(step_ms), 4)],
+            "slow_steps": [[i, round(t, 4)] for i, t in enumerate(step_ms)
+                           if t > 2 * statistics.median(step_ms)][:16],
             "miss_h2d_gbs": round(miss_gbs, 1),
             "miss_rows_per_step": round(misses / K, 1),
             "link_peak": link,
@@ -438,6 +494,7 @@ def run_gpu(args):
                                 "median_ms": round(statistics.median(call_ms), 5),
                                 "share_of_step_time": round(sum(call_ms) / sum(step_ms), 4)},
             "gpu_launches": st.launches() * K,
+            **backup_report(w, bev, link),
             "clocks": clk, "wall_s_timed_loop": round(wall, 3),
         }
     if not args.no_e2e:
@@ -502,7 +559,8 @@ def run_e2e(st, torch, K, Wm, rank, ws, zero_copy=True):
     total = 0.0
     h2d = d2h = 0
     calls = 0
-    for i in range(Wm + K):
+    untimed = SETTLE_STEPS + Wm
+    for i in range(untimed + K):
         step = i % steps_avail
         for j, (l, c) in enumerate(st.calls_of_step(step)):
             stage[j].numpy()[:] = st.sched_np[l][c]
@@ -514,7 +572,7 @@ def run_e2e(st, torch, K, Wm, rank, ws, zero_copy=True):
         graph.replay()
         e.record()
         e.synchronize()
-        if i >= Wm:
+        if i >= untimed:
             total += s.elapsed_time(e) * 1e-3
             ncalls = len(calls0)
             calls += ncalls
@@ -541,6 +599,7 @@ def run_config4(args, ws, rank, H):
     for l in range(w.num_layers):
         for r in range(w.num_requests):
             W.fill_host_rows(w, l, r, gpu.host_rows(l, r), int(w.seq_lens0[r]))
+    settle_host_pool(torch, H, gpu, w)
     sched = torch.from_numpy(W.topk_schedule(w)[0]).cuda()
     R, k = w.num_requests, w.top_k
     seq = torch.from_numpy(w.seq_lens0.astype(np.int32)).cuda()
@@ -691,6 +750,7 @@ def run_pipelined(args, ws, rank, H):
     for l in range(w.num_layers):
         for r in range(w.num_requests):
             W.fill_host_rows(w, l, r, gpu.host_rows(l, r), int(w.seq_lens0[r]))
+    settle_host_pool(torch, H, gpu, w)
     sched = {a: torch.from_numpy(x).cuda() for a, x in W.topk_schedule(w).items()}
     R, k = w.num_requests, w.top_k
     seq = torch.from_numpy(w.seq_lens0.astype(np.int32)).cuda()
