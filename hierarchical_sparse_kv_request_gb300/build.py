@@ -2,12 +2,14 @@
 
 Each .cu under csrc/ is compiled in parallel to an object, then linked into
 ``libhisparse.so`` next to this file.  A stamp of the sources and flags
-skips the work when nothing changed.
+skips the work when nothing changed; a file lock serialises concurrent
+builds (parallel test workers).
 """
 
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import hashlib
 import os
 import shutil
@@ -51,15 +53,20 @@ def _stamp(nvcc: str, extra: List[str]) -> str:
 def build_library(force: bool = False, verbose: bool = False,
                   extra_flags: List[str] = ()) -> str:
     """Compile and link libhisparse.so; returns its path."""
+    os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, "lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        return _build_locked(force, verbose, list(extra_flags))
+
+
+def _build_locked(force: bool, verbose: bool, extra: List[str]) -> str:
     nvcc = _nvcc()
-    extra = list(extra_flags)
     stamp = _stamp(nvcc, extra)
     stamp_file = os.path.join(BUILD, "stamp")
     if not force and os.path.exists(LIB) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
                 return LIB
-    os.makedirs(BUILD, exist_ok=True)
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
