@@ -47,7 +47,7 @@ class PagedProgram:
     """GPU handle and oracle side by side on one layer, driven by a seeded
     random program of admissions, calls, backups and releases."""
 
-    def __init__(self, R, D, k, hb, ratio, cap, B, copy_mode=None, seed=0):
+    def __init__(self, R, D, k, hb, ratio, cap, B, copy_mode=None, seed=0, resident_bs=0):
         self.R, self.D, self.k, self.hb, self.B = R, D, k, hb, B
         self.cap = [cap] * R
         self.w = W.custom(R, k, D, [1] * R, row_bytes=B, capacity=self.cap, ratio=ratio,
@@ -58,6 +58,7 @@ class PagedProgram:
         self.orc = O.Oracle.for_workload(self.w, track_bytes=True, host_block_tokens=hb)
         assert self.gpu.host_pool_info() == (hb, self.orc.pool_blocks, self.orc.pool_blocks)
         self.rng = np.random.default_rng(seed)
+        self.resident_bs = resident_bs      # > 0: resident page tables on half the calls
         self.active = [False] * R
         self.S = [0] * R
         self.gen = [0] * R          # admissions of each request index so far
@@ -154,8 +155,19 @@ class PagedProgram:
             if self.rng.random() < 0.2:
                 topk[r, self.rng.integers(0, k)] = -1
         t = torch.from_numpy(topk).cuda()
-        self.gpu.swap_in(0, t, torch.from_numpy(seq).cuda(), self.out, self.plan, self.cnt)
-        o = self.orc.swap_in(0, topk, seq)
+        if self.resident_bs and self.rng.random() < 0.5:
+            bs = self.resident_bs
+            nb = -(-max(self.cap) // bs)
+            tab = np.where(self.rng.random((R, nb)) < 0.2,
+                           self.rng.integers(0, 1000, (R, nb)), -1).astype(np.int32)
+            self.gpu.swap_in_resident(0, t, torch.from_numpy(seq).cuda(),
+                                      torch.from_numpy(tab).cuda(), bs, self.out, self.plan,
+                                      self.cnt)
+            o = self.orc.swap_in(0, topk, seq, tab, bs)
+            self.seen["resident_calls"] = self.seen.get("resident_calls", 0) + 1
+        else:
+            self.gpu.swap_in(0, t, torch.from_numpy(seq).cuda(), self.out, self.plan, self.cnt)
+            o = self.orc.swap_in(0, topk, seq)
         torch.cuda.synchronize()
         g = (self.out.cpu().numpy(), self.plan.cpu().numpy(), self.cnt.cpu().numpy(),
              self.gpu.status().cpu().numpy())
@@ -234,6 +246,15 @@ def test_random_paged_program(R, D, k, hb, ratio, cap, B, mode):
     assert seen["admit"] > 0 and seen["slow"] > 0 and seen["misses"] > 0 and seen["release"] > 0, seen
     if D < 1000:
         assert seen["pool_full"] > 0 and seen["no_host_row"] > 0 and seen["backup_no_row"] > 0, seen
+
+
+def test_random_paged_program_with_resident_pages():
+    """The resident-page tier in front of a paged host pool: resident
+    positions need no host row, so a request can resolve even where its
+    blocks are missing, as long as every miss has one."""
+    prog = PagedProgram(6, 64, 24, 8, 2, 500, 64, seed=77, resident_bs=7)
+    seen = prog.run(24)
+    assert seen.get("resident_calls", 0) > 0 and seen["misses"] > 0 and seen["slow"] > 0, seen
 
 
 def test_paged_graph_capture_and_reserve_on_stream():
