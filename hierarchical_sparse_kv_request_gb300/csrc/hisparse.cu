@@ -192,6 +192,17 @@ void give_back(hisparse_handle *h, int32_t id)
     h->lowest_free = std::min(h->lowest_free, id);
 }
 
+// Take back a block given back by a release that is being undone.
+void retake(hisparse_handle *h, int32_t id)
+{
+    h->used[id / 64] |= 1ull << (id % 64);
+    --h->free_blocks;
+}
+
+// First table entry of request r (the table is at most 2^31 entries: its
+// row must fit in the resolve kernel's shared memory).
+int32_t tbl_row(const hisparse_handle *h, int32_t r) { return r * h->tbl_stride; }
+
 // Table edits, merged into runs and applied on the stream, 128 runs a launch.
 struct RunList {
     std::vector<int32_t> first, value, len;
@@ -437,17 +448,28 @@ int hisparse_host_reserve(hisparse_t h, int32_t n, const int32_t *requests,
     if (need > h->free_blocks) return HISPARSE_ERR_CAPACITY;
     // [Arch] Ownership: logical host block allocation; the lowest free block
     // goes to each new table entry, in the order asked
+    const std::vector<int32_t> before(h->nblocks);
     RunList runs;
     for (int32_t i = 0; i < n; ++i) {
         const int32_t r = requests[i];
         const int64_t nb = (num_tokens[i] + h->hb - 1) / h->hb;
         while (h->nblocks[r] < nb) {
-            const int32_t idx = r * h->tbl_stride + h->nblocks[r]++;
+            const int32_t idx = tbl_row(h, r) + h->nblocks[r]++;
             h->tbl[idx] = take_lowest_free(h);
             runs.add(idx, h->tbl[idx]);
         }
     }
-    return cuda_status(runs.apply(h->d_tbl, as_stream(stream)));
+    const cudaError_t e = runs.apply(h->d_tbl, as_stream(stream));
+    if (e != cudaSuccess) {
+        // the device table may lag the host copy: undo the host side
+        for (int32_t r = 0; r < h->R; ++r)
+            for (; h->nblocks[r] > before[r]; --h->nblocks[r]) {
+                const int32_t idx = tbl_row(h, r) + h->nblocks[r] - 1;
+                give_back(h, h->tbl[idx]);
+                h->tbl[idx] = -1;
+            }
+    }
+    return cuda_status(e);
 }
 
 int hisparse_host_release(hisparse_t h, int32_t n, const int32_t *requests, void *stream)
@@ -457,17 +479,31 @@ int hisparse_host_release(hisparse_t h, int32_t n, const int32_t *requests, void
     for (int32_t i = 0; i < n; ++i)
         if (requests[i] < 0 || requests[i] >= h->R) return HISPARSE_ERR_INVALID_ARG;
     RunList runs;
+    std::vector<std::pair<int32_t, std::vector<int32_t>>> freed;   // to undo a failed launch
     for (int32_t i = 0; i < n; ++i) {
         const int32_t r = requests[i];
         if (h->nblocks[r] == 0) continue;
+        const int32_t row = tbl_row(h, r);
+        freed.emplace_back(r, std::vector<int32_t>(&h->tbl[row], &h->tbl[row] + h->nblocks[r]));
         for (int32_t b = 0; b < h->nblocks[r]; ++b) {
-            give_back(h, h->tbl[r * h->tbl_stride + b]);
-            h->tbl[r * h->tbl_stride + b] = -1;
+            give_back(h, h->tbl[row + b]);
+            h->tbl[row + b] = -1;
         }
-        runs.clear_range(r * h->tbl_stride, h->nblocks[r]);
+        runs.clear_range(row, h->nblocks[r]);
         h->nblocks[r] = 0;
     }
-    return cuda_status(runs.apply(h->d_tbl, as_stream(stream)));
+    const cudaError_t e = runs.apply(h->d_tbl, as_stream(stream));
+    if (e != cudaSuccess) {
+        for (auto &f : freed) {
+            const int32_t row = tbl_row(h, f.first);
+            for (size_t b = 0; b < f.second.size(); ++b) {
+                retake(h, f.second[b]);
+                h->tbl[row + b] = f.second[b];
+            }
+            h->nblocks[f.first] = (int32_t)f.second.size();
+        }
+    }
+    return cuda_status(e);
 }
 
 int hisparse_host_block_table(hisparse_t h, int32_t request, int32_t *ids, int32_t max_ids,
@@ -477,7 +513,7 @@ int hisparse_host_block_table(hisparse_t h, int32_t request, int32_t *ids, int32
     if (request < 0 || request >= h->R) return HISPARSE_ERR_INVALID_ARG;
     *count = h->nblocks[request];
     const int32_t n = std::min(max_ids, h->nblocks[request]);
-    if (n > 0) std::memcpy(ids, &h->tbl[(size_t)request * h->tbl_stride], sizeof(int32_t) * n);
+    if (n > 0) std::memcpy(ids, &h->tbl[tbl_row(h, request)], sizeof(int32_t) * n);
     return HISPARSE_OK;
 }
 
