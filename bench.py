@@ -830,68 +830,103 @@ def run_pipelined(args, ws, rank, H):
 # the CPU oracle (reference arm and cpu_baseline)
 # ----------------------------------------------------------------------------
 
+class OracleSteps:
+    """The oracle, single-threaded, stepping through a bounded sample of the
+    workload: its first requests (as many as keep the oracle's host rows
+    under 2 GB), decode step after decode step; at the end of the schedule
+    the requests are prefilled again (untimed) and the schedule restarts."""
+
+    def __init__(self, cfg: int):
+        import oracle as O
+        w = W.make_config(cfg)
+        per_req = int(w.host_capacity.max()) * w.row_bytes * w.num_layers
+        nreq = max(1, min(w.num_requests, (2 << 30) // per_req))
+        if nreq < w.num_requests:
+            w = W.make_config(cfg, num_requests=nreq)
+        self.w = w
+        self.sched = W.topk_schedule(w)
+        self.orc = O.Oracle.for_workload(w, track_bytes=True)
+        for l in range(w.num_layers):
+            for r in range(w.num_requests):
+                W.fill_host_rows(w, l, r, self.orc.host_rows(l, r), int(w.seq_lens0[r]))
+        self.rows = np.zeros((w.num_requests, w.row_bytes), dtype=np.uint8)
+        self.step_in_pass = w.steps      # forces a prefill before the first step
+        self.passes = 0
+        self.calls = 0
+
+    def step(self) -> float:
+        """One decode step (all swap-in calls, their replays, the backups);
+        returns its time in seconds."""
+        w, orc = self.w, self.orc
+        if self.step_in_pass >= w.steps:
+            orc.prefill(w.seq_lens0)
+            self.seq = w.seq_lens0.astype(np.int32).copy()
+            self.step_in_pass = 0
+            self.passes += 1
+        step = self.step_in_pass
+        t0 = time.perf_counter()
+        for sub in range(w.substeps):
+            for l in w.anchors:
+                plan = orc.swap_in(l, self.sched[l][step * w.substeps + sub], self.seq)
+                self.calls += 1
+                for lf in range(w.num_layers):          # skip layers replay the plan
+                    if w.anchor_of_layer[lf] == l:
+                        orc.replay(plan[1], plan[2], lf)
+        if w.backup:
+            for l in range(w.num_layers):
+                orc.backup(l, self.rows, self.seq)
+            self.seq += 1
+        dt = time.perf_counter() - t0
+        self.step_in_pass += 1
+        return dt
+
+    def rows_per_step(self) -> int:
+        w = self.w
+        return len(w.anchors) * w.substeps * w.num_requests * w.top_k
+
+    def sample(self, steps: int, busy: float) -> str:
+        w = self.w
+        return (f"{steps} decode steps x {w.num_requests} of {W.make_config(w.config_no).num_requests} "
+                f"requests of {w.name} ({self.passes} passes over its schedule): swap-in calls with "
+                f"their host-row copies, replays and backups, {busy:.1f} s on one core")
+
+
 def cpu_baseline(cfg: int, seconds: float):
-    """The oracle, single-threaded, on a bounded sample of the workload: its
-    first requests (as many as keep the oracle's host rows under 2 GB), whole
-    passes over the workload's decode steps (state re-prefilled between
-    passes, untimed) until `seconds` of oracle time."""
-    import oracle as O
-    w = W.make_config(cfg)
-    per_req = int(w.host_capacity.max()) * w.row_bytes * w.num_layers
-    nreq = max(1, min(w.num_requests, (2 << 30) // per_req))
-    if nreq < w.num_requests:
-        w = W.make_config(cfg, num_requests=nreq)
-    sched = W.topk_schedule(w)
-    orc = O.Oracle.for_workload(w, track_bytes=True)
-    for l in range(w.num_layers):
-        for r in range(w.num_requests):
-            W.fill_host_rows(w, l, r, orc.host_rows(l, r), int(w.seq_lens0[r]))
-    rows = np.zeros((w.num_requests, w.row_bytes), dtype=np.uint8)
-    done_calls = steps_done = passes = 0
-    busy = 0.0
+    """The oracle on a bounded sample of the workload for about `seconds`."""
+    run = OracleSteps(cfg)
+    busy, steps = 0.0, 0
     while busy < seconds:
-        orc.prefill(w.seq_lens0)
-        seq = w.seq_lens0.astype(np.int32).copy()
-        passes += 1
-        for step in range(w.steps):
-            t0 = time.perf_counter()
-            for sub in range(w.substeps):
-                for l in w.anchors:
-                    plan = orc.swap_in(l, sched[l][step * w.substeps + sub], seq)
-                    done_calls += 1
-                    for lf in range(w.num_layers):          # skip layers replay the plan
-                        if w.anchor_of_layer[lf] == l:
-                            orc.replay(plan[1], plan[2], lf)
-            if w.backup:
-                for l in range(w.num_layers):
-                    orc.backup(l, rows, seq)
-                seq += 1
-            busy += time.perf_counter() - t0
-            steps_done += 1
-            if busy >= seconds:
-                break
-    nrows = done_calls * w.num_requests * w.top_k
-    return {"value": round(nrows / busy, 1), "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps_done} decode steps ({passes} passes) x {w.num_requests} requests "
-                      f"of {w.name}: {done_calls} swap-in calls with their host-row copies, "
-                      f"replays and backups, {busy:.1f} s on one core"}
+        busy += run.step()
+        steps += 1
+    return {"value": round(run.rows_per_step() * steps / busy, 1), "unit": "rows/s", "cores": 1,
+            "kind": "oracle", "sample": run.sample(steps, busy)}
 
 
 def run_reference(args):
+    """The reference arm: the oracle, W untimed and K timed decode steps of
+    a bounded sample of the workload, on one host core (rank 0 only)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
-    cb = cpu_baseline(args.config, args.cpu_seconds)
-    w = W.make_config(args.config)
-    return {"impl": "reference", "metric": "resolved top-k rows/s", "value": cb["value"],
+    run = OracleSteps(args.config)
+    for _ in range(args.warmup):
+        run.step()
+    busy = sum(run.step() for _ in range(args.steps))
+    value = round(run.rows_per_step() * args.steps / busy, 1)
+    w = run.w
+    cb = {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+          "sample": run.sample(args.steps, busy)}
+    return {"impl": "reference", "metric": "resolved top-k rows/s", "value": value,
             "unit": "rows/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(busy / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int32+u8", "data": "synthetic (seeded)",
-            "config": {"workload": w.name, "requests": w.num_requests,
-                       "seq_len": int(w.seq_lens0.max()), "top_k": w.top_k,
-                       "device_buffer_size": w.device_buffer_size, "row_bytes": w.row_bytes},
+            "config": {"workload": w.name, "requests": W.make_config(args.config).num_requests,
+                       "requests_sampled": w.num_requests, "seq_len": int(w.seq_lens0.max()),
+                       "top_k": w.top_k, "device_buffer_size": w.device_buffer_size,
+                       "row_bytes": w.row_bytes},
             "cpu_baseline": cb,
-            "e2e": {"value": cb["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
