@@ -19,6 +19,7 @@ _SRC = os.path.join(_HERE, "hisparse_oracle.c")
 _LIB = os.path.join(_HERE, "libhisparse_oracle.so")
 
 OK, BAD_INDEX, DUPLICATE, BAD_SEQ_LEN, BAD_POSITION, BAD_RESIDENT, NO_HOST_ROW = 0, 1, 2, 3, 4, 5, 6
+CAPACITY = 7
 RESIDENT_FLAG = 1 << 30
 
 
@@ -55,6 +56,7 @@ def _load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.hso_free_blocks.restype = I
     lib.hso_free_blocks.argtypes = [P]
     lib.hso_reserve.argtypes = [P, I, P, P]
+    lib.hso_set_protected_calls.argtypes = [P, I]
     lib.hso_release.argtypes = [P, I, P]
     lib.hso_block_table.restype = I
     lib.hso_block_table.argtypes = [P, I, P]
@@ -162,6 +164,11 @@ class Oracle:
         n = self.hb * self.B
         buf = (ctypes.c_uint8 * n).from_address(p)
         return np.frombuffer(buf, dtype=np.uint8).reshape(self.hb, self.B)
+
+    def set_protected_calls(self, calls: int) -> None:
+        """Slots selected by each request's last `calls` calls are not victims."""
+        if self.lib.hso_set_protected_calls(self.h, calls) != 0:
+            raise ValueError("negative count")
 
     # -- paged host pool ----------------------------------------------------
     def reserve(self, requests, num_tokens) -> int:

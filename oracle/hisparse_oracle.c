@@ -40,7 +40,14 @@
  *     order asked.  A miss, a backup or a prefill that needs a row of a block
  *     not reserved sets status NO_HOST_ROW and leaves the request untouched.
  *     A plan then records the host row in the layer's pool (block * hb +
- *     token % hb), the "host slot" a replay reads.
+ *     token % hb), the "host slot" a replay reads;
+ *   - optional protection ([Arch] Resident device pages: speculative
+ *     verification steps share the hot state, and a later step may not reuse
+ *     a hot row before an earlier step has consumed it): with P > 0, a slot
+ *     selected by one of the request's last P calls (last_used >= tick - P,
+ *     prefill stamps excluded) is not a victim; a call whose misses outnumber
+ *     the other non-hit slots sets status CAPACITY and leaves the request
+ *     untouched.  P = 0 (the default) relies on stream order alone.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -53,6 +60,7 @@
 #define HSO_BAD_POSITION 4  /* backup position outside [0, capacity) */
 #define HSO_BAD_RESIDENT 5  /* a resident block id outside [-1, 2^30 / block_size) */
 #define HSO_NO_HOST_ROW 6   /* a needed host row lies in a block not reserved */
+#define HSO_CAPACITY 7      /* protected slots leave too few victims for the misses */
 
 /* A resident hit resolves to this flag OR'd with its row in the resident pool. */
 #define HSO_RESIDENT_FLAG 0x40000000
@@ -78,6 +86,7 @@ typedef struct hs_oracle {
     int32_t *nblocks;     /* [R] reserved blocks, always a prefix of the table */
     char *in_use;         /* [pool_blocks]                                    */
     int64_t host_rows;    /* rows of one layer's pool                        */
+    int32_t protect_calls; /* P: slots stamped by the last P calls are kept   */
     /* bytes (only with track_bytes) */
     uint8_t **host;       /* [L] -> [host_rows * B]  pinned host pool       */
     uint8_t **dev;        /* [L] -> [R * D * B]      device hot buffer      */
@@ -204,6 +213,15 @@ hs_oracle *hso_create_paged(int R, int L, int64_t B, int k, int D,
 }
 
 int32_t hso_pool_blocks(const hs_oracle *o) { return o->pool_blocks; }
+
+/* Protect the slots selected by each request's last `calls` swap-in calls
+ * (0 = no protection).  Returns -1 for a negative count. */
+int hso_set_protected_calls(hs_oracle *o, int32_t calls)
+{
+    if (calls < 0) return -1;
+    o->protect_calls = calls;
+    return 0;
+}
 
 int32_t hso_free_blocks(const hs_oracle *o)
 {
@@ -505,6 +523,22 @@ static void swap_in_request(hs_oracle *o, int a, int r, const int32_t *topk,
         if (!is_hit_slot[s]) { cand[nc].last_used = lu[s]; cand[nc].slot = s; ++nc; }
     qsort(cand, (size_t)nc, sizeof(lru_key), cmp_lru);
     /* k <= D and every hit uses one slot, so m <= k - hits <= D - hits = nc. */
+
+    /* Protected slots are not victims.  The candidates are sorted by
+     * last_used, so the first m are all unprotected exactly when at least m
+     * candidates are. */
+    if (o->protect_calls > 0) {
+        uint32_t p = (uint32_t)o->protect_calls;
+        uint32_t thr = tick > p ? tick - p : 1u;
+        int unprotected = 0;
+        for (int i = 0; i < nc; ++i) unprotected += cand[i].last_used < thr;
+        if (m > unprotected) {
+            *status = HSO_CAPACITY;
+            for (int j = 0; j < k; ++j) out[j] = -1;
+            free(done); free(is_hit_slot); free(miss); free(cand);
+            return;
+        }
+    }
 
     /* Refill: miss i evicts victim i and is copied from pinned host memory. */
     for (int i = 0; i < m; ++i) {

@@ -9,7 +9,11 @@ call are equally recent; they move to the back of the list in slot order,
 which is the tie-break this library specifies.  Misses are served in
 ascending token order.  Positions held in resident pages are answered from
 there first and never reach the list ([Arch] Resident device pages: a
-resident hit exits before the hot lookup).  Pure Python, tiny cases only.
+resident hit exits before the hot lookup).  With protection P > 0, the slots
+selected by the last P calls are kept out of the victims (the model keeps a
+history of each call's selected slots, not timestamps); when the misses
+outnumber the other non-hit slots the call fails and changes nothing.
+Pure Python, tiny cases only.
 """
 
 from __future__ import annotations
@@ -20,8 +24,11 @@ RESIDENT = 1 << 30   # flag of a position resolved from resident pages
 
 
 class ListLRU:
-    def __init__(self, D: int, seq_len: int):
+    def __init__(self, D: int, seq_len: int, protect: int = 0):
         self.D = D
+        self.protect = protect
+        self.history: List[set] = []       # slots selected by each call since prefill
+        self.failed = False                # the last call left too few victims
         n = min(seq_len, D)
         # prefill: the newest n tokens, oldest first, in slots 0..n-1
         self.token_in: List[Optional[int]] = [None] * D
@@ -39,13 +46,20 @@ class ListLRU:
         rows; those resolve to RESIDENT | row before anything else and leave
         the hot buffer alone."""
         resident = resident or {}
+        self.failed = False
         if seq_len <= self.D:                       # short: slot = token
+            self.history.append(set())
             return [RESIDENT | resident[t] if t in resident else t for t in topk], []
         wanted = [t for t in topk if t >= 0 and t not in resident]
         hit_slots = {self.slot_of[t] for t in wanted if t in self.slot_of}
         misses = sorted(t for t in wanted if t not in self.slot_of)
-        victims = [s for s in self.recency if s not in hit_slots][: len(misses)]
-        assert len(victims) == len(misses)
+        kept = set().union(*self.history[-self.protect:]) if self.protect else set()
+        free = [s for s in self.recency if s not in hit_slots and s not in kept]
+        if len(misses) > len(free):
+            self.failed = True
+            self.history.append(set())
+            return [-1] * len(topk), []
+        victims = free[: len(misses)]
         plan = []
         for t, v in zip(misses, victims):
             old = self.token_in[v]
@@ -55,6 +69,7 @@ class ListLRU:
             self.slot_of[t] = v
             plan.append((t, v))
         used = hit_slots | set(victims)
+        self.history.append(used)
         self.recency = [s for s in self.recency if s not in used] + sorted(used)
         out = [RESIDENT | resident[t] if t in resident else (self.slot_of[t] if t >= 0 else -1)
                for t in topk]

@@ -63,18 +63,22 @@ def test_golden_trace(name):
 # brute force against the recency-list model
 # ----------------------------------------------------------------------------
 
-def compare_with_model(D, k, seq_lens, programs, lib_path=None):
+def compare_with_model(D, k, seq_lens, programs, lib_path=None, protect=0, counts=None):
     """programs[r] = list of top-k rows for request r (same number of calls).
 
     Runs all requests in one oracle handle and each in its own ListLRU.
-    Returns the first mismatch as a string, or None.
+    Returns the first mismatch as a string, or None.  With protect > 0 the
+    slots of the last `protect` calls are kept (counts["capacity"] counts
+    the calls that failed for lack of victims).
     """
     R = len(programs)
     ncalls = len(programs[0])
     cap = [max(S, 1) for S in seq_lens]
     orc = O.Oracle(R, 1, 16, k, D, [-1], cap, track_bytes=False, lib_path=lib_path)
+    if protect:
+        orc.set_protected_calls(protect)
     orc.prefill(seq_lens)
-    models = [ListLRU(D, S) for S in seq_lens]
+    models = [ListLRU(D, S, protect) for S in seq_lens]
     for c in range(ncalls):
         topk = np.array([programs[r][c] for r in range(R)], dtype=np.int32)
         out, plan, cnt, st = orc.swap_in(0, topk, seq_lens)
@@ -83,6 +87,12 @@ def compare_with_model(D, k, seq_lens, programs, lib_path=None):
             return f"tick {tick} after call {c + 1}"
         for r in range(R):
             mo, mp = models[r].call(programs[r][c], seq_lens[r])
+            if models[r].failed:
+                if counts is not None:
+                    counts["capacity"] = counts.get("capacity", 0) + 1
+                if st[r] != O.CAPACITY or (out[r] != -1).any() or cnt[r] != 0:
+                    return f"r{r} c{c}: expected CAPACITY, got status {st[r]}"
+                continue
             if st[r] != 0:
                 return f"r{r} c{c}: status {st[r]}"
             if out[r].tolist() != mo:
@@ -192,6 +202,25 @@ def test_random_resident_tables_vs_list_model(seed, lib_path=None):
         tabs.append([np.where(rng.random(nb) < 0.3, rng.integers(0, 50, nb), -1).tolist()
                      for _ in range(ncalls)])
     assert compare_resident_with_model(D, k, S, bs, progs, tabs, lib_path) is None
+
+
+@pytest.mark.parametrize("D,S,k,ncalls,protect", [(4, 7, 2, 3, 2), (5, 8, 2, 3, 2), (4, 6, 3, 2, 1)])
+def test_exhaustive_protected_vs_list_model(D, S, k, ncalls, protect):
+    counts = {}
+    progs = _exhaustive_programs(S, k, ncalls)
+    assert compare_with_model(D, k, [S] * len(progs), progs, protect=protect, counts=counts) is None
+    assert counts.get("capacity", 0) > 0
+
+
+def test_random_protected_vs_list_model(lib_path=None):
+    """Protection of the last 1-3 calls on random programs with padding."""
+    rng = np.random.default_rng(31)
+    counts = {}
+    for protect in (1, 2, 3):
+        D, k, S, R = 10, 4, 30, 80
+        progs = _random_programs(rng, R, D, k, S, 12)
+        assert compare_with_model(D, k, [S] * R, progs, lib_path, protect, counts) is None
+    assert counts.get("capacity", 0) > 0
 
 
 def test_random_biased_reuse_vs_list_model():
@@ -394,11 +423,25 @@ def pin_replay_copies_plan_rows_to_other_layer(lib_path=None):
         orc.swap_in(1, sched[0], w.seq_lens0)     # skip layers hold no hot state
 
 
+def pin_protected_slots_vs_list_model(lib_path=None):
+    """The protected mode against the list model: exhaustive tiny programs
+    and random ones, with calls failing for lack of victims."""
+    counts = {}
+    for D, S, k, ncalls, protect in [(4, 7, 2, 3, 2), (4, 6, 3, 2, 1)]:
+        progs = _exhaustive_programs(S, k, ncalls)
+        assert compare_with_model(D, k, [S] * len(progs), progs, lib_path, protect, counts) is None
+    rng = np.random.default_rng(32)
+    for protect in (1, 3):
+        progs = _random_programs(rng, 40, 10, 4, 30, 10)
+        assert compare_with_model(10, 4, [30] * 40, progs, lib_path, protect, counts) is None
+    assert counts.get("capacity", 0) > 0
+
+
 PINS = [pin_invariants_tiny_workload, pin_prefill_last_k_is_all_hits,
         pin_repeat_is_all_hits, pin_disjoint_sets_closed_form,
         pin_errors_leave_state_untouched,
         pin_backup_grows_short_request_into_slow_path,
-        pin_replay_copies_plan_rows_to_other_layer]
+        pin_replay_copies_plan_rows_to_other_layer, pin_protected_slots_vs_list_model]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__[4:] for p in PINS])

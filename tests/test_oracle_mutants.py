@@ -108,6 +108,15 @@ MUTANTS = [
     ("prefill_without_rows",
      "                if (host_row_of(o, r, S - n + i) < 0) { st = HSO_NO_HOST_ROW; break; }",
      "                ;"),
+    ("protect_one_call_short",
+     "uint32_t thr = tick > p ? tick - p : 1u;",
+     "uint32_t thr = tick > p ? tick - p + 1u : 1u;"),
+    ("protect_includes_prefill_stamps",
+     "uint32_t thr = tick > p ? tick - p : 1u;",
+     "uint32_t thr = tick > p ? tick - p : 0u;"),
+    ("capacity_keeps_outputs",
+     "            *status = HSO_CAPACITY;\n            for (int j = 0; j < k; ++j) out[j] = -1;",
+     "            *status = HSO_CAPACITY;"),
     ("prefill_resets_other_requests",
      "        if (S == -1) continue;",
      "        if (S == -1) S = 0;"),
