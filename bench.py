@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--host-block-tokens", type=int, default=0,
                     help="paged host pool with blocks of this many tokens, each request's "
                          "blocks scattered over the pool (0: one contiguous region per request)")
+    ap.add_argument("--protect-calls", type=int, default=0,
+                    help="keep the hot rows of each request's last P swap-in calls (0: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -193,7 +195,8 @@ def reserve_scattered(gpu, caps, hb: int, seed: int, blocks_per_round: int = 8):
 
 
 class Setup:
-    def __init__(self, cfg: int, steps: int, rank: int, copy_mode: str, host_block_tokens: int = 0):
+    def __init__(self, cfg: int, steps: int, rank: int, copy_mode: str, host_block_tokens: int = 0,
+                 protect_calls: int = 0):
         import torch
         from hierarchical_sparse_kv_request_gb300 import hisparse as H
 
@@ -206,6 +209,7 @@ class Setup:
         self.hb = host_block_tokens
         self.gpu = H.HiSparse.for_workload(w, host_block_tokens=host_block_tokens)
         self.gpu.set_copy_mode(H.COPY_SPLIT if copy_mode == "split" else H.COPY_FUSED)
+        self.gpu.set_protected_calls(protect_calls)
         if self.hb:
             reserve_scattered(self.gpu, w.host_capacity, self.hb, w.seed)
         for l in range(w.num_layers):
@@ -373,7 +377,8 @@ def run_gpu(args):
 
     K, Wm = args.steps, args.warmup
     S0 = SETTLE_STEPS
-    st = Setup(args.config, S0 + K + Wm, rank, args.copy_mode, args.host_block_tokens)
+    st = Setup(args.config, S0 + K + Wm, rank, args.copy_mode, args.host_block_tokens,
+               args.protect_calls)
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -478,6 +483,7 @@ def run_gpu(args):
                        "substeps": w.substeps, "backup": w.backup, "copy_mode": args.copy_mode,
                        "host_pool": (f"paged: {st.hb}-token blocks scattered over the pool"
                                      if st.hb else "one contiguous region per request"),
+                       "protect_calls": args.protect_calls,
                        "l2": "flushed between timed steps (512 MB write)"},
             "us_per_decode_step": round(total_s / K * 1e6, 2),
             "step_ms_min_median_max": [round(min(step_ms), 4), round(statistics.median(step_ms), 4),

@@ -39,6 +39,7 @@ struct hisparse_handle {
     int32_t *d_plan_rows = nullptr, *d_plan_counts = nullptr;  // split-copy plan
     int32_t *d_deferred = nullptr;     // [R] requests left to the copy grid (auto mode)
     int32_t copy_mode = HISPARSE_COPY_FUSED;
+    int32_t protect_calls = 0;  // slots selected by the last this many calls are kept
     bool stage_s2t = false;   // resolve kernel stages the slot->token row
 
     // Paged host pool (hb > 0): pool_blocks blocks of hb rows per layer,
@@ -598,6 +599,7 @@ int swap_in_impl(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int
     a.res_block_size = resident_blocks ? block_size : 0;
     a.deferred = autom ? h->d_deferred : nullptr;
     a.defer_bytes = kAutoDeferBytes;
+    a.protect_calls = (uint32_t)h->protect_calls;
     const bool wide_copy = split || autom;
     a.plan_rows = out_plan ? out_plan->rows : (wide_copy ? h->d_plan_rows : nullptr);
     a.plan_counts = out_plan ? out_plan->counts : (wide_copy ? h->d_plan_counts : nullptr);
@@ -710,6 +712,13 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok, uint32_t
     return cuda_status(e);
 }
 
+int hisparse_set_protected_calls(hisparse_t h, int32_t calls)
+{
+    if (!h || calls < 0) return HISPARSE_ERR_INVALID_ARG;
+    h->protect_calls = calls;
+    return HISPARSE_OK;
+}
+
 int hisparse_set_copy_mode(hisparse_t h, int32_t mode)
 {
     if (!h || (mode != HISPARSE_COPY_FUSED && mode != HISPARSE_COPY_SPLIT && mode != HISPARSE_COPY_AUTO))
@@ -791,6 +800,7 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     a.res_block_size = 0;
     a.deferred = nullptr;
     a.defer_bytes = 0;
+    a.protect_calls = (uint32_t)h->protect_calls;
     a.plan_rows = scratch;
     a.plan_counts = scratch + (int64_t)h->R * h->k * 2;
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));

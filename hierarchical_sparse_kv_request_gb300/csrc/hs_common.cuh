@@ -19,6 +19,7 @@ constexpr int kStatusBadSeqLen = 3;
 constexpr int kStatusBadPosition = 4;
 constexpr int kStatusBadResident = 5;
 constexpr int kStatusNoHostRow = 6;
+constexpr int kStatusCapacity = 7;
 constexpr int32_t kResidentFlag = 1 << 30;  // marks a row of the resident pool
 
 // Hot state of one state-owning layer.  Per request r:
@@ -151,6 +152,7 @@ struct ResolveLaunch {
     int32_t res_block_size;
     int32_t *deferred;        // [R]: 1 = misses left to the copy grid; null = never defer
     int64_t defer_bytes;      // defer a request whose misses exceed this many bytes
+    uint32_t protect_calls;   // slots selected by the last this many calls are kept (0: off)
 };
 
 // Shared-memory bytes the resolve kernel needs for this geometry

@@ -340,6 +340,28 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     }
     __syncthreads();
 
+    // Protected slots ([Arch] Resident device pages: a later verification
+    // step may not reuse a hot row before an earlier step has consumed it):
+    // with P > 0, victims need a stamp below max(1, tick - P).  The list is
+    // sorted by stamp, so it is enough that the last victim, the m-th non-hit
+    // entry, has one; its owner looks the stamp up and tells the CTA.
+    if (a.protect_calls && m > 0) {
+        const uint32_t thr = tick > a.protect_calls ? tick - a.protect_calls : 1u;
+        uint32_t q = pre & 0xFFFFu;
+        for (int e = e0; e < e1; ++e) {
+            const int sl = sm.lru_s[e];
+            if (test_bit(sm.hitbits, sl)) continue;
+            if ((int)q == m - 1)
+                sm.warp_tot[0] = a.st.last_used[(int64_t)r * D + sl] >= thr ? 1u : 0u;
+            ++q;
+        }
+        __syncthreads();
+        if (sm.warp_tot[0]) {
+            finish_untouched<KT>(a, r, t, rid, kStatusCapacity, tick);
+            return;
+        }
+    }
+
     // First host chunks: loaded now, stored after the state writes below.
     const int64_t B = a.g.B;
     const int CH = a.g.chunks;

@@ -22,7 +22,7 @@ OK = 0
 ERR_INVALID_ARG, ERR_LAYOUT, ERR_CAPACITY, ERR_LAYER = -1, -2, -3, -4
 ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT = -5, -6, -7, -8
 STATUS_OK, STATUS_BAD_INDEX, STATUS_DUPLICATE, STATUS_BAD_SEQ_LEN, STATUS_BAD_POSITION = 0, 1, 2, 3, 4
-STATUS_BAD_RESIDENT, STATUS_NO_HOST_ROW = 5, 6
+STATUS_BAD_RESIDENT, STATUS_NO_HOST_ROW, STATUS_CAPACITY = 5, 6, 7
 RESIDENT_FLAG = 1 << 30
 COPY_FUSED, COPY_SPLIT, COPY_AUTO = 1, 2, 3
 
@@ -81,6 +81,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_status": [P, P],
         "hisparse_read_state": [P, I32, P, P, P, P, P, P],
         "hisparse_set_copy_mode": [P, I32],
+        "hisparse_set_protected_calls": [P, I32],
         "hisparse_version": [],
         "hisparse_synthetic_compute": [P, I64, I32, I32, P],
         "hisparse_link_probe": [P, P, I64, I32, P],
@@ -330,6 +331,11 @@ class HiSparse:
     def backup(self, layer: int, rows, positions, stream=None) -> None:
         _check(self.lib.hisparse_backup(self.h, layer, _addr(rows), _addr(positions),
                                         _stream(stream)), "hisparse_backup")
+
+    def set_protected_calls(self, calls: int) -> None:
+        """Keep the hot rows of each request's last `calls` calls (0: off)."""
+        _check(self.lib.hisparse_set_protected_calls(self.h, calls),
+               "hisparse_set_protected_calls")
 
     def set_copy_mode(self, mode: int) -> None:
         _check(self.lib.hisparse_set_copy_mode(self.h, mode), "hisparse_set_copy_mode")

@@ -73,6 +73,8 @@ extern "C" {
 #define HISPARSE_STATUS_BAD_RESIDENT 5 /* resident block id < -1 or too large */
 #define HISPARSE_STATUS_NO_HOST_ROW 6  /* paged pool: a needed host row lies in
                                           a block the request has not reserved */
+#define HISPARSE_STATUS_CAPACITY 7     /* protected slots leave too few victims
+                                          for the misses                      */
 
 /* A slot ID with this bit set names a row of the caller's resident pool
  * (see hisparse_swap_in_resident); hot slots are below D. */
@@ -403,6 +405,21 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok,
  *                                  alone copies such a volume slowly; with
  *                                  8 or more requests: the same as FUSED. */
 int hisparse_set_copy_mode(hisparse_t h, int32_t mode);
+
+/*
+ * hisparse_set_protected_calls: keep the hot rows of a request's last
+ * `calls` swap-in calls out of the victims ([Arch] Resident device pages:
+ * speculative verification steps share the request's hot state, and a later
+ * step may not reuse a hot row before an earlier step has consumed it).  A
+ * slot whose stamp is at least max(1, tick - calls) -- selected by one of
+ * those calls; prefill stamps never count -- is not evicted.  A call whose
+ * misses outnumber the remaining non-hit slots sets status CAPACITY (checked
+ * last) and leaves the request untouched, with -1 outputs and a 0 plan count.
+ * 0 (the default) turns protection off: sub-steps resolved and consumed in
+ * stream order need none.  Read at each swap-in launch (a captured graph
+ * keeps the value it was captured with).  INVALID_ARG for calls < 0.
+ */
+int hisparse_set_protected_calls(hisparse_t h, int32_t calls);
 
 /*
  * hisparse_swap_in_noalloc: hisparse_swap_in in the split copy shape (a

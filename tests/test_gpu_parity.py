@@ -124,6 +124,37 @@ def test_arguments_in_pinned_host_memory(mode):
     p.close()
 
 
+@pytest.mark.parametrize("protect,mode", [(1, H.COPY_FUSED), (2, H.COPY_FUSED),
+                                           (2, H.COPY_SPLIT), (3, H.COPY_AUTO)])
+def test_protected_slots_parity(protect, mode):
+    """Slots of each request's last P calls are kept; calls that would need
+    them fail with CAPACITY on both sides, everything else matches."""
+    R, k, D, S = 12, 24, 64, 300
+    lens = [S] * (R - 2) + [40, 64]          # two requests on the fast path
+    w = W.custom(R, k, D, lens, row_bytes=64, seed=21)
+    p = Pair(w, track_bytes=True, copy_mode=mode)
+    p.gpu.set_protected_calls(protect)
+    p.orc.set_protected_calls(protect)
+    rng = np.random.default_rng(protect * 10 + mode)
+    failed = 0
+    for c in range(24):
+        topk = np.full((R, k), -1, dtype=np.int32)
+        for r in range(R):
+            n = min(k, lens[r])
+            # half the picks among the last 2D tokens, so hits also occur
+            pool = rng.choice(lens[r], n, replace=False) if rng.random() < 0.5 else \
+                lens[r] - 1 - rng.choice(min(lens[r], 2 * D), n, replace=False)
+            topk[r, :n] = pool
+        g, o = p.swap_in(0, topk)
+        assert_call_equal(g, o, f"call {c}")
+        failed += int((g[3] == H.STATUS_CAPACITY).sum())
+        assert_state_equal(p, 0, f"call {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"call {c}")
+    if protect >= 2:
+        assert failed > 0
+    p.close()
+
+
 @pytest.mark.parametrize("record_plan", [True, False])
 def test_auto_copy_defers_requests_with_many_misses(record_plan):
     """Auto copy mode: requests whose misses exceed 256 KB leave them to the

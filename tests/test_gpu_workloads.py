@@ -176,12 +176,16 @@ def test_pipelined_index_share_graph_double_buffered_plans():
     p.close()
 
 
-def test_speculative_substeps_with_backups():
+@pytest.mark.parametrize("protect", [0, 1])
+def test_speculative_substeps_with_backups(protect):
     """256 x 32768 tokens, D 4096, 1152 B rows: 3 verification sub-steps per
-    decode step, each with its own plan, then one backup per step."""
-    w = W.make_config(5)
+    decode step, each with its own plan, then one backup per step.  With
+    protect = 1 each sub-step also keeps the previous sub-step's rows."""
+    w = W.make_config(5, steps=16 if protect == 0 else 6)
     sched = W.topk_schedule(w)[0]
     p = Pair(w, track_bytes=False)
+    p.gpu.set_protected_calls(protect)
+    p.orc.set_protected_calls(protect)
     R, k = w.num_requests, w.top_k
     plans = [torch.empty((R, k, 2), dtype=torch.int32, device="cuda") for _ in range(3)]
     cnts = [torch.empty(R, dtype=torch.int32, device="cuda") for _ in range(3)]
