@@ -38,9 +38,10 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2
 # (pinned pages the CPU has just filled, read by the GPU for the first time);
 # these steps absorb that transient whatever W is asked for.
 SETTLE_STEPS = 16
-# decode_40k's per-step working set (~18 MB) fits in L2 many times over; its
-# headline timing rotates through this many independent batches instead of
-# flushing L2 before every step (see run_rotation).
+# `--l2 rotate`: time K steps without a per-step flush by rotating through
+# this many independent batches (see run_rotation).  Not the default: the
+# batches' pinned pools span ~16x the host memory of one batch, and on some
+# boxes steps of some batches then ran 2-3x slower.
 ROTATE_BATCHES = 16
 ROTATE_SETTLE = 24   # untimed steps of each new batch: decode_40k's misses per step settle by ~20
 
@@ -61,11 +62,11 @@ def parse():
     ap.add_argument("--host-block-tokens", type=int, default=0,
                     help="paged host pool with blocks of this many tokens, each request's "
                          "blocks scattered over the pool (0: one contiguous region per request)")
-    ap.add_argument("--l2", default="auto", choices=["auto", "flush", "rotate"],
+    ap.add_argument("--l2", default="flush", choices=["flush", "rotate"],
                     help="keep each timed step's inputs out of L2 by flushing L2 before it "
-                         "(one event pair per step) or by rotating through independent batches "
-                         "whose inputs exceed L2 (one event pair around all K steps); auto: "
-                         "rotate for decode_40k, flush for the rest")
+                         "(one event pair per step; the default) or by rotating through "
+                         "independent batches whose inputs together exceed L2 (one event pair "
+                         "around all K steps)")
     ap.add_argument("--protect-calls", type=int, default=0,
                     help="keep the hot rows of each request's last P swap-in calls (0: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -458,8 +459,7 @@ def run_gpu(args):
 
     K, Wm = args.steps, args.warmup
     S0 = SETTLE_STEPS
-    rotate = (args.l2 == "rotate" or (args.l2 == "auto" and args.config == 2)) \
-        and not args.host_block_tokens and not args.profile
+    rotate = args.l2 == "rotate" and not args.host_block_tokens and not args.profile
     extra = rotation_steps(Wm, K) if rotate else 0
     st = Setup(args.config, S0 + K + Wm + extra, rank, args.copy_mode, args.host_block_tokens,
                args.protect_calls)
