@@ -47,7 +47,8 @@ class PagedProgram:
     """GPU handle and oracle side by side on one layer, driven by a seeded
     random program of admissions, calls, backups and releases."""
 
-    def __init__(self, R, D, k, hb, ratio, cap, B, copy_mode=None, seed=0, resident_bs=0):
+    def __init__(self, R, D, k, hb, ratio, cap, B, copy_mode=None, seed=0, resident_bs=0,
+                 noalloc=False, protect=0):
         self.R, self.D, self.k, self.hb, self.B = R, D, k, hb, B
         self.cap = [cap] * R
         self.w = W.custom(R, k, D, [1] * R, row_bytes=B, capacity=self.cap, ratio=ratio,
@@ -59,6 +60,10 @@ class PagedProgram:
         assert self.gpu.host_pool_info() == (hb, self.orc.pool_blocks, self.orc.pool_blocks)
         self.rng = np.random.default_rng(seed)
         self.resident_bs = resident_bs      # > 0: resident page tables on half the calls
+        self.noalloc = noalloc              # calls through hisparse_swap_in_noalloc
+        if protect:
+            self.gpu.set_protected_calls(protect)
+            self.orc.set_protected_calls(protect)
         self.active = [False] * R
         self.S = [0] * R
         self.gen = [0] * R          # admissions of each request index so far
@@ -165,12 +170,18 @@ class PagedProgram:
                                       self.cnt)
             o = self.orc.swap_in(0, topk, seq, tab, bs)
             self.seen["resident_calls"] = self.seen.get("resident_calls", 0) + 1
+        elif self.noalloc:
+            self.gpu.swap_in_noalloc(0, t, torch.from_numpy(seq).cuda(), self.out)
+            o = self.orc.swap_in(0, topk, seq)
         else:
             self.gpu.swap_in(0, t, torch.from_numpy(seq).cuda(), self.out, self.plan, self.cnt)
             o = self.orc.swap_in(0, topk, seq)
         torch.cuda.synchronize()
-        g = (self.out.cpu().numpy(), self.plan.cpu().numpy(), self.cnt.cpu().numpy(),
-             self.gpu.status().cpu().numpy())
+        if self.noalloc:       # no plan comes back: compare what does
+            g = (self.out.cpu().numpy(), o[1], o[2], self.gpu.status().cpu().numpy())
+        else:
+            g = (self.out.cpu().numpy(), self.plan.cpu().numpy(), self.cnt.cpu().numpy(),
+                 self.gpu.status().cpu().numpy())
         assert_call_equal(g, o, "paged call")
         self.status = g[3].copy()
         self.seen["no_host_row"] += int((g[3] == H.STATUS_NO_HOST_ROW).sum())
@@ -255,6 +266,15 @@ def test_random_paged_program_with_resident_pages():
     prog = PagedProgram(6, 64, 24, 8, 2, 500, 64, seed=77, resident_bs=7)
     seen = prog.run(24)
     assert seen.get("resident_calls", 0) > 0 and seen["misses"] > 0 and seen["slow"] > 0, seen
+
+
+@pytest.mark.parametrize("noalloc,protect", [(True, 0), (False, 2), (True, 1)])
+def test_random_paged_program_noalloc_and_protected(noalloc, protect):
+    """The allocation-free split copy and protected rows on a paged pool."""
+    prog = PagedProgram(6, 64, 24, 8, 2, 500, 64, seed=91 + protect, noalloc=noalloc,
+                        protect=protect)
+    seen = prog.run(20)
+    assert seen["misses"] > 0 and seen["slow"] > 0, seen
 
 
 def test_paged_graph_capture_and_reserve_on_stream():
