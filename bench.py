@@ -54,9 +54,9 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5, 6])
     ap.add_argument("--copy-mode", default="fused", choices=["fused", "split"])
-    ap.add_argument("--replay-ctas", type=int, default=None,
-                    help="configs 4 and 6: CTAs of the skip-layer replay launch "
-                         "(default 16 for config 4, 48 for config 6)")
+    ap.add_argument("--replay-ctas", type=int, default=16,
+                    help="configs 4 and 6: CTAs of the skip-layer replay launch (the guide's "
+                         "small fixed grid; default 16)")
     ap.add_argument("--no-prefetch", action="store_true",
                     help="config 4: replay skip layers in-line on the main stream")
     ap.add_argument("--host-block-tokens", type=int, default=0,
@@ -720,7 +720,8 @@ def run_e2e(st, torch, K, Wm, rank, ws, zero_copy=True):
 def run_config4(args, ws, rank, H):
     import torch
     K, Wm = args.steps, args.warmup
-    w = W.make_config(4, steps=K + Wm)
+    S0 = SETTLE_STEPS
+    w = W.make_config(4, steps=S0 + K + Wm)
     gpu = H.HiSparse.for_workload(w)
     for l in range(w.num_layers):
         for r in range(w.num_requests):
@@ -784,7 +785,9 @@ def run_config4(args, ws, rank, H):
                 marks[2].record()
 
     prefetch = not args.no_prefetch
-    for c in range(Wm):
+    clocks = Clocks(dist_env()[2])
+    clocks.start()
+    for c in range(S0 + Wm):
         step(c, prefetch)
     torch.cuda.synchronize()
     # the replay of the last warm-up plan onto the three skip layers, alone
@@ -796,8 +799,6 @@ def run_config4(args, ws, rank, H):
         e.synchronize()
         rep_ms.append(s.elapsed_time(e))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    clocks = Clocks(dist_env()[2])
-    clocks.start()
     times, anchor_ms = [], []
     miss = torch.zeros(K, dtype=torch.int64, device="cuda")
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -807,7 +808,7 @@ def run_config4(args, ws, rank, H):
         torch.cuda.synchronize()
         marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         s.record()
-        step(Wm + i, prefetch, marks)
+        step(S0 + Wm + i, prefetch, marks)
         e.record()
         e.synchronize()
         times.append(s.elapsed_time(e))
@@ -819,7 +820,7 @@ def run_config4(args, ws, rank, H):
         flush.zero_()
         torch.cuda.synchronize()
         a0.record()
-        gpu.swap_in(0, sched[(Wm + i) % sched.shape[0]], seq, out, plan, cnt)
+        gpu.swap_in(0, sched[(S0 + Wm + i) % sched.shape[0]], seq, out, plan, cnt)
         a1.record()
         a1.synchronize()
         anchor_ms.append(a0.elapsed_time(a1))
@@ -831,7 +832,7 @@ def run_config4(args, ws, rank, H):
     replay_bytes = misses * w.row_bytes * 3
     return {
         "metric": "resolved top-k rows/s", "value": round(R * k * K / (sum(times) * 1e-3), 1),
-        "unit": "rows/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+        "unit": "rows/s", "n_gpus": ws, "steps": K, "warmup": Wm, "settle_steps": S0,
         "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int32+u8", "data": "synthetic (seeded)",
         "config": {"workload": w.name, "requests": R, "seq_len": int(w.seq_lens0[0]),
@@ -870,7 +871,8 @@ def run_pipelined(args, ws, rank, H):
     the anchor layer, and no replays (compute-only reference)."""
     import torch
     K, Wm = args.steps, args.warmup
-    w = W.make_config(6, steps=K + Wm)
+    S0 = SETTLE_STEPS
+    w = W.make_config(6, steps=S0 + K + Wm)
     w.seed = replica_seed(w.seed, rank)
     gpu = H.HiSparse.for_workload(w)
     for l in range(w.num_layers):
@@ -909,9 +911,11 @@ def run_pipelined(args, ws, rank, H):
             H.synthetic_compute(buf, 3)
 
     results = {}
+    clocks = Clocks(dist_env()[2])
+    clocks.start()
     for mode in ("prefetch", "inline", "none"):
         gpu.prefill(seq)
-        for si in range(Wm):
+        for si in range(S0 + Wm):
             step(si, mode)
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True, external=True),
@@ -921,7 +925,7 @@ def run_pipelined(args, ws, rank, H):
             for i in range(K):
                 flush.zero_()
                 ev[i][0].record()
-                step(Wm + i, mode)
+                step(S0 + Wm + i, mode)
                 ev[i][1].record()
         torch.cuda.synchronize()
         graph.replay()
@@ -929,14 +933,16 @@ def run_pipelined(args, ws, rank, H):
         t = [a.elapsed_time(b) for a, b in ev]
         results[mode] = (statistics.median(t), sum(t) * 1e-3)
         del graph
+    clk = clocks.stop()
     med = {m: v[0] for m, v in results.items()}
     total_s = max_over_ranks(results["prefetch"][1], "cuda")
     rows = R * k * len(groups) * K
     return {
         "metric": "resolved top-k rows/s", "value": round(job_throughput(rows, ws, total_s), 1),
-        "unit": "rows/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+        "unit": "rows/s", "n_gpus": ws, "steps": K, "warmup": Wm, "settle_steps": S0,
         "ms_per_step": round(total_s / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int32+u8", "data": "synthetic (seeded)",
+        "clocks": clk,
         "config": {"workload": w.name, "requests": R, "seq_len": int(w.seq_lens0[0]),
                    "layers": "4 x (1 anchor + 3 skip)", "top_k": k,
                    "device_buffer_size": w.device_buffer_size, "row_bytes": w.row_bytes,
@@ -1058,8 +1064,6 @@ def run_reference(args):
 
 def main():
     args = parse()
-    if args.replay_ctas is None:
-        args.replay_ctas = 48 if args.config == 6 else 16
     if args.impl == "reference":
         res = run_reference(args)
     else:

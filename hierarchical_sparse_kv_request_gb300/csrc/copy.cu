@@ -10,19 +10,19 @@ namespace hs {
 namespace {
 
 constexpr int REPLAY_NT = 512;
-constexpr int REPLAY_UNROLL = 8;
+constexpr int REPLAY_ROWS = 8;     // plan rows a warp takes at a time
+constexpr int REPLAY_UNROLL = 11;  // host chunks in flight per lane (8 rows of 656 B: one pass)
 
 // Copy every (host slot -> device slot) pair of a plan, host row -> device
 // slot, for each of a list of layers.  A host slot is a token position in the
 // request's region, or, with a paged host pool, a row of the layer's pool.
-// Work items are 16-byte chunks of the rows, numbered layer by layer over
-// the concatenation of all requests' plan rows;
-// each CTA first builds the prefix sum of plan counts in shared memory
-// (clamped to [0, k]), then walks its items with REPLAY_UNROLL host loads in
-// flight per thread.  One launch covers all the skip layers of an anchor, so
-// its few CTAs are placed once, ahead of the compute they overlap, and stay
-// until every layer is copied.  Pairs whose host slot or device slot is out of
-// range are skipped.
+// Work units are plan rows, numbered layer by layer over the concatenation of
+// all requests' plan rows.  Each CTA first builds the prefix sum of plan
+// counts in shared memory (clamped to [0, k]); then each warp takes
+// REPLAY_ROWS rows at a time.  One launch covers all the skip layers of an
+// anchor, so its few CTAs are placed once, ahead of the compute they overlap,
+// and stay until every layer is copied.  Pairs whose host slot or device slot
+// is out of range are skipped.
 __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
 {
     extern __shared__ __align__(16) uint32_t rows_before[];  // [R + 1]
@@ -52,47 +52,67 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
     if (tid == 0) rows_before[R] = total_rows;
     __syncthreads();
 
+    // Each warp takes REPLAY_ROWS plan rows at a time: lanes 0..REPLAY_ROWS-1
+    // resolve one row each (its request by binary search over the prefix,
+    // its plan pair, the two row addresses) into shared memory, then the
+    // warp streams the chunks of all its rows with REPLAY_UNROLL host loads in
+    // flight per lane.  Plan pairs are read once per row, not per chunk.
+    __shared__ const uint8_t *row_src[REPLAY_NT / 32][REPLAY_ROWS];
+    __shared__ uint8_t *row_dst[REPLAY_NT / 32][REPLAY_ROWS];
     const int CH = a.g.chunks;
     const int64_t B = a.g.B;
-    const uint64_t per_layer = (uint64_t)total_rows * CH;
-    const uint64_t total = per_layer * (uint64_t)a.num_layers;
-    const uint64_t stride = (uint64_t)gridDim.x * REPLAY_NT;
-    for (uint64_t e = (uint64_t)blockIdx.x * REPLAY_NT + tid; e < total;
-         e += stride * REPLAY_UNROLL) {
-        const uint8_t *src[REPLAY_UNROLL];
-        uint8_t *dst[REPLAY_UNROLL];
-#pragma unroll
-        for (int u = 0; u < REPLAY_UNROLL; ++u) {
-            src[u] = nullptr;
-            dst[u] = nullptr;
-            const uint64_t ee = e + u * stride;
-            if (ee >= total) continue;
-            const int layer = (int)(ee / per_layer);
-            const uint64_t el = ee - (uint64_t)layer * per_layer;
-            const uint32_t row = (uint32_t)(el / CH);
-            const int c = (int)(el - (uint64_t)row * CH);
-            int lo = 0, hi = R;  // last r with rows_before[r] <= row
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (rows_before[mid] <= row) lo = mid; else hi = mid;
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint64_t per_layer = total_rows;
+    const uint64_t units = per_layer * (uint64_t)a.num_layers;
+    const uint64_t wstride = (uint64_t)gridDim.x * (REPLAY_NT / 32);
+    const int elems = REPLAY_ROWS * CH;
+    for (uint64_t u0 = (uint64_t)blockIdx.x * (REPLAY_NT / 32) + warp; u0 < units;
+         u0 += wstride * REPLAY_ROWS) {
+        if (lane < REPLAY_ROWS) {
+            const uint8_t *src = nullptr;
+            uint8_t *dst = nullptr;
+            const uint64_t u = u0 + (uint64_t)lane * wstride;
+            if (u < units) {
+                const int layer = (int)(u / per_layer);
+                const uint32_t row = (uint32_t)(u - (uint64_t)layer * per_layer);
+                int lo = 0, hi = R;  // last r with rows_before[r] <= row
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (rows_before[mid] <= row) lo = mid; else hi = mid;
+                }
+                const int r = lo;
+                const int32_t *pr = a.plan_rows + ((int64_t)r * k + (row - rows_before[r])) * 2;
+                const int32_t hslot = pr[0], slot = pr[1];
+                const int64_t limit = a.g.hb ? a.g.pool_rows : a.g.host_cap[r];
+                if (hslot >= 0 && (int64_t)hslot < limit && slot >= 0 && slot < D) {
+                    const int64_t hrow = a.g.hb ? (int64_t)hslot : a.g.host_off[r] + hslot;
+                    src = a.store[layer].host + hrow * B;
+                    dst = a.store[layer].dev + ((int64_t)r * D + slot) * B;
+                }
             }
-            const int r = lo;
-            const uint32_t i = row - rows_before[r];
-            const int32_t *pr = a.plan_rows + ((int64_t)r * k + i) * 2;
-            const int32_t hslot = pr[0], slot = pr[1];
-            const int64_t limit = a.g.hb ? a.g.pool_rows : a.g.host_cap[r];
-            if (hslot < 0 || (int64_t)hslot >= limit || slot < 0 || slot >= D) continue;
-            const int64_t hrow = a.g.hb ? (int64_t)hslot : a.g.host_off[r] + hslot;
-            src[u] = a.store[layer].host + hrow * B + c * 16;
-            dst[u] = a.store[layer].dev + ((int64_t)r * D + slot) * B + c * 16;
+            row_src[warp][lane] = src;
+            row_dst[warp][lane] = dst;
         }
-        uint4 v[REPLAY_UNROLL];
+        __syncwarp();
+        for (int e = lane; e < elems; e += 32 * REPLAY_UNROLL) {
+            uint4 v[REPLAY_UNROLL];
+            uint8_t *dst[REPLAY_UNROLL];
 #pragma unroll
-        for (int u = 0; u < REPLAY_UNROLL; ++u)
-            if (src[u]) v[u] = ld_host_v4(src[u]);
+            for (int q = 0; q < REPLAY_UNROLL; ++q) {
+                dst[q] = nullptr;
+                const int ee = e + q * 32;
+                if (ee >= elems) continue;
+                const int j = ee / CH, c = ee - j * CH;
+                const uint8_t *sp = row_src[warp][j];
+                if (!sp) continue;
+                v[q] = ld_host_v4(sp + c * 16);
+                dst[q] = row_dst[warp][j] + c * 16;
+            }
 #pragma unroll
-        for (int u = 0; u < REPLAY_UNROLL; ++u)
-            if (src[u]) st_v4(dst[u], v[u]);
+            for (int q = 0; q < REPLAY_UNROLL; ++q)
+                if (dst[q]) st_v4(dst[q], v[q]);
+        }
+        __syncwarp();
     }
 }
 
