@@ -569,9 +569,9 @@ def run_gpu(args):
             * calls_per_step * K + 24 * misses
         kernel_ms = statistics.mean(call_ms)
         traffic = None
-        if w.config_no == 2 and not st.split and not st.hb:
-            traffic = profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/resolve.cu",
-                                       "resolve_kernel_decode_40k.md")
+        summary = {2: "resolve_kernel_decode_40k.md", 5: "resolve_kernel_spec_verify.md"}.get(w.config_no)
+        if summary and not st.split and not st.hb:
+            traffic = profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/resolve.cu", summary)
         roof = {"bound": "host_link", "achieved": round(miss_gbs, 1),
                 "peak": link["h2d_copy_engine_gbs"], "unit": "GB/s",
                 "frac": round(miss_gbs / link["h2d_copy_engine_gbs"], 4),
