@@ -116,12 +116,18 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
     }
 }
 
-// Backup: one thread per 16-byte chunk of each request's new row.
+// Backup: one thread per 16-byte chunk of each request's new row, for each
+// listed layer.  The layers share the positions, so a bad position or a
+// missing host row gives the same status from every layer.
 __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
 {
     const int CH = a.g.chunks;
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= (int64_t)a.g.R * CH) return;
+    const int64_t per_layer = (int64_t)a.g.R * CH;
+    const int64_t e0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e0 >= per_layer * a.num_layers) return;
+    const int li = (int)(e0 / per_layer);
+    const int64_t e = e0 - (int64_t)li * per_layer;
+    const BackupLayer &L = a.layer[li];
     const int r = (int)(e / CH), c = (int)(e - (int64_t)r * CH);
     const int32_t p = a.positions[r];
     if (p == -1) return;
@@ -138,13 +144,13 @@ __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
     }
     const int64_t B = a.g.B;
     const int D = a.g.D;
-    const uint4 v = ld_dev_v4(a.rows + (int64_t)r * B + c * 16);
-    st_v4(a.host + row * B + c * 16, v);
+    const uint4 v = ld_dev_v4(L.rows + (int64_t)r * B + c * 16);
+    st_v4(L.host + row * B + c * 16, v);
     if (p < D) {
-        st_v4(a.dev + ((int64_t)r * D + p) * B + c * 16, v);
-        if (c == 0 && a.st.tok2slot) {
-            int32_t *t2s = a.st.tok2slot + a.g.host_off[r];
-            int32_t *s2t = a.st.slot2tok + (int64_t)r * D;
+        st_v4(L.dev + ((int64_t)r * D + p) * B + c * 16, v);
+        if (c == 0 && L.st.tok2slot) {
+            int32_t *t2s = L.st.tok2slot + a.g.host_off[r];
+            int32_t *s2t = L.st.slot2tok + (int64_t)r * D;
             const int32_t old_tok = s2t[p], old_slot = t2s[p];
             if (old_tok >= 0 && old_tok != p) t2s[old_tok] = -1;
             if (old_slot >= 0 && old_slot != p) s2t[old_slot] = -1;
@@ -256,7 +262,7 @@ cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s)
 
 cudaError_t launch_backup(const BackupLaunch &a, cudaStream_t s)
 {
-    const int64_t n = (int64_t)a.g.R * a.g.chunks;
+    const int64_t n = (int64_t)a.g.R * a.g.chunks * a.num_layers;
     const int blocks = (int)((n + 255) / 256);
     backup_kernel<<<blocks, 256, 0, s>>>(a);
     return cudaGetLastError();

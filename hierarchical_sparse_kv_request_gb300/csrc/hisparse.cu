@@ -665,23 +665,38 @@ int hisparse_replay_plan(hisparse_t h, const hisparse_plan *plan, int32_t layer,
     return hisparse_replay_plan_layers(h, plan, &layer, 1, num_ctas, stream);
 }
 
-int hisparse_backup(hisparse_t h, int32_t layer, const void *rows, const int32_t *positions,
-                    void *stream)
+int hisparse_backup_layers(hisparse_t h, const int32_t *layers, int32_t num_layers,
+                           const void *rows, const int32_t *positions, void *stream)
 {
-    if (!h || !rows || !positions) return HISPARSE_ERR_INVALID_ARG;
-    if (layer < 0 || layer >= h->L) return HISPARSE_ERR_LAYER;
+    if (!h || !layers || !rows || !positions) return HISPARSE_ERR_INVALID_ARG;
+    if (num_layers < 1 || num_layers > hs::kMaxBackupLayers) return HISPARSE_ERR_INVALID_ARG;
     if (!aligned16(rows)) return HISPARSE_ERR_ALIGNMENT;
+    for (int32_t i = 0; i < num_layers; ++i) {
+        if (layers[i] < 0 || layers[i] >= h->L) return HISPARSE_ERR_LAYER;
+        for (int32_t j = 0; j < i; ++j)
+            if (layers[j] == layers[i]) return HISPARSE_ERR_INVALID_ARG;
+    }
     if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
     hs::BackupLaunch b;
-    b.rows = static_cast<const uint8_t *>(rows);
+    const int64_t layer_bytes = (int64_t)h->R * h->B;
+    for (int32_t i = 0; i < num_layers; ++i) {
+        const hs::LayerStore s = layer_store(h, layers[i]);
+        b.layer[i].rows = static_cast<const uint8_t *>(rows) + i * layer_bytes;
+        b.layer[i].host = const_cast<uint8_t *>(s.host);
+        b.layer[i].dev = s.dev;
+        b.layer[i].st = h->state[layers[i]];
+    }
+    b.num_layers = num_layers;
     b.positions = positions;
-    const hs::LayerStore s = layer_store(h, layer);
-    b.host = const_cast<uint8_t *>(s.host);
-    b.dev = s.dev;
-    b.st = h->state[layer];
     b.g = geometry(h);
     b.status = h->d_status;
     return cuda_status(hs::launch_backup(b, as_stream(stream)));
+}
+
+int hisparse_backup(hisparse_t h, int32_t layer, const void *rows, const int32_t *positions,
+                    void *stream)
+{
+    return hisparse_backup_layers(h, &layer, 1, rows, positions, stream);
 }
 
 int hisparse_status(hisparse_t h, int32_t **dev_status)

@@ -179,12 +179,19 @@ struct ReplayLaunch {
 size_t replay_smem_bytes(int R);  // below the 48 KB default for R <= 8192
 cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s);
 
-struct BackupLaunch {
-    const uint8_t *rows;      // device [R][B]
-    const int32_t *positions; // device [R]
+constexpr int kMaxBackupLayers = 16;   // layers one backup launch writes
+
+struct BackupLayer {
+    const uint8_t *rows;      // device [R][B]: the layer's new rows
     uint8_t *host;            // layer's pinned pool (device-visible)
     uint8_t *dev;             // layer's hot buffer
     HotState st;              // tok2slot == nullptr for a skip layer
+};
+
+struct BackupLaunch {
+    BackupLayer layer[kMaxBackupLayers];
+    int num_layers;
+    const int32_t *positions; // device [R], shared by the layers
     Geometry g;
     int32_t *status;
 };

@@ -78,6 +78,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_replay_plan": [P, P, I32, I32, P],
         "hisparse_replay_plan_layers": [P, P, P, I32, I32, P],
         "hisparse_backup": [P, I32, P, P, P],
+        "hisparse_backup_layers": [P, P, I32, P, P, P],
         "hisparse_status": [P, P],
         "hisparse_read_state": [P, I32, P, P, P, P, P, P],
         "hisparse_set_copy_mode": [P, I32],
@@ -331,6 +332,13 @@ class HiSparse:
     def backup(self, layer: int, rows, positions, stream=None) -> None:
         _check(self.lib.hisparse_backup(self.h, layer, _addr(rows), _addr(positions),
                                         _stream(stream)), "hisparse_backup")
+
+    def backup_layers(self, layers, rows, positions, stream=None) -> None:
+        """hisparse_backup_layers: rows is a [len(layers)][R][B] uint8 device tensor."""
+        lay = np.ascontiguousarray(layers, dtype=np.int32)
+        _check(self.lib.hisparse_backup_layers(self.h, lay.ctypes.data, len(lay), _addr(rows),
+                                               _addr(positions), _stream(stream)),
+               "hisparse_backup_layers")
 
     def set_protected_calls(self, calls: int) -> None:
         """Keep the hot rows of each request's last `calls` calls (0: off)."""

@@ -372,6 +372,18 @@ int hisparse_backup(hisparse_t h, int32_t layer, const void *rows,
                     const int32_t *positions, void *stream);
 
 /*
+ * hisparse_backup_layers: hisparse_backup for several layers in one launch.
+ *   layers     host int32 [num_layers], distinct, 1 <= num_layers <= 16.
+ *   rows       device [num_layers][R][B] bytes, 16-byte aligned: the new rows
+ *              of layers[i] at rows + i * R * B.
+ *   positions  device int32 [R], shared by the layers.
+ * The result equals num_layers hisparse_backup calls.  A bad position or a
+ * missing host row gives every layer the same status, written once or more.
+ */
+int hisparse_backup_layers(hisparse_t h, const int32_t *layers, int32_t num_layers,
+                           const void *rows, const int32_t *positions, void *stream);
+
+/*
  * hisparse_status: device pointer to the int32 [R] status array.  Every
  * hisparse_swap_in and hisparse_prefill writes each request's entry;
  * hisparse_backup writes an entry only on error.  Read it stream-ordered.

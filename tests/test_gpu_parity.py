@@ -381,6 +381,38 @@ def test_malformed_rows_set_status_and_leave_state():
     p.close()
 
 
+def test_backup_layers_in_one_launch():
+    """hisparse_backup_layers on an anchor and two skip layers equals one
+    backup per layer: host rows, device rows of short requests, maps and
+    statuses (bad positions included)."""
+    R, k, D = 4, 8, 32
+    lens = [20, 31, 100, 300]
+    w = W.custom(R, k, D, lens, row_bytes=64, layers=3, anchor_of_layer=[-1, 0, 0],
+                 capacity=[40, 33, 120, 310], seed=8)
+    p = Pair(w, track_bytes=True)
+    rng = np.random.default_rng(2)
+    for step in range(6):
+        pos = p.seq.copy()
+        if step == 3:
+            pos[1] = 40                      # past request 1's capacity: BAD_POSITION
+        if step == 4:
+            pos[2] = -1                      # skipped
+        rows = rng.integers(0, 256, (3, R, 64), dtype=np.uint8)
+        p.gpu.backup_layers([0, 1, 2], torch.from_numpy(rows).cuda(),
+                            torch.from_numpy(pos.astype(np.int32)).cuda())
+        st = [p.orc.backup(l, rows[l], pos) for l in range(3)]
+        torch.cuda.synchronize()
+        got = p.gpu.status().cpu().numpy()
+        for r in range(R):
+            if st[0][r] != 0:
+                assert got[r] == st[0][r]
+        for l in range(3):
+            assert_device_bytes_equal_oracle(p, l, f"step {step} layer {l}")
+        assert_state_equal(p, 0, f"step {step}")
+        p.advance()
+    p.close()
+
+
 def test_fast_path_grows_into_slow_path_with_backups():
     R, k, D = 3, 16, 40
     lens = [30, 38, 70]
