@@ -124,9 +124,12 @@ def test_arguments_in_pinned_host_memory(mode):
     p.close()
 
 
-@pytest.mark.parametrize("protect,mode", [(1, H.COPY_FUSED), (2, H.COPY_FUSED),
-                                           (2, H.COPY_SPLIT), (3, H.COPY_AUTO)])
-def test_protected_slots_parity(protect, mode):
+@pytest.mark.parametrize("protect,mode,resident", [(1, H.COPY_FUSED, False),
+                                                    (2, H.COPY_FUSED, False),
+                                                    (2, H.COPY_SPLIT, False),
+                                                    (3, H.COPY_AUTO, False),
+                                                    (2, H.COPY_FUSED, True)])
+def test_protected_slots_parity(protect, mode, resident):
     """Slots of each request's last P calls are kept; calls that would need
     them fail with CAPACITY on both sides, everything else matches."""
     R, k, D, S = 12, 24, 64, 300
@@ -145,12 +148,16 @@ def test_protected_slots_parity(protect, mode):
             pool = rng.choice(lens[r], n, replace=False) if rng.random() < 0.5 else \
                 lens[r] - 1 - rng.choice(min(lens[r], 2 * D), n, replace=False)
             topk[r, :n] = pool
-        g, o = p.swap_in(0, topk)
+        if resident:     # resident pages of 5 tokens, about a quarter of them
+            tab = np.where(rng.random((R, 64)) < 0.25, rng.integers(0, 500, (R, 64)), -1)
+            g, o = p.swap_in(0, topk, resident=tab.astype(np.int32), block_size=5)
+        else:
+            g, o = p.swap_in(0, topk)
         assert_call_equal(g, o, f"call {c}")
         failed += int((g[3] == H.STATUS_CAPACITY).sum())
         assert_state_equal(p, 0, f"call {c}")
         assert_device_bytes_equal_oracle(p, 0, f"call {c}")
-    if protect >= 2:
+    if protect >= 2 and not resident:
         assert failed > 0
     p.close()
 
