@@ -58,6 +58,12 @@ struct hisparse_handle {
     int32_t lowest_free = 0;           // no block below this id is free
     int32_t *d_tbl = nullptr;
 
+    // Guard bands (HISPARSE_DEBUG_GUARDS=1 at create): every device array
+    // is allocated with kGuardBytes of a known pattern on each side, and
+    // hisparse_check_guards reports arrays whose bands were overwritten.
+    bool guards = false;
+    std::vector<std::pair<uint8_t *, size_t>> guarded;   // (array, bytes)
+
     int64_t layer_rows() const { return hb ? pool_rows : total_cap; }
 };
 
@@ -110,33 +116,50 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HISPARSE_OK : HISPARSE_ERR_CUDA; }
 
+constexpr size_t kGuardBytes = 4096;
+constexpr unsigned char kGuardByte = 0xA5;
+
 template <class T>
-cudaError_t dev_alloc(T **p, size_t count)
+cudaError_t dev_alloc(hisparse_handle *h, T **p, size_t count)
 {
-    return cudaMalloc(reinterpret_cast<void **>(p), count * sizeof(T));
+    const size_t bytes = count * sizeof(T);
+    if (!h->guards) return cudaMalloc(reinterpret_cast<void **>(p), bytes);
+    uint8_t *base = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&base), bytes + 2 * kGuardBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(base, kGuardByte, bytes + 2 * kGuardBytes);
+    *p = reinterpret_cast<T *>(base + kGuardBytes);
+    h->guarded.emplace_back(base + kGuardBytes, bytes);
+    return e;
+}
+
+void dev_free(const hisparse_handle *h, void *p)
+{
+    if (!p) return;
+    cudaFree(h->guards ? static_cast<uint8_t *>(p) - kGuardBytes : p);
 }
 
 void release(hisparse_handle *h)
 {
     if (!h) return;
     for (auto &st : h->state) {
-        cudaFree(st.tok2slot);
-        cudaFree(st.slot2tok);
-        cudaFree(st.last_used);
-        cudaFree(st.lru);
-        cudaFree(st.tick);
+        dev_free(h, st.tok2slot);
+        dev_free(h, st.slot2tok);
+        dev_free(h, st.last_used);
+        dev_free(h, st.lru);
+        dev_free(h, st.tick);
     }
-    cudaFree(h->d_layers);
-    cudaFree(h->d_plan_rows);
-    cudaFree(h->d_plan_counts);
-    cudaFree(h->d_deferred);
-    cudaFree(h->d_status);
-    cudaFree(h->d_zero);
-    cudaFree(h->d_off);
-    cudaFree(h->d_cap);
-    cudaFree(h->d_tbl);
-    cudaFree(h->dev_buf);
-    if (h->host_pool) cudaFreeHost(h->host_pool);
+    dev_free(h, h->d_layers);
+    dev_free(h, h->d_plan_rows);
+    dev_free(h, h->d_plan_counts);
+    dev_free(h, h->d_deferred);
+    dev_free(h, h->d_status);
+    dev_free(h, h->d_zero);
+    dev_free(h, h->d_off);
+    dev_free(h, h->d_cap);
+    dev_free(h, h->d_tbl);
+    dev_free(h, h->dev_buf);
+    if (h->host_pool) cudaFreeHost(h->host_pool - (h->guards ? kGuardBytes : 0));
     delete h;
 }
 
@@ -290,6 +313,8 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
 
     hisparse_handle *h = new (std::nothrow) hisparse_handle;
     if (!h) return HISPARSE_ERR_NO_MEMORY;
+    const char *guards = std::getenv("HISPARSE_DEBUG_GUARDS");
+    h->guards = guards && guards[0] == '1';
     h->R = layout->num_requests;
     h->L = layout->num_layers;
     h->k = layout->top_k;
@@ -343,43 +368,48 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
     // Pinned host pool, mapped into the device address space.  A test hook
     // makes this allocation fail on request so the failure path is exercised.
     const size_t pool_bytes = (size_t)h->L * h->layer_rows() * h->B;
+    const size_t band = h->guards ? kGuardBytes : 0;   // guard bands, see hisparse_check_guards
     const char *fail = std::getenv("HISPARSE_TEST_FAIL_PINNED_ALLOC");
+    uint8_t *pool_base = nullptr;
     if ((fail && fail[0] == '1') ||
-        cudaHostAlloc(reinterpret_cast<void **>(&h->host_pool), pool_bytes,
+        cudaHostAlloc(reinterpret_cast<void **>(&pool_base), pool_bytes + 2 * band,
                       cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
-        h->host_pool = nullptr;
         cudaGetLastError();
         release(h);
         return HISPARSE_ERR_NO_MEMORY;
     }
+    h->host_pool = pool_base + band;
+    std::memset(pool_base, kGuardByte, band);
     std::memset(h->host_pool, 0, pool_bytes);
-    if (cudaHostGetDevicePointer(reinterpret_cast<void **>(&h->host_pool_dev), h->host_pool, 0) !=
-        cudaSuccess) {
+    std::memset(h->host_pool + pool_bytes, kGuardByte, band);
+    uint8_t *pool_dev = nullptr;
+    if (cudaHostGetDevicePointer(reinterpret_cast<void **>(&pool_dev), pool_base, 0) != cudaSuccess) {
         release(h);
         return HISPARSE_ERR_CUDA;
     }
+    h->host_pool_dev = pool_dev + band;
 
     const size_t buf_bytes = (size_t)h->L * h->R * h->D * h->B;
     const size_t RD = (size_t)h->R * h->D;
-    bool ok = dev_alloc(&h->dev_buf, buf_bytes) == cudaSuccess &&
-              dev_alloc(&h->d_off, (size_t)h->R) == cudaSuccess &&
-              dev_alloc(&h->d_cap, (size_t)h->R) == cudaSuccess &&
-              dev_alloc(&h->d_status, (size_t)h->R) == cudaSuccess &&
-              dev_alloc(&h->d_zero, (size_t)h->R) == cudaSuccess &&
-              dev_alloc(&h->d_layers, (size_t)h->L) == cudaSuccess &&
-              dev_alloc(&h->d_plan_rows, (size_t)h->R * h->k * 2) == cudaSuccess &&
-              dev_alloc(&h->d_plan_counts, (size_t)h->R) == cudaSuccess &&
-              dev_alloc(&h->d_deferred, (size_t)h->R) == cudaSuccess &&
-              (!paged || dev_alloc(&h->d_tbl, h->tbl.size()) == cudaSuccess);
+    bool ok = dev_alloc(h, &h->dev_buf, buf_bytes) == cudaSuccess &&
+              dev_alloc(h, &h->d_off, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(h, &h->d_cap, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(h, &h->d_status, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(h, &h->d_zero, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(h, &h->d_layers, (size_t)h->L) == cudaSuccess &&
+              dev_alloc(h, &h->d_plan_rows, (size_t)h->R * h->k * 2) == cudaSuccess &&
+              dev_alloc(h, &h->d_plan_counts, (size_t)h->R) == cudaSuccess &&
+              dev_alloc(h, &h->d_deferred, (size_t)h->R) == cudaSuccess &&
+              (!paged || dev_alloc(h, &h->d_tbl, h->tbl.size()) == cudaSuccess);
     h->state.assign(h->L, hs::HotState{nullptr, nullptr, nullptr, nullptr, nullptr});
     for (int l = 0; ok && l < h->L; ++l) {
         if (h->anchor[l] >= 0) continue;
         hs::HotState &st = h->state[l];
-        ok = dev_alloc(&st.tok2slot, (size_t)h->total_cap) == cudaSuccess &&
-             dev_alloc(&st.slot2tok, RD) == cudaSuccess &&
-             dev_alloc(&st.last_used, RD) == cudaSuccess &&
-             dev_alloc(&st.lru, RD) == cudaSuccess &&
-             dev_alloc(&st.tick, (size_t)h->R) == cudaSuccess;
+        ok = dev_alloc(h, &st.tok2slot, (size_t)h->total_cap) == cudaSuccess &&
+             dev_alloc(h, &st.slot2tok, RD) == cudaSuccess &&
+             dev_alloc(h, &st.last_used, RD) == cudaSuccess &&
+             dev_alloc(h, &st.lru, RD) == cudaSuccess &&
+             dev_alloc(h, &st.tick, (size_t)h->R) == cudaSuccess;
     }
     if (!ok) {
         cudaGetLastError();
@@ -725,6 +755,31 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok, uint32_t
     }
     if (e == cudaSuccess && ticks) e = cudaMemcpy(ticks, st.tick, (size_t)h->R * 4, cudaMemcpyDeviceToHost);
     return cuda_status(e);
+}
+
+int hisparse_check_guards(hisparse_t h, int32_t *overwritten)
+{
+    if (!h || !overwritten) return HISPARSE_ERR_INVALID_ARG;
+    if (!h->guards) return HISPARSE_ERR_UNSUPPORTED;
+    if (cudaDeviceSynchronize() != cudaSuccess) return HISPARSE_ERR_CUDA;
+    std::vector<unsigned char> band(kGuardBytes);
+    int32_t bad = 0;
+    // the pinned pool's bands, read on the host
+    const size_t pool_bytes = (size_t)h->L * h->layer_rows() * h->B;
+    for (const uint8_t *q : {h->host_pool - kGuardBytes, h->host_pool + pool_bytes})
+        for (size_t i = 0; i < kGuardBytes; ++i)
+            if (q[i] != kGuardByte) { ++bad; break; }
+    for (const auto &g : h->guarded) {
+        for (int side = 0; side < 2; ++side) {
+            const uint8_t *src = side ? g.first + g.second : g.first - kGuardBytes;
+            if (cudaMemcpy(band.data(), src, kGuardBytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+                return HISPARSE_ERR_CUDA;
+            for (unsigned char b : band)
+                if (b != kGuardByte) { ++bad; break; }
+        }
+    }
+    *overwritten = bad;
+    return HISPARSE_OK;
 }
 
 int hisparse_set_protected_calls(hisparse_t h, int32_t calls)

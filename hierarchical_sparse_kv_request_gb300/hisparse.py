@@ -83,6 +83,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_read_state": [P, I32, P, P, P, P, P, P],
         "hisparse_set_copy_mode": [P, I32],
         "hisparse_set_protected_calls": [P, I32],
+        "hisparse_check_guards": [P, P],
         "hisparse_version": [],
         "hisparse_synthetic_compute": [P, I64, I32, I32, P],
         "hisparse_link_probe": [P, P, I64, I32, P],
@@ -339,6 +340,12 @@ class HiSparse:
         _check(self.lib.hisparse_backup_layers(self.h, lay.ctypes.data, len(lay), _addr(rows),
                                                _addr(positions), _stream(stream)),
                "hisparse_backup_layers")
+
+    def check_guards(self) -> int:
+        """Overwritten guard bands (handle created with HISPARSE_DEBUG_GUARDS=1)."""
+        n = ctypes.c_int32()
+        _check(self.lib.hisparse_check_guards(self.h, ctypes.byref(n)), "hisparse_check_guards")
+        return n.value
 
     def set_protected_calls(self, calls: int) -> None:
         """Keep the hot rows of each request's last `calls` calls (0: off)."""

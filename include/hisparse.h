@@ -459,6 +459,16 @@ int hisparse_set_protected_calls(hisparse_t h, int32_t calls);
 int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_idx,
                              const int32_t *seq_lens, int32_t *out_slot_ids, void *stream);
 
+/*
+ * hisparse_check_guards: for testing.  A handle created while the
+ * environment variable HISPARSE_DEBUG_GUARDS is "1" allocates every device
+ * array it owns with a 4 KB band of a known byte on each side.  This call
+ * synchronises the device and writes to *overwritten how many bands no
+ * longer hold that byte (0 = no write left its array).  UNSUPPORTED for a
+ * handle created without the bands.
+ */
+int hisparse_check_guards(hisparse_t h, int32_t *overwritten);
+
 /* Text of a return code (static storage). */
 const char *hisparse_error_string(int code);
 
