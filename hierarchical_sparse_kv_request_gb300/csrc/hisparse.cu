@@ -757,6 +757,89 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok, uint32_t
     return cuda_status(e);
 }
 
+int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
+                         const uint32_t *last_used, const uint32_t *ticks, int32_t rebuild_rows,
+                         void *stream)
+{
+    if (!h || !slot2tok || !last_used || !ticks) return HISPARSE_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->L || h->anchor[layer] >= 0) return HISPARSE_ERR_LAYER;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
+    const int R = h->R, D = h->D;
+    const size_t RD = (size_t)R * D;
+    // the token->slot map and the LRU order follow from slot->token and
+    // the stamps; a token may sit in one slot only, and (paged pool, when
+    // rows are rebuilt) must have a host row
+    std::vector<int32_t> t2s((size_t)h->total_cap, -1);
+    std::vector<uint16_t> lru(RD);
+    std::vector<int32_t> plan;       // (host slot, slot) pairs for the rebuild, [R][D][2]
+    std::vector<int32_t> counts(R, 0);
+    if (rebuild_rows) plan.assign(RD * 2, -1);
+    std::vector<int> order(D);
+    for (int r = 0; r < R; ++r) {
+        const int32_t *s2t = slot2tok + (size_t)r * D;
+        const uint32_t *lu = last_used + (size_t)r * D;
+        for (int sl = 0; sl < D; ++sl) {
+            const int32_t t = s2t[sl];
+            if (t == -1) continue;
+            if (t < 0 || t >= h->cap[r]) return HISPARSE_ERR_INVALID_ARG;
+            int32_t &m = t2s[(size_t)h->off[r] + t];
+            if (m != -1) return HISPARSE_ERR_INVALID_ARG;
+            m = sl;
+            if (rebuild_rows) {
+                int64_t row = t;
+                if (h->hb) {
+                    const int32_t id = h->tbl[(size_t)tbl_row(h, r) + t / h->hb];
+                    if (id < 0 || t / h->hb >= h->nblocks[r]) return HISPARSE_ERR_INVALID_ARG;
+                    row = (int64_t)id * h->hb + t % h->hb;
+                }
+                int32_t *pr = &plan[((size_t)r * D + counts[r]++) * 2];
+                pr[0] = (int32_t)row;
+                pr[1] = sl;
+            }
+        }
+        for (int i = 0; i < D; ++i) order[i] = i;
+        std::sort(order.begin(), order.end(), [&](int a, int b) {
+            return lu[a] != lu[b] ? lu[a] < lu[b] : a < b;
+        });
+        for (int i = 0; i < D; ++i) lru[(size_t)r * D + i] = (uint16_t)order[i];
+    }
+    const hs::HotState &st = h->state[layer];
+    cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+    if (e == cudaSuccess) e = cudaMemcpy(st.slot2tok, slot2tok, RD * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(st.last_used, last_used, RD * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(st.tok2slot, t2s.data(), t2s.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(st.lru, lru.data(), RD * 2, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(st.tick, ticks, (size_t)R * 4, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess || !rebuild_rows) return cuda_status(e);
+    // Rebuild the hot rows of this layer and of the layers that share its
+    // slots: the replay kernel over a plan of every filled slot (k = D).
+    int32_t *d_plan = nullptr, *d_counts = nullptr;
+    e = cudaMalloc(reinterpret_cast<void **>(&d_plan), plan.size() * 4);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&d_counts), (size_t)R * 4);
+    if (e == cudaSuccess) e = cudaMemcpy(d_plan, plan.data(), plan.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(d_counts, counts.data(), (size_t)R * 4, cudaMemcpyHostToDevice);
+    std::vector<int32_t> layers{layer};
+    for (int l = 0; l < h->L; ++l)
+        if (h->anchor[l] == layer) layers.push_back(l);
+    for (size_t i0 = 0; e == cudaSuccess && i0 < layers.size(); i0 += hs::kMaxReplayLayers) {
+        hs::ReplayLaunch c;
+        c.num_layers = (int)std::min(layers.size() - i0, (size_t)hs::kMaxReplayLayers);
+        for (int i = 0; i < c.num_layers; ++i) c.store[i] = layer_store(h, layers[i0 + i]);
+        c.plan_rows = d_plan;
+        c.plan_counts = d_counts;
+        c.g = geometry(h);
+        c.g.k = D;                     // plan rows of D pairs per request
+        c.num_ctas = h->num_sms;
+        c.programmatic = false;
+        c.only_if = nullptr;
+        e = hs::launch_replay(c, nullptr);
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    cudaFree(d_plan);
+    cudaFree(d_counts);
+    return cuda_status(e);
+}
+
 int hisparse_check_guards(hisparse_t h, int32_t *overwritten)
 {
     if (!h || !overwritten) return HISPARSE_ERR_INVALID_ARG;

@@ -81,6 +81,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_backup_layers": [P, P, I32, P, P, P],
         "hisparse_status": [P, P],
         "hisparse_read_state": [P, I32, P, P, P, P, P, P],
+        "hisparse_write_state": [P, I32, P, P, P, I32, P],
         "hisparse_set_copy_mode": [P, I32],
         "hisparse_set_protected_calls": [P, I32],
         "hisparse_check_guards": [P, P],
@@ -340,6 +341,17 @@ class HiSparse:
         _check(self.lib.hisparse_backup_layers(self.h, lay.ctypes.data, len(lay), _addr(rows),
                                                _addr(positions), _stream(stream)),
                "hisparse_backup_layers")
+
+    def write_state(self, layer: int, slot2tok, last_used, ticks, rebuild_rows: bool = True,
+                    stream=None) -> None:
+        """hisparse_write_state from numpy arrays (slot2tok [R][D] int32,
+        last_used [R][D] uint32, ticks [R] uint32)."""
+        s2t = np.ascontiguousarray(slot2tok, dtype=np.int32).reshape(self.R, self.D)
+        lu = np.ascontiguousarray(last_used, dtype=np.uint32).reshape(self.R, self.D)
+        tk = np.ascontiguousarray(ticks, dtype=np.uint32).reshape(self.R)
+        _check(self.lib.hisparse_write_state(self.h, layer, s2t.ctypes.data, lu.ctypes.data,
+                                             tk.ctypes.data, 1 if rebuild_rows else 0,
+                                             _stream(stream)), "hisparse_write_state")
 
     def check_guards(self) -> int:
         """Overwritten guard bands (handle created with HISPARSE_DEBUG_GUARDS=1)."""

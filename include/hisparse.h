@@ -402,6 +402,26 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok,
                         uint32_t *last_used, int32_t *tok2slot, int32_t *lru_order,
                         uint32_t *ticks, void *stream);
 
+/*
+ * hisparse_write_state: restore a state-owning layer's hot state from host
+ * arrays, e.g. ones saved by hisparse_read_state (checkpoint and resume).
+ *   slot2tok   host int32 [R][D]: -1 or a token in [0, host_capacity[r]),
+ *              no token twice within a request.
+ *   last_used  host uint32 [R][D]; ticks host uint32 [R].
+ *   rebuild_rows  nonzero: also copy each filled slot's row from the pinned
+ *              pool into this layer's hot buffer and those of the layers
+ *              anchored on it (with a paged pool, every such token's block
+ *              must be reserved).
+ * The token->slot map and the LRU order are derived (slots sorted by
+ * (last_used, slot)).  `stream` is synchronised first; the call is
+ * synchronous and allocates scratch for the rebuild.  INVALID_ARG for a
+ * malformed slot->token row (nothing is written), LAYER for a skip layer.
+ * Not for the decode path.
+ */
+int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
+                         const uint32_t *last_used, const uint32_t *ticks, int32_t rebuild_rows,
+                         void *stream);
+
 /* hisparse_set_copy_mode: how hisparse_swap_in (and _resident) copy the
  * misses; results are identical, only the launch shape differs.
  *   HISPARSE_COPY_FUSED (default)  each request's CTA copies its own rows:

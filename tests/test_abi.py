@@ -118,6 +118,8 @@ def test_null_arguments(lib):
     assert lib.hisparse_set_copy_mode(None, 1) == H.ERR_INVALID_ARG
     assert lib.hisparse_set_protected_calls(None, 1) == H.ERR_INVALID_ARG
     assert lib.hisparse_backup_layers(None, None, 1, None, None, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_write_state(None, 0, None, None, None, 1, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_check_guards(None, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_link_probe(None, None, 16, 0, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_synthetic_compute(None, 0, 1, 1, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_create_paged(None, 16, ctypes.byref(h)) == H.ERR_INVALID_ARG

@@ -388,6 +388,60 @@ def test_malformed_rows_set_status_and_leave_state():
     p.close()
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_checkpoint_and_resume_with_write_state(paged):
+    """hisparse_read_state -> hisparse_write_state restores a layer's hot
+    state and, with rebuild_rows, its hot rows (anchor and skip layer): the
+    calls that follow give what they gave the first time."""
+    R, k, D, S = 6, 16, 48, 400
+    lens = [S] * (R - 1) + [40]
+    w = W.custom(R, k, D, lens, row_bytes=64, layers=2, anchor_of_layer=[-1, 0], seed=13)
+    p = Pair(w, track_bytes=True, host_block_tokens=8 if paged else 0)
+    rng = np.random.default_rng(6)
+    progs = [np.stack([rng.choice(L, k, replace=False) for L in lens]).astype(np.int32)
+             for _ in range(10)]
+    for c in range(4):
+        g, o = p.swap_in(0, progs[c])
+        assert_call_equal(g, o, f"call {c}")
+    saved = p.gpu.read_state(0)
+    dev_saved = [p.gpu.device_buffer(l).cpu().numpy().copy() for l in range(2)]
+    first = []
+    for c in range(4, 10):
+        g, o = p.swap_in(0, progs[c])
+        assert_call_equal(g, o, f"call {c}")
+        first.append(g)
+    # lose the state, then restore it
+    p.gpu.prefill(torch.from_numpy(np.array(lens, dtype=np.int32) // 2).cuda())
+    torch.cuda.synchronize()
+    s2t, lu, t2s, lru, ticks = saved
+    p.gpu.write_state(0, s2t, lu, ticks, rebuild_rows=True)
+    again = p.gpu.read_state(0)
+    for a, b in zip(saved, again):
+        assert np.array_equal(a, b)
+    # the anchor's rows are back as they were, and the skip layer now holds
+    # the rows of the same tokens (nothing had replayed onto it)
+    dev = p.gpu.device_buffer(0).cpu().numpy()
+    for r in range(R):
+        filled = s2t[r] >= 0
+        assert np.array_equal(dev[r][filled], dev_saved[0][r][filled]), f"anchor r{r}"
+    for l in range(2):
+        assert_device_rows(p, l, s2t, ctx=f"layer {l} after the rebuild")
+    out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    plan = torch.empty((R, k, 2), dtype=torch.int32, device="cuda")
+    cnt = torch.empty(R, dtype=torch.int32, device="cuda")
+    seq = torch.from_numpy(np.array(lens, dtype=np.int32)).cuda()
+    for i, c in enumerate(range(4, 10)):
+        p.gpu.swap_in(0, torch.from_numpy(progs[c]).cuda(), seq, out, plan, cnt)
+        torch.cuda.synchronize()
+        g = (out.cpu().numpy(), plan.cpu().numpy(), cnt.cpu().numpy(), p.gpu.status().cpu().numpy())
+        assert_call_equal(g, first[i], f"resumed call {c}")
+    bad = s2t.copy()
+    bad[1, 0] = bad[1, 1] = 5                        # a token in two slots
+    with pytest.raises(H.HiSparseError):
+        p.gpu.write_state(0, bad, lu, ticks)
+    p.close()
+
+
 def test_backup_layers_in_one_launch():
     """hisparse_backup_layers on an anchor and two skip layers equals one
     backup per layer: host rows, device rows of short requests, maps and
