@@ -28,12 +28,16 @@
  *     NVLink-C2C on GB300).  No entry point keeps a caller pointer after it
  *     returns.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
- *     stream).  Calls that take a stream are asynchronous and stream-ordered:
- *     they never synchronise and never read device data back to the host
- *     ([Arch] Performance invariants: no device scalar readback, no
- *     CPU/device metadata round trip), and they launch one kernel ([Arch]:
- *     no extra launch) -- two for hisparse_swap_in in the split and auto
- *     copy modes -- so they can be captured in a CUDA graph.
+ *     stream).  The decode-path calls that take a stream (prefill, the
+ *     swap-ins, replays, backups, host block reservation and release) are
+ *     asynchronous and stream-ordered: they never synchronise and never read
+ *     device data back to the host ([Arch] Performance invariants: no device
+ *     scalar readback, no CPU/device metadata round trip), and they launch
+ *     one kernel ([Arch]: no extra launch) -- two for a swap-in in the split
+ *     and auto copy modes, one per 128 table runs for a reservation -- so
+ *     they can be captured in a CUDA graph.  hisparse_read_state and
+ *     hisparse_write_state synchronise `stream`; they are not for the
+ *     decode path.
  *   - Problems in the *data* (a bad top-k index, a duplicate, a bad
  *     position) are reported per request in a device status array (see
  *     hisparse_status); the affected request's state is left untouched.
