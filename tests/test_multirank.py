@@ -9,7 +9,6 @@ import os
 import socket
 import sys
 
-import pytest
 import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -23,7 +22,6 @@ def _free_port() -> int:
 
 def _rank_main(rank: int, world: int, port: int, q):
     sys.path.insert(0, ROOT)
-    import numpy as np
     import torch.distributed as dist
 
     import bench

@@ -10,7 +10,6 @@ import os
 import subprocess
 import sys
 
-import numpy as np
 import pytest
 
 import oracle as O
