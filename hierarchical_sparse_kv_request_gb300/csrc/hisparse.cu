@@ -360,7 +360,7 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
     // the slot->token row rides in shared memory when it fits
     h->stage_s2t = hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, true, h->tbl_stride) <=
                    (size_t)max_smem;
-    if (hs::resolve_prepare((size_t)max_smem) != cudaSuccess) {
+    if (hs::resolve_prepare((size_t)max_smem) != cudaSuccess || hs::copy_prepare() != cudaSuccess) {
         release(h);
         return HISPARSE_ERR_CUDA;
     }

@@ -177,6 +177,9 @@ struct ReplayLaunch {
     const int32_t *only_if;  // [R] or null: copy only requests whose entry is nonzero
 };
 size_t replay_smem_bytes(int R);  // below the 48 KB default for R <= 8192
+// Load the replay, backup, prefill and table kernels up front (at handle
+// creation, outside any capture), so no first launch waits for a load.
+cudaError_t copy_prepare();
 cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s);
 
 constexpr int kMaxBackupLayers = 16;   // layers one backup launch writes
