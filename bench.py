@@ -67,6 +67,10 @@ def parse():
                          "(one event pair per step; the default) or by rotating through "
                          "independent batches whose inputs together exceed L2 (one event pair "
                          "around all K steps)")
+    ap.add_argument("--resident-recent", type=int, default=0,
+                    help="the newest N tokens of every request sit in resident pages of 64 "
+                         "tokens (ids scattered over a shared pool), checked before the hot "
+                         "buffer (hisparse_swap_in_resident); 0: no resident tier")
     ap.add_argument("--protect-calls", type=int, default=0,
                     help="keep the hot rows of each request's last P swap-in calls (0: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -190,7 +194,8 @@ def run_rotation(args, st, torch, H, K, Wm, rank, ws, first_step):
     NB = ROTATE_BATCHES
     per = rotation_steps(Wm, K)
     batches = [st] + [Setup(args.config, per, rank, args.copy_mode, 0, args.protect_calls,
-                            batch=b, rows_from=st) for b in range(1, NB)]
+                            batch=b, rows_from=st, resident_recent=args.resident_recent)
+                      for b in range(1, NB)]
     for b in batches[1:]:
         settle_host_pool(torch, H, b.gpu, w)
     pos = [first_step] + [0] * (NB - 1)
@@ -270,7 +275,8 @@ def reserve_scattered(gpu, caps, hb: int, seed: int, blocks_per_round: int = 8):
 
 class Setup:
     def __init__(self, cfg: int, steps: int, rank: int, copy_mode: str, host_block_tokens: int = 0,
-                 protect_calls: int = 0, batch: int = 0, rows_from: "Setup" = None):
+                 protect_calls: int = 0, batch: int = 0, rows_from: "Setup" = None,
+                 resident_recent: int = 0):
         """One batch of the workload on its own handle.  batch > 0 gives an
         independent batch (its own seed, state and pool); rows_from copies the
         host rows of another batch instead of generating them again."""
@@ -316,7 +322,32 @@ class Setup:
                 for l in range(w.num_layers)]) for s in range(steps)])
             self.backup_rows = torch.from_numpy(rows).cuda()   # [steps][L][R][B]
         self.valid_per_call = R * k        # the schedule never pads
+        # resident pages: block b of request r is resident (some id of a
+        # shared paged pool, scattered) when it holds one of the newest
+        # `resident_recent` tokens
+        self.resident, self.res_bs = None, 64
+        if resident_recent:
+            bs = self.res_bs
+            nb = -(-int(w.host_capacity.max()) // bs)
+            tab = np.full((R, nb), -1, dtype=np.int32)
+            rng = np.random.default_rng(w.seed)
+            firsts = [max(0, int(w.seq_lens0[r]) - resident_recent) // bs for r in range(R)]
+            count = sum(nb - f for f in firsts)
+            ids = rng.permutation(count).astype(np.int32)
+            at = 0
+            for r, f in enumerate(firsts):
+                tab[r, f:] = ids[at: at + nb - f]
+                at += nb - f
+            self.resident = torch.from_numpy(tab).cuda()
         self.launches_per_step = 0
+
+    def swap(self, l, topk, out, plan, cnt):
+        """One swap-in call of layer l, with the resident tier if configured."""
+        if self.resident is not None:
+            self.gpu.swap_in_resident(l, topk, self.seq, self.resident, self.res_bs, out, plan,
+                                      cnt)
+        else:
+            self.gpu.swap_in(l, topk, self.seq, out, plan, cnt)
 
     def step(self, s: int, call_events=None, backup_events=None, cnts=None):
         """One decode step: every swap-in call of step s, then the backups.
@@ -328,7 +359,7 @@ class Setup:
         for i, (l, c) in enumerate(self.calls_of_step(s)):
             if call_events:
                 call_events[i][0].record()
-            g.swap_in(l, self.sched[l][c], self.seq, self.out, self.plans[i], cnts[i])
+            self.swap(l, self.sched[l][c], self.out, self.plans[i], cnts[i])
             if call_events:
                 call_events[i][1].record()
         if w.backup:
@@ -462,7 +493,7 @@ def run_gpu(args):
     rotate = args.l2 == "rotate" and not args.host_block_tokens and not args.profile
     extra = rotation_steps(Wm, K) if rotate else 0
     st = Setup(args.config, S0 + K + Wm + extra, rank, args.copy_mode, args.host_block_tokens,
-               args.protect_calls)
+               args.protect_calls, resident_recent=args.resident_recent)
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -574,7 +605,10 @@ def run_gpu(args):
         kernel_ms = statistics.mean(call_ms)
         traffic = None
         summary = {2: "resolve_kernel_decode_40k.md", 5: "resolve_kernel_spec_verify.md"}.get(w.config_no)
-        if summary and not st.split and not st.hb:
+        # the summaries were captured on the plain workloads (contiguous
+        # pool, fused copy, no resident pages, no protected rows)
+        if summary and not st.split and not st.hb and not args.resident_recent \
+                and not args.protect_calls:
             traffic = profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/resolve.cu", summary)
         roof = {"bound": "host_link", "achieved": round(miss_gbs, 1),
                 "peak": link["h2d_copy_engine_gbs"], "unit": "GB/s",
@@ -600,6 +634,7 @@ def run_gpu(args):
                        "host_pool": (f"paged: {st.hb}-token blocks scattered over the pool"
                                      if st.hb else "one contiguous region per request"),
                        "protect_calls": args.protect_calls,
+                       "resident_recent": args.resident_recent,
                        "l2": (f"inputs larger than L2: {ROTATE_BATCHES} independent batches of "
                               f"{w.num_requests} requests take the steps in turn (~270 MB of other "
                               f"batches' traffic between two steps of one batch); one CUDA event "
@@ -676,10 +711,9 @@ def run_e2e(st, torch, K, Wm, rank, ws, zero_copy=True):
                 dtopk[i].copy_(stage[i], non_blocking=True)
         for i, (l, _) in enumerate(calls0):
             if zero_copy:
-                g.swap_in(l, stage[i].data_ptr(), st.seq, host_out.data_ptr(), st.plans[i],
-                          st.cnts[i])
+                st.swap(l, stage[i].data_ptr(), host_out.data_ptr(), st.plans[i], st.cnts[i])
             else:
-                g.swap_in(l, dtopk[i], st.seq, st.out, st.plans[i], st.cnts[i])
+                st.swap(l, dtopk[i], st.out, st.plans[i], st.cnts[i])
         if w.backup:
             g.backup_layers(list(range(w.num_layers)), dback, st.seq)
             st.seq += 1
@@ -794,6 +828,7 @@ def run_config4(args, ws, rank, H):
         step(c, prefetch)
     torch.cuda.synchronize()
     # the replay of the last warm-up plan onto the three skip layers, alone
+    rep_rows = int(cnt.sum().item()) * 3
     rep_ms = []
     for _ in range(3):
         s.record()
@@ -833,6 +868,17 @@ def run_config4(args, ws, rank, H):
     exposed = statistics.median(times) - compute_ms - anchor
     misses = int(miss.sum().item())
     replay_bytes = misses * w.row_bytes * 3
+    link = measure_link_peak(torch, H) if rank == 0 else None
+    rep_gbs = rep_rows * w.row_bytes / (statistics.median(rep_ms) * 1e-3) / 1e9
+    roof = None
+    if link:
+        roof = {"bound": "host_link", "achieved": round(rep_gbs, 1),
+                "peak": link["h2d_copy_engine_gbs"], "unit": "GB/s",
+                "frac": round(rep_gbs / link["h2d_copy_engine_gbs"], 4),
+                "traffic": profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/copy.cu",
+                                            "replay_kernel_shared_index.md"),
+                "kernel": "replay_kernel (one launch, three skip layers, run alone)",
+                "peak_source": "measured in this run: 1 GiB pinned cudaMemcpyAsync H2D"}
     return {
         "metric": "resolved top-k rows/s", "value": round(R * k * K / (sum(times) * 1e-3), 1),
         "unit": "rows/s", "n_gpus": ws, "steps": K, "warmup": Wm, "settle_steps": S0,
@@ -851,6 +897,7 @@ def run_config4(args, ws, rank, H):
                                  "compute": round(statistics.median(p[2] for p in phases), 4)},
         "exposed_copy_ms": round(exposed, 4),
         "replay_bytes_per_step": replay_bytes // K,
+        "roofline": roof,
         "gpu_launches": (1 + 1 + 1) * K, "clocks": clk,
         "compute_stand_in": f"bf16 elementwise stream, 1 GiB x {passes} passes, 2 x 256-thread CTAs per SM",
         "step_ms_min_median_max": [round(min(times), 4), round(statistics.median(times), 4),
