@@ -1077,6 +1077,26 @@ class OracleSteps:
                 f"their host-row copies, replays and backups, {busy:.1f} s on one core")
 
 
+def host_cpu() -> dict:
+    """The host's logical CPU count and model, for the CPU baseline's record."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model name", "CPU part"):
+            for line in info.splitlines():
+                if line.startswith(key):
+                    model = line.split(":", 1)[1].strip()
+                    break
+            if model:
+                break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "machine": platform.machine(),
+            "model": model or platform.processor() or None}
+
+
 def cpu_baseline(cfg: int, seconds: float):
     """The oracle on a bounded sample of the workload for about `seconds`."""
     run = OracleSteps(cfg)
@@ -1085,7 +1105,7 @@ def cpu_baseline(cfg: int, seconds: float):
         busy += run.step()
         steps += 1
     return {"value": round(run.rows_per_step() * steps / busy, 1), "unit": "rows/s", "cores": 1,
-            "kind": "oracle", "sample": run.sample(steps, busy)}
+            "kind": "oracle", "sample": run.sample(steps, busy), "host": host_cpu()}
 
 
 def run_reference(args):
@@ -1101,7 +1121,7 @@ def run_reference(args):
     value = round(run.rows_per_step() * args.steps / busy, 1)
     w = run.w
     cb = {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-          "sample": run.sample(args.steps, busy)}
+          "sample": run.sample(args.steps, busy), "host": host_cpu()}
     return {"impl": "reference", "metric": "resolved top-k rows/s", "value": value,
             "unit": "rows/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(busy / args.steps * 1e3, 4),
