@@ -185,6 +185,48 @@ def test_auto_copy_defers_requests_with_many_misses(record_plan):
     p.close()
 
 
+@pytest.mark.parametrize("R,k,D,B,lens_of", [
+    # one request misses ~all of k = 2048 rows of 1152 B, the others are on
+    # the fast path or miss little
+    (16, 2048, 4096, 1152, lambda R: [60000] + [3000] * 7 + [9000] * (R - 8)),
+    # more requests than SMs: the CTAs run in two waves
+    (200, 128, 256, 1152, lambda R: [600 + 30 * (r % 7) for r in range(R)]),
+])
+def test_unbalanced_misses(R, k, D, B, lens_of):
+    """Requests whose miss volumes differ by orders of magnitude, eager and
+    from a CUDA graph, match the oracle byte for byte."""
+    lens = lens_of(R)
+    w = W.custom(R, k, D, lens, row_bytes=B, seed=31)
+    p = Pair(w, track_bytes=True)
+    rng = np.random.default_rng(32)
+    topk = _random_rows(rng, R, k, lens)
+    for c in range(5):
+        g, o = p.swap_in(0, topk, record_plan=c % 2 == 0)
+        assert_call_equal(g, o, f"call {c}")
+        assert_state_equal(p, 0, f"call {c}")
+        assert_device_bytes_equal_oracle(p, 0, f"call {c}")
+        topk = _reuse_rows(rng, topk, lens, keep=0.3 if c < 2 else 0.8)
+        topk[0] = _random_rows(rng, 1, k, lens[:1])[0]     # request 0 keeps missing
+    t = torch.from_numpy(topk).cuda()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        p.gpu.swap_in(0, t, p.seq_d, p.out, p.plan, p.cnt)
+    for c in range(5, 9):
+        t.copy_(torch.from_numpy(topk))
+        graph.replay()
+        o = p.orc.swap_in(0, topk, p.seq)
+        torch.cuda.synchronize()
+        g = (p.out.cpu().numpy(), p.plan.cpu().numpy(), p.cnt.cpu().numpy(),
+             p.gpu.status().cpu().numpy())
+        assert_call_equal(g, o, f"graph call {c}")
+        topk = _reuse_rows(rng, topk, lens, keep=0.5)
+        topk[0] = _random_rows(rng, 1, k, lens[:1])[0]
+    assert_state_equal(p, 0, "end")
+    assert_device_bytes_equal_oracle(p, 0, "end")
+    p.close()
+
+
 def test_split_copy_with_the_librarys_own_plan():
     """Split copy mode without a caller plan: the resolve grid records the
     misses in the handle's internal plan and the copy grid reads them."""
