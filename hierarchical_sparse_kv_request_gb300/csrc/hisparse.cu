@@ -779,6 +779,7 @@ int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
         const int32_t *s2t = slot2tok + (size_t)r * D;
         const uint32_t *lu = last_used + (size_t)r * D;
         for (int sl = 0; sl < D; ++sl) {
+            if (lu[sl] > ticks[r]) return HISPARSE_ERR_INVALID_ARG;   // a stamp from a later call
             const int32_t t = s2t[sl];
             if (t == -1) continue;
             if (t < 0 || t >= h->cap[r]) return HISPARSE_ERR_INVALID_ARG;
@@ -816,6 +817,11 @@ int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
     int32_t *d_plan = nullptr, *d_counts = nullptr;
     e = cudaMalloc(reinterpret_cast<void **>(&d_plan), plan.size() * 4);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&d_counts), (size_t)R * 4);
+    if (e == cudaErrorMemoryAllocation) {
+        cudaGetLastError();
+        cudaFree(d_plan);
+        return HISPARSE_ERR_NO_MEMORY;
+    }
     if (e == cudaSuccess) e = cudaMemcpy(d_plan, plan.data(), plan.size() * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(d_counts, counts.data(), (size_t)R * 4, cudaMemcpyHostToDevice);
     std::vector<int32_t> layers{layer};

@@ -211,7 +211,9 @@ int hisparse_create_paged(const hisparse_layout *layout, int32_t host_block_toke
  * stream-ordered launches on `stream` (one per 128 runs of consecutive
  * ids), so order the calls that use the new blocks after it.  Capturable.
  * The caller writes the rows of new blocks (hisparse_host_block_rows) before
- * the swap-in, backup or prefill that reads them.
+ * the swap-in, backup or prefill that reads them.  CUDA (a launch failed):
+ * the host copy is rolled back, but the device copy may hold part of the
+ * change; only hisparse_destroy is safe on the handle after that.
  */
 int hisparse_host_reserve(hisparse_t h, int32_t n, const int32_t *requests,
                           const int64_t *num_tokens, void *stream);
@@ -225,7 +227,7 @@ int hisparse_host_reserve(hisparse_t h, int32_t n, const int32_t *requests,
  * must not write its rows for a new owner until the GPU work that reads the
  * old owner's rows has completed ([Arch] Spill transaction: host pages are
  * republished only after the copy event is observed).  INVALID_ARG for a
- * bad request, nothing released.
+ * bad request, nothing released.  CUDA: as for hisparse_host_reserve.
  */
 int hisparse_host_release(hisparse_t h, int32_t n, const int32_t *requests, void *stream);
 
@@ -411,7 +413,9 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok,
  * arrays, e.g. ones saved by hisparse_read_state (checkpoint and resume).
  *   slot2tok   host int32 [R][D]: -1 or a token in [0, host_capacity[r]),
  *              no token twice within a request.
- *   last_used  host uint32 [R][D]; ticks host uint32 [R].
+ *   last_used  host uint32 [R][D]; ticks host uint32 [R]; every stamp of
+ *              request r is at most ticks[r] (a stamp is the tick of the
+ *              call that selected the slot).
  *   rebuild_rows  nonzero: also copy each filled slot's row from the pinned
  *              pool into this layer's hot buffer and those of the layers
  *              anchored on it (with a paged pool, every such token's block
@@ -419,8 +423,10 @@ int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok,
  * The token->slot map and the LRU order are derived (slots sorted by
  * (last_used, slot)).  `stream` is synchronised first; the call is
  * synchronous and allocates scratch for the rebuild.  INVALID_ARG for a
- * malformed slot->token row (nothing is written), LAYER for a skip layer.
- * Not for the decode path.
+ * malformed slot->token row or a stamp above its request's tick (nothing is
+ * written), LAYER for a skip layer, NO_MEMORY when the rebuild's scratch
+ * cannot be allocated (the state is written, the rows are not).  Not for
+ * the decode path.
  */
 int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
                          const uint32_t *last_used, const uint32_t *ticks, int32_t rebuild_rows,

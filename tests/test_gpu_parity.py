@@ -481,6 +481,10 @@ def test_checkpoint_and_resume_with_write_state(paged):
     bad[1, 0] = bad[1, 1] = 5                        # a token in two slots
     with pytest.raises(H.HiSparseError):
         p.gpu.write_state(0, bad, lu, ticks)
+    late = lu.copy()
+    late[2, 3] = ticks[2] + 1                        # a stamp from a call not made yet
+    with pytest.raises(H.HiSparseError):
+        p.gpu.write_state(0, s2t, late, ticks)
     p.close()
 
 
