@@ -239,23 +239,77 @@ def run_rotation(args, st, torch, H, K, Wm, rank, ws, first_step):
     return seconds, misses, NB
 
 
-def settle_host_pool(torch, H, gpu, w, chunk: int = 256 << 20):
-    """Set-up: read every pinned pool row once from the GPU after the host
-    has written them.  The first GPU reads of pinned pages the CPU has just
-    filled are much slower (measured on GB300: the first ~10 decode steps
-    after set-up took 2-25x the steady step), a transient of set-up that a
-    long-running decode loop does not see."""
+def pool_rows_and_bases(gpu, w):
+    """Rows per layer of the handle's pinned pool and each layer's first row."""
     hb, pool_blocks, _ = gpu.host_pool_info()
     rows = pool_blocks * hb if hb else int(w.host_capacity.sum())
+    bases = [gpu.host_block_rows(l, 0).ctypes.data if hb else gpu.host_rows_ptr(l, 0)
+             for l in range(w.num_layers)]
+    return rows, bases
+
+
+def settle_host_pool(torch, H, gpu, w, chunk: int = 256 << 20, seed: int = 1):
+    """Set-up: read every pinned pool row from the GPU after the host has
+    written them, once in order and once in a random order.  Measured on
+    GB300: the first decode steps after set-up took 2-25x the steady step;
+    the first random-order reads of a freshly pinned pool ran at 10-20 GB/s
+    even after an in-order read, and at ~209 GB/s from the second pass on,
+    whichever rows the second pass read.  A transient of set-up that a
+    long-running decode loop does not see."""
+    rows, bases = pool_rows_and_bases(gpu, w)
     nbytes = rows * w.row_bytes
     tmp = torch.empty(min(chunk, nbytes), dtype=torch.uint8, device="cuda")
-    for l in range(w.num_layers):
-        base = gpu.host_block_rows(l, 0).ctypes.data if hb else gpu.host_rows_ptr(l, 0)
+    for base in bases:
         for off in range(0, nbytes, chunk):
             n = min(chunk, nbytes - off)
             H.link_probe(base + off, tmp, n)
+        random_pass(torch, H, base, rows, w.row_bytes, tmp, seed)
     torch.cuda.synchronize()
     del tmp
+
+
+def random_pass(torch, H, base: int, rows: int, row_bytes: int, tmp, seed: int):
+    """Read all `rows` rows at pinned address `base` once, in a random order,
+    through `tmp` (a device buffer).  The first random-order reads of a
+    pinned pool, and the first after device or pinned memory is freed (as
+    torch's empty_cache and a freed pinned buffer do), run at 10-20 GB/s on
+    GB300 until the pool has been read so once."""
+    per = max(1, tmp.numel() // row_bytes)
+    order = torch.from_numpy(np.random.default_rng(seed).permutation(rows).astype(np.int64)).cuda()
+    for i in range(0, rows, per):
+        H.link_gather(base, row_bytes, order[i: i + per], tmp)
+    del order
+
+
+def random_row_ceiling(torch, H, gpu, w, nrows: int, reps: int = 8, seed: int = 2):
+    """What the miss copy's access pattern reaches on its own: nrows random
+    rows of layer 0's pinned pool (one call's miss rows), gathered by one
+    full-GPU launch after an L2 flush, median over `reps` draws."""
+    rows, bases = pool_rows_and_bases(gpu, w)
+    nrows = max(1, min(int(nrows), rows))
+    rng = np.random.default_rng(seed)
+    dst = torch.empty(nrows * w.row_bytes, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    random_pass(torch, H, bases[0], rows, w.row_bytes, flush, seed + 1)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms = []
+    for _ in range(reps):
+        idx = torch.from_numpy(np.sort(rng.choice(rows, nrows, replace=False)).astype(np.int64)).cuda()
+        flush.zero_()
+        torch.cuda.synchronize()
+        s.record()
+        H.link_gather(bases[0], w.row_bytes, idx, dst)
+        e.record()
+        e.synchronize()
+        ms.append(s.elapsed_time(e))
+    t = statistics.median(ms)
+    del dst, flush
+    torch.cuda.empty_cache()
+    return {"rows": nrows, "burst_bytes": nrows * w.row_bytes, "ms": round(t, 4),
+            "gbs": round(nrows * w.row_bytes / (t * 1e-3) / 1e9, 1),
+            "how": "one launch of hisparse_link_gather (one 1024-thread CTA per SM) over random "
+                   "rows of the pool, sorted; L2 flushed; median of 8 draws; its event pair "
+                   "included, as in the step timing"}
 
 
 def reserve_scattered(gpu, caps, hb: int, seed: int, blocks_per_round: int = 8):
@@ -503,8 +557,10 @@ def run_gpu(args):
     settle_host_pool(torch, H, st.gpu, w)
     # The last IG warm-up steps run inside the timed graph: the first steps of
     # a freshly instantiated graph ran up to 10x slower (mixed_len: 5-10 ms
-    # instead of 1.07 ms for the first two), and three graph steps absorb it.
-    IG = max(1, min(Wm, 3))
+    # instead of 1.07 ms for the first two; decode_40k: 0.37 and 0.14 ms for
+    # the first and third timed steps after three graph warm-up steps, in
+    # one run of several), so up to five graph steps absorb it.
+    IG = max(1, min(Wm, 5))
     for s in range(S0 + Wm - IG):
         st.step(s)
     torch.cuda.synchronize()
@@ -594,6 +650,8 @@ def run_gpu(args):
             "slow_steps": [[i, round(t, 4)] for i, t in enumerate(step_ms)
                            if t > 2 * statistics.median(step_ms)][:16]}
         link = measure_link_peak(torch, H)
+        ceiling = random_row_ceiling(torch, H, st.gpu, w, misses / (K * calls_per_step))
+        ceiling["achieved_frac"] = round(miss_gbs / ceiling["gbs"], 4) if ceiling["gbs"] else None
         peak_hbm, hbm_src = hbm_peak()
         # algorithmic bytes of the resolution (per slow-path request per call):
         # 16k + 4D + 24m + 8; per fast-path request: 8k
@@ -654,6 +712,7 @@ def run_gpu(args):
             "link_peak": link,
             "miss_h2d_frac_of_link_peak": round(miss_gbs / link["h2d_copy_engine_gbs"], 4),
             "roofline": roof, "roofline_resolution": roof_hbm,
+            "random_row_ceiling": ceiling,
             "dominant_kernel": {"name": "resolve_kernel" + (" + replay_kernel (split copy)" if st.split else ""),
                                 "launches": len(call_ms), "mean_ms": round(kernel_ms, 5),
                                 "median_ms": round(statistics.median(call_ms), 5),
@@ -963,7 +1022,7 @@ def run_pipelined(args, ws, rank, H):
     results = {}
     clocks = Clocks(dist_env()[2])
     clocks.start()
-    IG = max(1, min(Wm, 3))        # warm-up steps inside the graph (see run_gpu)
+    IG = max(1, min(Wm, 5))        # warm-up steps inside the graph (see run_gpu)
     for mode in ("prefetch", "inline", "none"):
         gpu.prefill(seq)
         for si in range(S0 + Wm - IG):

@@ -1007,4 +1007,22 @@ int hisparse_link_probe(const void *src, void *dst, int64_t bytes, int32_t num_c
     return cuda_status(hs::launch_link_probe(src, dst, bytes, ctas, as_stream(stream)));
 }
 
+int hisparse_link_gather(const void *src, int64_t row_bytes, const int64_t *rows, int64_t n,
+                         void *dst, int32_t num_ctas, void *stream)
+{
+    if (!src || !dst || !rows || n < 0 || row_bytes <= 0 || row_bytes % 16 != 0 ||
+        row_bytes / 16 > INT32_MAX || num_ctas < 0)
+        return HISPARSE_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return HISPARSE_ERR_ALIGNMENT;
+    if (n == 0) return HISPARSE_OK;
+    int ctas = num_ctas;
+    if (ctas == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&ctas, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return HISPARSE_ERR_CUDA;
+    }
+    return cuda_status(hs::launch_link_gather(src, row_bytes, rows, n, dst, ctas, as_stream(stream)));
+}
+
 }  // extern "C"

@@ -226,5 +226,7 @@ cudaError_t launch_synthetic_compute(void *buf, int64_t bytes, int32_t passes, i
                                      cudaStream_t s);
 cudaError_t launch_link_probe(const void *src, void *dst, int64_t bytes, int num_ctas,
                               cudaStream_t s);
+cudaError_t launch_link_gather(const void *src, int64_t row_bytes, const int64_t *rows, int64_t n,
+                               void *dst, int num_ctas, cudaStream_t s);
 
 }  // namespace hs

@@ -70,7 +70,53 @@ __global__ void __launch_bounds__(PROBE_NT) link_probe_kernel(const uint8_t *src
     }
 }
 
+// Row gather: dst row i <- src row rows[i], `row_chunks` 16-byte chunks a
+// row, 8 chunks in flight per thread (the access pattern of the miss copy).
+// Idx is the chunk index type: 32-bit whenever the chunks fit, so no load
+// waits behind a 64-bit division.
+template <typename Idx>
+__global__ void __launch_bounds__(PROBE_NT) link_gather_kernel(const uint8_t *src, uint8_t *dst,
+                                                               const int64_t *rows, Idx total,
+                                                               Idx row_chunks)
+{
+    const Idx stride = (Idx)gridDim.x * PROBE_NT;
+    const int64_t B = (int64_t)row_chunks * 16;
+    for (Idx e = (Idx)blockIdx.x * PROBE_NT + threadIdx.x; e < total;
+         e += stride * PROBE_UNROLL) {
+        uint4 v[PROBE_UNROLL];
+#pragma unroll
+        for (int u = 0; u < PROBE_UNROLL; ++u) {
+            const Idx ee = e + (Idx)u * stride;
+            if (ee < total) {
+                const Idx i = ee / row_chunks, c = ee - i * row_chunks;
+                v[u] = ld_host_v4(src + rows[i] * B + (int64_t)c * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < PROBE_UNROLL; ++u) {
+            const Idx ee = e + (Idx)u * stride;
+            if (ee < total) st_v4(dst + (int64_t)ee * 16, v[u]);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_link_gather(const void *src, int64_t row_bytes, const int64_t *rows, int64_t n,
+                               void *dst, int num_ctas, cudaStream_t s)
+{
+    const int64_t chunks = row_bytes / 16, total = n * chunks;
+    // the 32-bit kernel's last stride step must not wrap either
+    const int64_t reach = total + (int64_t)num_ctas * PROBE_NT * PROBE_UNROLL;
+    if (reach <= (int64_t)UINT32_MAX)
+        link_gather_kernel<uint32_t><<<num_ctas, PROBE_NT, 0, s>>>(
+            static_cast<const uint8_t *>(src), static_cast<uint8_t *>(dst), rows, (uint32_t)total,
+            (uint32_t)chunks);
+    else
+        link_gather_kernel<int64_t><<<num_ctas, PROBE_NT, 0, s>>>(
+            static_cast<const uint8_t *>(src), static_cast<uint8_t *>(dst), rows, total, chunks);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_synthetic_compute(void *buf, int64_t bytes, int32_t passes, int32_t ctas,
                                      cudaStream_t s)

@@ -43,7 +43,10 @@ namespace {
 
 constexpr int NT = 1024;       // threads per CTA
 constexpr int PREFETCH = 4;    // host chunks per thread loaded before the victims
-constexpr int COPY_UNROLL = 8; // host chunks in flight per thread in the copy loop
+// Host chunks in flight per thread in the copy loop.  Measured on decode_40k
+// (32 CTAs): 4 ends the launch ~1.3 us sooner than 8; 2 and 6 gain less, and
+// with 128 or 256 CTAs the depth makes no difference.
+constexpr int COPY_UNROLL = 4;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -88,6 +88,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_version": [],
         "hisparse_synthetic_compute": [P, I64, I32, I32, P],
         "hisparse_link_probe": [P, P, I64, I32, P],
+        "hisparse_link_gather": [P, I64, P, I64, P, I32, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -388,6 +389,15 @@ def synthetic_compute(buf, passes: int, ctas_per_sm: int = 2, stream=None) -> No
     _check(lib.hisparse_synthetic_compute(_addr(buf), buf.numel() * buf.element_size(), passes,
                                           ctas_per_sm, _stream(stream)),
            "hisparse_synthetic_compute")
+
+
+def link_gather(src, row_bytes: int, rows, dst, num_ctas: int = 0, stream=None) -> None:
+    """hisparse_link_gather: dst row i <- src row rows[i] (rows: device int64
+    tensor, every entry in range -- the kernel does not check)."""
+    lib = load_library()
+    _check(lib.hisparse_link_gather(_addr(src), row_bytes, _addr(rows), int(rows.numel()),
+                                    _addr(dst), num_ctas, _stream(stream)),
+           "hisparse_link_gather")
 
 
 def link_probe(src, dst, nbytes: int, num_ctas: int = 0, stream=None) -> None:

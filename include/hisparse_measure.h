@@ -50,6 +50,23 @@ int hisparse_synthetic_compute(void *buf, int64_t bytes, int32_t passes, int32_t
 int hisparse_link_probe(const void *src, void *dst, int64_t bytes, int32_t num_ctas,
                         void *stream);
 
+/*
+ * hisparse_link_gather: the miss copy's access pattern without the
+ * resolver: for i < n, row i of `dst` (device, n * row_bytes bytes) <- row
+ * rows[i] of `src` (pinned host memory mapped into the device address
+ * space, rows of row_bytes bytes), 16-byte loads with 8 in flight per
+ * thread, `num_ctas` CTAs of 1024 threads (0 = one per SM).  rows: device
+ * int64 [n], each in [0, rows of src) -- the caller guarantees the range;
+ * the kernel does not check it.  row_bytes a positive multiple of 16; src
+ * and dst 16-byte aligned.  Measures what random rows reach over the host
+ * link for a given burst ([Arch] Performance invariants), and reads a pool
+ * in random order once at set-up: the first random-order reads of a freshly
+ * pinned pool are much slower than later ones, and a sequential read does
+ * not remove that.  Errors: INVALID_ARG, ALIGNMENT, CUDA.
+ */
+int hisparse_link_gather(const void *src, int64_t row_bytes, const int64_t *rows, int64_t n,
+                         void *dst, int32_t num_ctas, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -121,6 +121,7 @@ def test_null_arguments(lib):
     assert lib.hisparse_write_state(None, 0, None, None, None, 1, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_check_guards(None, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_link_probe(None, None, 16, 0, None) == H.ERR_INVALID_ARG
+    assert lib.hisparse_link_gather(None, 16, None, 1, None, 0, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_synthetic_compute(None, 0, 1, 1, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_create_paged(None, 16, ctypes.byref(h)) == H.ERR_INVALID_ARG
     assert lib.hisparse_create_paged(None, 16, None) == H.ERR_INVALID_ARG
