@@ -25,6 +25,7 @@ STATUS_OK, STATUS_BAD_INDEX, STATUS_DUPLICATE, STATUS_BAD_SEQ_LEN, STATUS_BAD_PO
 STATUS_BAD_RESIDENT, STATUS_NO_HOST_ROW, STATUS_CAPACITY = 5, 6, 7
 RESIDENT_FLAG = 1 << 30
 COPY_FUSED, COPY_SPLIT, COPY_AUTO = 1, 2, 3
+NOALLOC_SCRATCH_BYTES = 4 << 20   # HISPARSE_NOALLOC_SCRATCH_BYTES
 
 
 class HiSparseError(RuntimeError):

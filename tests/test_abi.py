@@ -135,3 +135,34 @@ def test_null_arguments(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         H.load_library(str(tmp_path / "libhisparse.so"))
+
+
+def test_binding_constants_match_the_header():
+    """The Python binding's return codes, status codes, copy modes and sizes
+    are the values include/hisparse.h defines."""
+    text = open(os.path.join(ROOT, "include", "hisparse.h")).read()
+    defs = {}
+    for name, val in re.findall(r"#define\s+HISPARSE_(\w+)\s+(\([^)]*\)|-?\w+)", text):
+        v = val.strip("()")
+        if "<<" in v:
+            a, b = v.split("<<")
+            defs[name] = int(a) << int(b)
+        else:
+            try:
+                defs[name] = int(v, 0)
+            except ValueError:
+                pass
+    pairs = {"OK": H.OK, "ERR_INVALID_ARG": H.ERR_INVALID_ARG, "ERR_LAYOUT": H.ERR_LAYOUT,
+             "ERR_CAPACITY": H.ERR_CAPACITY, "ERR_LAYER": H.ERR_LAYER, "ERR_CUDA": H.ERR_CUDA,
+             "ERR_NO_MEMORY": H.ERR_NO_MEMORY, "ERR_UNSUPPORTED": H.ERR_UNSUPPORTED,
+             "ERR_ALIGNMENT": H.ERR_ALIGNMENT,
+             "STATUS_OK": H.STATUS_OK, "STATUS_BAD_INDEX": H.STATUS_BAD_INDEX,
+             "STATUS_DUPLICATE": H.STATUS_DUPLICATE, "STATUS_BAD_SEQ_LEN": H.STATUS_BAD_SEQ_LEN,
+             "STATUS_BAD_POSITION": H.STATUS_BAD_POSITION,
+             "STATUS_BAD_RESIDENT": H.STATUS_BAD_RESIDENT,
+             "STATUS_NO_HOST_ROW": H.STATUS_NO_HOST_ROW, "STATUS_CAPACITY": H.STATUS_CAPACITY,
+             "RESIDENT_FLAG": H.RESIDENT_FLAG, "COPY_FUSED": H.COPY_FUSED,
+             "COPY_SPLIT": H.COPY_SPLIT, "COPY_AUTO": H.COPY_AUTO,
+             "NOALLOC_SCRATCH_BYTES": H.NOALLOC_SCRATCH_BYTES}
+    for name, value in pairs.items():
+        assert defs.get(name) == value, (name, defs.get(name), value)

@@ -1,7 +1,8 @@
 """Random configurations, every feature mixed: request counts, top-k and
-buffer sizes (D % 8 != 0 included), row sizes, skip layers, copy modes,
-protected rows, resident pages, padding, malformed rows, backups on every
-layer and growth from the fast path into the slow one.  Each call's outputs,
+buffer sizes (D % 8 != 0 included), row sizes, skip layers, copy modes, the
+allocation-free swap-in, paged host pools, protected rows, resident pages,
+padding, malformed rows, backups on every layer and growth from the fast
+path into the slow one.  Each call's outputs,
 the hot state and every device byte are compared with the oracle."""
 
 import numpy as np
@@ -83,13 +84,15 @@ def test_random_configuration(seed):
     w = W.custom(R, k, D, lens, row_bytes=B, layers=L, anchor_of_layer=anchors, capacity=caps,
                  seed=seed)
     mode = [H.COPY_FUSED, H.COPY_SPLIT, H.COPY_AUTO][seed % 3]
-    p = Pair(w, track_bytes=True, copy_mode=mode)
+    hb = int(rng.choice([0, 0, 1, 7, 64]))         # paged host pool, whole capacity reserved
+    p = Pair(w, track_bytes=True, copy_mode=mode, host_block_tokens=hb)
+    noalloc_ok = R * (2 * k + 1) * 4 <= H.NOALLOC_SCRATCH_BYTES
     protect = int(rng.choice([0, 0, 1, 2]))
     p.gpu.set_protected_calls(protect)
     p.orc.set_protected_calls(protect)
     owners = [l for l in range(L) if anchors[l] == -1]      # layer 0 first
     skips = [l for l in range(L) if anchors[l] == 0]
-    ctx = f"seed {seed} (R {R} k {k} D {D} B {B} L {L} mode {mode} protect {protect})"
+    ctx = f"seed {seed} (R {R} k {k} D {D} B {B} L {L} mode {mode} protect {protect} hb {hb})"
     prev = {l: None for l in owners}
     for c in range(CALLS):
         for l0 in owners:
@@ -101,6 +104,15 @@ def test_random_configuration(seed):
                 nb = int(rng.integers(1, max(2, max(caps) // bs + 2)))
                 tab = np.where(rng.random((R, nb)) < 0.3, rng.integers(0, 1000, (R, nb)), -1)
                 tab = tab.astype(np.int32)
+            if tab is None and noalloc_ok and rng.random() < 0.25:
+                # the allocation-free swap-in: no plan comes back, so no replay
+                p.gpu.swap_in_noalloc(l0, torch.from_numpy(topk).cuda(), p.seq_d, p.out)
+                o = p.orc.swap_in(l0, topk, p.seq)
+                torch.cuda.synchronize()
+                g = (p.out.cpu().numpy(), o[1], o[2], p.gpu.status().cpu().numpy())
+                assert_call_equal(g, o, f"{ctx} call {c} layer {l0} (noalloc)")
+                assert_state_equal(p, l0, f"{ctx} call {c} layer {l0} (noalloc)")
+                continue
             g, o = p.swap_in(l0, topk, resident=tab, block_size=bs)
             assert_call_equal(g, o, f"{ctx} call {c} layer {l0}")
             assert_state_equal(p, l0, f"{ctx} call {c} layer {l0}")
