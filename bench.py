@@ -38,6 +38,7 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2
 # (pinned pages the CPU has just filled, read by the GPU for the first time);
 # these steps absorb that transient whatever W is asked for.
 SETTLE_STEPS = 16
+BREAKDOWN_STEPS = 16   # steps after the timed ones that time each launch on its own
 # `--l2 rotate`: time K steps without a per-step flush by rotating through
 # this many independent batches (see run_rotation).  Not the default: the
 # batches' pinned pools span ~16x the host memory of one batch, and on some
@@ -546,8 +547,8 @@ def run_gpu(args):
     S0 = SETTLE_STEPS
     rotate = args.l2 == "rotate" and not args.host_block_tokens and not args.profile
     extra = rotation_steps(Wm, K) if rotate else 0
-    st = Setup(args.config, S0 + K + Wm + extra, rank, args.copy_mode, args.host_block_tokens,
-               args.protect_calls, resident_recent=args.resident_recent)
+    st = Setup(args.config, S0 + K + Wm + BREAKDOWN_STEPS + extra, rank, args.copy_mode,
+               args.host_block_tokens, args.protect_calls, resident_recent=args.resident_recent)
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -568,20 +569,16 @@ def run_gpu(args):
     # The last IG warm-up steps and the K timed steps (each preceded by an
     # untimed L2 flush) are captured in one CUDA graph and replayed once, so
     # host launch gaps cannot leak into the per-step event times and the
-    # graph's first-replay cost falls on warm-up steps.  Event pairs bracket
-    # every whole step, and every swap-in call when a step has several.
-    ev = [(torch.cuda.Event(enable_timing=True, external=True),
-           torch.cuda.Event(enable_timing=True, external=True)) for _ in range(K)]
+    # graph's first-replay cost falls on warm-up steps.  One event pair
+    # brackets every whole step: an event pair costs ~5 us of GPU time on
+    # GB300, so the per-call breakdown of steps with several launches comes
+    # from BREAKDOWN_STEPS more steps after the timed ones, not from them.
+    def pairs(n):
+        return [(torch.cuda.Event(enable_timing=True, external=True),
+                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
+    ev = pairs(K)
     ncalls = len(st.calls_of_step(0))
-    kev = [[(torch.cuda.Event(enable_timing=True, external=True),
-             torch.cuda.Event(enable_timing=True, external=True)) for _ in range(ncalls)]
-           for _ in range(K)]
-    # An event pair costs ~5 us of GPU time on GB300, so a step that is a
-    # single swap-in launch is not bracketed twice: its step events time the
-    # launch itself.
     inner = ncalls > 1 or w.backup
-    bev = [(torch.cuda.Event(enable_timing=True, external=True),
-            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(K)] if w.backup else None
     miss = torch.zeros(K, dtype=torch.int64, device="cuda")
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
@@ -591,8 +588,7 @@ def run_gpu(args):
         for i in range(K):
             flush.zero_()
             ev[i][0].record()
-            st.step(S0 + Wm + i, call_events=kev[i] if inner else None,
-                    backup_events=bev[i] if bev else None)
+            st.step(S0 + Wm + i)
             ev[i][1].record()
             for c in st.cnts:
                 miss[i] += c.sum()
@@ -604,13 +600,32 @@ def run_gpu(args):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    call_ms = [a.elapsed_time(b) for row in kev for a, b in row] if inner else list(step_ms)
+    call_ms, bev, breakdown_ms = list(step_ms), None, list(step_ms)
+    if inner:
+        # per-call breakdown: each swap-in call and the step's backups in
+        # their own event pairs, over steps that follow the timed ones
+        M = min(K, BREAKDOWN_STEPS)
+        sev, kev = pairs(M), [pairs(ncalls) for _ in range(M)]
+        bev = [p for p in pairs(M)] if w.backup else None
+        graph2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph2):
+            for i in range(M):
+                flush.zero_()
+                sev[i][0].record()
+                st.step(S0 + Wm + K + i, call_events=kev[i], backup_events=bev[i] if bev else None)
+                sev[i][1].record()
+        torch.cuda.synchronize()
+        graph2.replay()
+        torch.cuda.synchronize()
+        call_ms = [a.elapsed_time(b) for row in kev for a, b in row]
+        breakdown_ms = [a.elapsed_time(b) for a, b in sev]
     flush_s = max_over_ranks(sum(step_ms) * 1e-3, "cuda")
     calls_per_step = len(w.anchors) * w.substeps
     rows_per_step = st.valid_per_call * calls_per_step
     flush_misses = int(miss.sum().item())
     if rotate:
-        rot_s, misses, nb = run_rotation(args, st, torch, H, K, Wm, rank, ws, S0 + Wm + K)
+        rot_s, misses, nb = run_rotation(args, st, torch, H, K, Wm, rank, ws,
+                                         S0 + Wm + K + (min(K, BREAKDOWN_STEPS) if inner else 0))
         total_s = max_over_ranks(rot_s, "cuda")
         call_ms = [total_s * 1e3 / K] * K      # one launch per step
     else:
@@ -716,7 +731,10 @@ def run_gpu(args):
             "dominant_kernel": {"name": "resolve_kernel" + (" + replay_kernel (split copy)" if st.split else ""),
                                 "launches": len(call_ms), "mean_ms": round(kernel_ms, 5),
                                 "median_ms": round(statistics.median(call_ms), 5),
-                                "share_of_step_time": round(sum(call_ms) * 1e-3 / total_s, 4)},
+                                "share_of_step_time": round(sum(call_ms) / sum(breakdown_ms), 4),
+                                "timed_on": ("the timed steps" if not inner else
+                                             f"{len(breakdown_ms)} steps after the timed ones, each call "
+                                             f"in its own event pair")},
             "gpu_launches": st.launches() * K,
             **backup_report(w, bev, link),
             "clocks": clk, "wall_s_timed_loop": round(wall, 3),
