@@ -835,7 +835,8 @@ def run_config4(args, ws, rank, H):
     import torch
     K, Wm = args.steps, args.warmup
     S0 = SETTLE_STEPS
-    w = W.make_config(4, steps=S0 + K + Wm)
+    PH = min(K, 8)     # steps after the timed ones that record the phase ends
+    w = W.make_config(4, steps=S0 + K + Wm + PH)
     gpu = H.HiSparse.for_workload(w)
     for l in range(w.num_layers):
         for r in range(w.num_requests):
@@ -921,14 +922,23 @@ def run_config4(args, ws, rank, H):
     for i in range(K):
         flush.zero_()
         torch.cuda.synchronize()
-        marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         s.record()
-        step(S0 + Wm + i, prefetch, marks)
+        step(S0 + Wm + i, prefetch)
         e.record()
         e.synchronize()
         times.append(s.elapsed_time(e))
-        phases.append([s.elapsed_time(m) for m in marks])
         miss[i] = cnt.sum()
+    # where each phase ends, from steps after the timed ones (the extra
+    # events would add their own cost to the timed steps)
+    for i in range(PH):
+        flush.zero_()
+        torch.cuda.synchronize()
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        s.record()
+        step(S0 + Wm + K + i, prefetch, marks)
+        e.record()
+        e.synchronize()
+        phases.append([s.elapsed_time(m) for m in marks])
     clk = clocks.stop()
     # the anchor swap-in alone, for the exposed-time arithmetic
     for i in range(min(K, 8)):
