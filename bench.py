@@ -601,7 +601,7 @@ def run_gpu(args):
     wall = time.perf_counter() - wall0
     step_ms = [a.elapsed_time(b) for a, b in ev]
     call_ms, bev, breakdown_ms = list(step_ms), None, list(step_ms)
-    if inner:
+    if inner and not args.profile:
         # per-call breakdown: each swap-in call and the step's backups in
         # their own event pairs, over steps that follow the timed ones
         M = min(K, BREAKDOWN_STEPS)
@@ -625,7 +625,7 @@ def run_gpu(args):
     flush_misses = int(miss.sum().item())
     if rotate:
         rot_s, misses, nb = run_rotation(args, st, torch, H, K, Wm, rank, ws,
-                                         S0 + Wm + K + (min(K, BREAKDOWN_STEPS) if inner else 0))
+                                         S0 + Wm + K + min(K, BREAKDOWN_STEPS))
         total_s = max_over_ranks(rot_s, "cuda")
         call_ms = [total_s * 1e3 / K] * K      # one launch per step
     else:
