@@ -719,7 +719,7 @@ def run_gpu(args):
                 "ms_per_step": round(flush_s / K * 1e3, 4),
                 "value": round(job_throughput(rows_per_step * K, ws, flush_s), 1),
                 "miss_rows_per_step": round(flush_misses / K, 1),
-                "note": "an event pair costs ~5 us of GPU time on this box",
+                "note": "an event pair costs ~5 us of GPU time on GB300 (measured)",
                 **step_stats}} if rotate else step_stats),
             "miss_h2d_gbs": round(miss_gbs, 1),
             "miss_rows_per_step": round(misses / K, 1),
