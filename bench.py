@@ -581,10 +581,18 @@ def run_gpu(args):
     inner = ncalls > 1 or w.backup
     miss = torch.zeros(K, dtype=torch.int64, device="cuda")
     graph = torch.cuda.CUDAGraph()
+    warm_ev = pairs(1)[0]
     with torch.cuda.graph(graph):
         for ws_ in range(S0 + Wm - IG, S0 + Wm):
             flush.zero_()
+            # the last warm-up step is bracketed by an untimed event pair: the
+            # first timed step still came out slow (0.11-0.37 ms against a
+            # 0.051 ms median on decode_40k) in some runs without one
+            if ws_ == S0 + Wm - 1:
+                warm_ev[0].record()
             st.step(ws_)
+            if ws_ == S0 + Wm - 1:
+                warm_ev[1].record()
         for i in range(K):
             flush.zero_()
             ev[i][0].record()
