@@ -296,7 +296,9 @@ int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream);
  *                 order.
  *   out_plan      NULL, or a plan (both pointers non-NULL) to record the
  *                 misses into.
- * Per request: the tick advances by one.  If S <= D the fast path applies:
+ * Per request: the tick advances by one (a uint32: a request must be
+ * restarted with hisparse_prefill, which resets its tick, before 2^32 - 1
+ * calls, or stamps stop ordering).  If S <= D the fast path applies:
  * out = topk, nothing else changes.  Otherwise each position is looked up
  * in the token->slot map; hits keep their slot; misses, in ascending token
  * order, take the non-hit slots with the smallest (last_used, slot) in that
