@@ -16,9 +16,10 @@
 //      chunks into registers, and those loads are in flight while the
 //      victims are chosen;
 //   3. the slot->token row is staged too, so once the victims are known all
-//      state writes are plain stores that never wait behind the host loads;
-//      they are issued before the prefetched rows are consumed, then every
-//      thread streams the rest of the rows.
+//      state writes are plain stores with no loads of their own (they still
+//      queue behind the thread's host loads in flight, which keep the link
+//      busy meanwhile); they are issued before the prefetched rows are
+//      consumed, then every thread streams the rest of the rows.
 //
 // With a paged host pool ([Arch] Ownership: tokens map to logical host
 // blocks), the request's host block table row is staged as well, under the
@@ -408,8 +409,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     }
     __syncthreads();
 
-    // State writes (stores only, so nothing here waits behind the host
-    // loads in flight).  Misses take victims by ascending token rank.
+    // State writes (stores only: no load of their own to wait for).  Misses
+    // take victims by ascending token rank.
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int j = tid + i * NT;
