@@ -685,7 +685,8 @@ def run_gpu(args):
             * calls_per_step * K + 24 * misses
         kernel_ms = statistics.mean(call_ms)
         traffic = None
-        summary = {2: "resolve_kernel_decode_40k.md", 5: "resolve_kernel_spec_verify.md"}.get(w.config_no)
+        summary = {2: "resolve_kernel_decode_40k.md", 3: "resolve_kernel_mixed_len.md",
+                   5: "resolve_kernel_spec_verify.md"}.get(w.config_no)
         # the summaries were captured on the plain workloads (contiguous
         # pool, fused copy, no resident pages, no protected rows)
         if summary and not st.split and not st.hb and not args.resident_recent \
