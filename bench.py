@@ -253,10 +253,10 @@ def settle_host_pool(torch, H, gpu, w, chunk: int = 256 << 20, seed: int = 1):
     """Set-up: read every pinned pool row from the GPU after the host has
     written them, once in order and once in a random order.  Measured on
     GB300: the first decode steps after set-up took 2-25x the steady step;
-    the first random-order reads of a freshly pinned pool ran at 10-20 GB/s
-    even after an in-order read, and at ~209 GB/s from the second pass on,
-    whichever rows the second pass read.  A transient of set-up that a
-    long-running decode loop does not see."""
+    in some runs the first random-order reads of a freshly pinned pool ran
+    at 10-20 GB/s even after an in-order read, and at ~209 GB/s from the
+    second pass on.  A transient of set-up that a long-running decode loop
+    does not see (the settle steps that follow absorb what is left)."""
     rows, bases = pool_rows_and_bases(gpu, w)
     nbytes = rows * w.row_bytes
     tmp = torch.empty(min(chunk, nbytes), dtype=torch.uint8, device="cuda")
@@ -271,10 +271,10 @@ def settle_host_pool(torch, H, gpu, w, chunk: int = 256 << 20, seed: int = 1):
 
 def random_pass(torch, H, base: int, rows: int, row_bytes: int, tmp, seed: int):
     """Read all `rows` rows at pinned address `base` once, in a random order,
-    through `tmp` (a device buffer).  The first random-order reads of a
-    pinned pool, and the first after device or pinned memory is freed (as
-    torch's empty_cache and a freed pinned buffer do), run at 10-20 GB/s on
-    GB300 until the pool has been read so once."""
+    through `tmp` (a device buffer).  On GB300 the first random-order reads
+    of a pinned pool, and the first after device or pinned memory is freed
+    (as torch's empty_cache and a freed pinned buffer do), ran at 10-20 GB/s
+    in some runs until the pool had been read so once."""
     per = max(1, tmp.numel() // row_bytes)
     order = torch.from_numpy(np.random.default_rng(seed).permutation(rows).astype(np.int64)).cuda()
     for i in range(0, rows, per):
