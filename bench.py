@@ -585,9 +585,8 @@ def run_gpu(args):
     with torch.cuda.graph(graph):
         for ws_ in range(S0 + Wm - IG, S0 + Wm):
             flush.zero_()
-            # the last warm-up step is bracketed by an untimed event pair: the
-            # first timed step still came out slow (0.11-0.37 ms against a
-            # 0.051 ms median on decode_40k) in some runs without one
+            # the last warm-up step is bracketed by an untimed event pair, so
+            # the graph's first external events are not those of a timed step
             if ws_ == S0 + Wm - 1:
                 warm_ev[0].record()
             st.step(ws_)
