@@ -36,6 +36,9 @@ def test_golden_trace_gpu(name):
     S0 = ops[0][1]["S"]
     w = W.custom(1, layout["k"], layout["D"], [S0], capacity=[layout["cap"]])
     p = Pair(w, track_bytes=True)
+    if layout.get("protect"):
+        p.gpu.set_protected_calls(layout["protect"])
+        p.orc.set_protected_calls(layout["protect"])
     resident = None
     for i, (op, a) in enumerate(ops[1:]):
         if op == "resident":

@@ -26,6 +26,8 @@ def run_trace_on_oracle(name, lib_path=None):
     layout, ops = load(name)
     D, k, cap = layout["D"], layout["k"], layout["cap"]
     orc = O.Oracle(1, 1, 16, k, D, [-1], [cap], track_bytes=True, lib_path=lib_path)
+    if layout.get("protect"):
+        orc.set_protected_calls(layout["protect"])
     S = None
     resident = None
     for op, a in ops:
