@@ -439,11 +439,56 @@ def pin_protected_slots_vs_list_model(lib_path=None):
     assert counts.get("capacity", 0) > 0
 
 
+def pin_all_resident_touches_nothing(lib_path=None):
+    """Closed form ([Arch] Resident device pages: a resident hit exits before
+    the hot-LRU lookup or a host copy): with every block of a request
+    resident, each position resolves to its resident row, nothing misses and
+    only the tick moves; the same holds on the fast path."""
+    rng = np.random.default_rng(8)
+    D, k, bs = 16, 8, 4
+    lens = [100, 12]                                 # slow path, fast path
+    orc = O.Oracle(2, 1, 16, k, D, [-1], lens, lib_path=lib_path)
+    orc.prefill(lens)
+    s2t0, lu0, t2s0, _ = orc.state(0)
+    nb = max(lens) // bs + 1
+    ids = rng.permutation(2 * nb).astype(np.int32).reshape(2, nb)
+    topk = np.stack([rng.choice(S, k, replace=False) for S in lens]).astype(np.int32)
+    out, plan, cnt, st = orc.swap_in(0, topk, lens, ids, bs)
+    assert (st == 0).all() and (cnt == 0).all()
+    want = (1 << 30) | (ids[np.arange(2)[:, None], topk // bs] * bs + topk % bs)
+    assert np.array_equal(out, want)
+    s2t, lu, t2s, tick = orc.state(0)
+    assert np.array_equal(s2t, s2t0) and np.array_equal(lu, lu0) and np.array_equal(t2s, t2s0)
+    assert (tick == 1).all()
+
+
+def pin_empty_resident_table_is_the_plain_call(lib_path=None):
+    """Special case: a resident table with no resident block gives exactly
+    the plain swap-in (outputs, plans, statuses and state)."""
+    rng = np.random.default_rng(9)
+    D, k = 12, 5
+    lens = [60, 10, 90]
+    a = O.Oracle(3, 1, 16, k, D, [-1], lens, lib_path=lib_path)
+    b = O.Oracle(3, 1, 16, k, D, [-1], lens, lib_path=lib_path)
+    a.prefill(lens)
+    b.prefill(lens)
+    empty = np.full((3, 7), -1, dtype=np.int32)
+    for c in range(12):
+        topk = np.stack([rng.choice(S, k, replace=False) for S in lens]).astype(np.int32)
+        ra = a.swap_in(0, topk, lens)
+        rb = b.swap_in(0, topk, lens, empty, 3)
+        for x, y in zip(ra, rb):
+            assert np.array_equal(x, y)
+    for x, y in zip(a.state(0), b.state(0)):
+        assert np.array_equal(x, y)
+
+
 PINS = [pin_invariants_tiny_workload, pin_prefill_last_k_is_all_hits,
         pin_repeat_is_all_hits, pin_disjoint_sets_closed_form,
         pin_errors_leave_state_untouched,
         pin_backup_grows_short_request_into_slow_path,
-        pin_replay_copies_plan_rows_to_other_layer, pin_protected_slots_vs_list_model]
+        pin_replay_copies_plan_rows_to_other_layer, pin_protected_slots_vs_list_model,
+        pin_all_resident_touches_nothing, pin_empty_resident_table_is_the_plain_call]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__[4:] for p in PINS])
