@@ -176,6 +176,8 @@ int validate_layout(const hisparse_layout *l, bool paged)
     if (l->num_requests > HISPARSE_MAX_REQUESTS || l->top_k > HISPARSE_MAX_TOP_K ||
         l->device_buffer_size > HISPARSE_MAX_DEVICE_BUFFER)
         return HISPARSE_ERR_UNSUPPORTED;
+    // a call's 16-byte miss chunks per request are counted in 32 bits
+    if ((int64_t)l->top_k * (l->row_bytes / 16) > INT32_MAX) return HISPARSE_ERR_UNSUPPORTED;
     bool any_owner = false;
     for (int i = 0; i < l->num_layers; ++i) {
         const int a = l->anchor_of_layer ? l->anchor_of_layer[i] : -1;

@@ -89,6 +89,8 @@ extern "C" {
 #define HISPARSE_MAX_DEVICE_BUFFER 32768
 #define HISPARSE_MAX_HOST_CAPACITY (1 << 20) /* tokens per request          */
 #define HISPARSE_MAX_REQUESTS 8192
+/* Also: top_k * row_bytes / 16 (a call's 16-byte miss chunks per request)
+ * at most 2^31 - 1, else create returns UNSUPPORTED. */
 #define HISPARSE_MAX_HOST_BLOCK_TOKENS 65536
 
 /* Copy strategy of hisparse_swap_in (see hisparse_set_copy_mode). */

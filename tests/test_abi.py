@@ -166,3 +166,10 @@ def test_binding_constants_match_the_header():
              "NOALLOC_SCRATCH_BYTES": H.NOALLOC_SCRATCH_BYTES}
     for name, value in pairs.items():
         assert defs.get(name) == value, (name, defs.get(name), value)
+
+
+def test_create_refuses_a_chunk_count_beyond_32_bits(lib):
+    """top_k x row_bytes / 16 above 2^31 - 1 is refused before any GPU work
+    (k 8192 with 4 MB rows on a single request would fit in HBM)."""
+    rc, h = _create(lib, R=1, L=1, B_=4 << 20, k=8192, D=8192, ratio=10, caps=(8192,))
+    assert rc == H.ERR_UNSUPPORTED
