@@ -39,6 +39,13 @@ L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2
 # these steps absorb that transient whatever W is asked for.
 SETTLE_STEPS = 16
 BREAKDOWN_STEPS = 16   # steps after the timed ones that time each launch on its own
+# Kernel-only timing: each round is one CUDA graph of KONLY_WARM untimed and
+# KONLY_STEPS timed (L2 flush, step) pairs with ONE event pair around the
+# timed ones, minus the same graph of flushes alone; no event sits between
+# the launches of the timed steps.
+KONLY_ROUNDS = 3
+KONLY_WARM = 5
+KONLY_STEPS = 16
 # `--l2 rotate`: time K steps without a per-step flush by rotating through
 # this many independent batches (see run_rotation).  Not the default: the
 # batches' pinned pools span ~16x the host memory of one batch, and on some
@@ -280,6 +287,110 @@ def random_pass(torch, H, base: int, rows: int, row_bytes: int, tmp, seed: int):
     for i in range(0, rows, per):
         H.link_gather(base, row_bytes, order[i: i + per], tmp)
     del order
+
+
+def graph_ms(torch, warm, timed, replays: int = 1):
+    """Capture warm() and then timed() between one event pair in a CUDA
+    graph; replay it `replays` times and return the event times (ms).  The
+    warm part absorbs the slow first launches of a fresh graph."""
+    e0 = torch.cuda.Event(enable_timing=True, external=True)
+    e1 = torch.cuda.Event(enable_timing=True, external=True)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        warm()
+        e0.record()
+        timed()
+        e1.record()
+    out = []
+    for _ in range(replays):
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    del g
+    return out
+
+
+def flush_only_ms(torch, flush, n: int) -> float:
+    """Time of n back-to-back L2 flushes in one graph (median of 3 replays)."""
+    def many(m):
+        def f():
+            for _ in range(m):
+                flush.zero_()
+        return f
+    return statistics.median(graph_ms(torch, many(KONLY_WARM), many(n), replays=3))
+
+
+def kernel_only(torch, st, flush, first_step: int):
+    """Kernel-only step time: per round, one graph of KONLY_STEPS (flush,
+    step) pairs bracketed by one event pair, minus the flushes alone.  The
+    per-step event pairs of the main timing cost ~5 us of GPU time each on
+    GB300; here no event sits between the launches.  Returns (ms per step
+    of each round, miss rows per step)."""
+    w = st.w
+    ncalls = len(st.calls_of_step(0))
+    fl = flush_only_ms(torch, flush, KONLY_STEPS)
+    rounds, misses = [], 0
+    s = first_step
+    for _ in range(KONLY_ROUNDS):
+        cnt = [[torch.zeros(w.num_requests, dtype=torch.int32, device="cuda") for _ in range(ncalls)]
+               for _ in range(KONLY_STEPS)]
+        base = s
+
+        def warm():
+            for i in range(KONLY_WARM):
+                flush.zero_()
+                st.step(base + i)
+
+        def timed():
+            for i in range(KONLY_STEPS):
+                flush.zero_()
+                st.step(base + KONLY_WARM + i, cnts=cnt[i])
+        t = graph_ms(torch, warm, timed)[0]
+        rounds.append((t - fl) / KONLY_STEPS)
+        misses += int(sum(int(c.sum().item()) for row in cnt for c in row))
+        s += KONLY_WARM + KONLY_STEPS
+    return rounds, misses / (KONLY_ROUNDS * KONLY_STEPS), fl / KONLY_STEPS
+
+
+def random_row_ceiling_kernel_only(torch, H, gpu, w, nrows: int, seed: int = 3):
+    """The gather ceiling taken like the kernel-only step time: one graph of
+    KONLY_STEPS (flush, gather of a fresh draw of nrows random pool rows)
+    pairs with one event pair around them, minus the flushes alone, median of
+    KONLY_ROUNDS rounds.  A gather knows all its rows at launch, so its time
+    bounds from below what any kernel that must first find its misses can
+    reach for the same rows."""
+    rows, bases = pool_rows_and_bases(gpu, w)
+    nrows = max(1, min(int(nrows), rows))
+    rng = np.random.default_rng(seed)
+    dst = torch.empty(nrows * w.row_bytes, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    fl = flush_only_ms(torch, flush, KONLY_STEPS)
+    per = []
+    for _ in range(KONLY_ROUNDS):
+        idx = [torch.from_numpy(np.sort(rng.choice(rows, nrows, replace=False)).astype(np.int64)).cuda()
+               for _ in range(KONLY_WARM + KONLY_STEPS)]
+
+        def warm():
+            for i in range(KONLY_WARM):
+                flush.zero_()
+                H.link_gather(bases[0], w.row_bytes, idx[i], dst)
+
+        def timed():
+            for i in range(KONLY_STEPS):
+                flush.zero_()
+                H.link_gather(bases[0], w.row_bytes, idx[KONLY_WARM + i], dst)
+        per.append((graph_ms(torch, warm, timed)[0] - fl) / KONLY_STEPS)
+        del idx
+    t = statistics.median(per)
+    del dst, flush
+    torch.cuda.empty_cache()
+    return {"rows": nrows, "burst_bytes": nrows * w.row_bytes, "ms": round(t, 5),
+            "rounds_ms": [round(x, 5) for x in per],
+            "gbs": round(nrows * w.row_bytes / (t * 1e-3) / 1e9, 1),
+            "how": f"graphs of {KONLY_STEPS} (L2 flush, hisparse_link_gather of a fresh draw of "
+                   f"random pool rows, one 1024-thread CTA per SM) with one event pair around "
+                   f"them, minus the same flushes alone; median of {KONLY_ROUNDS} rounds"}
 
 
 def random_row_ceiling(torch, H, gpu, w, nrows: int, reps: int = 8, seed: int = 2):
@@ -547,7 +658,8 @@ def run_gpu(args):
     S0 = SETTLE_STEPS
     rotate = args.l2 == "rotate" and not args.host_block_tokens and not args.profile
     extra = rotation_steps(Wm, K) if rotate else 0
-    st = Setup(args.config, S0 + K + Wm + BREAKDOWN_STEPS + extra, rank, args.copy_mode,
+    konly_steps = KONLY_ROUNDS * (KONLY_WARM + KONLY_STEPS)
+    st = Setup(args.config, S0 + K + Wm + BREAKDOWN_STEPS + konly_steps + extra, rank, args.copy_mode,
                args.host_block_tokens, args.protect_calls, resident_recent=args.resident_recent)
     st.split = args.copy_mode == "split"
     w = st.w
@@ -608,6 +720,7 @@ def run_gpu(args):
     wall = time.perf_counter() - wall0
     step_ms = [a.elapsed_time(b) for a, b in ev]
     call_ms, bev, breakdown_ms = list(step_ms), None, list(step_ms)
+    next_step = S0 + Wm + K          # the first schedule step not run yet
     if inner and not args.profile:
         # per-call breakdown: each swap-in call and the step's backups in
         # their own event pairs, over steps that follow the timed ones
@@ -624,15 +737,23 @@ def run_gpu(args):
         torch.cuda.synchronize()
         graph2.replay()
         torch.cuda.synchronize()
+        next_step += M
         call_ms = [a.elapsed_time(b) for row in kev for a, b in row]
         breakdown_ms = [a.elapsed_time(b) for a, b in sev]
+    konly = None
+    if not args.profile:
+        k_rounds, k_miss, k_flush = kernel_only(torch, st, flush, next_step)
+        next_step += konly_steps
+        konly = {"ms_per_step": round(statistics.median(k_rounds), 5),
+                 "rounds_ms": [round(x, 5) for x in k_rounds],
+                 "miss_rows_per_step": round(k_miss, 1),
+                 "flush_ms_subtracted": round(k_flush, 5)}
     flush_s = max_over_ranks(sum(step_ms) * 1e-3, "cuda")
     calls_per_step = len(w.anchors) * w.substeps
     rows_per_step = st.valid_per_call * calls_per_step
     flush_misses = int(miss.sum().item())
     if rotate:
-        rot_s, misses, nb = run_rotation(args, st, torch, H, K, Wm, rank, ws,
-                                         S0 + Wm + K + min(K, BREAKDOWN_STEPS))
+        rot_s, misses, nb = run_rotation(args, st, torch, H, K, Wm, rank, ws, next_step)
         total_s = max_over_ranks(rot_s, "cuda")
         call_ms = [total_s * 1e3 / K] * K      # one launch per step
     else:
@@ -691,10 +812,31 @@ def run_gpu(args):
         if summary and not st.split and not st.hb and not args.resident_recent \
                 and not args.protect_calls:
             traffic = profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/resolve.cu", summary)
-        roof = {"bound": "host_link", "achieved": round(miss_gbs, 1),
-                "peak": link["h2d_copy_engine_gbs"], "unit": "GB/s",
-                "frac": round(miss_gbs / link["h2d_copy_engine_gbs"], 4),
+        peak_link = link["h2d_copy_engine_gbs"]
+        # The roofline takes the kernel-only step time: one event pair around
+        # many back-to-back (flush, step) pairs, minus the flushes.  For a
+        # one-launch step (decode_40k) that is the resolve kernel's own
+        # duration; for steps of several launches it is the step's GPU time,
+        # backups included (so the figure is conservative there).
+        ko_ms = konly["ms_per_step"]
+        ko_gbs = konly["miss_rows_per_step"] * w.row_bytes / (ko_ms * 1e-3) / 1e9
+        single = st.launches() == 1
+        konly.update({"miss_h2d_gbs": round(ko_gbs, 1),
+                      "frac_of_link_peak": round(ko_gbs / peak_link, 4),
+                      "how": f"{KONLY_ROUNDS} rounds, each one CUDA graph of {KONLY_WARM} untimed and "
+                             f"{KONLY_STEPS} timed (512 MB L2 flush, step) pairs with one event pair "
+                             f"around the timed ones, minus the same graph of flushes alone; the "
+                             f"median round", "value": round(job_throughput(rows_per_step, ws, ko_ms * 1e-3), 1),
+                      "is": "the resolve kernel's duration (one launch per step)" if single else
+                            "the step's GPU time (all its launches)"})
+        ceiling_ko = random_row_ceiling_kernel_only(torch, H, st.gpu, w, misses / (K * calls_per_step))
+        ceiling_ko["achieved_frac"] = round(ko_gbs / ceiling_ko["gbs"], 4) if single else None
+        roof = {"bound": "host_link", "achieved": round(ko_gbs, 1),
+                "peak": peak_link, "unit": "GB/s",
+                "frac": round(ko_gbs / peak_link, 4),
+                "frac_with_step_event_pairs": round(miss_gbs / peak_link, 4),
                 "traffic": traffic, "kernel": "resolve_kernel (fused resolve + miss copy)",
+                "timing": "miss bytes per step over the kernel-only step time (kernel_only)",
                 "peak_source": "measured in this run: 1 GiB pinned cudaMemcpyAsync H2D"}
         roof_hbm = {"bound": "hbm", "achieved": round(res_bytes / total_s / 1e9, 1),
                     "peak": peak_hbm, "unit": "GB/s",
@@ -736,6 +878,8 @@ def run_gpu(args):
             "miss_h2d_frac_of_link_peak": round(miss_gbs / link["h2d_copy_engine_gbs"], 4),
             "roofline": roof, "roofline_resolution": roof_hbm,
             "random_row_ceiling": ceiling,
+            "random_row_ceiling_kernel_only": ceiling_ko,
+            "kernel_only": konly,
             "dominant_kernel": {"name": "resolve_kernel" + (" + replay_kernel (split copy)" if st.split else ""),
                                 "launches": len(call_ms), "mean_ms": round(kernel_ms, 5),
                                 "median_ms": round(statistics.median(call_ms), 5),

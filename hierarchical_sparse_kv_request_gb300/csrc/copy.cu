@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
 
 // Backup: one thread per 16-byte chunk of each request's new row, for each
 // listed layer.  The layers share the positions, so a bad position or a
-// missing host row gives the same status from every layer.
+// missing host row sets the same status bit from every layer.
 __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
 {
     const int CH = a.g.chunks;
@@ -133,13 +133,13 @@ __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
     if (p == -1) return;
     const int64_t cap = a.g.host_cap[r];
     if (p < 0 || (int64_t)p >= cap) {
-        if (c == 0) a.status[r] = kStatusBadPosition;
+        if (c == 0) record_status(a.status, r, kStatusBadPosition);
         return;
     }
     // with a paged host pool the position's block must be reserved
     const int64_t row = host_row_of(a.g, r, p);
     if (row < 0) {
-        if (c == 0) a.status[r] = kStatusNoHostRow;
+        if (c == 0) record_status(a.status, r, kStatusNoHostRow);
         return;
     }
     const int64_t B = a.g.B;
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(256) prefill_kernel(const int32_t *seq_lens,
     if (S == -1) return;
     const int64_t cap = g.host_cap[r];
     if (S < 0 || (int64_t)S > cap) {
-        if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusBadSeqLen;
+        if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) record_status(status, r, kStatusBadSeqLen);
         return;
     }
     const int D = g.D;
@@ -187,11 +187,10 @@ __global__ void __launch_bounds__(256) prefill_kernel(const int32_t *seq_lens,
                 missing |= g.host_tbl[(int64_t)r * g.tbl_stride + b] < 0;
         }
         if (__syncthreads_or(missing)) {
-            if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusNoHostRow;
+            if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) record_status(status, r, kStatusNoHostRow);
             return;
         }
     }
-    if (l == 0 && blockIdx.x == 0 && threadIdx.x == 0) status[r] = kStatusOk;
     const LayerDescDev L = layers[l];
     const int64_t off = g.host_off[r];
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

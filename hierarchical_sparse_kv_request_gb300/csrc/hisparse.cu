@@ -11,13 +11,22 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
-#include <mutex>
 #include <new>
 #include <vector>
 
 #include "hisparse.h"
 #include "hisparse_measure.h"
 #include "hs_common.cuh"
+
+// Scratch of the allocation-free swap-in (hisparse_swap_in_noalloc): the miss
+// plan that its resolve grid hands to its copy grid lives in this fixed array
+// instead of device memory obtained from cudaMalloc.  Each GPU that loads the
+// library holds its own copy (HISPARSE_NOALLOC_SCRATCH_BYTES) until the
+// process exits.  Layout: (host slot, slot) pairs of request r at
+// [r * k * 2, ...), then R miss counts after the pairs region.  Host code only
+// sees a stand-in for the symbol; hisparse_create looks up the device address
+// of the array with the handle's device current and keeps it in the handle.
+static __device__ __align__(256) int32_t g_noalloc_scratch[HISPARSE_NOALLOC_SCRATCH_BYTES / 4];
 
 struct hisparse_handle {
     int device = 0;
@@ -38,6 +47,7 @@ struct hisparse_handle {
     hs::LayerDescDev *d_layers = nullptr;
     int32_t *d_plan_rows = nullptr, *d_plan_counts = nullptr;  // split-copy plan
     int32_t *d_deferred = nullptr;     // [R] requests left to the copy grid (auto mode)
+    int32_t *noalloc_scratch = nullptr; // device address of g_noalloc_scratch on this device
     int32_t copy_mode = HISPARSE_COPY_FUSED;
     int32_t protect_calls = 0;  // slots selected by the last this many calls are kept
     bool stage_s2t = false;   // resolve kernel stages the slot->token row
@@ -271,7 +281,7 @@ struct RunList {
 
 extern "C" {
 
-int hisparse_version(void) { return 100; }
+int hisparse_version(void) { return 200; }
 
 const char *hisparse_error_string(int code)
 {
@@ -365,6 +375,19 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
     if (hs::resolve_prepare((size_t)max_smem) != cudaSuccess || hs::copy_prepare() != cudaSuccess) {
         release(h);
         return HISPARSE_ERR_CUDA;
+    }
+    // The allocation-free swap-in's scratch array: looking its address up
+    // here, with the handle's device current, also loads the module that holds
+    // it (CUDA loads modules lazily by default), so that call itself never
+    // loads, looks up or allocates anything.
+    {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            release(h);
+            return HISPARSE_ERR_CUDA;
+        }
+        h->noalloc_scratch = static_cast<int32_t *>(p);
     }
 
     // Pinned host pool, mapped into the device address space.  A test hook
@@ -738,6 +761,13 @@ int hisparse_status(hisparse_t h, int32_t **dev_status)
     return HISPARSE_OK;
 }
 
+int hisparse_status_clear(hisparse_t h, void *stream)
+{
+    if (!h) return HISPARSE_ERR_INVALID_ARG;
+    if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(h->d_status, 0, sizeof(int32_t) * h->R, as_stream(stream)));
+}
+
 int hisparse_read_state(hisparse_t h, int32_t layer, int32_t *slot2tok, uint32_t *last_used,
                         int32_t *tok2slot, int32_t *lru_order, uint32_t *ticks, void *stream)
 {
@@ -890,44 +920,6 @@ int hisparse_set_copy_mode(hisparse_t h, int32_t mode)
 
 }  // extern "C"
 
-// ---- allocation-free split copy --------------------------------------------
-//
-// The miss plan that the resolve grid hands to the copy grid lives in this
-// fixed array instead of device memory obtained from cudaMalloc.  Each GPU
-// that loads the library holds its own copy (HISPARSE_NOALLOC_SCRATCH_BYTES)
-// until the process exits.  Layout: (token, slot) pairs of request r at
-// [r * k * 2, ...), then R miss counts after the pairs region.
-static __device__ __align__(256) int32_t g_noalloc_scratch[HISPARSE_NOALLOC_SCRATCH_BYTES / 4];
-
-namespace {
-
-constexpr int kNoallocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-int32_t *g_noalloc_addr[kNoallocMaxDevices] = {};
-
-// Device address of this device's copy of the array.  Host code only holds a
-// stand-in for the symbol, so the address is looked up once per device, with
-// that device current, and cached.
-int noalloc_scratch(int32_t **out)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return HISPARSE_ERR_CUDA;
-    if (dev < 0 || dev >= kNoallocMaxDevices) return HISPARSE_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return HISPARSE_ERR_CUDA;
-        }
-        g_noalloc_addr[dev] = static_cast<int32_t *>(p);
-    }
-    *out = g_noalloc_addr[dev];
-    return HISPARSE_OK;
-}
-
-}  // namespace
-
 extern "C" {
 
 int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_idx,
@@ -939,9 +931,7 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     // the pairs of all requests plus one count per request must fit the array
     const int64_t need = ((int64_t)h->R * h->k * 2 + h->R) * 4;
     if (need > HISPARSE_NOALLOC_SCRATCH_BYTES) return HISPARSE_ERR_UNSUPPORTED;
-    int32_t *scratch = nullptr;
-    const int rc = noalloc_scratch(&scratch);
-    if (rc != HISPARSE_OK) return rc;
+    int32_t *scratch = h->noalloc_scratch;   // looked up by hisparse_create
     // Nothing needs clearing between calls: the resolve grid writes every
     // request's count, and the copy grid reads only the pairs those counts
     // cover.

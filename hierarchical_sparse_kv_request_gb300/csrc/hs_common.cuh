@@ -70,6 +70,16 @@ __device__ __forceinline__ int64_t host_row_of(const Geometry &g, int r, int64_t
     return id < 0 ? -1 : (int64_t)id * g.hb + t % g.hb;
 }
 
+// Per-request status word: an error with code c sets bit c; calls that
+// succeed leave the word alone, so an error stays visible until the caller
+// clears the word (no device readback on the decode path: [Arch]
+// Performance invariants).  An atomic OR: the CTAs of several layers of one
+// launch, or of overlapping launches, may record into the same word.
+__device__ __forceinline__ void record_status(int32_t *status, int r, int code)
+{
+    atomicOr(status + r, 1 << code);
+}
+
 // ---------------------------------------------------------------------------
 // Memory access helpers.
 // ---------------------------------------------------------------------------

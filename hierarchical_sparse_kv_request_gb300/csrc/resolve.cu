@@ -138,7 +138,7 @@ __device__ __forceinline__ void finish_untouched(const ResolveLaunch &a, int r,
         a.out[(int64_t)r * k + j] = v;
     }
     if (threadIdx.x == 0) {
-        a.status[r] = status;
+        if (status != kStatusOk) record_status(a.status, r, status);
         if (a.plan_counts) a.plan_counts[r] = 0;
         if (a.deferred) a.deferred[r] = 0;
         a.st.tick[r] = tick;
@@ -450,7 +450,6 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         }
     }
     if (tid == 0) {
-        a.status[r] = kStatusOk;
         if (a.plan_counts) a.plan_counts[r] = m;
         if (a.deferred) a.deferred[r] = defer ? 1 : 0;
         a.st.tick[r] = tick;

@@ -23,9 +23,16 @@ ERR_INVALID_ARG, ERR_LAYOUT, ERR_CAPACITY, ERR_LAYER = -1, -2, -3, -4
 ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT = -5, -6, -7, -8
 STATUS_OK, STATUS_BAD_INDEX, STATUS_DUPLICATE, STATUS_BAD_SEQ_LEN, STATUS_BAD_POSITION = 0, 1, 2, 3, 4
 STATUS_BAD_RESIDENT, STATUS_NO_HOST_ROW, STATUS_CAPACITY = 5, 6, 7
+
+
+def STATUS_BIT(code: int) -> int:
+    """The bit a status code sets in a request's status word."""
+    return 1 << code
+
+
 RESIDENT_FLAG = 1 << 30
 COPY_FUSED, COPY_SPLIT, COPY_AUTO = 1, 2, 3
-NOALLOC_SCRATCH_BYTES = 4 << 20   # HISPARSE_NOALLOC_SCRATCH_BYTES
+NOALLOC_SCRATCH_BYTES = 8 << 20   # HISPARSE_NOALLOC_SCRATCH_BYTES
 
 
 class HiSparseError(RuntimeError):
@@ -81,6 +88,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_backup": [P, I32, P, P, P],
         "hisparse_backup_layers": [P, P, I32, P, P, P],
         "hisparse_status": [P, P],
+        "hisparse_status_clear": [P, P],
         "hisparse_read_state": [P, I32, P, P, P, P, P, P],
         "hisparse_write_state": [P, I32, P, P, P, I32, P],
         "hisparse_set_copy_mode": [P, I32],
@@ -274,8 +282,14 @@ class HiSparse:
         _check(self.lib.hisparse_status(self.h, ctypes.byref(p)), "hisparse_status")
         return p.value
 
+    def status_clear(self, stream=None) -> None:
+        """hisparse_status_clear: zero every request's status word (stream-ordered)."""
+        _check(self.lib.hisparse_status_clear(self.h, _stream(stream)), "hisparse_status_clear")
+
     def status(self):
-        """torch int32 CUDA tensor [R] aliasing the status array."""
+        """torch int32 CUDA tensor [R] aliasing the status words: bit
+        STATUS_BIT(code) of entry r is set for every error code request r met
+        since the handle was created or the words were last cleared."""
         import torch
 
         class _View:

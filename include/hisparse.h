@@ -39,8 +39,9 @@
  *     hisparse_write_state synchronise `stream`; they are not for the
  *     decode path.
  *   - Problems in the *data* (a bad top-k index, a duplicate, a bad
- *     position) are reported per request in a device status array (see
- *     hisparse_status); the affected request's state is left untouched.
+ *     position) are recorded per request in a device status word that keeps
+ *     them until cleared (see hisparse_status); the affected request's state
+ *     is left untouched.
  *   - A handle is not thread-safe; calls on one handle must be ordered by
  *     the caller (one stream, or events between streams).
  *   - A handle belongs to the device current at hisparse_create; calls that
@@ -68,7 +69,9 @@ extern "C" {
 #define HISPARSE_ERR_UNSUPPORTED (-7)  /* beyond this library's size limits   */
 #define HISPARSE_ERR_ALIGNMENT (-8)    /* pointer not 16-byte aligned         */
 
-/* ---- per-request status codes (device array, see hisparse_status) ----- */
+/* ---- per-request status codes (see hisparse_status: the device array
+ * holds, per request, a word with bit HISPARSE_STATUS_BIT(code) set for every
+ * error code met since the last hisparse_status_clear) ------------------ */
 #define HISPARSE_STATUS_OK 0
 #define HISPARSE_STATUS_BAD_INDEX 1    /* entry outside {-1} U [0, seq_len)   */
 #define HISPARSE_STATUS_DUPLICATE 2    /* a position selected twice           */
@@ -79,6 +82,8 @@ extern "C" {
                                           a block the request has not reserved */
 #define HISPARSE_STATUS_CAPACITY 7     /* protected slots leave too few victims
                                           for the misses                      */
+
+#define HISPARSE_STATUS_BIT(code) (1 << (code))
 
 /* A slot ID with this bit set names a row of the caller's resident pool
  * (see hisparse_swap_in_resident); hot slots are below D. */
@@ -310,7 +315,7 @@ int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream);
  * untouched and writes -1 to its outputs and 0 to its plan count; so does,
  * with a paged host pool, a miss whose host block the request has not
  * reserved (status NO_HOST_ROW, checked last).
- * Errors: INVALID_ARG, LAYER (skip layer or out of range), ALIGNMENT.
+ * Errors: INVALID_ARG, LAYER (skip layer or out of range).
  */
 int hisparse_swap_in(hisparse_t h, int32_t layer, const int32_t *topk_idx,
                      const int32_t *seq_lens, int32_t *out_slot_ids,
@@ -388,17 +393,31 @@ int hisparse_backup(hisparse_t h, int32_t layer, const void *rows,
  *              of layers[i] at rows + i * R * B.
  *   positions  device int32 [R], shared by the layers.
  * The result equals num_layers hisparse_backup calls.  A bad position or a
- * missing host row gives every layer the same status, written once or more.
+ * missing host row sets the same status bit from every layer.
  */
 int hisparse_backup_layers(hisparse_t h, const int32_t *layers, int32_t num_layers,
                            const void *rows, const int32_t *positions, void *stream);
 
 /*
- * hisparse_status: device pointer to the int32 [R] status array.  Every
- * hisparse_swap_in and hisparse_prefill writes each request's entry;
- * hisparse_backup writes an entry only on error.  Read it stream-ordered.
+ * hisparse_status: device pointer to the int32 [R] status array ([Arch]
+ * Performance invariants: no device readback on the decode path, so a data
+ * error stays on the device until the caller reads it).  Entry r is a word
+ * of error bits: every call that meets an error for request r -- a swap-in
+ * (any variant, any layer), a prefill or a backup -- sets bit
+ * HISPARSE_STATUS_BIT(code) of it, and calls that succeed leave it alone, so
+ * an error of layer 0 is still visible after a whole multi-layer step (for
+ * example one CUDA graph) has run.  0 = no error since the handle was created
+ * or the word was last cleared (hisparse_status_clear).  The entry is
+ * written with an atomic OR.  Read it stream-ordered.
  */
 int hisparse_status(hisparse_t h, int32_t **dev_status);
+
+/*
+ * hisparse_status_clear: reset every request's status word to 0, stream-
+ * ordered on `stream` (one memset node; capturable).  Nothing else clears
+ * it.  Errors: INVALID_ARG, CUDA.
+ */
+int hisparse_status_clear(hisparse_t h, void *stream);
 
 /*
  * hisparse_read_state: synchronous copy of a state-owning layer's hot state
@@ -474,22 +493,24 @@ int hisparse_set_protected_calls(hisparse_t h, int32_t calls);
  * is owned up front by one pool, or a call site that runs where allocation
  * is forbidden.  The miss plan handed from the resolve grid to the copy grid
  * lives in a fixed array of HISPARSE_NOALLOC_SCRATCH_BYTES inside the library
- * (one per GPU, held from the library's loading until the process exits)
- * instead of memory from cudaMalloc; this call allocates nothing, and no plan
- * is returned to the caller.  Arguments, results and status codes are those
- * of hisparse_swap_in with out_plan = NULL.
+ * (one per GPU, held until the process exits) instead of memory from
+ * cudaMalloc; this call allocates nothing, and no plan is returned to the
+ * caller.  Arguments, results and status codes are those of hisparse_swap_in
+ * with out_plan = NULL.
  *   - The array must hold (2 * top_k + 1) * num_requests int32 values; a
  *     larger handle gets HISPARSE_ERR_UNSUPPORTED and nothing is launched.
- *   - The first call on each device looks the array's device address up
- *     (cudaGetSymbolAddress) with that device current and caches it; make
- *     that first call outside any stream capture.
+ *   - hisparse_create looks the array's device address up
+ *     (cudaGetSymbolAddress, with the handle's device current), which also
+ *     loads the part of the library that holds it, and keeps the address in
+ *     the handle; this call itself loads, looks up and allocates nothing.
+ *     After a device reset the handle is invalid anyway: create a new one.
  *   - Every call on a device shares the one array and leaves the last call's
  *     contents in it.  Each call writes everything it later reads, so nothing
  *     needs clearing, but calls whose work overlaps on the GPU (two streams,
  *     two handles) race on it: order them.
  * The pages this library follows have no counterpart to this call.
  */
-#define HISPARSE_NOALLOC_SCRATCH_BYTES (4 << 20)
+#define HISPARSE_NOALLOC_SCRATCH_BYTES (8 << 20)
 int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_idx,
                              const int32_t *seq_lens, int32_t *out_slot_ids, void *stream);
 

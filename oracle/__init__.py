@@ -73,6 +73,8 @@ def _load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.hso_replay.argtypes = [P, P, P, I]
     lib.hso_backup.argtypes = [P, I, P, P, P]
     lib.hso_state.argtypes = [P, I, P, P, P, P]
+    lib.hso_status_word.argtypes = [P, P]
+    lib.hso_status_clear.argtypes = [P]
     lib.hso_total_capacity.restype = I64
     lib.hso_total_capacity.argtypes = [P]
     _libs[path] = lib
@@ -236,6 +238,16 @@ class Oracle:
         if self.lib.hso_backup(self.h, layer, _ptr(rw), _ptr(pos), _ptr(st)) != 0:
             raise ValueError("bad layer")
         return st
+
+    def status_word(self) -> np.ndarray:
+        """int32 [R]: per request, the OR of (1 << code) over every error
+        code a call returned for it since creation or the last clear."""
+        words = np.empty(self.R, dtype=np.int32)
+        self.lib.hso_status_word(self.h, _ptr(words))
+        return words
+
+    def status_clear(self) -> None:
+        self.lib.hso_status_clear(self.h)
 
     def state(self, layer: int):
         """(slot2tok [R][D], last_used [R][D], tok2slot [total_cap], ticks [R])."""

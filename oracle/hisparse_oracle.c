@@ -41,6 +41,14 @@
  *     not reserved sets status NO_HOST_ROW and leaves the request untouched.
  *     A plan then records the host row in the layer's pool (block * hb +
  *     token % hb), the "host slot" a replay reads;
+ *   - per-request status word ([Arch] Performance invariants: no device
+ *     readback on the decode path, so an error has to stay recorded on the
+ *     device until the caller reads it, even when later calls of the same
+ *     step -- other layers, later sub-steps, backups -- succeed): besides each
+ *     call's own status code, every request keeps a word of error bits; a
+ *     call that ends with code c != OK for the request ORs bit c (1 << c) into
+ *     it -- swap-ins, prefills and backups alike, on any layer -- and a
+ *     successful call leaves it alone.  Only an explicit clear resets it;
  *   - optional protection ([Arch] Resident device pages: speculative
  *     verification steps share the hot state, and a later step may not reuse
  *     a hot row before an earlier step has consumed it): with P > 0, a slot
@@ -87,6 +95,7 @@ typedef struct hs_oracle {
     char *in_use;         /* [pool_blocks]                                    */
     int64_t host_rows;    /* rows of one layer's pool                        */
     int32_t protect_calls; /* P: slots stamped by the last P calls are kept   */
+    int32_t *status_word; /* [R] OR of (1 << code) over the errors since clear */
     /* bytes (only with track_bytes) */
     uint8_t **host;       /* [L] -> [host_rows * B]  pinned host pool       */
     uint8_t **dev;        /* [L] -> [R * D * B]      device hot buffer      */
@@ -108,7 +117,7 @@ static void hso_free(hs_oracle *o)
     free(o->tok2slot); free(o->slot2tok); free(o->last_used); free(o->tick);
     free(o->host); free(o->dev);
     free(o->blocks); free(o->nblocks); free(o->in_use);
-    free(o->anchor); free(o->cap); free(o->host_off);
+    free(o->anchor); free(o->cap); free(o->host_off); free(o->status_word);
     free(o);
 }
 
@@ -126,13 +135,14 @@ static hs_oracle *create(int R, int L, int64_t B, int k, int D,
     o->anchor = (int *)malloc(sizeof(int) * (size_t)L);
     o->cap = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
     o->host_off = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
+    o->status_word = (int32_t *)calloc((size_t)R, sizeof(int32_t));
     o->tok2slot = (int32_t **)calloc((size_t)L, sizeof(int32_t *));
     o->slot2tok = (int32_t **)calloc((size_t)L, sizeof(int32_t *));
     o->last_used = (uint32_t **)calloc((size_t)L, sizeof(uint32_t *));
     o->tick = (uint32_t **)calloc((size_t)L, sizeof(uint32_t *));
     o->host = (uint8_t **)calloc((size_t)L, sizeof(uint8_t *));
     o->dev = (uint8_t **)calloc((size_t)L, sizeof(uint8_t *));
-    if (!o->anchor || !o->cap || !o->host_off || !o->tok2slot || !o->slot2tok ||
+    if (!o->anchor || !o->cap || !o->host_off || !o->status_word || !o->tok2slot || !o->slot2tok ||
         !o->last_used || !o->tick || !o->host || !o->dev) { hso_free(o); return NULL; }
     int64_t off = 0;
     for (int r = 0; r < R; ++r) {
@@ -228,6 +238,25 @@ int32_t hso_free_blocks(const hs_oracle *o)
     int32_t n = 0;
     for (int32_t b = 0; b < o->pool_blocks; ++b) n += !o->in_use[b];
     return n;
+}
+
+/* Record a call's status code for request r in its status word: an error
+ * (code != OK) sets bit `code`; OK changes nothing. */
+static void note_status(hs_oracle *o, int r, int32_t code)
+{
+    if (code != HSO_OK) o->status_word[r] |= (int32_t)1 << code;
+}
+
+/* Copy out the R status words. */
+void hso_status_word(const hs_oracle *o, int32_t *words)
+{
+    memcpy(words, o->status_word, sizeof(int32_t) * (size_t)o->R);
+}
+
+/* Reset every request's status word to 0 (no error recorded). */
+void hso_status_clear(hs_oracle *o)
+{
+    memset(o->status_word, 0, sizeof(int32_t) * (size_t)o->R);
 }
 
 /* Host row (in the layer's pool) of token t of request r; -1 when the
@@ -362,6 +391,7 @@ int hso_prefill(hs_oracle *o, const int32_t *seq_lens, int32_t *status)
             for (int32_t i = 0; i < n; ++i)
                 if (host_row_of(o, r, S - n + i) < 0) { st = HSO_NO_HOST_ROW; break; }
         if (status) status[r] = st;
+        note_status(o, r, st);
         if (st != HSO_OK) continue;
         for (int l = 0; l < o->L; ++l) {
             if (o->anchor[l] < 0) {
@@ -585,6 +615,7 @@ int hso_swap_in_resident(hs_oracle *o, int layer, const int32_t *topk, const int
         swap_in_request(o, layer, r, topk + (int64_t)r * o->k, seq_lens[r], tick, &rt,
                         out + (int64_t)r * o->k, plan + (int64_t)r * o->k * 2,
                         count + r, status + r);
+        note_status(o, r, status[r]);
     }
     return 0;
 }
@@ -636,8 +667,16 @@ int hso_backup(hs_oracle *o, int layer, const uint8_t *rows, const int32_t *posi
         int32_t p = positions[r];
         status[r] = HSO_OK;
         if (p == -1) continue;
-        if (p < 0 || p >= o->cap[r]) { status[r] = HSO_BAD_POSITION; continue; }
-        if (host_row_of(o, r, p) < 0) { status[r] = HSO_NO_HOST_ROW; continue; }
+        if (p < 0 || p >= o->cap[r]) {
+            status[r] = HSO_BAD_POSITION;
+            note_status(o, r, status[r]);
+            continue;
+        }
+        if (host_row_of(o, r, p) < 0) {
+            status[r] = HSO_NO_HOST_ROW;
+            note_status(o, r, status[r]);
+            continue;
+        }
         if (o->track_bytes)
             memcpy(hso_host_row(o, layer, r, p), rows + (int64_t)r * o->B, (size_t)o->B);
         if (p < o->D) {

@@ -24,8 +24,18 @@ def _kv(tokens: List[str]) -> Dict[str, str]:
     return dict(t.split("=", 1) for t in tokens)
 
 
+def _checks(kv: Dict[str, str], op: dict) -> dict:
+    """The optional status= (the op's own code, default 0) and word= (the
+    request's status word after the op) of a prefill or backup line."""
+    op["status"] = int(kv.get("status", 0))
+    if "word" in kv:
+        op["word"] = int(kv["word"])
+    return op
+
+
 def load(name: str) -> Tuple[Dict[str, int], List[Tuple[str, dict]]]:
-    """Returns (layout {D,k,cap}, [(op, args)]), op in prefill/call/backup."""
+    """Returns (layout {D,k,cap}, [(op, args)]), op in
+    prefill/call/backup/resident/clear."""
     layout, ops = None, []
     with open(os.path.join(GOLDEN, name)) as f:
         for line in f:
@@ -37,7 +47,7 @@ def load(name: str) -> Tuple[Dict[str, int], List[Tuple[str, dict]]]:
             if head == "layout":
                 layout = {k: int(v) for k, v in kv.items()}
             elif head == "prefill":
-                ops.append(("prefill", {"S": int(kv["S"])}))
+                ops.append(("prefill", _checks(kv, {"S": int(kv["S"])})))
             elif head == "call":
                 ops.append(("call", {"S": int(kv["S"]), "topk": _ints(kv["topk"])}))
             elif head == "expect":
@@ -46,8 +56,12 @@ def load(name: str) -> Tuple[Dict[str, int], List[Tuple[str, dict]]]:
                 ops[-1][1]["expect"] = {
                     "out": _ints(kv["out"]), "plan": plan, "status": int(kv["status"]),
                     "slot2tok": _ints(kv["slot2tok"]), "last_used": _ints(kv["last_used"])}
+                if "word" in kv:
+                    ops[-1][1]["expect"]["word"] = int(kv["word"])
             elif head == "backup":
-                ops.append(("backup", {"pos": int(kv["pos"])}))
+                ops.append(("backup", _checks(kv, {"pos": int(kv["pos"])})))
+            elif head == "clear":
+                ops.append(("clear", {}))
             elif head == "resident":
                 ops.append(("resident", {"ids": _ints(kv["ids"])}))
             else:

@@ -89,13 +89,20 @@ class Pair:
         self.orc.close()
 
     def swap_in(self, layer: int, topk: np.ndarray, plan=None, cnt=None, record_plan=True,
-                resident=None, block_size: int = 0):
-        """One call on both sides; returns (gpu results, oracle results).
-        With record_plan=False the library gets no plan to fill; the GPU
+                resident=None, block_size: int = 0, clear_status: bool = True):
+        """One call on both sides; returns (gpu results, oracle results): the
+        GPU's fourth item is the library's status words, the oracle's its
+        per-call status codes.  With clear_status (the default) both sides'
+        status words are cleared first, so each GPU word is exactly the bit
+        of the call's own code (see assert_call_equal).  With
+        record_plan=False the library gets no plan to fill; the GPU
         plan/count results are then the oracle's (nothing to compare).
         resident: optional int32 [R][max_blocks] resident block table."""
         plan = self.plan if plan is None else plan
         cnt = self.cnt if cnt is None else cnt
+        if clear_status:
+            self.gpu.status_clear()
+            self.orc.status_clear()
         t = torch.from_numpy(np.ascontiguousarray(topk, dtype=np.int32)).cuda()
         if resident is not None:
             rb = torch.from_numpy(np.ascontiguousarray(resident, dtype=np.int32)).cuda()
@@ -115,8 +122,11 @@ class Pair:
         self.last = (g, o)
         return g, o
 
-    def backup(self, layer: int, positions: np.ndarray):
-        """Back up each request's row at `positions` (generator rows)."""
+    def backup(self, layer: int, positions: np.ndarray, clear_status: bool = True):
+        """Back up each request's row at `positions` (generator rows); returns
+        the oracle's per-call status codes.  With clear_status (the default)
+        both status words are cleared first and the library's words are
+        checked against the bits of those codes."""
         w = self.w
         rows = np.zeros((w.num_requests, w.row_bytes), dtype=np.uint8)
         for r in range(w.num_requests):
@@ -124,9 +134,15 @@ class Pair:
                 rows[r] = W.kv_rows(w, layer, r, [int(positions[r])])[0]
         rows_d = torch.from_numpy(rows).cuda()
         pos_d = torch.from_numpy(np.ascontiguousarray(positions, dtype=np.int32)).cuda()
+        if clear_status:
+            self.gpu.status_clear()
+            self.orc.status_clear()
         self.gpu.backup(layer, rows_d, pos_d)
         st = self.orc.backup(layer, rows, positions)
         torch.cuda.synchronize()
+        if clear_status:
+            got = self.gpu.status().cpu().numpy()
+            assert np.array_equal(got, status_bits(st)), f"backup status words {got} != {st}"
         return st
 
     def advance(self, delta: int = 1):
@@ -134,10 +150,21 @@ class Pair:
         self.seq_d.copy_(torch.from_numpy(self.seq))
 
 
+def status_bits(codes) -> np.ndarray:
+    """The status word each per-call code gives on a cleared word (bit c for
+    code c, 0 for OK)."""
+    c = np.asarray(codes, dtype=np.int64)
+    return np.where(c != 0, np.left_shift(1, c), 0).astype(np.int32)
+
+
 def assert_call_equal(g, o, ctx=""):
+    """g: the library's (out, plan, count, status words); o: the oracle's
+    (out, plan, count, per-call codes).  The words must be the bits of the
+    codes: the words were cleared before the call, or no error was recorded
+    since they last were."""
     out, plan, cnt, st = g
     o_out, o_plan, o_cnt, o_st = o
-    assert np.array_equal(st, o_st), f"{ctx}: status {st} != {o_st}"
+    assert np.array_equal(st, status_bits(o_st)), f"{ctx}: status words {st} != codes {o_st}"
     assert np.array_equal(cnt, o_cnt), f"{ctx}: miss counts differ"
     assert np.array_equal(out, o_out), f"{ctx}: slot ids differ"
     for r in range(out.shape[0]):

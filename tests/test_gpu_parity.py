@@ -11,7 +11,7 @@ import torch
 import oracle as O
 from golden_trace import load, names
 from harness import (Pair, assert_call_equal, assert_device_bytes_equal_oracle,
-                     assert_device_rows, assert_state_equal)
+                     assert_device_rows, assert_state_equal, status_bits)
 from hierarchical_sparse_kv_request_gb300 import hisparse as H
 from hierarchical_sparse_kv_request_gb300 import workload as W
 
@@ -39,24 +39,44 @@ def test_golden_trace_gpu(name):
     if layout.get("protect"):
         p.gpu.set_protected_calls(layout["protect"])
         p.orc.set_protected_calls(layout["protect"])
+    # a trace that states status words keeps them across its ops (cleared
+    # only by its own `clear` lines); the others clear them before each op
+    words = any(op == "clear" or "word" in a or "word" in a.get("expect", {})
+                for op, a in ops)
     resident = None
     for i, (op, a) in enumerate(ops[1:]):
         if op == "resident":
             resident = np.array([a["ids"]], dtype=np.int32)
             continue
-        if op == "backup":
-            st = p.backup(0, np.array([a["pos"]], dtype=np.int32))
-            assert st[0] == 0
+        if op == "clear":
+            p.gpu.status_clear()
+            p.orc.status_clear()
+            continue
+        if op in ("backup", "prefill"):
+            if op == "backup":
+                st = p.backup(0, np.array([a["pos"]], dtype=np.int32), clear_status=not words)
+            else:
+                p.gpu.prefill(torch.tensor([a["S"]], dtype=torch.int32, device="cuda"))
+                st = p.orc.prefill([a["S"]])
+                torch.cuda.synchronize()
+            assert st[0] == a["status"]
+            if "word" in a:
+                assert int(p.gpu.status().cpu()[0]) == a["word"] == int(p.orc.status_word()[0])
             continue
         if a["S"] != p.seq[0]:                # grown by backups since the last call
             p.advance(a["S"] - int(p.seq[0]))
         g, o = p.swap_in(0, np.array([a["topk"]], dtype=np.int32), resident=resident,
-                         block_size=layout.get("bs", 0))
-        assert_call_equal(g, o, f"{name} op {i}")
+                         block_size=layout.get("bs", 0), clear_status=not words)
         e = a["expect"]
         out, plan, cnt, st = g
+        if words:
+            assert int(st[0]) == e["word"] == int(p.orc.status_word()[0])
+            assert int(o[3][0]) == e["status"]
+            g = (out, plan, cnt, status_bits(o[3]))   # the rest of the call, compared below
+        assert_call_equal(g, o, f"{name} op {i}")
         assert out[0].tolist() == e["out"]
-        assert int(st[0]) == e["status"]
+        if not words:
+            assert int(st[0]) == (1 << e["status"] if e["status"] else 0)
         assert [tuple(x) for x in plan[0, : cnt[0]].tolist()] == e["plan"]
         s2t = assert_state_equal(p, 0, f"{name} op {i}")
         assert s2t[0].tolist() == e["slot2tok"]
@@ -414,7 +434,8 @@ def test_malformed_rows_set_status_and_leave_state():
     bad[4, 4] = 10           # fast path, out of range (S = 10)
     g, o = p.swap_in(0, bad)
     assert_call_equal(g, o)
-    assert g[3].tolist() == [O.BAD_INDEX, O.DUPLICATE, O.BAD_INDEX, O.BAD_INDEX, O.BAD_INDEX, 0]
+    assert g[3].tolist() == [1 << O.BAD_INDEX, 1 << O.DUPLICATE, 1 << O.BAD_INDEX,
+                             1 << O.BAD_INDEX, 1 << O.BAD_INDEX, 0]
     assert (g[0][:5] == -1).all()
     after = p.gpu.read_state(0)
     # requests 0..4 untouched: their slot maps, stamps and LRU order
@@ -428,7 +449,7 @@ def test_malformed_rows_set_status_and_leave_state():
     p.seq_d.copy_(torch.from_numpy(p.seq))
     g, o = p.swap_in(0, good)
     assert_call_equal(g, o)
-    assert g[3][5] == O.BAD_SEQ_LEN
+    assert g[3][5] == 1 << O.BAD_SEQ_LEN
     assert_state_equal(p, 0)
     p.close()
 
@@ -508,14 +529,15 @@ def test_backup_layers_in_one_launch():
         if step == 4:
             pos[2] = -1                      # skipped
         rows = rng.integers(0, 256, (3, R, 64), dtype=np.uint8)
+        p.gpu.status_clear()
+        p.orc.status_clear()
         p.gpu.backup_layers([0, 1, 2], torch.from_numpy(rows).cuda(),
                             torch.from_numpy(pos.astype(np.int32)).cuda())
         st = [p.orc.backup(l, rows[l], pos) for l in range(3)]
         torch.cuda.synchronize()
         got = p.gpu.status().cpu().numpy()
-        for r in range(R):
-            if st[0][r] != 0:
-                assert got[r] == st[0][r]
+        assert np.array_equal(got, p.orc.status_word()), f"step {step}: status words"
+        assert np.array_equal(got, status_bits(st[0]))
         for l in range(3):
             assert_device_bytes_equal_oracle(p, l, f"step {step} layer {l}")
         assert_state_equal(p, 0, f"step {step}")
@@ -544,7 +566,7 @@ def test_fast_path_grows_into_slow_path_with_backups():
     pos = np.array([-1, 10_000, -1], dtype=np.int32)
     st = p.backup(0, pos)
     assert st.tolist() == [0, O.BAD_POSITION, 0]
-    assert p.gpu.status().cpu().numpy()[1] == O.BAD_POSITION
+    assert p.gpu.status().cpu().numpy()[1] == 1 << O.BAD_POSITION
     p.close()
 
 

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from harness import Pair, assert_call_equal, assert_device_rows, assert_state_equal
+from harness import Pair, assert_call_equal, assert_device_rows, assert_state_equal, status_bits
 from hierarchical_sparse_kv_request_gb300 import hisparse as H
 from hierarchical_sparse_kv_request_gb300 import workload as W
 
@@ -176,6 +176,67 @@ def test_pipelined_index_share_graph_double_buffered_plans():
     p.close()
 
 
+def test_pipelined_index_share_full_size():
+    """The benchmark's launch shape of the pipelined 16-layer schedule at full
+    size: 32 requests x 40000 tokens, 4 anchors each followed by 3 skip
+    layers, plans double-buffered between the groups, the whole decode step
+    one CUDA graph with the replays pre-issued on a side stream next to the
+    stand-in compute.  Every step: every anchor's slot IDs, statuses and miss
+    counts and its hot state against the oracle; the plans left in the two
+    buffers (anchors 2 and 3, which write them last) pair by pair; and the
+    skip layers' device rows, a sample per layer (every slot at the end), so
+    the plans of anchors 0 and 1, overwritten within the step, are checked
+    by what their replays copied."""
+    w = W.make_config(6, steps=10)
+    sched = W.topk_schedule(w)
+    p = Pair(w, track_bytes=False)
+    R, k = w.num_requests, w.top_k
+    plans = [torch.empty((R, k, 2), dtype=torch.int32, device="cuda") for _ in range(2)]
+    cnts = [torch.zeros(R, dtype=torch.int32, device="cuda") for _ in range(2)]
+    outs = {a: torch.empty((R, k), dtype=torch.int32, device="cuda") for a in w.anchors}
+    tk = {a: torch.empty((R, k), dtype=torch.int32, device="cuda") for a in w.anchors}
+    side = torch.cuda.Stream(priority=-1)
+    buf = torch.zeros(160 << 20, dtype=torch.bfloat16, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for gi, a in enumerate(w.anchors):
+            P, C = plans[gi % 2], cnts[gi % 2]
+            p.gpu.swap_in(a, tk[a], p.seq_d, outs[a], P, C)
+            ev = torch.cuda.Event()
+            ev.record()
+            side.wait_event(ev)
+            p.gpu.replay_plan_layers(P, C, [a + 1, a + 2, a + 3], num_ctas=16, stream=side)
+            done = torch.cuda.Event()
+            done.record(side)
+            H.synthetic_compute(buf, 1)
+            torch.cuda.current_stream().wait_event(done)
+            H.synthetic_compute(buf, 3)
+    misses = 0
+    for step in range(w.steps):
+        for a in w.anchors:
+            tk[a].copy_(torch.from_numpy(sched[a][step]))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert (p.gpu.status().cpu().numpy() == 0).all(), f"step {step}: status words"
+        last = {}
+        for gi, a in enumerate(w.anchors):
+            o = p.orc.swap_in(a, sched[a][step], p.seq)
+            last[gi % 2] = o
+            g = (outs[a].cpu().numpy(), o[1], o[2], status_bits(np.zeros(R)))
+            assert_call_equal(g, o, f"step {step} anchor {a}")
+            misses += int(o[2].sum())
+            s2t = assert_state_equal(p, a, f"step {step} anchor {a}")
+            final = step == w.steps - 1
+            for l in (a, a + 1, a + 2, a + 3):
+                assert_device_rows(p, l, s2t, sample=None if final else 32, seed=step,
+                                   ctx=f"step {step} layer {l}")
+        for b, o in last.items():             # anchors 2 and 3 wrote the buffers last
+            g = (o[0], plans[b].cpu().numpy(), cnts[b].cpu().numpy(), status_bits(o[3]))
+            assert_call_equal(g, o, f"step {step} plan buffer {b}")
+    assert misses > 0
+    p.close()
+
+
 @pytest.mark.parametrize("protect", [0, 1])
 def test_speculative_substeps_with_backups(protect):
     """256 x 32768 tokens, D 4096, 1152 B rows: 3 verification sub-steps per
@@ -197,7 +258,7 @@ def test_speculative_substeps_with_backups(protect):
             oracle_calls.append(o)
         # each sub-step's plan row is still intact after the later sub-steps
         for sub, o in enumerate(oracle_calls):
-            g = (o[0], plans[sub].cpu().numpy(), cnts[sub].cpu().numpy(), o[3])
+            g = (o[0], plans[sub].cpu().numpy(), cnts[sub].cpu().numpy(), status_bits(o[3]))
             assert_call_equal(g, o, f"step {step} plan {sub} after the step")
         st = p.backup(0, p.seq.copy())
         assert (st == 0).all()

@@ -33,14 +33,19 @@ def run_trace_on_oracle(name, lib_path=None):
     for op, a in ops:
         if op == "resident":
             resident = np.array([a["ids"]], dtype=np.int32)
-        elif op == "prefill":
-            S = a["S"]
-            orc.host_rows(0, 0)[:] = np.arange(cap, dtype=np.uint8)[:, None]
-            orc.prefill([S])
-        elif op == "backup":
-            row = np.full((1, 16), 200 + a["pos"], dtype=np.uint8)
-            st = orc.backup(0, row, [a["pos"]])
-            assert st[0] == 0
+        elif op == "clear":
+            orc.status_clear()
+        elif op in ("prefill", "backup"):
+            if op == "prefill":
+                orc.host_rows(0, 0)[:] = np.arange(cap, dtype=np.uint8)[:, None]
+                st = orc.prefill([a["S"]])
+            else:
+                row = np.full((1, 16), (200 + a["pos"]) % 256, dtype=np.uint8)
+                st = orc.backup(0, row, [a["pos"]])
+            got = {"status": int(st[0]), "word": int(orc.status_word()[0])}
+            want = {"status": a["status"], "word": a.get("word", got["word"])}
+            if got != want:
+                return got, want
         else:
             out, plan, cnt, st = orc.swap_in(0, np.array([a["topk"]]), [a["S"]],
                                              resident, layout.get("bs", 0))
@@ -48,9 +53,11 @@ def run_trace_on_oracle(name, lib_path=None):
             s2t, lu, _, _ = orc.state(0)
             got = {"out": out[0].tolist(), "status": int(st[0]),
                    "plan": [tuple(p) for p in plan[0, : cnt[0]].tolist()],
-                   "slot2tok": s2t[0].tolist(), "last_used": lu[0].tolist()}
+                   "slot2tok": s2t[0].tolist(), "last_used": lu[0].tolist(),
+                   "word": int(orc.status_word()[0])}
             want = {"out": e["out"], "status": e["status"], "plan": e["plan"],
-                    "slot2tok": e["slot2tok"], "last_used": e["last_used"]}
+                    "slot2tok": e["slot2tok"], "last_used": e["last_used"],
+                    "word": e.get("word", got["word"])}
             if got != want:
                 return got, want
     return None
@@ -483,12 +490,48 @@ def pin_empty_resident_table_is_the_plain_call(lib_path=None):
         assert np.array_equal(x, y)
 
 
+def pin_status_word_survives_later_layers_and_backups(lib_path=None):
+    """Hand-worked: the status word of a request keeps an error of layer 0
+    while layer 1's call and a backup succeed, collects the bits of several
+    calls, layers and kinds, and is reset only by a clear ([Arch] Performance
+    invariants: no device readback, so an error must stay on the device until
+    the caller reads it).  Bit c stands for status code c."""
+    D, k, S = 8, 4, 20
+    orc = O.Oracle(3, 2, 16, k, D, [-1, -1], [S + 2] * 3, lib_path=lib_path)
+    assert orc.prefill([S, S, S]).tolist() == [0, 0, 0]
+    assert orc.status_word().tolist() == [0, 0, 0]
+    good = np.array([[0, 1, 2, 3], [4, 5, 6, 7], [8, 9, 10, 11]], dtype=np.int32)
+    bad = good.copy()
+    bad[1, 2] = S                                    # request 1: outside [0, S)
+    assert orc.swap_in(0, bad, [S, S, S])[3].tolist() == [0, O.BAD_INDEX, 0]
+    assert orc.swap_in(1, good, [S, S, S])[3].tolist() == [0, 0, 0]
+    assert orc.status_word().tolist() == [0, 1 << O.BAD_INDEX, 0]
+    rows = np.zeros((3, 16), dtype=np.uint8)
+    assert orc.backup(1, rows, [S, S, S])[0] == 0       # a good backup changes nothing
+    assert orc.status_word().tolist() == [0, 1 << O.BAD_INDEX, 0]
+    assert orc.backup(1, rows, [S + 2, -1, S])[0] == O.BAD_POSITION
+    dup = good.copy()
+    dup[1, 3] = dup[1, 0]                            # request 1: a duplicate on layer 1
+    assert orc.swap_in(1, dup, [S, S, S])[3].tolist() == [0, O.DUPLICATE, 0]
+    assert orc.status_word().tolist() == [1 << O.BAD_POSITION,
+                                          (1 << O.BAD_INDEX) | (1 << O.DUPLICATE), 0]
+    assert orc.prefill([-1, -1, S + 3])[2] == O.BAD_SEQ_LEN
+    assert orc.status_word().tolist() == [1 << O.BAD_POSITION,
+                                          (1 << O.BAD_INDEX) | (1 << O.DUPLICATE),
+                                          1 << O.BAD_SEQ_LEN]
+    orc.status_clear()
+    assert orc.status_word().tolist() == [0, 0, 0]
+    assert orc.swap_in(0, good, [S, S, S])[3].tolist() == [0, 0, 0]
+    assert orc.status_word().tolist() == [0, 0, 0]
+
+
 PINS = [pin_invariants_tiny_workload, pin_prefill_last_k_is_all_hits,
         pin_repeat_is_all_hits, pin_disjoint_sets_closed_form,
         pin_errors_leave_state_untouched,
         pin_backup_grows_short_request_into_slow_path,
         pin_replay_copies_plan_rows_to_other_layer, pin_protected_slots_vs_list_model,
-        pin_all_resident_touches_nothing, pin_empty_resident_table_is_the_plain_call]
+        pin_all_resident_touches_nothing, pin_empty_resident_table_is_the_plain_call,
+        pin_status_word_survives_later_layers_and_backups]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__[4:] for p in PINS])

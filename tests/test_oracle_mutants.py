@@ -102,7 +102,8 @@ MUTANTS = [
      "            *status = HSO_NO_HOST_ROW;\n            for (int j = 0; j < k; ++j) out[j] = -1;\n            free(done); free(is_hit_slot); free(miss);\n            return;",
      "            break;"),
     ("paged_backup_without_block",
-     "        if (host_row_of(o, r, p) < 0) { status[r] = HSO_NO_HOST_ROW; continue; }\n",
+     "        if (host_row_of(o, r, p) < 0) {\n            status[r] = HSO_NO_HOST_ROW;\n"
+     "            note_status(o, r, status[r]);\n            continue;\n        }\n",
      ""),
     ("prefill_without_rows",
      "                if (host_row_of(o, r, S - n + i) < 0) { st = HSO_NO_HOST_ROW; break; }",
@@ -116,6 +117,21 @@ MUTANTS = [
     ("capacity_keeps_outputs",
      "            *status = HSO_CAPACITY;\n            for (int j = 0; j < k; ++j) out[j] = -1;",
      "            *status = HSO_CAPACITY;"),
+    ("status_word_overwritten",
+     "if (code != HSO_OK) o->status_word[r] |= (int32_t)1 << code;",
+     "if (code != HSO_OK) o->status_word[r] = (int32_t)1 << code;"),
+    ("status_word_cleared_by_success",
+     "if (code != HSO_OK) o->status_word[r] |= (int32_t)1 << code;",
+     "o->status_word[r] = code != HSO_OK ? (o->status_word[r] | ((int32_t)1 << code)) : 0;"),
+    ("status_word_holds_code_not_bit",
+     "if (code != HSO_OK) o->status_word[r] |= (int32_t)1 << code;",
+     "if (code != HSO_OK) o->status_word[r] |= code;"),
+    ("backup_error_not_recorded",
+     "            status[r] = HSO_BAD_POSITION;\n            note_status(o, r, status[r]);",
+     "            status[r] = HSO_BAD_POSITION;"),
+    ("prefill_error_not_recorded",
+     "        note_status(o, r, st);\n",
+     ""),
     ("prefill_resets_other_requests",
      "        if (S == -1) continue;",
      "        if (S == -1) S = 0;"),
