@@ -79,8 +79,18 @@ def parse():
                     help="the newest N tokens of every request sit in resident pages of 64 "
                          "tokens (ids scattered over a shared pool), checked before the hot "
                          "buffer (hisparse_swap_in_resident); 0: no resident tier")
+    ap.add_argument("--stage-rows", type=int, default=0,
+                    help="miss rows per request staged through shared memory by the "
+                         "bulk-copy engine (hisparse_set_stage_rows; -1: as many as fit)")
+    ap.add_argument("--programmatic", action="store_true",
+                    help="launch swap-ins and backups with a programmatic dependency "
+                         "(hisparse_set_programmatic_launch)")
     ap.add_argument("--protect-calls", type=int, default=0,
                     help="keep the hot rows of each request's last P swap-in calls (0: off)")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="the default run (decode_40k, one GPU) also times mixed_len, "
+                         "shared_index and spec_verify in child processes and reports them "
+                         "under other_configs; this skips them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -202,7 +212,8 @@ def run_rotation(args, st, torch, H, K, Wm, rank, ws, first_step):
     NB = ROTATE_BATCHES
     per = rotation_steps(Wm, K)
     batches = [st] + [Setup(args.config, per, rank, args.copy_mode, 0, args.protect_calls,
-                            batch=b, rows_from=st, resident_recent=args.resident_recent)
+                            batch=b, rows_from=st, resident_recent=args.resident_recent,
+                            stage_rows=args.stage_rows, programmatic=args.programmatic)
                       for b in range(1, NB)]
     for b in batches[1:]:
         settle_host_pool(torch, H, b.gpu, w)
@@ -353,6 +364,29 @@ def kernel_only(torch, st, flush, first_step: int):
     return rounds, misses / (KONLY_ROUNDS * KONLY_STEPS), fl / KONLY_STEPS
 
 
+def backup_kernel_only(torch, st, flush, step: int) -> float:
+    """One backup launch of every layer's new row, timed like kernel_only:
+    KONLY_STEPS (flush, backup) pairs in a graph with one event pair around
+    them, minus the flushes; the same positions each time (a backup of a row
+    that is already there writes the same bytes again).  Median of
+    KONLY_ROUNDS rounds, ms per launch."""
+    w = st.w
+    layers = list(range(w.num_layers))
+    fl = flush_only_ms(torch, flush, KONLY_STEPS)
+
+    def warm():
+        for _ in range(KONLY_WARM):
+            flush.zero_()
+            st.gpu.backup_layers(layers, st.backup_rows[step], st.seq)
+
+    def timed():
+        for _ in range(KONLY_STEPS):
+            flush.zero_()
+            st.gpu.backup_layers(layers, st.backup_rows[step], st.seq)
+    return statistics.median((graph_ms(torch, warm, timed)[0] - fl) / KONLY_STEPS
+                             for _ in range(KONLY_ROUNDS))
+
+
 def random_row_ceiling_kernel_only(torch, H, gpu, w, nrows: int, seed: int = 3):
     """The gather ceiling taken like the kernel-only step time: one graph of
     KONLY_STEPS (flush, gather of a fresh draw of nrows random pool rows)
@@ -442,7 +476,7 @@ def reserve_scattered(gpu, caps, hb: int, seed: int, blocks_per_round: int = 8):
 class Setup:
     def __init__(self, cfg: int, steps: int, rank: int, copy_mode: str, host_block_tokens: int = 0,
                  protect_calls: int = 0, batch: int = 0, rows_from: "Setup" = None,
-                 resident_recent: int = 0):
+                 resident_recent: int = 0, stage_rows: int = 0, programmatic: bool = False):
         """One batch of the workload on its own handle.  batch > 0 gives an
         independent batch (its own seed, state and pool); rows_from copies the
         host rows of another batch instead of generating them again."""
@@ -459,6 +493,8 @@ class Setup:
         self.gpu = H.HiSparse.for_workload(w, host_block_tokens=host_block_tokens)
         self.gpu.set_copy_mode(H.COPY_SPLIT if copy_mode == "split" else H.COPY_FUSED)
         self.gpu.set_protected_calls(protect_calls)
+        self.gpu.set_stage_rows(stage_rows)
+        self.gpu.set_programmatic_launch(programmatic)
         if self.hb:
             reserve_scattered(self.gpu, w.host_capacity, self.hb, w.seed)
         for l in range(w.num_layers):
@@ -554,24 +590,41 @@ class Setup:
         return n
 
 
-def backup_report(w, bev, link):
+def backup_report(w, bev, link, kernel_only_ms=None):
     """Eager-backup D2H rate: the step's R x L rows over the time of its
-    backup launches (one event pair around them), against the D2H copy peak.
-    The rows are small (R x B per layer), so the launches are latency-bound."""
+    backup launch, against the D2H copy peak: with one event pair around the
+    launch (its ~5 us included), and kernel-only (backup_kernel_only).  The
+    rows are small (R x B per layer), so the launch is latency-bound."""
     if not bev:
         return {}
     ms = statistics.median([a.elapsed_time(b) for a, b in bev])
     nbytes = w.num_requests * w.num_layers * w.row_bytes
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"backup": {"bytes_per_step": nbytes, "launches_per_step": 1,
-                       "median_ms": round(ms, 5), "d2h_gbs": round(gbs, 2),
-                       "frac_of_d2h_peak": round(gbs / link["d2h_copy_engine_gbs"], 4),
-                       "note": "one event pair around the step's backup launches; "
-                               "includes the ~5 us cost of the pair itself"}}
+    out = {"bytes_per_step": nbytes, "launches_per_step": 1,
+           "median_ms": round(ms, 5), "d2h_gbs": round(gbs, 2),
+           "frac_of_d2h_peak": round(gbs / link["d2h_copy_engine_gbs"], 4),
+           "note": "median_ms: one event pair around the step's backup launch, the ~5 us "
+                   "cost of the pair included"}
+    if kernel_only_ms:
+        kg = nbytes / (kernel_only_ms * 1e-3) / 1e9
+        out.update({"kernel_only_ms": round(kernel_only_ms, 5), "kernel_only_d2h_gbs": round(kg, 2),
+                    "kernel_only_frac_of_d2h_peak": round(kg / link["d2h_copy_engine_gbs"], 4)})
+    return {"backup": out}
+
+
+PEAK_SOURCE = ("measured in this run: the higher of a 1 GiB pinned cudaMemcpyAsync H2D "
+               "(best of 10) and SM loads of the same mapped pinned buffer (best of 5)")
+
+
+def link_peak_gbs(link) -> float:
+    """The host-link roofline: the higher of the copy engine's and the SM
+    loads' sequential H2D rates (one slow copy-engine sample must not lower
+    the denominator)."""
+    return max(link["h2d_copy_engine_gbs"], link["h2d_sm_loads_gbs"])
 
 
 def measure_link_peak(torch, H):
-    """Pinned host->device bandwidth: 1 GiB cudaMemcpyAsync (best of 5), and
+    """Pinned host->device bandwidth: 1 GiB cudaMemcpyAsync (best of 10), and
     what SM loads of mapped pinned memory reach (best of 5)."""
     n = 1 << 30
     src = torch.empty(n, dtype=torch.uint8).pin_memory()
@@ -579,7 +632,7 @@ def measure_link_peak(torch, H):
     dst = torch.empty(n, dtype=torch.uint8, device="cuda")
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     best_ce = 0.0
-    for _ in range(5):
+    for _ in range(10):
         torch.cuda.synchronize()
         s.record()
         dst.copy_(src, non_blocking=True)
@@ -660,7 +713,8 @@ def run_gpu(args):
     extra = rotation_steps(Wm, K) if rotate else 0
     konly_steps = KONLY_ROUNDS * (KONLY_WARM + KONLY_STEPS)
     st = Setup(args.config, S0 + K + Wm + BREAKDOWN_STEPS + konly_steps + extra, rank, args.copy_mode,
-               args.host_block_tokens, args.protect_calls, resident_recent=args.resident_recent)
+               args.host_block_tokens, args.protect_calls, resident_recent=args.resident_recent,
+               stage_rows=args.stage_rows, programmatic=args.programmatic)
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -741,8 +795,11 @@ def run_gpu(args):
         call_ms = [a.elapsed_time(b) for row in kev for a, b in row]
         breakdown_ms = [a.elapsed_time(b) for a, b in sev]
     konly = None
+    bk_ms = None
     if not args.profile:
         k_rounds, k_miss, k_flush = kernel_only(torch, st, flush, next_step)
+        if w.backup:
+            bk_ms = backup_kernel_only(torch, st, flush, next_step + konly_steps - 1)
         next_step += konly_steps
         konly = {"ms_per_step": round(statistics.median(k_rounds), 5),
                  "rounds_ms": [round(x, 5) for x in k_rounds],
@@ -812,7 +869,7 @@ def run_gpu(args):
         if summary and not st.split and not st.hb and not args.resident_recent \
                 and not args.protect_calls:
             traffic = profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/resolve.cu", summary)
-        peak_link = link["h2d_copy_engine_gbs"]
+        peak_link = link_peak_gbs(link)
         # The roofline takes the kernel-only step time: one event pair around
         # many back-to-back (flush, step) pairs, minus the flushes.  For a
         # one-launch step (decode_40k) that is the resolve kernel's own
@@ -837,7 +894,7 @@ def run_gpu(args):
                 "frac_with_step_event_pairs": round(miss_gbs / peak_link, 4),
                 "traffic": traffic, "kernel": "resolve_kernel (fused resolve + miss copy)",
                 "timing": "miss bytes per step over the kernel-only step time (kernel_only)",
-                "peak_source": "measured in this run: 1 GiB pinned cudaMemcpyAsync H2D"}
+                "peak_source": PEAK_SOURCE}
         roof_hbm = {"bound": "hbm", "achieved": round(res_bytes / total_s / 1e9, 1),
                     "peak": peak_hbm, "unit": "GB/s",
                     "frac": round(res_bytes / total_s / 1e9 / peak_hbm, 4),
@@ -857,6 +914,8 @@ def run_gpu(args):
                        "host_pool": (f"paged: {st.hb}-token blocks scattered over the pool"
                                      if st.hb else "one contiguous region per request"),
                        "protect_calls": args.protect_calls,
+                       "stage_rows": args.stage_rows,
+                       "programmatic_launch": args.programmatic,
                        "resident_recent": args.resident_recent,
                        "l2": (f"inputs larger than L2: {ROTATE_BATCHES} independent batches of "
                               f"{w.num_requests} requests take the steps in turn (~270 MB of other "
@@ -875,7 +934,7 @@ def run_gpu(args):
             "miss_rows_per_step": round(misses / K, 1),
             "cold_step_after_prefill": cold,
             "link_peak": link,
-            "miss_h2d_frac_of_link_peak": round(miss_gbs / link["h2d_copy_engine_gbs"], 4),
+            "miss_h2d_frac_of_link_peak": round(miss_gbs / peak_link, 4),
             "roofline": roof, "roofline_resolution": roof_hbm,
             "random_row_ceiling": ceiling,
             "random_row_ceiling_kernel_only": ceiling_ko,
@@ -888,7 +947,7 @@ def run_gpu(args):
                                              f"{len(breakdown_ms)} steps after the timed ones, each call "
                                              f"in its own event pair")},
             "gpu_launches": st.launches() * K,
-            **backup_report(w, bev, link),
+            **backup_report(w, bev, link, bk_ms),
             "clocks": clk, "wall_s_timed_loop": round(wall, 3),
         }
     if not args.no_e2e:
@@ -1112,12 +1171,12 @@ def run_config4(args, ws, rank, H):
     roof = None
     if link:
         roof = {"bound": "host_link", "achieved": round(rep_gbs, 1),
-                "peak": link["h2d_copy_engine_gbs"], "unit": "GB/s",
-                "frac": round(rep_gbs / link["h2d_copy_engine_gbs"], 4),
+                "peak": link_peak_gbs(link), "unit": "GB/s",
+                "frac": round(rep_gbs / link_peak_gbs(link), 4),
                 "traffic": profiled_traffic("hierarchical_sparse_kv_request_gb300/csrc/copy.cu",
                                             "replay_kernel_shared_index.md"),
                 "kernel": "replay_kernel (one launch, three skip layers, run alone)",
-                "peak_source": "measured in this run: 1 GiB pinned cudaMemcpyAsync H2D"}
+                "peak_source": PEAK_SOURCE}
     return {
         "metric": "resolved top-k rows/s", "value": round(R * k * K / (sum(times) * 1e-3), 1),
         "unit": "rows/s", "n_gpus": ws, "steps": K, "warmup": Wm, "settle_steps": S0,
@@ -1375,12 +1434,55 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+# The default run's other workloads: timed in child processes after
+# decode_40k, fewer steps each (their steps are 20-70x longer).
+OTHER_CONFIGS = (3, 4, 5)
+OTHER_STEPS = 8
+OTHER_KEYS = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline",
+              "kernel_only", "miss_h2d_gbs", "miss_rows_per_step", "miss_h2d_frac_of_link_peak",
+              "random_row_ceiling_kernel_only", "step_ms_min_median_max", "slow_steps", "backup",
+              "dominant_kernel", "clocks", "gpu_launches", "exposed_copy_ms", "compute_ms",
+              "anchor_swap_in_ms", "replays_alone_ms", "step_ms_median", "link_peak")
+
+
+def run_other_configs(args) -> dict:
+    """mixed_len, shared_index and spec_verify, each `bench.py --config N`
+    in a child process (its own CUDA context and pinned pools), with the
+    same timing rules; the fields that describe the run are kept."""
+    out = {}
+    for cfg in OTHER_CONFIGS:
+        name = W.make_config(cfg).name
+        cmd = [sys.executable, os.path.abspath(__file__), "--config", str(cfg),
+               "--steps", str(OTHER_STEPS), "--warmup", str(max(3, min(args.warmup, 5))),
+               "--no-cpu-baseline", "--no-e2e", "--no-other-configs"]
+        try:
+            res = subprocess.run(cmd, capture_output=True, text=True, timeout=900)
+        except subprocess.TimeoutExpired:
+            out[name] = {"error": "timed out after 900 s"}
+            continue
+        lines = [x for x in res.stdout.strip().splitlines() if x.startswith("{")]
+        if res.returncode != 0 or not lines:
+            out[name] = {"error": f"rc {res.returncode}: " + res.stderr.strip()[-400:]}
+            continue
+        d = json.loads(lines[-1])
+        out[name] = {k: d[k] for k in OTHER_KEYS if k in d}
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         res = run_reference(args)
     else:
         res = run_gpu(args)
+        ws = dist_env()[0]
+        if (res is not None and ws == 1 and args.config == 2 and not args.no_other_configs
+                and not args.profile):
+            import gc
+            import torch
+            gc.collect()               # the decode_40k handles and pools go first
+            torch.cuda.empty_cache()
+            res["other_configs"] = run_other_configs(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 

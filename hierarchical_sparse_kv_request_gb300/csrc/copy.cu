@@ -116,19 +116,32 @@ __global__ void __launch_bounds__(REPLAY_NT) replay_kernel(ReplayLaunch a)
     }
 }
 
-// Backup: one thread per 16-byte chunk of each request's new row, for each
-// listed layer.  The layers share the positions, so a bad position or a
-// missing host row sets the same status bit from every layer.
+// Backup: one thread per 16-byte chunk of each request's new row; the thread
+// writes that chunk in every listed layer.  Latency is all there is to this
+// launch (R x B bytes a layer), so the chunk loads of the first layers go out
+// together with the position lookup, and each group of BACKUP_GROUP layers
+// has all its loads in flight before any of its stores.  The layers share the
+// positions, so a bad position or a missing host row sets one status bit for
+// all of them.
+constexpr int BACKUP_GROUP = 4;
+
 __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
 {
+    // with a programmatic launch (see launch_backup) this grid may start
+    // before the previous kernel of the stream ends: wait for it before
+    // reading anything (without one the wait returns at once)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int CH = a.g.chunks;
-    const int64_t per_layer = (int64_t)a.g.R * CH;
-    const int64_t e0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e0 >= per_layer * a.num_layers) return;
-    const int li = (int)(e0 / per_layer);
-    const int64_t e = e0 - (int64_t)li * per_layer;
-    const BackupLayer &L = a.layer[li];
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= (int64_t)a.g.R * CH) return;
     const int r = (int)(e / CH), c = (int)(e - (int64_t)r * CH);
+    const int64_t B = a.g.B;
+    const int D = a.g.D;
+    const int L = a.num_layers;
+    uint4 v[BACKUP_GROUP];
+#pragma unroll
+    for (int u = 0; u < BACKUP_GROUP; ++u)
+        if (u < L) v[u] = ld_dev_v4(a.layer[u].rows + (int64_t)r * B + c * 16);
     const int32_t p = a.positions[r];
     if (p == -1) return;
     const int64_t cap = a.g.host_cap[r];
@@ -142,15 +155,28 @@ __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
         if (c == 0) record_status(a.status, r, kStatusNoHostRow);
         return;
     }
-    const int64_t B = a.g.B;
-    const int D = a.g.D;
-    const uint4 v = ld_dev_v4(L.rows + (int64_t)r * B + c * 16);
-    st_v4(L.host + row * B + c * 16, v);
-    if (p < D) {
-        st_v4(L.dev + ((int64_t)r * D + p) * B + c * 16, v);
-        if (c == 0 && L.st.tok2slot) {
-            int32_t *t2s = L.st.tok2slot + a.g.host_off[r];
-            int32_t *s2t = L.st.slot2tok + (int64_t)r * D;
+    for (int l0 = 0; l0 < L; l0 += BACKUP_GROUP) {
+        if (l0 > 0) {
+#pragma unroll
+            for (int u = 0; u < BACKUP_GROUP; ++u)
+                if (l0 + u < L) v[u] = ld_dev_v4(a.layer[l0 + u].rows + (int64_t)r * B + c * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < BACKUP_GROUP; ++u) {
+            if (l0 + u >= L) continue;
+            const BackupLayer &Ly = a.layer[l0 + u];
+            st_v4(Ly.host + row * B + c * 16, v[u]);
+            if (p < D) st_v4(Ly.dev + ((int64_t)r * D + p) * B + c * 16, v[u]);
+        }
+    }
+    // a short request (p < D) holds every token at slot = token: pair slot
+    // p with token p in the maps of the layers that own state
+    if (p < D && c == 0) {
+        for (int li = 0; li < L; ++li) {
+            const BackupLayer &Ly = a.layer[li];
+            if (!Ly.st.tok2slot) continue;
+            int32_t *t2s = Ly.st.tok2slot + a.g.host_off[r];
+            int32_t *s2t = Ly.st.slot2tok + (int64_t)r * D;
             const int32_t old_tok = s2t[p], old_slot = t2s[p];
             if (old_tok >= 0 && old_tok != p) t2s[old_tok] = -1;
             if (old_slot >= 0 && old_slot != p) s2t[old_slot] = -1;
@@ -275,10 +301,21 @@ cudaError_t launch_replay(const ReplayLaunch &a, cudaStream_t s)
 
 cudaError_t launch_backup(const BackupLaunch &a, cudaStream_t s)
 {
-    const int64_t n = (int64_t)a.g.R * a.g.chunks * a.num_layers;
-    const int blocks = (int)((n + 255) / 256);
-    backup_kernel<<<blocks, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    const int64_t n = (int64_t)a.g.R * a.g.chunks;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((n + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (a.programmatic) {
+        // a backup usually follows the step's last swap-in: placed under its
+        // tail, it waits for it on the device (griddepcontrol.wait)
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, backup_kernel, a);
 }
 
 cudaError_t launch_prefill(const int32_t *seq_lens, const LayerDescDev *layers, int num_layers,

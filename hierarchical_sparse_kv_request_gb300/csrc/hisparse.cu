@@ -50,6 +50,9 @@ struct hisparse_handle {
     int32_t *noalloc_scratch = nullptr; // device address of g_noalloc_scratch on this device
     int32_t copy_mode = HISPARSE_COPY_FUSED;
     int32_t protect_calls = 0;  // slots selected by the last this many calls are kept
+    int32_t max_stage_rows = 0; // miss rows per request the resolve CTA's shared memory holds
+    int32_t stage_rows = 0;     // of those, how many the fused copy stages (set_stage_rows)
+    bool programmatic = false;  // swap-ins and backups launched with a programmatic dependency
     bool stage_s2t = false;   // resolve kernel stages the slot->token row
 
     // Paged host pool (hb > 0): pool_blocks blocks of hb rows per layer,
@@ -364,14 +367,19 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
     }
     int max_smem = 0;
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
-    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, false, h->tbl_stride) > (size_t)max_smem ||
+    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, false, h->tbl_stride, 0, h->B) >
+            (size_t)max_smem ||
         hs::replay_smem_bytes(h->R) > (size_t)max_smem) {
         release(h);
         return HISPARSE_ERR_UNSUPPORTED;
     }
-    // the slot->token row rides in shared memory when it fits
-    h->stage_s2t = hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, true, h->tbl_stride) <=
-                   (size_t)max_smem;
+    // the slot->token row rides in shared memory when it fits; the shared
+    // memory left over stages miss rows for the bulk-copy engine
+    h->stage_s2t = hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, true, h->tbl_stride, 0,
+                                          h->B) <= (size_t)max_smem;
+    h->max_stage_rows = hs::resolve_stage_rows(h->k, h->D, (int)h->max_cap, h->stage_s2t,
+                                               h->tbl_stride, h->B, (size_t)max_smem);
+    h->stage_rows = 0;          // measured: staging is slower on the benchmarked shapes
     if (hs::resolve_prepare((size_t)max_smem) != cudaSuccess || hs::copy_prepare() != cudaSuccess) {
         release(h);
         return HISPARSE_ERR_CUDA;
@@ -655,6 +663,9 @@ int swap_in_impl(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int
     a.deferred = autom ? h->d_deferred : nullptr;
     a.defer_bytes = kAutoDeferBytes;
     a.protect_calls = (uint32_t)h->protect_calls;
+    // rows go through shared memory only when this CTA copies them for sure
+    a.stage_rows = (!split && !autom) ? h->stage_rows : 0;
+    a.programmatic = h->programmatic;
     const bool wide_copy = split || autom;
     a.plan_rows = out_plan ? out_plan->rows : (wide_copy ? h->d_plan_rows : nullptr);
     a.plan_counts = out_plan ? out_plan->counts : (wide_copy ? h->d_plan_counts : nullptr);
@@ -745,6 +756,7 @@ int hisparse_backup_layers(hisparse_t h, const int32_t *layers, int32_t num_laye
     b.positions = positions;
     b.g = geometry(h);
     b.status = h->d_status;
+    b.programmatic = h->programmatic;
     return cuda_status(hs::launch_backup(b, as_stream(stream)));
 }
 
@@ -910,6 +922,20 @@ int hisparse_set_protected_calls(hisparse_t h, int32_t calls)
     return HISPARSE_OK;
 }
 
+int hisparse_set_programmatic_launch(hisparse_t h, int32_t on)
+{
+    if (!h || (on != 0 && on != 1)) return HISPARSE_ERR_INVALID_ARG;
+    h->programmatic = on == 1;
+    return HISPARSE_OK;
+}
+
+int hisparse_set_stage_rows(hisparse_t h, int32_t rows)
+{
+    if (!h || rows < -1) return HISPARSE_ERR_INVALID_ARG;
+    h->stage_rows = rows == -1 ? h->max_stage_rows : std::min(rows, h->max_stage_rows);
+    return HISPARSE_OK;
+}
+
 int hisparse_set_copy_mode(hisparse_t h, int32_t mode)
 {
     if (!h || (mode != HISPARSE_COPY_FUSED && mode != HISPARSE_COPY_SPLIT && mode != HISPARSE_COPY_AUTO))
@@ -952,6 +978,8 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     a.deferred = nullptr;
     a.defer_bytes = 0;
     a.protect_calls = (uint32_t)h->protect_calls;
+    a.stage_rows = 0;
+    a.programmatic = h->programmatic;
     a.plan_rows = scratch;
     a.plan_counts = scratch + (int64_t)h->R * h->k * 2;
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));

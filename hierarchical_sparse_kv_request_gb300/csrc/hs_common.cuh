@@ -20,6 +20,7 @@ constexpr int kStatusBadPosition = 4;
 constexpr int kStatusBadResident = 5;
 constexpr int kStatusNoHostRow = 6;
 constexpr int kStatusCapacity = 7;
+constexpr int kStatusCopyTimeout = 8;
 constexpr int32_t kResidentFlag = 1 << 30;  // marks a row of the resident pool
 
 // Hot state of one state-owning layer.  Per request r:
@@ -163,11 +164,20 @@ struct ResolveLaunch {
     int32_t *deferred;        // [R]: 1 = misses left to the copy grid; null = never defer
     int64_t defer_bytes;      // defer a request whose misses exceed this many bytes
     uint32_t protect_calls;   // slots selected by the last this many calls are kept (0: off)
+    int32_t stage_rows;       // misses fetched into shared memory by the bulk-copy engine
+                              // (0: none; only with fused_copy and no deferral)
+    bool programmatic;        // launch with a programmatic dependency on the stream's
+                              // previous kernel (it waits for it on the device)
 };
 
 // Shared-memory bytes the resolve kernel needs for this geometry
-// (tbl_stride: the host block table row staged per request, 0 = none).
-size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int tbl_stride);
+// (tbl_stride: the host block table row staged per request, 0 = none;
+// stage_rows rows of B bytes for the bulk-copy engine).
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int tbl_stride,
+                          int stage_rows, int64_t B);
+// The most rows the bulk-copy engine can stage within max_smem (at most k).
+int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, int tbl_stride, int64_t B,
+                       size_t max_smem);
 int resolve_threads();
 // Allow every instantiation of the resolve kernel up to `smem` bytes of
 // dynamic shared memory (called at handle creation, outside any capture).
@@ -207,6 +217,7 @@ struct BackupLaunch {
     const int32_t *positions; // device [R], shared by the layers
     Geometry g;
     int32_t *status;
+    bool programmatic;        // as ResolveLaunch::programmatic
 };
 cudaError_t launch_backup(const BackupLaunch &a, cudaStream_t s);
 

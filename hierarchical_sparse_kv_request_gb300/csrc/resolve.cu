@@ -9,23 +9,34 @@
 // host row into it).
 //
 // The miss copies cross the host link and dominate the call, so everything
-// else is arranged around starting them early and keeping them going:
-//   1. the LRU list is staged into shared memory with asynchronous copies
-//      issued at kernel start, under the first global round trips;
-//   2. once the sorted miss list exists, every thread loads its first host
-//      chunks into registers, and those loads are in flight while the
-//      victims are chosen;
-//   3. the slot->token row is staged too, so once the victims are known all
-//      state writes are plain stores with no loads of their own (they still
-//      queue behind the thread's host loads in flight, which keep the link
-//      busy meanwhile); they are issued before the prefetched rows are
-//      consumed, then every thread streams the rest of the rows.
+// else is arranged around starting them as early as possible and keeping
+// them going:
+//   1. the LRU list (and the slot->token row) are staged into shared memory
+//      with asynchronous copies issued at kernel start, under the first
+//      global round trips;
+//   2. a miss is known as soon as its token->slot lookup returns, long before
+//      its victim slot is: at classification every miss takes an arrival
+//      index (a warp-aggregated shared-memory counter).  The first
+//      `stage_rows` misses to arrive have their host rows fetched at once
+//      into shared memory by the bulk-copy engine (cp.async.bulk, completion
+//      on an mbarrier), with no register or load slot held; the rest form a
+//      "leftover" list whose first chunks every thread loads into registers
+//      right after classification;
+//   3. then the block scans give each miss its rank in token order and its
+//      victim; all state writes are plain stores (the slot->token row is
+//      staged, so no write waits on a load of its own);
+//   4. finally the leftover chunks are stored (the rest streamed), and once
+//      the mbarrier completes the staged rows go from shared memory to their
+//      victim slots with bulk stores.
+// Only the bytes' route differs from a copy in rank order; where each row
+// lands is fixed by its rank, so the results are the same.
 //
 // With a paged host pool ([Arch] Ownership: tokens map to logical host
 // blocks), the request's host block table row is staged as well, under the
 // token->slot round trip; a miss whose block is not reserved stops the call
-// for that request (status NO_HOST_ROW), and miss rows are addressed, and
-// recorded in the plan, by their row in the layer's pool.
+// for that request (status NO_HOST_ROW, and nothing is fetched for it), and
+// miss rows are addressed, and recorded in the plan, by their row in the
+// layer's pool.
 //
 // Exact LRU without sorting.  The request's slots are kept in a list `lru`
 // ordered by (last_used, slot).  One call stamps every selected slot (hits and
@@ -43,27 +54,34 @@ namespace hs {
 namespace {
 
 constexpr int NT = 1024;       // threads per CTA
-// Host chunks per thread loaded before the victims are chosen, by the number
-// of top-k entries per thread.  Deeper is faster (decode_40k, measured: 4
-// -> 8 took a step from 54.1 to 52.3 us), as far as the 64 registers of a
-// 1024-thread CTA hold them without spilling.
-template <int KT> __host__ __device__ constexpr int prefetch_depth() { return KT == 2 ? 8 : 4; }
+// Leftover host chunks per thread loaded right after classification, by the
+// number of top-k entries per thread: as many as the 64 registers of a
+// 1024-thread CTA hold without spilling (deeper was faster on decode_40k
+// while it did not spill: 4 -> 8 took a step from 54.1 to 52.3 us).
+template <int KT> __host__ __device__ constexpr int prefetch_depth() { return KT == 2 ? 8 : (KT == 8 ? 2 : 4); }
 // Host chunks in flight per thread in the copy loop.  Measured on decode_40k
 // (32 CTAs): 4 ends the launch ~1.3 us sooner than 8; 2 and 6 gain less, and
 // with 128 or 256 CTAs the depth makes no difference.
 constexpr int COPY_UNROLL = 4;
+// How long a CTA waits for its staged rows before it gives up on them (2 s
+// of the GPU's global timer): far beyond any copy that completes (a call
+// moves at most a few MB per CTA), so reaching it means a fault of the copy,
+// which is recorded (status COPY_TIMEOUT) instead of waited for forever.
+constexpr uint64_t kWaitNs = 2000000000ull;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct SmemPlan {
-    size_t hit, sel, miss, lru, s2t, tbl, chunk, vict, mtok, total;
+    size_t hit, sel, miss, lru, s2t, tbl, chunk, vict, lrow, avict, bar, cnt, stage, total;
 };
 
 // Shared memory of the CTA: bitmaps over slots and tokens, the staged LRU
-// list, optionally the staged slot->token row and host block table row, and
-// miss rows and victims by miss rank.
+// list, optionally the staged slot->token row and host block table row,
+// victims by miss rank and by arrival index, the leftover host rows, the
+// staging mbarrier and arrival counter, and
+// `stage_rows` rows of B bytes staged by the bulk-copy engine.
 __host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t,
-                                              int tbl_stride)
+                                              int tbl_stride, int stage_rows, int64_t B)
 {
     SmemPlan p;
     const size_t DW = (size_t)(D + 31) / 32, MW = (size_t)(max_cap + 31) / 32;
@@ -76,7 +94,12 @@ __host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool st
     p.tbl = o;   o += (size_t)tbl_stride * 4;   // a multiple of 16
     p.chunk = o; o = align_up(o + (size_t)NT * 2, 4);
     p.vict = o;  o = align_up(o + (size_t)k * 2, 4);
-    p.mtok = o;  o += (size_t)k * 4;
+    p.lrow = o;  o += (size_t)k * 4;
+    p.avict = o; o = align_up(o + (size_t)k * 2, 8);
+    p.bar = o;   o += 8;
+    p.cnt = o;   o += 8;
+    p.stage = align_up(o, 128);
+    o = p.stage + (size_t)stage_rows * (size_t)B;
     p.total = align_up(o, 16);
     return p;
 }
@@ -91,8 +114,52 @@ struct Smem {
     int32_t *tbl_s;      // [tbl_stride] staged host block table row (null: no paged pool)
     uint16_t *chunk_pre; // [NT]  misses before each thread's chunk of missbits
     uint16_t *victims;   // [k]   victim slot of miss rank i
-    int32_t *misstok;    // [k]   host row of miss rank i (token, or pool row when paged)
+    int32_t *left_row;   // [k]   host row of leftover q = arrival SR + q (token, or pool
+                         //       row when paged)
+    uint16_t *arr_vict;  // [k]   victim slot of the miss with arrival index j
+    uint64_t *bar;       //       mbarrier of the staged rows
+    uint32_t *arrived;   //       misses that took an arrival index
+    uint32_t *flags;     //       error flags of the CTA's classification (kFlag*)
+    uint8_t *stage;      // [stage_rows][B] rows fetched by the bulk-copy engine
 };
+
+// KT small signed indices (each in [-1, 32767]) packed two to a register.
+template <int KT>
+struct PackedIdx {
+    uint32_t w[(KT + 1) / 2];
+    __device__ __forceinline__ int32_t get(int i) const
+    {
+        return (int32_t)(int16_t)(uint16_t)(w[i >> 1] >> ((i & 1) * 16));
+    }
+    __device__ __forceinline__ void set(int i, int32_t v)
+    {
+        const int sh = (i & 1) * 16;
+        w[i >> 1] = (w[i >> 1] & ~(0xFFFFu << sh)) | ((uint32_t)(uint16_t)v << sh);
+    }
+};
+
+// Classification outcomes, OR-ed over the CTA in one barrier.
+constexpr uint32_t kFlagBad = 1, kFlagDup = 2, kFlagBadRes = 4, kFlagNoHost = 8;
+
+// OR of `f` over the CTA: one warp reduction, one shared atomic per warp
+// and one barrier.  *word must be 0 and published by an earlier barrier.
+__device__ __forceinline__ uint32_t block_or(uint32_t f, uint32_t *word)
+{
+    f = __reduce_or_sync(0xffffffffu, f);
+    if ((threadIdx.x & 31) == 0 && f) atomicOr(word, f);
+    __syncthreads();
+    return *word;
+}
+
+// The status a call's flags give (BAD_INDEX, then DUPLICATE, BAD_RESIDENT
+// and NO_HOST_ROW), or OK.
+__device__ __forceinline__ int status_of(uint32_t flags)
+{
+    return (flags & kFlagBad) ? kStatusBadIndex
+           : (flags & kFlagDup) ? kStatusDuplicate
+           : (flags & kFlagBadRes) ? kStatusBadResident
+           : (flags & kFlagNoHost) ? kStatusNoHostRow : kStatusOk;
+}
 
 __device__ __forceinline__ bool test_bit(const uint32_t *bits, int i)
 {
@@ -106,6 +173,82 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// ---- bulk-copy engine (TMA, non-tensor form) and its mbarrier --------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t arrivals)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(arrivals)
+                 : "memory");
+    // make the initialised barrier visible to the bulk-copy engine
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// One arrival of this thread, announcing `bytes` more to be delivered.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait for phase 0 of the staging barrier; false after kWaitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar)
+{
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, 0))
+        if (global_ns() - t0 > kWaitNs) return false;
+    return true;
+}
+// Wait for the staged rows of request r.  If they do not all land within
+// the bound, record COPY_TIMEOUT and wait once more (bounded as well) so
+// that no copy is still writing this CTA's shared memory when it exits.
+__device__ __forceinline__ bool staged_rows_landed(uint64_t *bar, int32_t *status, int r)
+{
+    if (mbar_wait_bounded(bar)) return true;
+    record_status(status, r, kStatusCopyTimeout);
+    mbar_wait_bounded(bar);
+    return false;
+}
+// gmem (here pinned host memory through its device address) -> smem, `bytes`
+// a multiple of 16 from 16-byte aligned addresses; completes on `bar`.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// smem -> gmem; tracked in the issuing thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Resident row of position t from its block id `id` (-1: not resident), or
 // -2 when the id is malformed (below -1, or rows reaching the flag bit).
@@ -149,14 +292,18 @@ template <int KT>
 __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
 {
     constexpr int PREFETCH = prefetch_depth<KT>();
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
     const int r = blockIdx.x;
     const int tid = threadIdx.x;
+    const int lane = tid & 31;
     const int k = a.g.k, D = a.g.D;
     const int DW = (D + 31) >> 5;
+    const int64_t B = a.g.B;
+    const int CH = a.g.chunks;
+    const int SR = a.stage_rows;   // rows the bulk-copy engine may stage (0: none)
 
     const int32_t hb = a.g.hb;
-    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t, hb ? a.g.tbl_stride : 0);
+    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t, hb ? a.g.tbl_stride : 0, SR, B);
     Smem sm;
     sm.warp_tot = reinterpret_cast<uint32_t *>(smem_raw);
     sm.hitbits = reinterpret_cast<uint32_t *>(smem_raw + sp.hit);
@@ -167,10 +314,23 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     sm.tbl_s = hb ? reinterpret_cast<int32_t *>(smem_raw + sp.tbl) : nullptr;
     sm.chunk_pre = reinterpret_cast<uint16_t *>(smem_raw + sp.chunk);
     sm.victims = reinterpret_cast<uint16_t *>(smem_raw + sp.vict);
-    sm.misstok = reinterpret_cast<int32_t *>(smem_raw + sp.mtok);
+    sm.left_row = reinterpret_cast<int32_t *>(smem_raw + sp.lrow);
+    sm.arr_vict = reinterpret_cast<uint16_t *>(smem_raw + sp.avict);
+    sm.bar = reinterpret_cast<uint64_t *>(smem_raw + sp.bar);
+    sm.arrived = reinterpret_cast<uint32_t *>(smem_raw + sp.cnt);
+    sm.flags = sm.arrived + 1;
+    sm.stage = smem_raw + sp.stage;
 
-    // A copy grid launched with a programmatic dependency may be scheduled
-    // now; it still waits for this grid to finish before reading the plan.
+    // Launched behind another kernel with a programmatic dependency, this
+    // grid may start while that one still runs (its CTAs are placed and set
+    // up under the other's tail); nothing from global memory is read before
+    // the other grid has completed and its writes are visible.  Without such
+    // a dependency the wait returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Only now may the next launch start early: by then every grid before
+    // this one has completed, so a swap-in that follows never reads hot
+    // state that an older call is still writing.  (A copy grid launched
+    // behind this one still waits for this grid before reading the plan.)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- loads that do not depend on each other --------------------------
@@ -217,24 +377,19 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     if (S <= D) {
         const int mw = (S + 31) >> 5;
         for (int w = tid; w < mw; w += NT) sm.missbits[w] = 0u;
+        if (tid == 0) *sm.flags = 0u;
         __syncthreads();
-        bool bad = false, dup = false, badres = false;
+        uint32_t f = 0;
 #pragma unroll
         for (int i = 0; i < KT; ++i) {
             const int32_t x = t[i];
             if (x == -1) continue;
-            if (x < 0 || x >= S) { bad = true; continue; }
-            badres |= resident_row(rid[i], x, a.res_block_size) == -2;
+            if (x < 0 || x >= S) { f |= kFlagBad; continue; }
+            if (resident_row(rid[i], x, a.res_block_size) == -2) f |= kFlagBadRes;
             const uint32_t bit = 1u << (x & 31);
-            dup |= (atomicOr(&sm.missbits[x >> 5], bit) & bit) != 0u;
+            if (atomicOr(&sm.missbits[x >> 5], bit) & bit) f |= kFlagDup;
         }
-        bad = __syncthreads_or(bad);
-        dup = __syncthreads_or(dup);
-        badres = __syncthreads_or(badres);
-        finish_untouched<KT>(a, r, t, rid,
-                             bad ? kStatusBadIndex
-                                 : (dup ? kStatusDuplicate : (badres ? kStatusBadResident : kStatusOk)),
-                             tick);
+        finish_untouched<KT>(a, r, t, rid, status_of(block_or(f, sm.flags)), tick);
         return;
     }
 
@@ -267,43 +422,102 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (sm.s2t_s)
             for (int i = tid; i < D; i += NT) sm.s2t_s[i] = slot2tok[i];
     }
+    if (tid == 0) {
+        *sm.arrived = 0u;
+        *sm.flags = 0u;
+        if (SR) mbar_init(sm.bar, NT);   // every thread arrives once
+    }
     cp_async_wait_all();
     __syncthreads();
 
     // Classify.  A resident position is marked in the token bitmap only to
     // catch duplicates; its bit is cleared again before the misses are
-    // ranked, and it never touches the hot state.
-    bool bad = false, dup = false, badres = false, nohost = false;
+    // ranked, and it never touches the hot state.  A miss with a host row is
+    // also marked for the early fetch below.
+    uint32_t f = 0;       // kFlag* of this thread's entries
+    uint32_t miss = 0;    // bit i: entry i is a miss with a host row
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int32_t x = t[i];
         if (x == -1) continue;
-        if (x < 0 || x >= S) { bad = true; continue; }
+        if (x < 0 || x >= S) { f |= kFlagBad; continue; }
         rid[i] = resident_row(rid[i], x, a.res_block_size);   // now the row
-        badres |= rid[i] == -2;
-        if (rid[i] == -1 && s[i] < 0 && hb) nohost |= sm.tbl_s[x / hb] < 0;
+        if (rid[i] == -2) f |= kFlagBadRes;
+        if (rid[i] == -1 && s[i] < 0) {
+            if (hb && sm.tbl_s[x / hb] < 0) f |= kFlagNoHost;
+            else miss |= 1u << i;
+        }
         if (rid[i] < 0 && s[i] >= 0) {
             const uint32_t bit = 1u << (s[i] & 31);
-            dup |= (atomicOr(&sm.hitbits[s[i] >> 5], bit) & bit) != 0u;
+            if (atomicOr(&sm.hitbits[s[i] >> 5], bit) & bit) f |= kFlagDup;
         } else {
             const uint32_t bit = 1u << (x & 31);
-            dup |= (atomicOr(&sm.missbits[x >> 5], bit) & bit) != 0u;
+            if (atomicOr(&sm.missbits[x >> 5], bit) & bit) f |= kFlagDup;
         }
     }
-    bad = __syncthreads_or(bad);
-    dup = __syncthreads_or(dup);
-    badres = __syncthreads_or(badres);
-    nohost = __syncthreads_or(nohost);
-    if (bad || dup || badres || nohost) {
+
+    // Arrival indices (warp-aggregated), and the early fetch: arrival j <
+    // SR stages the row in shared memory row j by the bulk-copy engine; the
+    // others become leftover j - SR.  The host row is known now; only the
+    // victim slot waits for the scans below.
+    const uint8_t *hrow0 = a.store.host + (hb ? 0 : off) * B;
+    uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
+    PackedIdx<KT> arr;    // arrival index of entry i (a miss), else -1
+    uint32_t staged_bytes = 0;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        arr.set(i, -1);
+        const bool mine = (miss >> i) & 1u;
+        const unsigned mask = __ballot_sync(0xffffffffu, mine);
+        if (mask == 0u) continue;
+        const int leader = __ffs(mask) - 1;
+        uint32_t base = 0;
+        if (lane == leader) base = atomicAdd(sm.arrived, (uint32_t)__popc(mask));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        if (!mine) continue;
+        const int32_t j = (int32_t)(base + __popc(mask & ((1u << lane) - 1u)));
+        arr.set(i, j);
+        if (j < SR) staged_bytes += (uint32_t)B;
+        else sm.left_row[j - SR] = host_slot(t[i]);
+    }
+    if (SR) {
+        mbar_arrive_expect_tx(sm.bar, staged_bytes);
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+            const int32_t j = arr.get(i);
+            if (j >= 0 && j < SR)
+                bulk_load(sm.stage + (int64_t)j * B, hrow0 + (int64_t)host_slot(t[i]) * B,
+                          (uint32_t)B, sm.bar);
+        }
+    }
+    const uint32_t flags = block_or(f, sm.flags);
+    if (flags) {
+        // staged rows may still be landing in shared memory
+        if (SR) staged_rows_landed(sm.bar, a.status, r);
 #pragma unroll
         for (int i = 0; i < KT; ++i) rid[i] = -1;
-        finish_untouched<KT>(a, r, t, rid,
-                             bad ? kStatusBadIndex
-                                 : (dup ? kStatusDuplicate
-                                        : (badres ? kStatusBadResident : kStatusNoHostRow)),
-                             tick);
+        finish_untouched<KT>(a, r, t, rid, status_of(flags), tick);
         return;
     }
+
+    // Leftover chunks: loaded now, stored after the state writes below.  In
+    // a call without errors every miss took one arrival index, so the count
+    // is the call's miss count m.  (A request with many misses can leave its
+    // copies to a full-GPU copy grid launched behind this kernel.)
+    const int m_arr = (int)*sm.arrived;
+    const bool defer = a.deferred && (int64_t)m_arr * B > a.defer_bytes;
+    const int nleft = (a.fused_copy && !defer) ? max(m_arr - SR, 0) : 0;
+    const int total = nleft * CH;
+    uint4 pv[PREFETCH];
+#pragma unroll
+    for (int u = 0; u < PREFETCH; ++u) {
+        const int e = tid + u * NT;
+        if (e < total) {
+            const int q = e / CH, c = e - q * CH;
+            pv[u] = ld_host_v4(hrow0 + (int64_t)sm.left_row[q] * B + c * 16);
+        }
+    }
+
     if (a.resident) {
 #pragma unroll
         for (int i = 0; i < KT; ++i)
@@ -336,18 +550,6 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int m = (int)(tot >> 16);
     const int h = D - (int)(tot & 0xFFFFu);
     sm.chunk_pre[tid] = (uint16_t)(pre >> 16);
-    {   // the sorted miss list: enumerate this thread's words in order
-        uint32_t rank = pre >> 16;
-        for (int w = w0; w < w1; ++w) {
-            uint32_t bits = sm.missbits[w];
-            while (bits) {
-                const int b = __ffs(bits) - 1;
-                bits &= bits - 1u;
-                sm.misstok[rank++] = host_slot(w * 32 + b);
-            }
-        }
-    }
-    __syncthreads();
 
     // Protected slots ([Arch] Resident device pages: a later verification
     // step may not reuse a hot row before an earlier step has consumed it):
@@ -357,6 +559,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     if (a.protect_calls && m > 0) {
         const uint32_t thr = tick > a.protect_calls ? tick - a.protect_calls : 1u;
         uint32_t q = pre & 0xFFFFu;
+        __syncthreads();   // the scan's total is read; warp_tot[0] is free again
         for (int e = e0; e < e1; ++e) {
             const int sl = sm.lru_s[e];
             if (test_bit(sm.hitbits, sl)) continue;
@@ -366,27 +569,9 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         }
         __syncthreads();
         if (sm.warp_tot[0]) {
+            if (SR) staged_rows_landed(sm.bar, a.status, r);
             finish_untouched<KT>(a, r, t, rid, kStatusCapacity, tick);
             return;
-        }
-    }
-
-    // First host chunks: loaded now, stored after the state writes below.
-    const int64_t B = a.g.B;
-    const int CH = a.g.chunks;
-    // A request with many misses can leave its copies to a full-GPU copy
-    // grid launched behind this kernel: one SM alone moves them slowly.
-    const bool defer = a.deferred && (int64_t)m * B > a.defer_bytes;
-    const int total = (a.fused_copy && !defer) ? m * CH : 0;
-    const uint8_t *hrow0 = a.store.host + (hb ? 0 : off) * B;
-    uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
-    uint4 pv[PREFETCH];
-#pragma unroll
-    for (int u = 0; u < PREFETCH; ++u) {
-        const int e = tid + u * NT;
-        if (e < total) {
-            const int i = e / CH, c = e - i * CH;
-            pv[u] = ld_host_v4(hrow0 + (int64_t)sm.misstok[i] * B + c * 16);
         }
     }
 
@@ -410,7 +595,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     __syncthreads();
 
     // State writes (stores only: no load of their own to wait for).  Misses
-    // take victims by ascending token rank.
+    // take victims by ascending token rank; each victim is also filed under
+    // the miss's arrival index, where the copies below look it up.
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int j = tid + i * NT;
@@ -422,6 +608,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         for (int q = owner * WC; q < w; ++q) rank += __popc(sm.missbits[q]);
         rank += __popc(sm.missbits[w] & ((1u << (x & 31)) - 1u));
         const int v = sm.victims[rank];
+        sm.arr_vict[arr.get(i)] = (uint16_t)v;
         const int32_t old = sm.s2t_s ? sm.s2t_s[v] : slot2tok[v];
         if (old >= 0 && (int64_t)old < cap) tok2slot[old] = -1;
         slot2tok[v] = x;
@@ -434,7 +621,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         }
     }
     // Selected slots (hits and victims) go to the back of the list in slot
-    // order and are stamped with the tick.
+    // order and are stamped with the tick.  (The scan's barriers also publish
+    // the leftover victims written above.)
     {
         uint32_t *last_used = a.st.last_used + (int64_t)r * D;
         const uint32_t w = tid < DW ? (sm.hitbits[tid] | sm.selbits[tid]) : 0u;
@@ -456,12 +644,13 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     }
 
     // ---- miss copies: pinned host rows -> victim slots ---------------------
+    // the leftovers: the chunks loaded above, then the rest streamed
 #pragma unroll
     for (int u = 0; u < PREFETCH; ++u) {
         const int e = tid + u * NT;
         if (e < total) {
-            const int i = e / CH, c = e - i * CH;
-            st_v4(drow0 + (int64_t)sm.victims[i] * B + c * 16, pv[u]);
+            const int q = e / CH, c = e - q * CH;
+            st_v4(drow0 + (int64_t)sm.arr_vict[SR + q] * B + c * 16, pv[u]);
         }
     }
     for (int e = PREFETCH * NT + tid; e < total; e += NT * COPY_UNROLL) {
@@ -472,22 +661,49 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
             const int ee = e + u * NT;
             dst[u] = nullptr;
             if (ee < total) {
-                const int i = ee / CH, c = ee - i * CH;
-                v[u] = ld_host_v4(hrow0 + (int64_t)sm.misstok[i] * B + c * 16);
-                dst[u] = drow0 + (int64_t)sm.victims[i] * B + c * 16;
+                const int q = ee / CH, c = ee - q * CH;
+                v[u] = ld_host_v4(hrow0 + (int64_t)sm.left_row[q] * B + c * 16);
+                dst[u] = drow0 + (int64_t)sm.arr_vict[SR + q] * B + c * 16;
             }
         }
 #pragma unroll
         for (int u = 0; u < COPY_UNROLL; ++u)
             if (dst[u]) st_v4(dst[u], v[u]);
     }
+    // the staged rows, once they have all landed, one bulk store per row
+    if (SR) {
+        if (!staged_rows_landed(sm.bar, a.status, r)) return;
+        const int nstaged = min(m_arr, SR);
+        if (tid < nstaged) {
+            fence_proxy_async();
+            for (int j = tid; j < nstaged; j += NT)
+                bulk_store(drow0 + (int64_t)sm.arr_vict[j] * B, sm.stage + (int64_t)j * B,
+                           (uint32_t)B);
+            bulk_commit();
+            bulk_wait_read();
+        }
+    }
 }
 
 template <int KT>
 cudaError_t launch_kt(const ResolveLaunch &a, cudaStream_t s, size_t smem)
 {
-    resolve_kernel<KT><<<a.g.R, NT, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.g.R);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (a.programmatic) {
+        // programmatic dependency on the previous kernel of the stream: this
+        // grid may be placed before that one ends and waits for it on the
+        // device (griddepcontrol.wait at the kernel's start)
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, resolve_kernel<KT>, a);
 }
 
 template <int KT>
@@ -499,9 +715,19 @@ cudaError_t prepare_kt(size_t smem)
 
 }  // namespace
 
-size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int tbl_stride)
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int tbl_stride,
+                          int stage_rows, int64_t B)
 {
-    return plan_smem(k, D, max_cap, stage_s2t, tbl_stride).total;
+    return plan_smem(k, D, max_cap, stage_s2t, tbl_stride, stage_rows, B).total;
+}
+
+int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, int tbl_stride, int64_t B,
+                       size_t max_smem)
+{
+    const size_t base = resolve_smem_bytes(k, D, max_cap, stage_s2t, tbl_stride, 0, B);
+    const size_t room = align_up(base, 128) + 16 <= max_smem ? max_smem - align_up(base, 128) - 16 : 0;
+    const int64_t rows = (int64_t)(room / (size_t)B);
+    return (int)(rows < k ? rows : k);
 }
 
 int resolve_threads() { return NT; }
@@ -518,7 +744,7 @@ cudaError_t resolve_prepare(size_t smem)
 cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s)
 {
     const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t,
-                                           a.g.hb ? a.g.tbl_stride : 0);
+                                           a.g.hb ? a.g.tbl_stride : 0, a.stage_rows, a.g.B);
     const int kt = (a.g.k + NT - 1) / NT;
     if (kt <= 1) return launch_kt<1>(a, s, smem);
     if (kt <= 2) return launch_kt<2>(a, s, smem);

@@ -22,7 +22,7 @@ OK = 0
 ERR_INVALID_ARG, ERR_LAYOUT, ERR_CAPACITY, ERR_LAYER = -1, -2, -3, -4
 ERR_CUDA, ERR_NO_MEMORY, ERR_UNSUPPORTED, ERR_ALIGNMENT = -5, -6, -7, -8
 STATUS_OK, STATUS_BAD_INDEX, STATUS_DUPLICATE, STATUS_BAD_SEQ_LEN, STATUS_BAD_POSITION = 0, 1, 2, 3, 4
-STATUS_BAD_RESIDENT, STATUS_NO_HOST_ROW, STATUS_CAPACITY = 5, 6, 7
+STATUS_BAD_RESIDENT, STATUS_NO_HOST_ROW, STATUS_CAPACITY, STATUS_COPY_TIMEOUT = 5, 6, 7, 8
 
 
 def STATUS_BIT(code: int) -> int:
@@ -93,6 +93,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_write_state": [P, I32, P, P, P, I32, P],
         "hisparse_set_copy_mode": [P, I32],
         "hisparse_set_protected_calls": [P, I32],
+        "hisparse_set_stage_rows": [P, I32],
+        "hisparse_set_programmatic_launch": [P, I32],
         "hisparse_check_guards": [P, P],
         "hisparse_version": [],
         "hisparse_synthetic_compute": [P, I64, I32, I32, P],
@@ -379,6 +381,17 @@ class HiSparse:
         """Keep the hot rows of each request's last `calls` calls (0: off)."""
         _check(self.lib.hisparse_set_protected_calls(self.h, calls),
                "hisparse_set_protected_calls")
+
+    def set_stage_rows(self, rows: int) -> None:
+        """Miss rows per request the fused copy stages through shared memory
+        with the bulk-copy engine (0: none, the default; -1: as many as fit)."""
+        _check(self.lib.hisparse_set_stage_rows(self.h, rows), "hisparse_set_stage_rows")
+
+    def set_programmatic_launch(self, on: bool) -> None:
+        """Launch swap-ins and backups with a programmatic dependency on the
+        stream's previous kernel (off by default)."""
+        _check(self.lib.hisparse_set_programmatic_launch(self.h, 1 if on else 0),
+               "hisparse_set_programmatic_launch")
 
     def set_copy_mode(self, mode: int) -> None:
         _check(self.lib.hisparse_set_copy_mode(self.h, mode), "hisparse_set_copy_mode")

@@ -21,6 +21,7 @@ fp32 scales + bf16 rope = 656 B, or 576 bf16 values = 1152 B).
 from __future__ import annotations
 
 import dataclasses
+import os
 from typing import Dict, List, Optional
 
 import numpy as np
@@ -276,22 +277,56 @@ class TopkSource:
         return cur.astype(np.int32)
 
 
-def topk_schedule(w: Workload) -> Dict[int, np.ndarray]:
+def _stream_calls(w: Workload, layer: int, r: int) -> np.ndarray:
+    """int32 [steps*substeps][k]: the top-k sets of one (layer, request)."""
+    calls = w.steps * w.substeps
+    src = TopkSource(w, layer, r)
+    out = np.empty((calls, w.top_k), dtype=np.int32)
+    for c in range(calls):
+        out[c] = src.next(int(w.seq_lens_at(c // w.substeps)[r]))
+    return out
+
+
+def _stream_job(args) -> np.ndarray:
+    return _stream_calls(*args)
+
+
+# Schedules with more index draws than this are generated by a pool of
+# worker processes (each (layer, request) stream is independent, so the
+# result is the same either way).
+_PARALLEL_DRAWS = 1 << 22
+
+
+def topk_schedule(w: Workload, workers: Optional[int] = None) -> Dict[int, np.ndarray]:
     """All top-k inputs: {anchor layer: int32 [steps*substeps][R][k]}.
 
     Call c of a layer is decode step c // substeps; sets chain across
-    sub-steps and decode steps alike.
+    sub-steps and decode steps alike.  `workers` > 1 spreads the independent
+    (layer, request) streams over that many processes (started with
+    "spawn", never forked); None picks a pool for large schedules.
     """
-    out = {}
     calls = w.steps * w.substeps
+    jobs = [(l, r) for l in w.anchors for r in range(w.num_requests)]
+    if workers is None:
+        big = len(jobs) * calls * w.top_k > _PARALLEL_DRAWS
+        workers = min(16, os.cpu_count() or 1, len(jobs)) if big else 1
+    rows = None
+    if workers > 1:
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        try:
+            with cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn")) as ex:
+                rows = list(ex.map(_stream_job, [(w, l, r) for l, r in jobs],
+                                   chunksize=max(1, len(jobs) // (4 * workers))))
+        except cf.process.BrokenProcessPool:
+            rows = None     # e.g. a main script the workers cannot import: go serial
+    if rows is None:
+        rows = [_stream_calls(w, l, r) for l, r in jobs]
+    out = {}
     for l in w.anchors:
-        arr = np.empty((calls, w.num_requests, w.top_k), dtype=np.int32)
-        for r in range(w.num_requests):
-            src = TopkSource(w, l, r)
-            for c in range(calls):
-                S = int(w.seq_lens_at(c // w.substeps)[r])
-                arr[c, r] = src.next(S)
-        out[l] = arr
+        out[l] = np.empty((calls, w.num_requests, w.top_k), dtype=np.int32)
+    for (l, r), a in zip(jobs, rows):
+        out[l][:, r] = a
     return out
 
 

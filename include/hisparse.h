@@ -82,6 +82,10 @@ extern "C" {
                                           a block the request has not reserved */
 #define HISPARSE_STATUS_CAPACITY 7     /* protected slots leave too few victims
                                           for the misses                      */
+#define HISPARSE_STATUS_COPY_TIMEOUT 8 /* rows staged by the bulk-copy engine
+                                          did not all arrive within the wait
+                                          bound (not expected; the request's
+                                          new slots may hold stale bytes)      */
 
 #define HISPARSE_STATUS_BIT(code) (1 << (code))
 
@@ -470,6 +474,42 @@ int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
  *                                  alone copies such a volume slowly; with
  *                                  8 or more requests: the same as FUSED. */
 int hisparse_set_copy_mode(hisparse_t h, int32_t mode);
+
+/*
+ * hisparse_set_stage_rows: how the fused copy (HISPARSE_COPY_FUSED) moves a
+ * request's miss rows.  With rows > 0, the first `rows` misses of a request
+ * to be found are fetched by the bulk-copy engine (cp.async.bulk) into the
+ * resolving CTA's shared memory as soon as their lookups return, before their
+ * victim slots are known, and stored to their slots once the victims are
+ * chosen; the others are loaded by the CTA's threads into registers right
+ * after classification.  0 (the default) stages none; -1 stages as many as
+ * the shared memory left over by the resolver holds (~259 rows of 656 B at
+ * k 2048, D 6144); a larger count is clamped to that.  Results are
+ * identical whatever the count; only the route of the bytes differs.
+ * Measured on GB300 (kernel-only step time): decode_40k 45.6 us with 0,
+ * 46.5 us with 16, 48.9 us with 64 and 57.6 us with all; mixed_len 1.009 ms
+ * with 0, 1.003 ms with all; spec_verify 3.576 ms with 0, 3.591 ms with
+ * all.  Read at each swap-in launch.  INVALID_ARG for rows < -1.
+ */
+int hisparse_set_stage_rows(hisparse_t h, int32_t rows);
+
+/*
+ * hisparse_set_programmatic_launch: on = 1 launches the swap-in's resolve grid
+ * and the backups with a programmatic dependency on the previous kernel of
+ * the stream (programmatic dependent launch): when that kernel signals its
+ * dependents early (griddepcontrol.launch_dependents, or
+ * cudaTriggerProgrammaticLaunchCompletion), this library's grid is placed on
+ * free SMs before it ends and waits on the device (griddepcontrol.wait)
+ * before it reads anything; a resolve grid signals its own dependents only
+ * after that wait, so a swap-in never starts while an older call that is not
+ * the one just before it still runs.  on = 0 (the default) launches plainly.
+ * Results are identical either way.  Measured on GB300: decode_40k steps
+ * (each resolve behind an L2-flush kernel that signals nothing) +0.45 us;
+ * mixed_len (4 resolves and a backup back to back) -2 us per 1.01 ms step;
+ * spec_verify -1.6 us per 3.58 ms step.  Read at each launch (a captured
+ * graph keeps the launch as captured).  INVALID_ARG unless on is 0 or 1.
+ */
+int hisparse_set_programmatic_launch(hisparse_t h, int32_t on);
 
 /*
  * hisparse_set_protected_calls: keep the hot rows of a request's last

@@ -117,6 +117,9 @@ def test_null_arguments(lib):
     assert lib.hisparse_read_state(None, 0, None, None, None, None, None, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_set_copy_mode(None, 1) == H.ERR_INVALID_ARG
     assert lib.hisparse_set_protected_calls(None, 1) == H.ERR_INVALID_ARG
+    assert lib.hisparse_set_stage_rows(None, 1) == H.ERR_INVALID_ARG
+    assert lib.hisparse_set_programmatic_launch(None, 1) == H.ERR_INVALID_ARG
+    assert lib.hisparse_status_clear(None, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_backup_layers(None, None, 1, None, None, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_write_state(None, 0, None, None, None, 1, None) == H.ERR_INVALID_ARG
     assert lib.hisparse_check_guards(None, None) == H.ERR_INVALID_ARG
@@ -161,6 +164,7 @@ def test_binding_constants_match_the_header():
              "STATUS_BAD_POSITION": H.STATUS_BAD_POSITION,
              "STATUS_BAD_RESIDENT": H.STATUS_BAD_RESIDENT,
              "STATUS_NO_HOST_ROW": H.STATUS_NO_HOST_ROW, "STATUS_CAPACITY": H.STATUS_CAPACITY,
+             "STATUS_COPY_TIMEOUT": H.STATUS_COPY_TIMEOUT,
              "RESIDENT_FLAG": H.RESIDENT_FLAG, "COPY_FUSED": H.COPY_FUSED,
              "COPY_SPLIT": H.COPY_SPLIT, "COPY_AUTO": H.COPY_AUTO,
              "NOALLOC_SCRATCH_BYTES": H.NOALLOC_SCRATCH_BYTES}

@@ -9,7 +9,8 @@ import numpy as np
 import pytest
 import torch
 
-from harness import Pair, assert_call_equal, assert_device_bytes_equal_oracle, assert_state_equal
+from harness import (Pair, assert_call_equal, assert_device_bytes_equal_oracle, assert_state_equal,
+                     status_bits)
 from hierarchical_sparse_kv_request_gb300 import hisparse as H
 from hierarchical_sparse_kv_request_gb300 import workload as W
 
@@ -76,6 +77,16 @@ def draw_topk(rng, seq, k, prev):
     return topk
 
 
+def check_call(p, g, o, cleared, ctx):
+    """The call's results against the oracle's: the status words equal the
+    oracle's words always, and the bits of the call's own codes when they
+    were cleared before it."""
+    assert np.array_equal(g[3], p.orc.status_word()), f"{ctx}: status words"
+    if not cleared:
+        g = (g[0], g[1], g[2], status_bits(o[3]))
+    assert_call_equal(g, o, ctx)
+
+
 @pytest.mark.parametrize("seed", range(48))
 def test_random_configuration(seed):
     rng = np.random.default_rng(1000 + seed)
@@ -104,17 +115,26 @@ def test_random_configuration(seed):
                 nb = int(rng.integers(1, max(2, max(caps) // bs + 2)))
                 tab = np.where(rng.random((R, nb)) < 0.3, rng.integers(0, 1000, (R, nb)), -1)
                 tab = tab.astype(np.int32)
+            # the status words are cleared before some calls only; they must
+            # equal the oracle's after every call either way
+            clear = rng.random() < 0.5
+            # staged rows through shared memory: none, a few, or as many as fit
+            p.gpu.set_stage_rows(int(rng.choice([-1, -1, 0, 1, 5])))
+            p.gpu.set_programmatic_launch(bool(rng.random() < 0.5))
             if tab is None and noalloc_ok and rng.random() < 0.25:
                 # the allocation-free swap-in: no plan comes back, so no replay
+                if clear:
+                    p.gpu.status_clear()
+                    p.orc.status_clear()
                 p.gpu.swap_in_noalloc(l0, torch.from_numpy(topk).cuda(), p.seq_d, p.out)
                 o = p.orc.swap_in(l0, topk, p.seq)
                 torch.cuda.synchronize()
                 g = (p.out.cpu().numpy(), o[1], o[2], p.gpu.status().cpu().numpy())
-                assert_call_equal(g, o, f"{ctx} call {c} layer {l0} (noalloc)")
+                check_call(p, g, o, clear, f"{ctx} call {c} layer {l0} (noalloc)")
                 assert_state_equal(p, l0, f"{ctx} call {c} layer {l0} (noalloc)")
                 continue
-            g, o = p.swap_in(l0, topk, resident=tab, block_size=bs)
-            assert_call_equal(g, o, f"{ctx} call {c} layer {l0}")
+            g, o = p.swap_in(l0, topk, resident=tab, block_size=bs, clear_status=clear)
+            check_call(p, g, o, clear, f"{ctx} call {c} layer {l0}")
             assert_state_equal(p, l0, f"{ctx} call {c} layer {l0}")
             if l0 == 0 and skips:       # the skip layers replay layer 0's plan
                 p.gpu.replay_plan_layers(p.plan, p.cnt, skips, num_ctas=int(rng.integers(1, 40)))

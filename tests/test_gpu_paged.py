@@ -59,6 +59,7 @@ class PagedProgram:
         self.orc = O.Oracle.for_workload(self.w, track_bytes=True, host_block_tokens=hb)
         assert self.gpu.host_pool_info() == (hb, self.orc.pool_blocks, self.orc.pool_blocks)
         self.rng = np.random.default_rng(seed)
+        self.rng_words = np.random.default_rng(seed + 7919)   # when to clear the status words
         self.resident_bs = resident_bs      # > 0: resident page tables on half the calls
         self.noalloc = noalloc              # calls through hisparse_swap_in_noalloc
         if protect:
@@ -166,7 +167,7 @@ class PagedProgram:
             if self.rng.random() < 0.2:
                 topk[r, self.rng.integers(0, k)] = -1
         t = torch.from_numpy(topk).cuda()
-        cleared = self.rng.random() < 0.5
+        cleared = self.rng_words.random() < 0.5
         if cleared:
             self.gpu.status_clear()
             self.orc.status_clear()

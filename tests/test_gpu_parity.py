@@ -177,7 +177,7 @@ def test_protected_slots_parity(protect, mode, resident):
         else:
             g, o = p.swap_in(0, topk)
         assert_call_equal(g, o, f"call {c}")
-        failed += int((g[3] == H.STATUS_CAPACITY).sum())
+        failed += int((o[3] == H.STATUS_CAPACITY).sum())
         assert_state_equal(p, 0, f"call {c}")
         assert_device_bytes_equal_oracle(p, 0, f"call {c}")
     if protect >= 2 and not resident:
@@ -338,7 +338,7 @@ def test_resident_tier_parity(bs, frac, lens):
     tab[1, inside[0] // bs] = -3
     g, o = p.swap_in(0, topk, resident=tab, block_size=bs)
     assert_call_equal(g, o, "malformed")
-    assert g[3][1] == H.STATUS_BAD_RESIDENT and (g[0][1] == -1).all()
+    assert g[3][1] == H.STATUS_BIT(H.STATUS_BAD_RESIDENT) and (g[0][1] == -1).all()
     after = p.gpu.read_state(0)
     assert np.array_equal(before[0][1], after[0][1]) and np.array_equal(before[1][1], after[1][1])
     p.close()

@@ -45,6 +45,9 @@ def test_layer0_error_survives_a_captured_four_layer_step():
     rows_d = torch.empty((L, R, B), dtype=torch.uint8, device="cuda")
     pos_d = torch.empty(R, dtype=torch.int32, device="cuda")
     one = torch.ones(R, dtype=torch.int32, device="cuda")
+    # the layers' swap-ins and the backup follow each other with programmatic
+    # dependencies inside the graph
+    p.gpu.set_programmatic_launch(True)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for l in range(L):
