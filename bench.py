@@ -82,6 +82,9 @@ def parse():
     ap.add_argument("--stage-rows", type=int, default=0,
                     help="miss rows per request staged through shared memory by the "
                          "bulk-copy engine (hisparse_set_stage_rows; -1: as many as fit)")
+    ap.add_argument("--copy-ctas", type=int, default=0,
+                    help="CTAs per request of a fused-copy swap-in (hisparse_set_copy_ctas; "
+                         "0: the library's default)")
     ap.add_argument("--programmatic", action="store_true",
                     help="launch swap-ins and backups with a programmatic dependency "
                          "(hisparse_set_programmatic_launch)")
@@ -213,7 +216,8 @@ def run_rotation(args, st, torch, H, K, Wm, rank, ws, first_step):
     per = rotation_steps(Wm, K)
     batches = [st] + [Setup(args.config, per, rank, args.copy_mode, 0, args.protect_calls,
                             batch=b, rows_from=st, resident_recent=args.resident_recent,
-                            stage_rows=args.stage_rows, programmatic=args.programmatic)
+                            stage_rows=args.stage_rows, programmatic=args.programmatic,
+               copy_ctas=args.copy_ctas)
                       for b in range(1, NB)]
     for b in batches[1:]:
         settle_host_pool(torch, H, b.gpu, w)
@@ -476,7 +480,8 @@ def reserve_scattered(gpu, caps, hb: int, seed: int, blocks_per_round: int = 8):
 class Setup:
     def __init__(self, cfg: int, steps: int, rank: int, copy_mode: str, host_block_tokens: int = 0,
                  protect_calls: int = 0, batch: int = 0, rows_from: "Setup" = None,
-                 resident_recent: int = 0, stage_rows: int = 0, programmatic: bool = False):
+                 resident_recent: int = 0, stage_rows: int = 0, programmatic: bool = False,
+                 copy_ctas: int = 0):
         """One batch of the workload on its own handle.  batch > 0 gives an
         independent batch (its own seed, state and pool); rows_from copies the
         host rows of another batch instead of generating them again."""
@@ -495,6 +500,8 @@ class Setup:
         self.gpu.set_protected_calls(protect_calls)
         self.gpu.set_stage_rows(stage_rows)
         self.gpu.set_programmatic_launch(programmatic)
+        if copy_ctas:
+            self.gpu.set_copy_ctas(copy_ctas)
         if self.hb:
             reserve_scattered(self.gpu, w.host_capacity, self.hb, w.seed)
         for l in range(w.num_layers):
@@ -714,7 +721,8 @@ def run_gpu(args):
     konly_steps = KONLY_ROUNDS * (KONLY_WARM + KONLY_STEPS)
     st = Setup(args.config, S0 + K + Wm + BREAKDOWN_STEPS + konly_steps + extra, rank, args.copy_mode,
                args.host_block_tokens, args.protect_calls, resident_recent=args.resident_recent,
-               stage_rows=args.stage_rows, programmatic=args.programmatic)
+               stage_rows=args.stage_rows, programmatic=args.programmatic,
+               copy_ctas=args.copy_ctas)
     st.split = args.copy_mode == "split"
     w = st.w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -916,6 +924,7 @@ def run_gpu(args):
                        "protect_calls": args.protect_calls,
                        "stage_rows": args.stage_rows,
                        "programmatic_launch": args.programmatic,
+                       "copy_ctas_per_request": st.gpu.copy_ctas(),
                        "resident_recent": args.resident_recent,
                        "l2": (f"inputs larger than L2: {ROTATE_BATCHES} independent batches of "
                               f"{w.num_requests} requests take the steps in turn (~270 MB of other "
@@ -1437,7 +1446,7 @@ def run_reference(args):
 # The default run's other workloads: timed in child processes after
 # decode_40k, fewer steps each (their steps are 20-70x longer).
 OTHER_CONFIGS = (3, 4, 5)
-OTHER_STEPS = 8
+OTHER_STEPS = 32
 OTHER_KEYS = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline",
               "kernel_only", "miss_h2d_gbs", "miss_rows_per_step", "miss_h2d_frac_of_link_peak",
               "random_row_ceiling_kernel_only", "step_ms_min_median_max", "slow_steps", "backup",

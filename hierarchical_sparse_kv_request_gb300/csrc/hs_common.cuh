@@ -158,6 +158,8 @@ struct ResolveLaunch {
     int32_t max_cap;       // largest host capacity (sizes the miss bitmap)
     bool fused_copy;       // copy the misses in this kernel
     bool stage_s2t;        // stage the slot->token row in shared memory
+    bool inv_lookup;       // with stage_s2t: find hits through an inverse table built in
+                           // shared memory from the staged row, not by a gather
     const int32_t *resident;  // [R][res_max_blocks] resident block ids, or null
     int32_t res_max_blocks;
     int32_t res_block_size;
@@ -168,20 +170,27 @@ struct ResolveLaunch {
                               // (0: none; only with fused_copy and no deferral)
     bool programmatic;        // launch with a programmatic dependency on the stream's
                               // previous kernel (it waits for it on the device)
+    int32_t ncopy;            // copier CTAs per request (a cluster of 1 + ncopy CTAs:
+                              // the resolver does no copy); 0: the resolver copies.
+                              // Needs fused_copy, no deferral and stage_rows == 0.
 };
 
 // Shared-memory bytes the resolve kernel needs for this geometry
 // (tbl_stride: the host block table row staged per request, 0 = none;
 // stage_rows rows of B bytes for the bulk-copy engine).
-size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int tbl_stride,
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, bool inv, int tbl_stride,
                           int stage_rows, int64_t B);
 // The most rows the bulk-copy engine can stage within max_smem (at most k).
-int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, int tbl_stride, int64_t B,
-                       size_t max_smem);
+int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, bool inv, int tbl_stride,
+                       int64_t B, size_t max_smem);
 int resolve_threads();
 // Allow every instantiation of the resolve kernel up to `smem` bytes of
 // dynamic shared memory (called at handle creation, outside any capture).
 cudaError_t resolve_prepare(size_t smem);
+// Clusters of `ctas` resolve CTAs with `smem` bytes each that the GPU can
+// hold at once (the resolve instantiation for top_k k).
+constexpr int kMaxCopyCtas = 4;
+cudaError_t resolve_max_clusters(int k, int ctas, size_t smem, int *clusters);
 cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s);
 
 constexpr int kMaxReplayLayers = 16;  // layers one replay launch copies for

@@ -54,15 +54,14 @@ namespace hs {
 namespace {
 
 constexpr int NT = 1024;       // threads per CTA
-// Leftover host chunks per thread loaded right after classification, by the
-// number of top-k entries per thread: as many as the 64 registers of a
-// 1024-thread CTA hold without spilling (deeper was faster on decode_40k
-// while it did not spill: 4 -> 8 took a step from 54.1 to 52.3 us).
-template <int KT> __host__ __device__ constexpr int prefetch_depth() { return KT == 2 ? 8 : (KT == 8 ? 2 : 4); }
-// Host chunks in flight per thread in the copy loop.  Measured on decode_40k
-// (32 CTAs): 4 ends the launch ~1.3 us sooner than 8; 2 and 6 gain less, and
-// with 128 or 256 CTAs the depth makes no difference.
-constexpr int COPY_UNROLL = 4;
+// Host chunks in flight per thread.  The copy keeps a window of COPY_WINDOW
+// loads per thread: storing a chunk frees its register for the load of the
+// chunk COPY_WINDOW steps ahead, so the link's queue never drains between
+// batches.  The first EARLY_LOADS<KT> chunks of the window are loaded right
+// after classification, before the victims are known (KT: top-k entries per
+// thread; these registers stay live through the block scans).
+constexpr int COPY_WINDOW = 8;
+template <int KT> __host__ __device__ constexpr int early_loads() { return KT == 8 ? 2 : 4; }
 // How long a CTA waits for its staged rows before it gives up on them (2 s
 // of the GPU's global timer): far beyond any copy that completes (a call
 // moves at most a few MB per CTA), so reaching it means a fault of the copy,
@@ -72,15 +71,16 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct SmemPlan {
-    size_t hit, sel, miss, lru, s2t, tbl, chunk, vict, lrow, avict, bar, cnt, stage, total;
+    size_t hit, sel, miss, lru, s2t, inv, tbl, chunk, vict, lrow, avict, bar, cnt, stage, total;
 };
 
 // Shared memory of the CTA: bitmaps over slots and tokens, the staged LRU
-// list, optionally the staged slot->token row and host block table row,
-// victims by miss rank and by arrival index, the leftover host rows, the
-// staging mbarrier and arrival counter, and
-// `stage_rows` rows of B bytes staged by the bulk-copy engine.
-__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t,
+// list, optionally the staged slot->token row (and, with it, an inverse
+// token->slot table over [0, max_cap)) and host block table row, victims by
+// miss rank and by arrival index, the leftover host rows, the staging
+// mbarrier and arrival counter, and `stage_rows` rows of B bytes staged by
+// the bulk-copy engine.
+__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t, bool inv,
                                               int tbl_stride, int stage_rows, int64_t B)
 {
     SmemPlan p;
@@ -91,13 +91,14 @@ __host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool st
     p.miss = o;  o += MW * 4;
     p.lru = align_up(o, 16); o = p.lru + align_up((size_t)D * 2, 16);
     p.s2t = o;   o += stage_s2t ? align_up((size_t)D * 4, 16) : 0;
+    p.inv = o;   o += (stage_s2t && inv) ? align_up((size_t)max_cap * 2, 16) : 0;
     p.tbl = o;   o += (size_t)tbl_stride * 4;   // a multiple of 16
     p.chunk = o; o = align_up(o + (size_t)NT * 2, 4);
     p.vict = o;  o = align_up(o + (size_t)k * 2, 4);
     p.lrow = o;  o += (size_t)k * 4;
     p.avict = o; o = align_up(o + (size_t)k * 2, 8);
     p.bar = o;   o += 8;
-    p.cnt = o;   o += 8;
+    p.cnt = o;   o += 16;
     p.stage = align_up(o, 128);
     o = p.stage + (size_t)stage_rows * (size_t)B;
     p.total = align_up(o, 16);
@@ -111,6 +112,8 @@ struct Smem {
     uint32_t *missbits;  // [MW]  miss tokens (and, on the fast path, all tokens)
     uint16_t *lru_s;     // [D]   staged LRU list
     int32_t *s2t_s;      // [D]   staged slot->token row (null when not staged)
+    uint16_t *inv;       // [max_cap] slot of each token, built from s2t_s (null: the
+                         //       token->slot map in global memory is gathered instead)
     int32_t *tbl_s;      // [tbl_stride] staged host block table row (null: no paged pool)
     uint16_t *chunk_pre; // [NT]  misses before each thread's chunk of missbits
     uint16_t *victims;   // [k]   victim slot of miss rank i
@@ -120,6 +123,9 @@ struct Smem {
     uint64_t *bar;       //       mbarrier of the staged rows
     uint32_t *arrived;   //       misses that took an arrival index
     uint32_t *flags;     //       error flags of the CTA's classification (kFlag*)
+    uint32_t *pub;       // [2]   in a copier CTA: the misses to load (written by the
+                         //       resolver before the first cluster barrier) and to
+                         //       store (before the second)
     uint8_t *stage;      // [stage_rows][B] rows fetched by the bulk-copy engine
 };
 
@@ -173,6 +179,8 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// all but this thread's most recent group of asynchronous copies have landed
+__device__ __forceinline__ void cp_async_wait_but_last() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // ---- bulk-copy engine (TMA, non-tensor form) and its mbarrier --------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -250,6 +258,35 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// ---- thread-block clusters: one resolver CTA and its copier CTAs ----------
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of the cluster arrives once per phase, then waits for the
+// phase; arrive releases this thread's earlier writes (shared memory of
+// other CTAs included) and wait acquires everyone's.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// Store to the same shared-memory location in CTA `rank` of the cluster
+// (every CTA of the launch has the same shared-memory layout).
+__device__ __forceinline__ uint32_t remote_addr(const void *local, uint32_t rank)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ void st_remote_u32(const uint32_t *local, uint32_t rank, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote_addr(local, rank)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_remote_u16(const uint16_t *local, uint32_t rank, uint16_t v)
+{
+    asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(remote_addr(local, rank)), "h"(v) : "memory");
+}
+
 // Resident row of position t from its block id `id` (-1: not resident), or
 // -2 when the id is malformed (below -1, or rows reaching the flag bit).
 __device__ __forceinline__ int32_t resident_row(int32_t id, int32_t t, int32_t bs)
@@ -288,12 +325,72 @@ __device__ __forceinline__ void finish_untouched(const ResolveLaunch &a, int r,
     }
 }
 
+// A copier CTA (rank c >= 1 of request r's cluster of 1 + ncopy CTAs).  It
+// resolves nothing and touches no hot state: it loads the miss rows the
+// resolver (rank 0) lists in this CTA's shared memory at classification, and
+// stores them into the victim slots the resolver files there once the block
+// scans have chosen them.  Its SM issues host loads and nothing else, so
+// they queue behind nothing, and the resolver's own stores to the hot state
+// queue behind no host loads.  Copier c takes the rounds n of NT chunks of
+// the list with n % ncopy == c - 1.
+__device__ __forceinline__ void copier_main(const ResolveLaunch &a, const Smem &sm, int r, int c,
+                                            int ncopy)
+{
+    const int tid = threadIdx.x;
+    const int D = a.g.D, CH = a.g.chunks;
+    const int64_t B = a.g.B;
+    const int32_t S = a.seq_lens[r];
+    const int64_t cap = a.g.host_cap[r];
+    // the resolver takes its paths without a copy (a malformed length, the
+    // fast path) on the same test, and then never reaches a cluster barrier
+    if (S < 0 || (int64_t)S > cap || S <= D) return;
+    const uint8_t *hrow0 = a.store.host + (a.g.hb ? 0 : a.g.host_off[r]) * B;
+    uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
+    cluster_arrive();
+    cluster_wait();                       // phase 1: the leftover list is in
+    const int total = (int)sm.pub[0] * CH;
+    if (total == 0) return;               // an error, or no miss: no phase 2
+    // Arrive for phase 2 before loading: the phase then ends as soon as the
+    // resolver has filed the victims, not when this CTA's last thread has
+    // got its loads out (host loads in flight hold up the issue of more).
+    cluster_arrive();
+    const int first = (c - 1) * NT + tid, stride = ncopy * NT;
+    auto chunk_src = [&](int e) -> const uint8_t * {
+        const int q = e / CH, cc = e - q * CH;
+        return hrow0 + (int64_t)sm.left_row[q] * B + cc * 16;
+    };
+    uint4 pv[COPY_WINDOW];
+#pragma unroll
+    for (int u = 0; u < COPY_WINDOW; ++u) {
+        const int e = first + u * stride;
+        if (e < total) pv[u] = ld_host_v4(chunk_src(e));
+    }
+    cluster_wait();                       // phase 2: the victims are in
+    if (sm.pub[1] == 0) return;           // no copy after all (protected rows)
+    for (int e0 = first; e0 < total; e0 += COPY_WINDOW * stride) {
+#pragma unroll
+        for (int u = 0; u < COPY_WINDOW; ++u) {
+            const int e = e0 + u * stride;
+            if (e < total) {
+                const int q = e / CH, cc = e - q * CH;
+                st_v4(drow0 + (int64_t)sm.arr_vict[q] * B + cc * 16, pv[u]);
+                const int e2 = e + COPY_WINDOW * stride;
+                if (e2 < total) pv[u] = ld_host_v4(chunk_src(e2));
+            }
+        }
+    }
+}
+
 template <int KT>
 __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
 {
-    constexpr int PREFETCH = prefetch_depth<KT>();
+    constexpr int EARLY = early_loads<KT>();
+    static_assert(EARLY <= COPY_WINDOW, "the early loads are the first of the window");
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    const int r = blockIdx.x;
+    // With copier CTAs (a cluster launch of 1 + ncopy CTAs per request) this
+    // CTA resolves request r if it is rank 0 of its cluster, else copies.
+    const int ncopy = a.ncopy;
+    const int r = blockIdx.x / (ncopy + 1);
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int k = a.g.k, D = a.g.D;
@@ -303,7 +400,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int SR = a.stage_rows;   // rows the bulk-copy engine may stage (0: none)
 
     const int32_t hb = a.g.hb;
-    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t, hb ? a.g.tbl_stride : 0, SR, B);
+    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t, a.inv_lookup,
+                                  hb ? a.g.tbl_stride : 0, SR, B);
     Smem sm;
     sm.warp_tot = reinterpret_cast<uint32_t *>(smem_raw);
     sm.hitbits = reinterpret_cast<uint32_t *>(smem_raw + sp.hit);
@@ -311,6 +409,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     sm.missbits = reinterpret_cast<uint32_t *>(smem_raw + sp.miss);
     sm.lru_s = reinterpret_cast<uint16_t *>(smem_raw + sp.lru);
     sm.s2t_s = a.stage_s2t ? reinterpret_cast<int32_t *>(smem_raw + sp.s2t) : nullptr;
+    sm.inv = (a.stage_s2t && a.inv_lookup) ? reinterpret_cast<uint16_t *>(smem_raw + sp.inv) : nullptr;
     sm.tbl_s = hb ? reinterpret_cast<int32_t *>(smem_raw + sp.tbl) : nullptr;
     sm.chunk_pre = reinterpret_cast<uint16_t *>(smem_raw + sp.chunk);
     sm.victims = reinterpret_cast<uint16_t *>(smem_raw + sp.vict);
@@ -319,6 +418,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     sm.bar = reinterpret_cast<uint64_t *>(smem_raw + sp.bar);
     sm.arrived = reinterpret_cast<uint32_t *>(smem_raw + sp.cnt);
     sm.flags = sm.arrived + 1;
+    sm.pub = sm.arrived + 2;
     sm.stage = smem_raw + sp.stage;
 
     // Launched behind another kernel with a programmatic dependency, this
@@ -332,6 +432,13 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     // state that an older call is still writing.  (A copy grid launched
     // behind this one still waits for this grid before reading the plan.)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (ncopy) {
+        const int rank = (int)cluster_rank();
+        if (rank != 0) {
+            copier_main(a, sm, r, rank, ncopy);
+            return;
+        }
+    }
 
     // ---- loads that do not depend on each other --------------------------
     const int32_t S = a.seq_lens[r];
@@ -344,16 +451,17 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         const int j = tid + i * NT;
         t[i] = j < k ? a.topk[(int64_t)r * k + j] : -1;
     }
-    // Stage the LRU list and the slot->token row with asynchronous copies;
-    // they land under the round trips above.  (16-byte rows need D % 8 == 0.)
+    // Stage the slot->token row, then the LRU list, with asynchronous
+    // copies (two groups); they land under the round trips above.  (16-byte
+    // rows need D % 8 == 0.)
     const uint16_t *lru = a.st.lru + (int64_t)r * D;
     int32_t *slot2tok = a.st.slot2tok + (int64_t)r * D;
     const bool staged_async = (D & 7) == 0;
-    if (staged_async) {
+    if (staged_async && sm.s2t_s)
+        for (int i = tid; i < (D >> 2); i += NT) cp_async16(sm.s2t_s + i * 4, slot2tok + i * 4);
+    cp_async_commit();
+    if (staged_async)
         for (int i = tid; i < (D >> 3); i += NT) cp_async16(sm.lru_s + i * 8, lru + i * 8);
-        if (sm.s2t_s)
-            for (int i = tid; i < (D >> 2); i += NT) cp_async16(sm.s2t_s + i * 4, slot2tok + i * 4);
-    }
     cp_async_commit();
     // Resident pages first ([Arch] Resident device pages; Hot lookup and
     // LRU): gather the block id of every position's block (-1 when there is
@@ -407,12 +515,17 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     auto host_slot = [&](int32_t x) -> int32_t {
         return hb ? sm.tbl_s[x / hb] * hb + x % hb : x;
     };
+    // Hit lookup: the slot of each top-k token, or -1.  Without the inverse
+    // table, a gather of the token->slot map (a round trip to global memory
+    // that starts only once the top-k row is in).
     int32_t *tok2slot = a.st.tok2slot + off;
     int32_t s[KT];
+    if (!sm.inv) {
 #pragma unroll
-    for (int i = 0; i < KT; ++i) {
-        s[i] = (t[i] >= 0 && t[i] < S) ? tok2slot[t[i]] : -1;
-        if (s[i] >= D) s[i] = -1;  // never true for state this library wrote
+        for (int i = 0; i < KT; ++i) {
+            s[i] = (t[i] >= 0 && t[i] < S) ? tok2slot[t[i]] : -1;
+            if (s[i] >= D) s[i] = -1;  // never true for state this library wrote
+        }
     }
     const int mw = (S + 31) >> 5;
     for (int w = tid; w < mw; w += NT) sm.missbits[w] = 0u;
@@ -427,8 +540,32 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         *sm.flags = 0u;
         if (SR) mbar_init(sm.bar, NT);   // every thread arrives once
     }
-    cp_async_wait_all();
-    __syncthreads();
+    if (sm.inv) {
+        // With the inverse table the lookup needs only the staged
+        // slot->token row, whose copy was issued at the start: every slot
+        // files itself under its token, and a token's entry counts only if
+        // that slot still holds the token (so entries of tokens that no slot
+        // holds, never written, are harmless: the maps are mutual inverses).
+        if (hb) cp_async_wait_all();   // the block table row is needed too
+        else cp_async_wait_but_last();  // the LRU list may still be landing
+        __syncthreads();
+        for (int sl = tid; sl < D; sl += NT) {
+            const int32_t x = sm.s2t_s[sl];
+            if (x >= 0 && x < a.max_cap) sm.inv[x] = (uint16_t)sl;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+            s[i] = -1;
+            if (t[i] >= 0 && t[i] < S) {
+                const int v = sm.inv[t[i]];
+                if (v < D && sm.s2t_s[v] == t[i]) s[i] = v;
+            }
+        }
+    } else {
+        cp_async_wait_all();
+        __syncthreads();
+    }
 
     // Classify.  A resident position is marked in the token bitmap only to
     // catch duplicates; its bit is cleared again before the misses are
@@ -477,8 +614,14 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (!mine) continue;
         const int32_t j = (int32_t)(base + __popc(mask & ((1u << lane) - 1u)));
         arr.set(i, j);
-        if (j < SR) staged_bytes += (uint32_t)B;
-        else sm.left_row[j - SR] = host_slot(t[i]);
+        if (j < SR) {
+            staged_bytes += (uint32_t)B;
+        } else if (ncopy) {
+            const uint32_t row = (uint32_t)host_slot(t[i]);
+            for (int q = 1; q <= ncopy; ++q) st_remote_u32((const uint32_t *)&sm.left_row[j], q, row);
+        } else {
+            sm.left_row[j - SR] = host_slot(t[i]);
+        }
     }
     if (SR) {
         mbar_arrive_expect_tx(sm.bar, staged_bytes);
@@ -490,32 +633,46 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
                           (uint32_t)B, sm.bar);
         }
     }
+    cp_async_wait_all();   // the LRU list, before the barrier that publishes it
     const uint32_t flags = block_or(f, sm.flags);
+    // Copiers: the list goes out now (count 0 on an error: nothing to copy).
+    // Phase 2 follows only if the count is nonzero (`copying`); a copier
+    // that reads 0 leaves after phase 1.
+    const bool copying = ncopy && !flags && *sm.arrived > 0u;
+    if (ncopy) {
+        if (tid == 0)
+            for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[0], q, flags ? 0u : *sm.arrived);
+        cluster_arrive();
+    }
     if (flags) {
         // staged rows may still be landing in shared memory
         if (SR) staged_rows_landed(sm.bar, a.status, r);
 #pragma unroll
         for (int i = 0; i < KT; ++i) rid[i] = -1;
         finish_untouched<KT>(a, r, t, rid, status_of(flags), tick);
+        if (ncopy) cluster_wait();
         return;
     }
 
-    // Leftover chunks: loaded now, stored after the state writes below.  In
-    // a call without errors every miss took one arrival index, so the count
-    // is the call's miss count m.  (A request with many misses can leave its
+    // Leftover chunks: chunk e is chunk e % CH of leftover e / CH.  Thread
+    // tid copies chunks tid, tid + NT, tid + 2 NT, ...; the first EARLY of
+    // them are loaded now and stored after the state writes below.  In a
+    // call without errors every miss took one arrival index, so the count is
+    // the call's miss count m.  (A request with many misses can leave its
     // copies to a full-GPU copy grid launched behind this kernel.)
     const int m_arr = (int)*sm.arrived;
     const bool defer = a.deferred && (int64_t)m_arr * B > a.defer_bytes;
-    const int nleft = (a.fused_copy && !defer) ? max(m_arr - SR, 0) : 0;
+    const int nleft = (a.fused_copy && !defer && !ncopy) ? max(m_arr - SR, 0) : 0;
     const int total = nleft * CH;
-    uint4 pv[PREFETCH];
+    auto chunk_src = [&](int e) -> const uint8_t * {
+        const int q = e / CH, c = e - q * CH;
+        return hrow0 + (int64_t)sm.left_row[q] * B + c * 16;
+    };
+    uint4 pv[COPY_WINDOW];
 #pragma unroll
-    for (int u = 0; u < PREFETCH; ++u) {
+    for (int u = 0; u < EARLY; ++u) {
         const int e = tid + u * NT;
-        if (e < total) {
-            const int q = e / CH, c = e - q * CH;
-            pv[u] = ld_host_v4(hrow0 + (int64_t)sm.left_row[q] * B + c * 16);
-        }
+        if (e < total) pv[u] = ld_host_v4(chunk_src(e));
     }
 
     if (a.resident) {
@@ -571,6 +728,15 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (sm.warp_tot[0]) {
             if (SR) staged_rows_landed(sm.bar, a.status, r);
             finish_untouched<KT>(a, r, t, rid, kStatusCapacity, tick);
+            if (ncopy) {
+                cluster_wait();
+                if (copying) {   // the copiers wait in phase 2: no copy after all
+                    if (tid == 0)
+                        for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[1], q, 0u);
+                    cluster_arrive();
+                    cluster_wait();
+                }
+            }
             return;
         }
     }
@@ -608,7 +774,10 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         for (int q = owner * WC; q < w; ++q) rank += __popc(sm.missbits[q]);
         rank += __popc(sm.missbits[w] & ((1u << (x & 31)) - 1u));
         const int v = sm.victims[rank];
-        sm.arr_vict[arr.get(i)] = (uint16_t)v;
+        if (ncopy)
+            for (int q = 1; q <= ncopy; ++q) st_remote_u16(&sm.arr_vict[arr.get(i)], q, (uint16_t)v);
+        else
+            sm.arr_vict[arr.get(i)] = (uint16_t)v;
         const int32_t old = sm.s2t_s ? sm.s2t_s[v] : slot2tok[v];
         if (old >= 0 && (int64_t)old < cap) tok2slot[old] = -1;
         slot2tok[v] = x;
@@ -618,6 +787,15 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
             int32_t *pr = a.plan_rows + ((int64_t)r * k + rank) * 2;
             pr[0] = host_slot(x);
             pr[1] = v;
+        }
+    }
+    // The copiers may store their rows now (phase 2).
+    if (ncopy) {
+        cluster_wait();
+        if (copying) {
+            if (tid == 0)
+                for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[1], q, 1u);
+            cluster_arrive();
         }
     }
     // Selected slots (hits and victims) go to the back of the list in slot
@@ -642,33 +820,30 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (a.deferred) a.deferred[r] = defer ? 1 : 0;
         a.st.tick[r] = tick;
     }
+    if (copying) cluster_wait();
 
     // ---- miss copies: pinned host rows -> victim slots ---------------------
-    // the leftovers: the chunks loaded above, then the rest streamed
+    // The leftovers through a window of COPY_WINDOW loads per thread: the
+    // rest of the window is loaded now; then each stored chunk's register
+    // takes the load of the thread's chunk COPY_WINDOW steps ahead.  Loads
+    // return in about the order they were issued, so every thread keeps
+    // COPY_WINDOW loads in flight until its last ones.
 #pragma unroll
-    for (int u = 0; u < PREFETCH; ++u) {
+    for (int u = EARLY; u < COPY_WINDOW; ++u) {
         const int e = tid + u * NT;
-        if (e < total) {
-            const int q = e / CH, c = e - q * CH;
-            st_v4(drow0 + (int64_t)sm.arr_vict[SR + q] * B + c * 16, pv[u]);
-        }
+        if (e < total) pv[u] = ld_host_v4(chunk_src(e));
     }
-    for (int e = PREFETCH * NT + tid; e < total; e += NT * COPY_UNROLL) {
-        uint4 v[COPY_UNROLL];
-        uint8_t *dst[COPY_UNROLL];
+    for (int e0 = tid; e0 < total; e0 += COPY_WINDOW * NT) {
 #pragma unroll
-        for (int u = 0; u < COPY_UNROLL; ++u) {
-            const int ee = e + u * NT;
-            dst[u] = nullptr;
-            if (ee < total) {
-                const int q = ee / CH, c = ee - q * CH;
-                v[u] = ld_host_v4(hrow0 + (int64_t)sm.left_row[q] * B + c * 16);
-                dst[u] = drow0 + (int64_t)sm.arr_vict[SR + q] * B + c * 16;
+        for (int u = 0; u < COPY_WINDOW; ++u) {
+            const int e = e0 + u * NT;
+            if (e < total) {
+                const int q = e / CH, c = e - q * CH;
+                st_v4(drow0 + (int64_t)sm.arr_vict[SR + q] * B + c * 16, pv[u]);
+                const int e2 = e + COPY_WINDOW * NT;
+                if (e2 < total) pv[u] = ld_host_v4(chunk_src(e2));
             }
         }
-#pragma unroll
-        for (int u = 0; u < COPY_UNROLL; ++u)
-            if (dst[u]) st_v4(dst[u], v[u]);
     }
     // the staged rows, once they have all landed, one bulk store per row
     if (SR) {
@@ -689,20 +864,30 @@ template <int KT>
 cudaError_t launch_kt(const ResolveLaunch &a, cudaStream_t s, size_t smem)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.g.R);
+    cfg.gridDim = dim3(a.g.R * (1 + a.ncopy));
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int n = 0;
     if (a.programmatic) {
         // programmatic dependency on the previous kernel of the stream: this
         // grid may be placed before that one ends and waits for it on the
         // device (griddepcontrol.wait at the kernel's start)
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
     }
+    if (a.ncopy) {
+        // one cluster per request: the resolver and its copiers
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 1 + a.ncopy;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, resolve_kernel<KT>, a);
 }
 
@@ -715,16 +900,16 @@ cudaError_t prepare_kt(size_t smem)
 
 }  // namespace
 
-size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int tbl_stride,
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, bool inv, int tbl_stride,
                           int stage_rows, int64_t B)
 {
-    return plan_smem(k, D, max_cap, stage_s2t, tbl_stride, stage_rows, B).total;
+    return plan_smem(k, D, max_cap, stage_s2t, inv, tbl_stride, stage_rows, B).total;
 }
 
-int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, int tbl_stride, int64_t B,
-                       size_t max_smem)
+int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, bool inv, int tbl_stride,
+                       int64_t B, size_t max_smem)
 {
-    const size_t base = resolve_smem_bytes(k, D, max_cap, stage_s2t, tbl_stride, 0, B);
+    const size_t base = resolve_smem_bytes(k, D, max_cap, stage_s2t, inv, tbl_stride, 0, B);
     const size_t room = align_up(base, 128) + 16 <= max_smem ? max_smem - align_up(base, 128) - 16 : 0;
     const int64_t rows = (int64_t)(room / (size_t)B);
     return (int)(rows < k ? rows : k);
@@ -741,9 +926,35 @@ cudaError_t resolve_prepare(size_t smem)
     return e;
 }
 
+template <int KT>
+cudaError_t max_clusters_kt(int ctas, size_t smem, int *clusters)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, resolve_kernel<KT>, &cfg);
+}
+
+cudaError_t resolve_max_clusters(int k, int ctas, size_t smem, int *clusters)
+{
+    const int kt = (k + NT - 1) / NT;
+    if (kt <= 1) return max_clusters_kt<1>(ctas, smem, clusters);
+    if (kt <= 2) return max_clusters_kt<2>(ctas, smem, clusters);
+    if (kt <= 4) return max_clusters_kt<4>(ctas, smem, clusters);
+    return max_clusters_kt<8>(ctas, smem, clusters);
+}
+
 cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s)
 {
-    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t,
+    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t, a.inv_lookup,
                                            a.g.hb ? a.g.tbl_stride : 0, a.stage_rows, a.g.B);
     const int kt = (a.g.k + NT - 1) / NT;
     if (kt <= 1) return launch_kt<1>(a, s, smem);

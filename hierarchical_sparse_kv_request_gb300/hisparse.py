@@ -95,6 +95,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "hisparse_set_protected_calls": [P, I32],
         "hisparse_set_stage_rows": [P, I32],
         "hisparse_set_programmatic_launch": [P, I32],
+        "hisparse_set_copy_ctas": [P, I32],
+        "hisparse_get_copy_ctas": [P, P],
         "hisparse_check_guards": [P, P],
         "hisparse_version": [],
         "hisparse_synthetic_compute": [P, I64, I32, I32, P],
@@ -386,6 +388,18 @@ class HiSparse:
         """Miss rows per request the fused copy stages through shared memory
         with the bulk-copy engine (0: none, the default; -1: as many as fit)."""
         _check(self.lib.hisparse_set_stage_rows(self.h, rows), "hisparse_set_stage_rows")
+
+    def set_copy_ctas(self, ctas: int) -> None:
+        """CTAs per request of a fused-copy swap-in: 1 resolves and copies in
+        one CTA; 2-4 form a cluster whose rank 0 resolves and whose other
+        CTAs copy (hisparse_set_copy_ctas)."""
+        _check(self.lib.hisparse_set_copy_ctas(self.h, ctas), "hisparse_set_copy_ctas")
+
+    def copy_ctas(self) -> int:
+        """CTAs per request that fused-copy swap-ins use now."""
+        v = ctypes.c_int32(0)
+        _check(self.lib.hisparse_get_copy_ctas(self.h, ctypes.byref(v)), "hisparse_get_copy_ctas")
+        return int(v.value)
 
     def set_programmatic_launch(self, on: bool) -> None:
         """Launch swap-ins and backups with a programmatic dependency on the

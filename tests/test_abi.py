@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_error_strings(lib):
-    assert lib.hisparse_version() == 200
+    assert lib.hisparse_version() == 201
     for code in range(0, -9, -1):
         assert lib.hisparse_error_string(code) not in (None, b"unknown error")
     assert lib.hisparse_error_string(-99) == b"unknown error"

@@ -19,7 +19,7 @@ PROGRAM = r"""
 
 int main(void)
 {
-    if (hisparse_version() != 200) return 1;
+    if (hisparse_version() != 201) return 1;
     if (strcmp(hisparse_error_string(HISPARSE_OK), "ok") != 0) return 2;
     if (hisparse_swap_in(NULL, 0, NULL, NULL, NULL, NULL, NULL) != HISPARSE_ERR_INVALID_ARG) return 3;
     if (hisparse_create(NULL, NULL) != HISPARSE_ERR_INVALID_ARG) return 4;

@@ -118,8 +118,11 @@ def test_random_configuration(seed):
             # the status words are cleared before some calls only; they must
             # equal the oracle's after every call either way
             clear = rng.random() < 0.5
-            # staged rows through shared memory: none, a few, or as many as fit
-            p.gpu.set_stage_rows(int(rng.choice([-1, -1, 0, 1, 5])))
+            # the copy in the resolving CTA (with staged rows through shared
+            # memory: none, a few, or as many as fit) or in copier CTAs
+            ctas = int(rng.choice([1, 1, 2, 3, 4]))
+            p.gpu.set_copy_ctas(ctas)
+            p.gpu.set_stage_rows(int(rng.choice([-1, -1, 0, 1, 5])) if ctas == 1 else 0)
             p.gpu.set_programmatic_launch(bool(rng.random() < 0.5))
             if tab is None and noalloc_ok and rng.random() < 0.25:
                 # the allocation-free swap-in: no plan comes back, so no replay

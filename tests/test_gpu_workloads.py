@@ -28,11 +28,14 @@ def _built():
     yield
 
 
-def test_decode_40k_all_steps():
-    """32 x 40000 tokens, k 2048, D 6144, 656 B rows, 64 decode steps."""
+@pytest.mark.parametrize("copy_ctas", [1, 2, 4])
+def test_decode_40k_all_steps(copy_ctas):
+    """32 x 40000 tokens, k 2048, D 6144, 656 B rows, 64 decode steps; the
+    copy in the resolving CTA, or in 1 or 3 copier CTAs per request."""
     w = W.make_config(2)
     sched = W.topk_schedule(w)[0]
     p = Pair(w, track_bytes=False)
+    p.gpu.set_copy_ctas(copy_ctas)
     misses = 0
     for c in range(w.steps):
         g, o = p.swap_in(0, sched[c])
@@ -52,6 +55,7 @@ def test_decode_40k_with_resident_recent_pages():
     w = W.make_config(2, steps=16)
     sched = W.topk_schedule(w)[0]
     p = Pair(w, track_bytes=False)
+    p.gpu.set_copy_ctas(2)
     R, bs = w.num_requests, 64
     nb = 40000 // bs + 1
     rng = np.random.default_rng(9)
