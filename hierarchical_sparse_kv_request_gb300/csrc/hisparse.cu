@@ -55,6 +55,15 @@ struct hisparse_handle {
     bool programmatic = false;  // swap-ins and backups launched with a programmatic dependency
     int32_t copy_ctas = 1;      // CTAs per request that run a fused-copy swap-in (1: the
                                 // resolving CTA copies; more: a cluster, see set_copy_ctas)
+    // The handle's last kernel launch: its stream, and the layers whose hot
+    // state, device rows or host rows it wrote (all of them after a prefill,
+    // a host block table edit or a state write).  A programmatic swap-in on
+    // the same stream whose layer that launch left alone reads before it
+    // waits (ResolveLaunch::wait_late).
+    bool last_known = false;
+    cudaStream_t last_stream = nullptr;
+    bool last_all = true;
+    std::vector<uint8_t> last_wrote;   // [L]
     bool stage_s2t = false;   // resolve kernel stages the slot->token row
     bool inv_lookup = false;  // ... and finds hits through an inverse table in shared memory
 
@@ -131,6 +140,30 @@ bool on_own_device(const hisparse_handle *h)
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HISPARSE_OK : HISPARSE_ERR_CUDA; }
+
+void note_launch_all(hisparse_handle *h, cudaStream_t s)
+{
+    h->last_known = true;
+    h->last_stream = s;
+    h->last_all = true;
+}
+
+void note_launch_layers(hisparse_handle *h, cudaStream_t s, const int32_t *layers, int n)
+{
+    h->last_known = true;
+    h->last_stream = s;
+    h->last_all = false;
+    h->last_wrote.assign(h->L, 0);
+    for (int i = 0; i < n; ++i) h->last_wrote[layers[i]] = 1;
+}
+
+// True if the handle's last launch was on stream s and wrote nothing of
+// `layer`: a kernel launched now, programmatically behind it, may read that
+// layer's state and rows before the last launch has completed.
+bool left_layer_alone(const hisparse_handle *h, cudaStream_t s, int32_t layer)
+{
+    return h->last_known && !h->last_all && h->last_stream == s && !h->last_wrote[layer];
+}
 
 // Dynamic shared memory of the handle's resolve launches without staged rows.
 size_t resolve_smem(const hisparse_handle *h)
@@ -554,6 +587,7 @@ int hisparse_host_reserve(hisparse_t h, int32_t n, const int32_t *requests,
             runs.add(idx, h->tbl[idx]);
         }
     }
+    note_launch_all(h, as_stream(stream));
     const cudaError_t e = runs.apply(h->d_tbl, as_stream(stream));
     if (e != cudaSuccess) {
         // the device table may lag the host copy: undo the host side
@@ -587,6 +621,7 @@ int hisparse_host_release(hisparse_t h, int32_t n, const int32_t *requests, void
         runs.clear_range(row, h->nblocks[r]);
         h->nblocks[r] = 0;
     }
+    note_launch_all(h, as_stream(stream));
     const cudaError_t e = runs.apply(h->d_tbl, as_stream(stream));
     if (e != cudaSuccess) {
         for (auto &f : freed) {
@@ -658,6 +693,7 @@ int hisparse_prefill(hisparse_t h, const int32_t *seq_lens, void *stream)
 {
     if (!h || !seq_lens) return HISPARSE_ERR_INVALID_ARG;
     if (!on_own_device(h)) return HISPARSE_ERR_INVALID_ARG;
+    note_launch_all(h, as_stream(stream));
     return cuda_status(hs::launch_prefill(seq_lens, h->d_layers, h->L, geometry(h), h->d_status,
                                           as_stream(stream)));
 }
@@ -698,12 +734,14 @@ int swap_in_impl(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int
     // rows go through shared memory only when this CTA copies them for sure
     a.stage_rows = (!split && !autom) ? h->stage_rows : 0;
     a.programmatic = h->programmatic;
+    a.wait_late = h->programmatic && left_layer_alone(h, as_stream(stream), layer);
     // copier CTAs only where the resolving CTA would copy every row itself
     a.ncopy = (!split && !autom && a.stage_rows == 0) ? h->copy_ctas - 1 : 0;
     const bool wide_copy = split || autom;
     a.plan_rows = out_plan ? out_plan->rows : (wide_copy ? h->d_plan_rows : nullptr);
     a.plan_counts = out_plan ? out_plan->counts : (wide_copy ? h->d_plan_counts : nullptr);
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));
+    note_launch_layers(h, as_stream(stream), &layer, 1);
     if (e != cudaSuccess || !wide_copy) return cuda_status(e);
     hs::ReplayLaunch c;
     c.plan_rows = a.plan_rows;
@@ -756,6 +794,7 @@ int hisparse_replay_plan_layers(hisparse_t h, const hisparse_plan *plan, const i
     c.num_ctas = num_ctas ? num_ctas : 16;
     c.programmatic = false;
     c.only_if = nullptr;
+    note_launch_layers(h, as_stream(stream), layers, num_layers);
     return cuda_status(hs::launch_replay(c, as_stream(stream)));
 }
 
@@ -791,6 +830,7 @@ int hisparse_backup_layers(hisparse_t h, const int32_t *layers, int32_t num_laye
     b.g = geometry(h);
     b.status = h->d_status;
     b.programmatic = h->programmatic;
+    note_launch_layers(h, as_stream(stream), layers, num_layers);
     return cuda_status(hs::launch_backup(b, as_stream(stream)));
 }
 
@@ -884,6 +924,7 @@ int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
     }
     const hs::HotState &st = h->state[layer];
     cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+    note_launch_all(h, as_stream(stream));
     if (e == cudaSuccess) e = cudaMemcpy(st.slot2tok, slot2tok, RD * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(st.last_used, last_used, RD * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(st.tok2slot, t2s.data(), t2s.size() * 4, cudaMemcpyHostToDevice);
@@ -916,6 +957,7 @@ int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
         c.num_ctas = h->num_sms;
         c.programmatic = false;
         c.only_if = nullptr;
+        note_launch_all(h, nullptr);
         e = hs::launch_replay(c, nullptr);
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -1040,9 +1082,11 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     a.stage_rows = 0;
     a.programmatic = h->programmatic;
     a.ncopy = 0;
+    a.wait_late = false;
     a.plan_rows = scratch;
     a.plan_counts = scratch + (int64_t)h->R * h->k * 2;
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));
+    note_launch_layers(h, as_stream(stream), &layer, 1);
     if (e != cudaSuccess) return HISPARSE_ERR_CUDA;
     hs::ReplayLaunch c;
     c.plan_rows = a.plan_rows;

@@ -170,6 +170,9 @@ struct ResolveLaunch {
                               // (0: none; only with fused_copy and no deferral)
     bool programmatic;        // launch with a programmatic dependency on the stream's
                               // previous kernel (it waits for it on the device)
+    bool wait_late;           // with programmatic: read the inputs and this layer's state
+                              // before waiting for the previous kernel (which the host
+                              // has checked wrote none of it); wait before writing
     int32_t ncopy;            // copier CTAs per request (a cluster of 1 + ncopy CTAs:
                               // the resolver does no copy); 0: the resolver copies.
                               // Needs fused_copy, no deferral and stage_rows == 0.

@@ -296,6 +296,18 @@ __device__ __forceinline__ int32_t resident_row(int32_t id, int32_t t, int32_t b
     return id * bs + t % bs;
 }
 
+// With a late wait (ResolveLaunch::wait_late) the grid reads its inputs and
+// this layer's state before the previous kernel of the stream has completed,
+// and waits for it (griddepcontrol.wait) only before its first write to
+// global memory; only then may the next launch start early.
+__device__ __forceinline__ void late_grid_wait(const ResolveLaunch &a)
+{
+    if (a.wait_late) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+}
+
 // Final writes of a request whose call ends without touching its state; on
 // success (the fast path) each position resolves to its resident row or to
 // slot = position.
@@ -306,6 +318,7 @@ __device__ __forceinline__ void finish_untouched(const ResolveLaunch &a, int r,
 {
     const int k = a.g.k;
     cp_async_wait_all();  // staged rows may still be landing in shared memory
+    late_grid_wait(a);
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
         const int j = threadIdx.x + i * NT;
@@ -423,18 +436,25 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
 
     // Launched behind another kernel with a programmatic dependency, this
     // grid may start while that one still runs (its CTAs are placed and set
-    // up under the other's tail); nothing from global memory is read before
-    // the other grid has completed and its writes are visible.  Without such
-    // a dependency the wait returns at once.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // Only now may the next launch start early: by then every grid before
-    // this one has completed, so a swap-in that follows never reads hot
+    // up under the other's tail).  Normally nothing from global memory is
+    // read before the other grid has completed and its writes are visible
+    // (without such a dependency the wait returns at once); only then may the
+    // next launch start early, so a swap-in that follows never reads hot
     // state that an older call is still writing.  (A copy grid launched
     // behind this one still waits for this grid before reading the plan.)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // With wait_late the host has checked that the previous launch wrote
+    // nothing this call reads (see late_grid_wait).
+    if (!a.wait_late) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     if (ncopy) {
         const int rank = (int)cluster_rank();
         if (rank != 0) {
+            // A copier's reads (host rows) follow its resolver's list, and its
+            // stores the resolver's wait (phase 2); it never holds up the next
+            // launch, which its resolver's later signal gates.
+            if (a.wait_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             copier_main(a, sm, r, rank, ncopy);
             return;
         }
@@ -674,6 +694,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         const int e = tid + u * NT;
         if (e < total) pv[u] = ld_host_v4(chunk_src(e));
     }
+    late_grid_wait(a);   // the first global writes follow
 
     if (a.resident) {
 #pragma unroll

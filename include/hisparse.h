@@ -526,15 +526,28 @@ int hisparse_get_copy_ctas(hisparse_t h, int32_t *ctas);
  * the stream (programmatic dependent launch): when that kernel signals its
  * dependents early (griddepcontrol.launch_dependents, or
  * cudaTriggerProgrammaticLaunchCompletion), this library's grid is placed on
- * free SMs before it ends and waits on the device (griddepcontrol.wait)
- * before it reads anything; a resolve grid signals its own dependents only
- * after that wait, so a swap-in never starts while an older call that is not
- * the one just before it still runs.  on = 0 (the default) launches plainly.
- * Results are identical either way.  Measured on GB300: decode_40k steps
- * (each resolve behind an L2-flush kernel that signals nothing) +0.45 us;
- * mixed_len (4 resolves and a backup back to back) -2 us per 1.01 ms step;
- * spec_verify -1.6 us per 3.58 ms step.  Read at each launch (a captured
- * graph keeps the launch as captured).  INVALID_ARG unless on is 0 or 1.
+ * free SMs before it ends and waits for it on the device (griddepcontrol.wait).
+ * A grid waits before it reads anything, except a swap-in whose previous
+ * kernel on the stream, as far as this handle knows, is one of its own
+ * launches on that stream that wrote nothing of the swap-in's layer (its hot
+ * state, device rows or host rows; a prefill, a host block table edit or a
+ * state write counts as writing every layer): that swap-in reads its
+ * inputs, the layer's state and its first host rows at once, and waits only
+ * before its first write to global memory.  Either way a grid signals its
+ * own dependents only after its wait, so a swap-in never starts while an
+ * older call that is not the one just before it still runs.  The caller's
+ * part: a kernel of its own that it places directly before a library call on
+ * the stream, if launched so that it may signal early, must have written the
+ * call's inputs (top-k rows, lengths, backup rows and positions, resident
+ * tables) and be done with the library's device rows before it signals.
+ * on = 0 (the default) launches plainly.  Results are identical either way.
+ * Measured on GB300, kernel-only step times against on = 0 (two
+ * interleaved runs each): mixed_len (4 resolves on 4 layers and a backup,
+ * back to back) 1.0117 against 1.0190 ms; spec_verify (3 sub-steps on one
+ * layer and a backup) 3.591 against 3.594 ms; decode_40k steps (each resolve
+ * behind an L2-flush kernel that signals nothing) +0.45 us.  Read at each launch (a
+ * captured graph keeps the launch as captured).  INVALID_ARG unless on is 0
+ * or 1.
  */
 int hisparse_set_programmatic_launch(hisparse_t h, int32_t on);
 
