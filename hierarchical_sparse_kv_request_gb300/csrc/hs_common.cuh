@@ -170,6 +170,7 @@ struct ResolveLaunch {
                               // (0: none; only with fused_copy and no deferral)
     bool programmatic;        // launch with a programmatic dependency on the stream's
                               // previous kernel (it waits for it on the device)
+    bool aligned_rows;        // copy in 64-byte-aligned spans of whole rows (else flat)
     bool wait_late;           // with programmatic: read the inputs and this layer's state
                               // before waiting for the previous kernel (which the host
                               // has checked wrote none of it); wait before writing

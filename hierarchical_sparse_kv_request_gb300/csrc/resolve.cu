@@ -287,6 +287,44 @@ __device__ __forceinline__ void st_remote_u16(const uint16_t *local, uint32_t ra
     asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(remote_addr(local, rank)), "h"(v) : "memory");
 }
 
+// Which 16-byte chunk of the leftover list a thread's n-th copy moves.
+//  - flat: chunk e = first + n * stride of the list, chunk e % CH of
+//    leftover e / CH (consecutive lanes take consecutive chunks);
+//  - unit-aligned: a warp's n-th task is first + n * stride; task (q, h) is
+//    the h-th 512 bytes of the 64-byte-aligned span around leftover q's host
+//    row, one 16-byte piece per lane, and lanes whose piece lies outside the
+//    row move nothing.  No 64-byte unit of host memory is then split between
+//    two warp loads.  Measured on GB300 (gathers of random pinned rows):
+//    656-byte rows 1.7-4% faster this way, 1152-byte rows 1-3% slower.
+struct CopyMap {
+    int CH, H, limit, first, stride, items, lane;
+    bool aligned;
+    __device__ __forceinline__ CopyMap(bool al, int rows, int ch, int first_, int stride_)
+        : CH(ch), H((ch + 3 + 31) / 32), first(first_), stride(stride_),
+          lane((int)(threadIdx.x & 31)), aligned(al)
+    {
+        limit = rows * (al ? H : ch);
+        items = limit > first ? (limit - first + stride - 1) / stride : 0;
+    }
+    // leftover q and chunk c of item n; false if it moves nothing
+    __device__ __forceinline__ bool at(int n, const int32_t *left_row, const uint8_t *hrow0,
+                                       int64_t B, int &q, int &c) const
+    {
+        if (n >= items) return false;
+        const int e = first + n * stride;
+        if (!aligned) {
+            q = e / CH;
+            c = e - q * CH;
+            return true;
+        }
+        q = e / H;
+        const int h = e - q * H;
+        const int delta = (int)((reinterpret_cast<uintptr_t>(hrow0 + (int64_t)left_row[q] * B) >> 4) & 3);
+        c = h * 32 + lane - delta;
+        return c >= 0 && c < CH;
+    }
+};
+
 // Resident row of position t from its block id `id` (-1: not resident), or
 // -2 when the id is malformed (below -1, or rows reaching the flag bit).
 __device__ __forceinline__ int32_t resident_row(int32_t id, int32_t t, int32_t bs)
@@ -361,35 +399,32 @@ __device__ __forceinline__ void copier_main(const ResolveLaunch &a, const Smem &
     uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
     cluster_arrive();
     cluster_wait();                       // phase 1: the leftover list is in
-    const int total = (int)sm.pub[0] * CH;
-    if (total == 0) return;               // an error, or no miss: no phase 2
+    if (sm.pub[0] == 0) return;           // an error, or no miss: no phase 2
     // Arrive for phase 2 before loading: the phase then ends as soon as the
     // resolver has filed the victims, not when this CTA's last thread has
     // got its loads out (host loads in flight hold up the issue of more).
     cluster_arrive();
-    const int first = (c - 1) * NT + tid, stride = ncopy * NT;
-    auto chunk_src = [&](int e) -> const uint8_t * {
-        const int q = e / CH, cc = e - q * CH;
-        return hrow0 + (int64_t)sm.left_row[q] * B + cc * 16;
-    };
+    const int rows = (int)sm.pub[0];
+    const CopyMap map = a.aligned_rows
+                            ? CopyMap(true, rows, CH, (c - 1) * (NT / 32) + (tid >> 5), ncopy * (NT / 32))
+                            : CopyMap(false, rows, CH, (c - 1) * NT + tid, ncopy * NT);
+    const int32_t *lrow = sm.left_row;
     uint4 pv[COPY_WINDOW];
 #pragma unroll
     for (int u = 0; u < COPY_WINDOW; ++u) {
-        const int e = first + u * stride;
-        if (e < total) pv[u] = ld_host_v4(chunk_src(e));
+        int q, cc;
+        if (map.at(u, lrow, hrow0, B, q, cc)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + cc * 16);
     }
     cluster_wait();                       // phase 2: the victims are in
     if (sm.pub[1] == 0) return;           // no copy after all (protected rows)
-    for (int e0 = first; e0 < total; e0 += COPY_WINDOW * stride) {
+    for (int n0 = 0; n0 < map.items; n0 += COPY_WINDOW) {
 #pragma unroll
         for (int u = 0; u < COPY_WINDOW; ++u) {
-            const int e = e0 + u * stride;
-            if (e < total) {
-                const int q = e / CH, cc = e - q * CH;
+            int q, cc;
+            if (map.at(n0 + u, lrow, hrow0, B, q, cc))
                 st_v4(drow0 + (int64_t)sm.arr_vict[q] * B + cc * 16, pv[u]);
-                const int e2 = e + COPY_WINDOW * stride;
-                if (e2 < total) pv[u] = ld_host_v4(chunk_src(e2));
-            }
+            if (map.at(n0 + u + COPY_WINDOW, lrow, hrow0, B, q, cc))
+                pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + cc * 16);
         }
     }
 }
@@ -683,16 +718,14 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int m_arr = (int)*sm.arrived;
     const bool defer = a.deferred && (int64_t)m_arr * B > a.defer_bytes;
     const int nleft = (a.fused_copy && !defer && !ncopy) ? max(m_arr - SR, 0) : 0;
-    const int total = nleft * CH;
-    auto chunk_src = [&](int e) -> const uint8_t * {
-        const int q = e / CH, c = e - q * CH;
-        return hrow0 + (int64_t)sm.left_row[q] * B + c * 16;
-    };
+    const CopyMap map = a.aligned_rows ? CopyMap(true, nleft, CH, tid >> 5, NT / 32)
+                                       : CopyMap(false, nleft, CH, tid, NT);
+    const int32_t *lrow = sm.left_row;
     uint4 pv[COPY_WINDOW];
 #pragma unroll
     for (int u = 0; u < EARLY; ++u) {
-        const int e = tid + u * NT;
-        if (e < total) pv[u] = ld_host_v4(chunk_src(e));
+        int q, c;
+        if (map.at(u, lrow, hrow0, B, q, c)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + c * 16);
     }
     late_grid_wait(a);   // the first global writes follow
 
@@ -851,19 +884,17 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     // COPY_WINDOW loads in flight until its last ones.
 #pragma unroll
     for (int u = EARLY; u < COPY_WINDOW; ++u) {
-        const int e = tid + u * NT;
-        if (e < total) pv[u] = ld_host_v4(chunk_src(e));
+        int q, c;
+        if (map.at(u, lrow, hrow0, B, q, c)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + c * 16);
     }
-    for (int e0 = tid; e0 < total; e0 += COPY_WINDOW * NT) {
+    for (int n0 = 0; n0 < map.items; n0 += COPY_WINDOW) {
 #pragma unroll
         for (int u = 0; u < COPY_WINDOW; ++u) {
-            const int e = e0 + u * NT;
-            if (e < total) {
-                const int q = e / CH, c = e - q * CH;
+            int q, c;
+            if (map.at(n0 + u, lrow, hrow0, B, q, c))
                 st_v4(drow0 + (int64_t)sm.arr_vict[SR + q] * B + c * 16, pv[u]);
-                const int e2 = e + COPY_WINDOW * NT;
-                if (e2 < total) pv[u] = ld_host_v4(chunk_src(e2));
-            }
+            if (map.at(n0 + u + COPY_WINDOW, lrow, hrow0, B, q, c))
+                pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + c * 16);
         }
     }
     // the staged rows, once they have all landed, one bulk store per row
