@@ -1056,7 +1056,9 @@ def run_config4(args, ws, rank, H):
     K, Wm = args.steps, args.warmup
     S0 = SETTLE_STEPS
     PH = min(K, 8)     # steps after the timed ones that record the phase ends
-    w = W.make_config(4, steps=S0 + K + Wm + PH)
+    # each timed step is followed by a reference step (no replay), so the
+    # schedule covers 2K timed steps
+    w = W.make_config(4, steps=S0 + 2 * K + Wm + PH)
     gpu = H.HiSparse.for_workload(w)
     for l in range(w.num_layers):
         for r in range(w.num_requests):
@@ -1092,13 +1094,16 @@ def run_config4(args, ws, rank, H):
         e.synchronize()
         comp_ms.append(s.elapsed_time(e))
     compute_ms = statistics.median(comp_ms)
-    def step(c, prefetch=True, marks=None):
+    def step(c, prefetch=True, marks=None, replay=True):
         """Anchor swap-in, three skip-layer replays, stand-in compute.
-        marks, if given: events after the anchor, the replays, the compute."""
+        marks, if given: events after the anchor, the replays, the compute.
+        replay=False: the reference step, anchor swap-in and compute only."""
         gpu.swap_in(0, sched[c], seq, out, plan, cnt)
         if marks:
             marks[0].record()
-        if prefetch:
+        if not replay:
+            H.synthetic_compute(buf, passes)
+        elif prefetch:
             ev = torch.cuda.Event()
             ev.record()
             side.wait_event(ev)
@@ -1135,19 +1140,24 @@ def run_config4(args, ws, rank, H):
         e.synchronize()
         rep_ms.append(s.elapsed_time(e))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    times, anchor_ms = [], []
+    # Timed steps alternate with reference steps (anchor swap-in and compute,
+    # no replay) on the next schedule entry: the exposed copy time is the
+    # difference of their medians, taken under the same conditions.
+    times, ref_times, anchor_ms = [], [], []
     miss = torch.zeros(K, dtype=torch.int64, device="cuda")
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     phases = []
     for i in range(K):
-        flush.zero_()
-        torch.cuda.synchronize()
-        s.record()
-        step(S0 + Wm + i, prefetch)
-        e.record()
-        e.synchronize()
-        times.append(s.elapsed_time(e))
-        miss[i] = cnt.sum()
+        for replay in (True, False):
+            flush.zero_()
+            torch.cuda.synchronize()
+            s.record()
+            step(S0 + Wm + 2 * i + (0 if replay else 1), prefetch, replay=replay)
+            e.record()
+            e.synchronize()
+            (times if replay else ref_times).append(s.elapsed_time(e))
+            if replay:
+                miss[i] = cnt.sum()
     # where each phase ends, from steps after the timed ones (the extra
     # events would add their own cost to the timed steps)
     for i in range(PH):
@@ -1155,7 +1165,7 @@ def run_config4(args, ws, rank, H):
         torch.cuda.synchronize()
         marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         s.record()
-        step(S0 + Wm + K + i, prefetch, marks)
+        step(S0 + Wm + 2 * K + i, prefetch, marks)
         e.record()
         e.synchronize()
         phases.append([s.elapsed_time(m) for m in marks])
@@ -1165,14 +1175,14 @@ def run_config4(args, ws, rank, H):
         flush.zero_()
         torch.cuda.synchronize()
         a0.record()
-        gpu.swap_in(0, sched[(S0 + Wm + i) % sched.shape[0]], seq, out, plan, cnt)
+        gpu.swap_in(0, sched[(S0 + Wm + 2 * i) % sched.shape[0]], seq, out, plan, cnt)
         a1.record()
         a1.synchronize()
         anchor_ms.append(a0.elapsed_time(a1))
     step_ms = statistics.mean(times)
     anchor = statistics.median(anchor_ms)
     # exposed copy time from medians (a single slow step should not decide it)
-    exposed = statistics.median(times) - compute_ms - anchor
+    exposed = statistics.median(times) - statistics.median(ref_times)
     misses = int(miss.sum().item())
     replay_bytes = misses * w.row_bytes * 3
     link = measure_link_peak(torch, H) if rank == 0 else None
@@ -1198,6 +1208,7 @@ def run_config4(args, ws, rank, H):
                    "replay_launches_per_step": 1,
                    "l2": "flushed between timed steps (512 MB write)"},
         "compute_ms": round(compute_ms, 4), "anchor_swap_in_ms": round(anchor, 4),
+        "reference_step_ms_median": round(statistics.median(ref_times), 4),
         "replays_alone_ms": round(statistics.median(rep_ms), 4),
         "phase_ends_ms_median": {"anchor": round(statistics.median(p[0] for p in phases), 4),
                                  "replays": round(statistics.median(p[1] for p in phases), 4),
@@ -1455,7 +1466,8 @@ OTHER_KEYS = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "conf
               "kernel_only", "miss_h2d_gbs", "miss_rows_per_step", "miss_h2d_frac_of_link_peak",
               "random_row_ceiling_kernel_only", "step_ms_min_median_max", "slow_steps", "backup",
               "dominant_kernel", "clocks", "gpu_launches", "exposed_copy_ms", "compute_ms",
-              "anchor_swap_in_ms", "replays_alone_ms", "step_ms_median", "link_peak")
+              "anchor_swap_in_ms", "replays_alone_ms", "reference_step_ms_median", "step_ms_median",
+              "link_peak")
 
 
 def run_other_configs(args) -> dict:
