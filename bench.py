@@ -954,7 +954,12 @@ def run_gpu(args):
                                 "share_of_step_time": round(sum(call_ms) / sum(breakdown_ms), 4),
                                 "timed_on": ("the timed steps" if not inner else
                                              f"{len(breakdown_ms)} steps after the timed ones, each call "
-                                             f"in its own event pair")},
+                                             f"in its own event pair"),
+                                "note": "mean_ms and median_ms are event-pair times: each includes the "
+                                        "~5 us that an event pair costs on this GPU",
+                                **({"kernel_only_mean_ms": ko_ms,
+                                    "kernel_only_is": "one launch per step: the kernel_only step time"}
+                                   if single and not st.split else {})},
             "gpu_launches": st.launches() * K,
             **backup_report(w, bev, link, bk_ms),
             "clocks": clk, "wall_s_timed_loop": round(wall, 3),

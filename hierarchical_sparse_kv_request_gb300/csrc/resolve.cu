@@ -6,28 +6,33 @@
 // handling with a host-to-device copy; [Arch] "HiSparse local KV offload
 // architecture", Hot lookup and LRU: a hot row is used in place and
 // refreshes the GPU LRU, a miss takes the LRU victim and copies the pinned
-// host row into it).
+// host row into it).  With copier CTAs the launch is a thread-block cluster
+// per request: rank 0 resolves, the other ranks only copy.
 //
 // The miss copies cross the host link and dominate the call, so everything
 // else is arranged around starting them as early as possible and keeping
 // them going:
-//   1. the LRU list (and the slot->token row) are staged into shared memory
+//   1. the slot->token row and the LRU list are staged into shared memory
 //      with asynchronous copies issued at kernel start, under the first
-//      global round trips;
-//   2. a miss is known as soon as its token->slot lookup returns, long before
-//      its victim slot is: at classification every miss takes an arrival
-//      index (a warp-aggregated shared-memory counter).  The first
-//      `stage_rows` misses to arrive have their host rows fetched at once
-//      into shared memory by the bulk-copy engine (cp.async.bulk, completion
-//      on an mbarrier), with no register or load slot held; the rest form a
-//      "leftover" list whose first chunks every thread loads into registers
-//      right after classification;
+//      global round trip; when it fits, the staged row also yields an inverse
+//      token->slot table in shared memory, so the hit lookup needs no gather
+//      of the token->slot map after the top-k row arrives;
+//   2. a miss is known as soon as its lookup returns, long before its victim
+//      slot is: at classification every miss takes an arrival index (a
+//      warp-aggregated shared-memory counter) and its host row goes on a
+//      list.  Right after classification the first chunks of that list are
+//      loaded into registers (or, optionally, the first `stage_rows` rows are
+//      fetched into shared memory by the bulk-copy engine); with copier CTAs
+//      the list goes to them instead (distributed shared memory, released by
+//      a cluster barrier) and they load it at once;
 //   3. then the block scans give each miss its rank in token order and its
 //      victim; all state writes are plain stores (the slot->token row is
-//      staged, so no write waits on a load of its own);
-//   4. finally the leftover chunks are stored (the rest streamed), and once
-//      the mbarrier completes the staged rows go from shared memory to their
-//      victim slots with bulk stores.
+//      staged, so no write waits on a load of its own), and each victim is
+//      filed under its miss's arrival index (in the copiers' shared memory,
+//      released by the second cluster barrier);
+//   4. finally the rows are stored to their victims while a rolling window
+//      of 8 loads per thread keeps the link busy to the end.  Rows under
+//      1 KB are copied in 64-byte-aligned spans of one row per warp load.
 // Only the bytes' route differs from a copy in rank order; where each row
 // lands is fixed by its rank, so the results are the same.
 //
