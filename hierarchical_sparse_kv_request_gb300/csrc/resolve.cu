@@ -99,9 +99,9 @@ __host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool st
     p.inv = o;   o += (stage_s2t && inv) ? align_up((size_t)max_cap * 2, 16) : 0;
     p.tbl = o;   o += (size_t)tbl_stride * 4;   // a multiple of 16
     p.chunk = o; o = align_up(o + (size_t)NT * 2, 4);
-    p.vict = o;  o = align_up(o + (size_t)k * 2, 4);
-    p.lrow = o;  o += (size_t)k * 4;
-    p.avict = o; o = align_up(o + (size_t)k * 2, 8);
+    p.vict = o;  o = align_up(o + (size_t)k * 2, 16);
+    p.lrow = o;  o += align_up((size_t)k * 4, 16);   // 16-byte rows: copied to copiers
+    p.avict = o; o += align_up((size_t)k * 2, 16);
     p.bar = o;   o += 8;
     p.cnt = o;   o += 16;
     p.stage = align_up(o, 128);
@@ -287,9 +287,22 @@ __device__ __forceinline__ void st_remote_u32(const uint32_t *local, uint32_t ra
 {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote_addr(local, rank)), "r"(v) : "memory");
 }
-__device__ __forceinline__ void st_remote_u16(const uint16_t *local, uint32_t rank, uint16_t v)
+__device__ __forceinline__ void st_remote_v4(const void *local, uint32_t rank, uint4 v)
 {
-    asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(remote_addr(local, rank)), "h"(v) : "memory");
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote_addr(local, rank)),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+// Copy `bytes` (a multiple of 16; 16-byte aligned) of this CTA's shared
+// memory to the same place in every copier CTA, one 16-byte store per thread
+// and copier.
+__device__ __forceinline__ void copy_to_copiers(const void *local, uint32_t bytes, int ncopy)
+{
+    const uint4 *src = reinterpret_cast<const uint4 *>(local);
+    for (uint32_t v = threadIdx.x; v < bytes / 16; v += blockDim.x) {
+        const uint4 x = src[v];
+        for (int q = 1; q <= ncopy; ++q) st_remote_v4(src + v, (uint32_t)q, x);
+    }
 }
 
 // Which 16-byte chunk of the leftover list a thread's n-th copy moves.
@@ -661,27 +674,41 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
     PackedIdx<KT> arr;    // arrival index of entry i (a miss), else -1
     uint32_t staged_bytes = 0;
+    {
+        uint32_t in_warp = 0;
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+            const bool mine = (miss >> i) & 1u;
+            const unsigned mask = __ballot_sync(0xffffffffu, mine);
+            arr.set(i, mine ? (int32_t)(in_warp + __popc(mask & ((1u << lane) - 1u))) : -1);
+            in_warp += (uint32_t)__popc(mask);
+        }
+        const uint32_t wf = __reduce_or_sync(0xffffffffu, f);
+        if (lane == 0) sm.warp_tot[tid >> 5] = (wf << 16) | in_warp;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    uint32_t flags, m_all, warp_base;
+    {
+        const uint32_t v = sm.warp_tot[lane];
+        flags = __reduce_or_sync(0xffffffffu, v >> 16);
+        uint32_t incl = v & 0xFFFFu;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        m_all = __shfl_sync(0xffffffffu, incl, 31);
+        const uint32_t before = __shfl_sync(0xffffffffu, incl, ((tid >> 5) + 31) & 31);
+        warp_base = (tid >> 5) ? before : 0u;
+    }
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
-        arr.set(i, -1);
-        const bool mine = (miss >> i) & 1u;
-        const unsigned mask = __ballot_sync(0xffffffffu, mine);
-        if (mask == 0u) continue;
-        const int leader = __ffs(mask) - 1;
-        uint32_t base = 0;
-        if (lane == leader) base = atomicAdd(sm.arrived, (uint32_t)__popc(mask));
-        base = __shfl_sync(0xffffffffu, base, leader);
-        if (!mine) continue;
-        const int32_t j = (int32_t)(base + __popc(mask & ((1u << lane) - 1u)));
+        if (arr.get(i) < 0) continue;
+        const int32_t j = (int32_t)warp_base + arr.get(i);
         arr.set(i, j);
-        if (j < SR) {
-            staged_bytes += (uint32_t)B;
-        } else if (ncopy) {
-            const uint32_t row = (uint32_t)host_slot(t[i]);
-            for (int q = 1; q <= ncopy; ++q) st_remote_u32((const uint32_t *)&sm.left_row[j], q, row);
-        } else {
-            sm.left_row[j - SR] = host_slot(t[i]);
-        }
+        if (j < SR) staged_bytes += (uint32_t)B;
+        else sm.left_row[j - SR] = host_slot(t[i]);
     }
     if (SR) {
         mbar_arrive_expect_tx(sm.bar, staged_bytes);
@@ -693,15 +720,20 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
                           (uint32_t)B, sm.bar);
         }
     }
-    cp_async_wait_all();   // the LRU list, before the barrier that publishes it
-    const uint32_t flags = block_or(f, sm.flags);
     // Copiers: the list goes out now (count 0 on an error: nothing to copy).
     // Phase 2 follows only if the count is nonzero (`copying`); a copier
     // that reads 0 leaves after phase 1.
-    const bool copying = ncopy && !flags && *sm.arrived > 0u;
+    // The leftover rows are in shared memory (for the early loads below),
+    // and with copiers they go out now: 16 bytes a thread, then the count (0
+    // on an error: nothing to copy), released by the first cluster barrier.
+    // Phase 2 follows only if the count is nonzero (`copying`); a copier that
+    // reads 0 leaves after phase 1.
+    __syncthreads();
+    const bool copying = ncopy && !flags && m_all > 0u;
     if (ncopy) {
+        if (copying) copy_to_copiers(sm.left_row, (m_all * 4u + 15u) / 16u * 16u, ncopy);
         if (tid == 0)
-            for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[0], q, flags ? 0u : *sm.arrived);
+            for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[0], q, flags ? 0u : m_all);
         cluster_arrive();
     }
     if (flags) {
@@ -720,7 +752,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     // call without errors every miss took one arrival index, so the count is
     // the call's miss count m.  (A request with many misses can leave its
     // copies to a full-GPU copy grid launched behind this kernel.)
-    const int m_arr = (int)*sm.arrived;
+    const int m_arr = (int)m_all;
     const bool defer = a.deferred && (int64_t)m_arr * B > a.defer_bytes;
     const int nleft = (a.fused_copy && !defer && !ncopy) ? max(m_arr - SR, 0) : 0;
     const CopyMap map = a.aligned_rows ? CopyMap(true, nleft, CH, tid >> 5, NT / 32)
@@ -833,10 +865,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         for (int q = owner * WC; q < w; ++q) rank += __popc(sm.missbits[q]);
         rank += __popc(sm.missbits[w] & ((1u << (x & 31)) - 1u));
         const int v = sm.victims[rank];
-        if (ncopy)
-            for (int q = 1; q <= ncopy; ++q) st_remote_u16(&sm.arr_vict[arr.get(i)], q, (uint16_t)v);
-        else
-            sm.arr_vict[arr.get(i)] = (uint16_t)v;
+        sm.arr_vict[arr.get(i)] = (uint16_t)v;
         const int32_t old = sm.s2t_s ? sm.s2t_s[v] : slot2tok[v];
         if (old >= 0 && (int64_t)old < cap) tok2slot[old] = -1;
         slot2tok[v] = x;
@@ -848,10 +877,12 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
             pr[1] = v;
         }
     }
-    // The copiers may store their rows now (phase 2).
+    // The copiers may store their rows now (phase 2): the victims go out.
     if (ncopy) {
         cluster_wait();
         if (copying) {
+            __syncthreads();
+            copy_to_copiers(sm.arr_vict, (m_all * 2u + 15u) / 16u * 16u, ncopy);
             if (tid == 0)
                 for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[1], q, 1u);
             cluster_arrive();
