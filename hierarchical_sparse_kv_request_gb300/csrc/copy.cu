@@ -182,6 +182,11 @@ __global__ void __launch_bounds__(256) backup_kernel(BackupLaunch a)
             if (old_slot >= 0 && old_slot != p) s2t[old_slot] = -1;
             s2t[p] = p;
             t2s[p] = p;
+            if (Ly.st.resbits) {   // token old_tok leaves the buffer, token p is in it
+                uint32_t *rb = Ly.st.resbits + (int64_t)r * Ly.st.res_words;
+                if (old_tok >= 0 && old_tok != p) atomicAnd(&rb[old_tok >> 5], ~(1u << (old_tok & 31)));
+                atomicOr(&rb[p >> 5], 1u << (p & 31));
+            }
         }
     }
 }
@@ -234,6 +239,17 @@ __global__ void __launch_bounds__(256) prefill_kernel(const int32_t *seq_lens,
             lru[s] = (uint16_t)s;
         }
         if (gt == 0) L.st.tick[r] = 0u;
+        if (L.st.resbits) {   // tokens [S - n, S) have slots
+            uint32_t *rb = L.st.resbits + (int64_t)r * L.st.res_words;
+            const int64_t lo = S - n, hi = S;
+            for (int64_t w = gt; w < L.st.res_words; w += gs) {
+                const int64_t t0 = w * 32;
+                const int64_t a = lo > t0 ? lo - t0 : 0, b = hi < t0 + 32 ? hi - t0 : 32;
+                uint32_t word = 0u;
+                if (b > a) word = (b - a == 32) ? ~0u : (((1u << (b - a)) - 1u) << a);
+                rb[w] = word;
+            }
+        }
     }
     const int CH = g.chunks;
     const int64_t B = g.B;

@@ -209,6 +209,7 @@ void release(hisparse_handle *h)
         dev_free(h, st.last_used);
         dev_free(h, st.lru);
         dev_free(h, st.tick);
+        dev_free(h, st.resbits);
     }
     dev_free(h, h->d_layers);
     dev_free(h, h->d_plan_rows);
@@ -503,7 +504,10 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
               dev_alloc(h, &h->d_plan_counts, (size_t)h->R) == cudaSuccess &&
               dev_alloc(h, &h->d_deferred, (size_t)h->R) == cudaSuccess &&
               (!paged || dev_alloc(h, &h->d_tbl, h->tbl.size()) == cudaSuccess);
-    h->state.assign(h->L, hs::HotState{nullptr, nullptr, nullptr, nullptr, nullptr});
+    h->state.assign(h->L, hs::HotState{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0});
+    // The resident-token bitmap is kept where the resolve kernel reads it:
+    // with the inverse-table lookup.
+    const int32_t res_words = (int32_t)(((h->max_cap + 31) / 32 + 3) / 4 * 4);
     for (int l = 0; ok && l < h->L; ++l) {
         if (h->anchor[l] >= 0) continue;
         hs::HotState &st = h->state[l];
@@ -511,7 +515,10 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
              dev_alloc(h, &st.slot2tok, RD) == cudaSuccess &&
              dev_alloc(h, &st.last_used, RD) == cudaSuccess &&
              dev_alloc(h, &st.lru, RD) == cudaSuccess &&
-             dev_alloc(h, &st.tick, (size_t)h->R) == cudaSuccess;
+             dev_alloc(h, &st.tick, (size_t)h->R) == cudaSuccess &&
+             (!h->inv_lookup ||
+              dev_alloc(h, &st.resbits, (size_t)h->R * res_words) == cudaSuccess);
+        if (st.resbits) st.res_words = res_words;
     }
     if (!ok) {
         cudaGetLastError();
@@ -934,6 +941,14 @@ int hisparse_write_state(hisparse_t h, int32_t layer, const int32_t *slot2tok,
     if (e == cudaSuccess) e = cudaMemcpy(st.slot2tok, slot2tok, RD * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(st.last_used, last_used, RD * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(st.tok2slot, t2s.data(), t2s.size() * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && st.resbits) {
+        std::vector<uint32_t> bits((size_t)R * st.res_words, 0u);
+        for (int r = 0; r < R; ++r)
+            for (int64_t t = 0; t < h->cap[r]; ++t)
+                if (t2s[(size_t)h->off[r] + t] >= 0)
+                    bits[(size_t)r * st.res_words + t / 32] |= 1u << (t % 32);
+        e = cudaMemcpy(st.resbits, bits.data(), bits.size() * 4, cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) e = cudaMemcpy(st.lru, lru.data(), RD * 2, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(st.tick, ticks, (size_t)R * 4, cudaMemcpyHostToDevice);
     if (e != cudaSuccess || !rebuild_rows) return cuda_status(e);

@@ -36,6 +36,12 @@ struct HotState {
     uint32_t *last_used;
     uint16_t *lru;
     uint32_t *tick;
+    // Optional (null: not kept): resbits[r*res_words + t/32] bit t%32 is set
+    // exactly when token t of request r has a slot (tok2slot >= 0).  Every
+    // kernel that changes the maps keeps it; the resolve kernel stages a
+    // request's row to tell misses from hits before the slots are known.
+    uint32_t *resbits;
+    int32_t res_words;   // words per request row (a multiple of 4)
 };
 
 // Storage of one layer: the pinned host pool as seen from the device and

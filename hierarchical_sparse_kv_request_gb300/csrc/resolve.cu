@@ -76,7 +76,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct SmemPlan {
-    size_t hit, sel, miss, lru, s2t, inv, tbl, chunk, vict, lrow, avict, bar, cnt, stage, total;
+    size_t hit, sel, miss, lru, s2t, inv, res, dup, tbl, chunk, vict, lrow, avict, bar, cnt, stage,
+        total;
 };
 
 // Shared memory of the CTA: bitmaps over slots and tokens, the staged LRU
@@ -97,6 +98,12 @@ __host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool st
     p.lru = align_up(o, 16); o = p.lru + align_up((size_t)D * 2, 16);
     p.s2t = o;   o += stage_s2t ? align_up((size_t)D * 4, 16) : 0;
     p.inv = o;   o += (stage_s2t && inv) ? align_up((size_t)max_cap * 2, 16) : 0;
+    // with the inverse table: the staged resident-token bitmap row (16-byte
+    // rows) and a token bitmap that catches duplicates
+    p.res = o;   o += (stage_s2t && inv) ? align_up((size_t)MW * 4, 16) : 0;
+    p.dup = o;   o += (stage_s2t && inv) ? align_up(MW * 4, 16) : 0;   // the block table row
+                                                                      // after it is staged in
+                                                                      // 16-byte copies
     p.tbl = o;   o += (size_t)tbl_stride * 4;   // a multiple of 16
     p.chunk = o; o = align_up(o + (size_t)NT * 2, 4);
     p.vict = o;  o = align_up(o + (size_t)k * 2, 16);
@@ -119,6 +126,8 @@ struct Smem {
     int32_t *s2t_s;      // [D]   staged slot->token row (null when not staged)
     uint16_t *inv;       // [max_cap] slot of each token, built from s2t_s (null: the
                          //       token->slot map in global memory is gathered instead)
+    uint32_t *res_s;     // [MW]  staged resident-token bitmap row (null: not kept)
+    uint32_t *dupbits;   // [MW]  tokens of this call, to catch duplicates (with res_s)
     int32_t *tbl_s;      // [tbl_stride] staged host block table row (null: no paged pool)
     uint16_t *chunk_pre; // [NT]  misses before each thread's chunk of missbits
     uint16_t *victims;   // [k]   victim slot of miss rank i
@@ -184,8 +193,10 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// all but this thread's most recent group of asynchronous copies have landed
+// all but this thread's most recent group (two groups) of asynchronous copies
+// have landed
 __device__ __forceinline__ void cp_async_wait_but_last() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_but_last2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 
 // ---- bulk-copy engine (TMA, non-tensor form) and its mbarrier --------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -476,6 +487,9 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     sm.lru_s = reinterpret_cast<uint16_t *>(smem_raw + sp.lru);
     sm.s2t_s = a.stage_s2t ? reinterpret_cast<int32_t *>(smem_raw + sp.s2t) : nullptr;
     sm.inv = (a.stage_s2t && a.inv_lookup) ? reinterpret_cast<uint16_t *>(smem_raw + sp.inv) : nullptr;
+    const bool early_classify = sm.inv && a.st.resbits;
+    sm.res_s = early_classify ? reinterpret_cast<uint32_t *>(smem_raw + sp.res) : nullptr;
+    sm.dupbits = early_classify ? reinterpret_cast<uint32_t *>(smem_raw + sp.dup) : nullptr;
     sm.tbl_s = hb ? reinterpret_cast<int32_t *>(smem_raw + sp.tbl) : nullptr;
     sm.chunk_pre = reinterpret_cast<uint16_t *>(smem_raw + sp.chunk);
     sm.victims = reinterpret_cast<uint16_t *>(smem_raw + sp.vict);
@@ -524,12 +538,17 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         const int j = tid + i * NT;
         t[i] = j < k ? a.topk[(int64_t)r * k + j] : -1;
     }
-    // Stage the slot->token row, then the LRU list, with asynchronous
-    // copies (two groups); they land under the round trips above.  (16-byte
-    // rows need D % 8 == 0.)
+    // Stage the resident-token bitmap row (if kept), the slot->token row and
+    // the LRU list with asynchronous copies (three groups); they land under
+    // the round trips above.  (16-byte rows need D % 8 == 0.)
     const uint16_t *lru = a.st.lru + (int64_t)r * D;
     int32_t *slot2tok = a.st.slot2tok + (int64_t)r * D;
     const bool staged_async = (D & 7) == 0;
+    if (sm.res_s) {   // the resident-token bitmap row first: classification needs it first
+        const uint32_t *rb = a.st.resbits + (int64_t)r * a.st.res_words;
+        for (int i = tid; i < (a.st.res_words >> 2); i += NT) cp_async16(sm.res_s + i * 4, rb + i * 4);
+    }
+    cp_async_commit();
     if (staged_async && sm.s2t_s)
         for (int i = tid; i < (D >> 2); i += NT) cp_async16(sm.s2t_s + i * 4, slot2tok + i * 4);
     cp_async_commit();
@@ -602,6 +621,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     }
     const int mw = (S + 31) >> 5;
     for (int w = tid; w < mw; w += NT) sm.missbits[w] = 0u;
+    if (sm.dupbits)
+        for (int w = tid; w < mw; w += NT) sm.dupbits[w] = 0u;
     for (int w = tid; w < DW; w += NT) { sm.hitbits[w] = 0u; sm.selbits[w] = 0u; }
     if (!staged_async) {
         for (int i = tid; i < D; i += NT) sm.lru_s[i] = lru[i];
@@ -613,7 +634,16 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         *sm.flags = 0u;
         if (SR) mbar_init(sm.bar, NT);   // every thread arrives once
     }
-    if (sm.inv) {
+    if (sm.res_s) {
+        // Misses first: the staged resident-token bitmap tells a miss from a
+        // hit before any slot is known; the hits' slots come from the inverse
+        // table once the miss list is out (below).
+        if (hb) cp_async_wait_all();   // the block table row is needed too
+        else cp_async_wait_but_last2();  // the slot->token row and LRU list may still land
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < KT; ++i) s[i] = -1;
+    } else if (sm.inv) {
         // With the inverse table the lookup needs only the staged
         // slot->token row, whose copy was issued at the start: every slot
         // files itself under its token, and a token's entry counts only if
@@ -653,15 +683,28 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (x < 0 || x >= S) { f |= kFlagBad; continue; }
         rid[i] = resident_row(rid[i], x, a.res_block_size);   // now the row
         if (rid[i] == -2) f |= kFlagBadRes;
+        const uint32_t bit = 1u << (x & 31);
+        if (sm.res_s) {
+            // duplicates by token; a miss is a non-resident token without a slot
+            if (atomicOr(&sm.dupbits[x >> 5], bit) & bit) f |= kFlagDup;
+            if (rid[i] == -1 && !(sm.res_s[x >> 5] & bit)) {
+                if (hb && sm.tbl_s[x / hb] < 0) {
+                    f |= kFlagNoHost;
+                } else {
+                    miss |= 1u << i;
+                    atomicOr(&sm.missbits[x >> 5], bit);
+                }
+            }
+            continue;
+        }
         if (rid[i] == -1 && s[i] < 0) {
             if (hb && sm.tbl_s[x / hb] < 0) f |= kFlagNoHost;
             else miss |= 1u << i;
         }
         if (rid[i] < 0 && s[i] >= 0) {
-            const uint32_t bit = 1u << (s[i] & 31);
-            if (atomicOr(&sm.hitbits[s[i] >> 5], bit) & bit) f |= kFlagDup;
+            const uint32_t sbit = 1u << (s[i] & 31);
+            if (atomicOr(&sm.hitbits[s[i] >> 5], sbit) & sbit) f |= kFlagDup;
         } else {
-            const uint32_t bit = 1u << (x & 31);
             if (atomicOr(&sm.missbits[x >> 5], bit) & bit) f |= kFlagDup;
         }
     }
@@ -686,7 +729,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         const uint32_t wf = __reduce_or_sync(0xffffffffu, f);
         if (lane == 0) sm.warp_tot[tid >> 5] = (wf << 16) | in_warp;
     }
-    cp_async_wait_all();
+    if (!sm.res_s) cp_async_wait_all();   // the LRU list, published by this barrier
     __syncthreads();
     uint32_t flags, m_all, warp_base;
     {
@@ -765,6 +808,29 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (map.at(u, lrow, hrow0, B, q, c)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + c * 16);
     }
     late_grid_wait(a);   // the first global writes follow
+
+    if (sm.res_s) {
+        // The hits' slots, from the inverse table of the staged slot->token
+        // row (landed by now, with the LRU list): every slot files itself
+        // under its token; a hit's entry is the slot that holds it.
+        cp_async_wait_all();
+        __syncthreads();
+        for (int sl = tid; sl < D; sl += NT) {
+            const int32_t x = sm.s2t_s[sl];
+            if (x >= 0 && x < a.max_cap) sm.inv[x] = (uint16_t)sl;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+            if (t[i] < 0 || t[i] >= S || rid[i] != -1 || ((miss >> i) & 1u)) continue;
+            const int v = sm.inv[t[i]];
+            if (v < D && sm.s2t_s[v] == t[i]) {
+                s[i] = v;
+                atomicOr(&sm.hitbits[v >> 5], 1u << (v & 31));
+            }
+        }
+        __syncthreads();   // the hit bitmap is complete
+    }
 
     if (a.resident) {
 #pragma unroll
@@ -851,6 +917,9 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     }
     __syncthreads();
 
+    // The resident-token bitmap row in global memory, if kept: evicted tokens
+    // leave it, misses enter it (atomics: threads share its words).
+    uint32_t *resg = a.st.resbits ? a.st.resbits + (int64_t)r * a.st.res_words : nullptr;
     // State writes (stores only: no load of their own to wait for).  Misses
     // take victims by ascending token rank; each victim is also filed under
     // the miss's arrival index, where the copies below look it up.
@@ -867,9 +936,13 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         const int v = sm.victims[rank];
         sm.arr_vict[arr.get(i)] = (uint16_t)v;
         const int32_t old = sm.s2t_s ? sm.s2t_s[v] : slot2tok[v];
-        if (old >= 0 && (int64_t)old < cap) tok2slot[old] = -1;
+        if (old >= 0 && (int64_t)old < cap) {
+            tok2slot[old] = -1;
+            if (resg) atomicAnd(&resg[old >> 5], ~(1u << (old & 31)));
+        }
         slot2tok[v] = x;
         tok2slot[x] = v;
+        if (resg) atomicOr(&resg[x >> 5], 1u << (x & 31));
         out[j] = v;
         if (a.plan_rows) {
             int32_t *pr = a.plan_rows + ((int64_t)r * k + rank) * 2;
