@@ -65,7 +65,7 @@ struct hisparse_handle {
     bool last_all = true;
     std::vector<uint8_t> last_wrote;   // [L]
     bool stage_s2t = false;   // resolve kernel stages the slot->token row
-    bool inv_lookup = false;  // ... and finds hits through an inverse table in shared memory
+    int32_t lookup = hs::kLookupGather;  // ... and tells misses from hits this way
 
     // Paged host pool (hb > 0): pool_blocks blocks of hb rows per layer,
     // handed to requests by hisparse_host_reserve.  `tbl` is the host copy of
@@ -173,7 +173,7 @@ bool left_layer_alone(const hisparse_handle *h, cudaStream_t s, int32_t layer)
 // Dynamic shared memory of the handle's resolve launches without staged rows.
 size_t resolve_smem(const hisparse_handle *h)
 {
-    return hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, h->stage_s2t, h->inv_lookup,
+    return hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, h->stage_s2t, h->lookup,
                                   h->hb ? h->tbl_stride : 0, 0, h->B);
 }
 
@@ -416,7 +416,8 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
     }
     int max_smem = 0;
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
-    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, false, false, h->tbl_stride, 0, h->B) >
+    if (hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, false, hs::kLookupGather, h->tbl_stride,
+                               0, h->B) >
             (size_t)max_smem ||
         hs::replay_smem_bytes(h->R) > (size_t)max_smem) {
         release(h);
@@ -425,16 +426,21 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
     // The slot->token row rides in shared memory when it fits, and with it,
     // when that fits too, an inverse table over the request's tokens: the
     // hit lookup then needs no gather of the token->slot map, whose round
-    // trip otherwise sits between the top-k row and the first host loads.
-    // The shared memory left over stages miss rows for the bulk-copy engine.
-    h->stage_s2t = hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, true, false, h->tbl_stride,
-                                          0, h->B) <= (size_t)max_smem;
-    h->inv_lookup = h->stage_s2t &&
-                    hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, true, true, h->tbl_stride,
-                                           0, h->B) <= (size_t)max_smem;
+    // trip otherwise sits between the top-k row and the first host loads;
+    // and when the request's resident-token bitmap row fits as well, the
+    // misses are known from it before any slot (hs::kLookup*).  The shared
+    // memory left over stages miss rows for the bulk-copy engine.
+    auto fits = [&](bool s2t, int lookup) {
+        return hs::resolve_smem_bytes(h->k, h->D, (int)h->max_cap, s2t, lookup, h->tbl_stride, 0,
+                                      h->B) <= (size_t)max_smem;
+    };
+    h->stage_s2t = fits(true, hs::kLookupGather);
+    h->lookup = !h->stage_s2t ? hs::kLookupGather
+                : fits(true, hs::kLookupResident) ? hs::kLookupResident
+                : fits(true, hs::kLookupInverse) ? hs::kLookupInverse
+                : hs::kLookupGather;
     h->max_stage_rows = hs::resolve_stage_rows(h->k, h->D, (int)h->max_cap, h->stage_s2t,
-                                               h->inv_lookup, h->tbl_stride, h->B,
-                                               (size_t)max_smem);
+                                               h->lookup, h->tbl_stride, h->B, (size_t)max_smem);
     h->stage_rows = 0;          // measured: staging is slower on the benchmarked shapes
     if (hs::resolve_prepare((size_t)max_smem) != cudaSuccess || hs::copy_prepare() != cudaSuccess) {
         release(h);
@@ -516,7 +522,7 @@ int create_impl(const hisparse_layout *layout, int32_t host_block_tokens, hispar
              dev_alloc(h, &st.last_used, RD) == cudaSuccess &&
              dev_alloc(h, &st.lru, RD) == cudaSuccess &&
              dev_alloc(h, &st.tick, (size_t)h->R) == cudaSuccess &&
-             (!h->inv_lookup ||
+             (h->lookup < hs::kLookupResident ||
               dev_alloc(h, &st.resbits, (size_t)h->R * res_words) == cudaSuccess);
         if (st.resbits) st.res_words = res_words;
     }
@@ -736,7 +742,7 @@ int swap_in_impl(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int
     const bool autom = h->copy_mode == HISPARSE_COPY_AUTO && h->R < kAutoDeferBelowRequests;
     a.fused_copy = !split;
     a.stage_s2t = h->stage_s2t;
-    a.inv_lookup = h->inv_lookup;
+    a.lookup = h->lookup;
     a.resident = resident_blocks;
     a.res_max_blocks = resident_blocks ? max_blocks : 0;
     a.res_block_size = resident_blocks ? block_size : 0;
@@ -1093,7 +1099,7 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     a.max_cap = (int32_t)h->max_cap;
     a.fused_copy = false;
     a.stage_s2t = h->stage_s2t;
-    a.inv_lookup = h->inv_lookup;
+    a.lookup = h->lookup;
     a.resident = nullptr;
     a.res_max_blocks = 0;
     a.res_block_size = 0;

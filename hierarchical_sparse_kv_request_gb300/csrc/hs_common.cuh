@@ -151,6 +151,16 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
 // ---------------------------------------------------------------------------
 // Kernel launchers (defined in the .cu files).
 // ---------------------------------------------------------------------------
+// How the resolve kernel tells misses from hits (each needs the staged
+// slot->token row and more shared memory than the one before):
+//   kLookupGather    gather the token->slot map for the top-k row;
+//   kLookupInverse   an inverse token->slot table built in shared memory
+//                    from the staged slot->token row;
+//   kLookupResident  misses first from the request's staged resident-token
+//                    bitmap row (HotState::resbits), then the inverse table
+//                    for the hits' slots.
+constexpr int32_t kLookupGather = 0, kLookupInverse = 1, kLookupResident = 2;
+
 struct ResolveLaunch {
     const int32_t *topk;
     const int32_t *seq_lens;
@@ -164,8 +174,7 @@ struct ResolveLaunch {
     int32_t max_cap;       // largest host capacity (sizes the miss bitmap)
     bool fused_copy;       // copy the misses in this kernel
     bool stage_s2t;        // stage the slot->token row in shared memory
-    bool inv_lookup;       // with stage_s2t: find hits through an inverse table built in
-                           // shared memory from the staged row, not by a gather
+    int32_t lookup;        // with stage_s2t, kLookup*: how misses and hits are told apart
     const int32_t *resident;  // [R][res_max_blocks] resident block ids, or null
     int32_t res_max_blocks;
     int32_t res_block_size;
@@ -188,10 +197,10 @@ struct ResolveLaunch {
 // Shared-memory bytes the resolve kernel needs for this geometry
 // (tbl_stride: the host block table row staged per request, 0 = none;
 // stage_rows rows of B bytes for the bulk-copy engine).
-size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, bool inv, int tbl_stride,
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int lookup, int tbl_stride,
                           int stage_rows, int64_t B);
 // The most rows the bulk-copy engine can stage within max_smem (at most k).
-int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, bool inv, int tbl_stride,
+int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, int lookup, int tbl_stride,
                        int64_t B, size_t max_smem);
 int resolve_threads();
 // Allow every instantiation of the resolve kernel up to `smem` bytes of

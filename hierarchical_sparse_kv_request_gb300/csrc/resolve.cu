@@ -86,7 +86,7 @@ struct SmemPlan {
 // miss rank and by arrival index, the leftover host rows, the staging
 // mbarrier and arrival counter, and `stage_rows` rows of B bytes staged by
 // the bulk-copy engine.
-__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t, bool inv,
+__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t, int lookup,
                                               int tbl_stride, int stage_rows, int64_t B)
 {
     SmemPlan p;
@@ -97,11 +97,12 @@ __host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool st
     p.miss = o;  o += MW * 4;
     p.lru = align_up(o, 16); o = p.lru + align_up((size_t)D * 2, 16);
     p.s2t = o;   o += stage_s2t ? align_up((size_t)D * 4, 16) : 0;
-    p.inv = o;   o += (stage_s2t && inv) ? align_up((size_t)max_cap * 2, 16) : 0;
+    p.inv = o;   o += (stage_s2t && lookup >= kLookupInverse) ? align_up((size_t)max_cap * 2, 16) : 0;
     // with the inverse table: the staged resident-token bitmap row (16-byte
     // rows) and a token bitmap that catches duplicates
-    p.res = o;   o += (stage_s2t && inv) ? align_up((size_t)MW * 4, 16) : 0;
-    p.dup = o;   o += (stage_s2t && inv) ? align_up(MW * 4, 16) : 0;   // the block table row
+    const bool res = stage_s2t && lookup >= kLookupResident;
+    p.res = o;   o += res ? align_up((size_t)MW * 4, 16) : 0;
+    p.dup = o;   o += res ? align_up(MW * 4, 16) : 0;   // the block table row
                                                                       // after it is staged in
                                                                       // 16-byte copies
     p.tbl = o;   o += (size_t)tbl_stride * 4;   // a multiple of 16
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int SR = a.stage_rows;   // rows the bulk-copy engine may stage (0: none)
 
     const int32_t hb = a.g.hb;
-    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t, a.inv_lookup,
+    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t, a.lookup,
                                   hb ? a.g.tbl_stride : 0, SR, B);
     Smem sm;
     sm.warp_tot = reinterpret_cast<uint32_t *>(smem_raw);
@@ -486,8 +487,9 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     sm.missbits = reinterpret_cast<uint32_t *>(smem_raw + sp.miss);
     sm.lru_s = reinterpret_cast<uint16_t *>(smem_raw + sp.lru);
     sm.s2t_s = a.stage_s2t ? reinterpret_cast<int32_t *>(smem_raw + sp.s2t) : nullptr;
-    sm.inv = (a.stage_s2t && a.inv_lookup) ? reinterpret_cast<uint16_t *>(smem_raw + sp.inv) : nullptr;
-    const bool early_classify = sm.inv && a.st.resbits;
+    sm.inv = (a.stage_s2t && a.lookup >= kLookupInverse) ? reinterpret_cast<uint16_t *>(smem_raw + sp.inv)
+                                                         : nullptr;
+    const bool early_classify = sm.inv && a.lookup >= kLookupResident && a.st.resbits;
     sm.res_s = early_classify ? reinterpret_cast<uint32_t *>(smem_raw + sp.res) : nullptr;
     sm.dupbits = early_classify ? reinterpret_cast<uint32_t *>(smem_raw + sp.dup) : nullptr;
     sm.tbl_s = hb ? reinterpret_cast<int32_t *>(smem_raw + sp.tbl) : nullptr;
@@ -1061,16 +1063,16 @@ cudaError_t prepare_kt(size_t smem)
 
 }  // namespace
 
-size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, bool inv, int tbl_stride,
+size_t resolve_smem_bytes(int k, int D, int max_cap, bool stage_s2t, int lookup, int tbl_stride,
                           int stage_rows, int64_t B)
 {
-    return plan_smem(k, D, max_cap, stage_s2t, inv, tbl_stride, stage_rows, B).total;
+    return plan_smem(k, D, max_cap, stage_s2t, lookup, tbl_stride, stage_rows, B).total;
 }
 
-int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, bool inv, int tbl_stride,
+int resolve_stage_rows(int k, int D, int max_cap, bool stage_s2t, int lookup, int tbl_stride,
                        int64_t B, size_t max_smem)
 {
-    const size_t base = resolve_smem_bytes(k, D, max_cap, stage_s2t, inv, tbl_stride, 0, B);
+    const size_t base = resolve_smem_bytes(k, D, max_cap, stage_s2t, lookup, tbl_stride, 0, B);
     const size_t room = align_up(base, 128) + 16 <= max_smem ? max_smem - align_up(base, 128) - 16 : 0;
     const int64_t rows = (int64_t)(room / (size_t)B);
     return (int)(rows < k ? rows : k);
@@ -1115,7 +1117,7 @@ cudaError_t resolve_max_clusters(int k, int ctas, size_t smem, int *clusters)
 
 cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s)
 {
-    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t, a.inv_lookup,
+    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t, a.lookup,
                                            a.g.hb ? a.g.tbl_stride : 0, a.stage_rows, a.g.B);
     const int kt = (a.g.k + NT - 1) / NT;
     if (kt <= 1) return launch_kt<1>(a, s, smem);

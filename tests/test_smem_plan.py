@@ -2,7 +2,8 @@
 that is staged or copied in 16-byte units (cp.async, vector stores to the
 copier CTAs, bulk copies) starts on a 16-byte boundary, and the mbarrier on
 an 8-byte one, for a grid of shapes that covers every option (staged
-slot->token row, inverse table, paged block table, staged rows).  A region
+slot->token row, inverse table, resident-token bitmap, paged block table,
+staged rows).  A region
 off its boundary would be a misaligned-address fault on the GPU; this finds
 it without one.  The check compiles the kernel's source file into a host
 program (nvcc; no GPU needed) and calls its plan function."""
@@ -26,7 +27,7 @@ int main()
         for (int D : {k, k + 1, k + 3, k + 7, k + 299, 6144, 32768})
             for (int cap : {1, 31, 33, 100, 4097, 40064, 82000, 700000})
                 for (int s2t = 0; s2t < 2; ++s2t)
-                    for (int inv = 0; inv < 2; ++inv)
+                    for (int inv = 0; inv < 3; ++inv)
                         for (int tbl : {0, 4, 8, 1252})
                             for (int sr : {0, 1, 5})
                                 for (long B : {16L, 48L, 656L, 1152L}) {
