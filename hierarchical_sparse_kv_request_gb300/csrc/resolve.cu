@@ -459,6 +459,145 @@ __device__ __forceinline__ void copier_main(const ResolveLaunch &a, const Smem &
     }
 }
 
+// Misses and their arrival indices, from the staged resident-token bitmap
+// row: entry i of this thread (top-k entry tid + i NT) is a miss when it is a
+// valid position, not a resident page, its bit is clear and it has a host row.
+// The indices run over [0, m) in (warp, entry, lane) order: warp ballots place
+// each miss within its warp, one barrier publishes the warps' counts (and
+// error flags) through warp_tot, and each warp scans them for its base.  The
+// resolver and self-classifying copiers both number the misses this way, from
+// the same inputs, so they build the same list.
+template <int KT>
+__device__ __forceinline__ void number_misses(uint32_t miss, uint32_t f, uint32_t *warp_tot,
+                                              PackedIdx<KT> &arr, uint32_t &flags, uint32_t &m_all)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t in_warp = 0;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        const bool mine = (miss >> i) & 1u;
+        const unsigned mask = __ballot_sync(0xffffffffu, mine);
+        arr.set(i, mine ? (int32_t)(in_warp + __popc(mask & ((1u << lane) - 1u))) : -1);
+        in_warp += (uint32_t)__popc(mask);
+    }
+    const uint32_t wf = __reduce_or_sync(0xffffffffu, f);
+    if (lane == 0) warp_tot[warp] = (wf << 16) | in_warp;   // in_warp <= 32 KT
+    __syncthreads();
+    static_assert(NT == 32 * 32, "one count per lane");
+    const uint32_t v = warp_tot[lane];
+    flags = __reduce_or_sync(0xffffffffu, v >> 16);
+    uint32_t incl = v & 0xFFFFu;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    m_all = __shfl_sync(0xffffffffu, incl, 31);
+    const uint32_t before = __shfl_sync(0xffffffffu, incl, (warp + 31) & 31);
+    const uint32_t base = warp ? before : 0u;
+#pragma unroll
+    for (int i = 0; i < KT; ++i)
+        if (arr.get(i) >= 0) arr.set(i, (int32_t)base + arr.get(i));
+}
+
+// A self-classifying copier CTA (with the resident-token bitmap): it stages
+// the request's bitmap row itself, classifies the top-k row as the resolver
+// does and numbers the misses the same way, so it has the list of host rows
+// without a message, and starts its loads as soon as its own classification
+// is done.  One cluster barrier follows: the resolver arrives once it has
+// filed the victims in this CTA's shared memory (or found that nothing is to
+// be copied) and set sm.pub[1]; this CTA arrives at once and waits for it
+// before it stores, and always before it leaves, since the resolver writes
+// into its shared memory on every path.
+template <int KT>
+__device__ __forceinline__ void copier_self(const ResolveLaunch &a, const Smem &sm, int r, int c,
+                                            int ncopy)
+{
+    const int tid = threadIdx.x;
+    const int k = a.g.k, D = a.g.D, CH = a.g.chunks;
+    const int64_t B = a.g.B;
+    const int32_t hb = a.g.hb;
+    const int32_t S = a.seq_lens[r];
+    const int64_t off = a.g.host_off[r];
+    const int64_t cap = a.g.host_cap[r];
+    int32_t t[KT];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        const int j = tid + i * NT;
+        t[i] = j < k ? a.topk[(int64_t)r * k + j] : -1;
+    }
+    const uint32_t *rb = a.st.resbits + (int64_t)r * a.st.res_words;
+    for (int i = tid; i < (a.st.res_words >> 2); i += NT) cp_async16(sm.res_s + i * 4, rb + i * 4);
+    cp_async_commit();
+    int32_t rid[KT];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        rid[i] = -1;
+        if (a.resident && t[i] >= 0 && t[i] < S && t[i] <= cap) {
+            const int32_t b = t[i] / a.res_block_size;
+            if (b < a.res_max_blocks) rid[i] = a.resident[(int64_t)r * a.res_max_blocks + b];
+        }
+    }
+    // the resolver's paths without a copy (a malformed length, the fast
+    // path), taken by it on the same test, reach no cluster barrier
+    if (S < 0 || (int64_t)S > cap || S <= D) {
+        cp_async_wait_all();
+        return;
+    }
+    if (hb) {
+        const int32_t *tbl = a.g.host_tbl + (int64_t)r * a.g.tbl_stride;
+        const int nq = (int)(((int64_t)S + 4LL * hb - 1) / (4LL * hb));
+        for (int i = tid; i < nq; i += NT) cp_async16(sm.tbl_s + i * 4, tbl + i * 4);
+        cp_async_commit();
+    }
+    cluster_arrive();
+    cp_async_wait_all();
+    __syncthreads();
+    uint32_t miss = 0;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        const int32_t x = t[i];
+        if (x < 0 || x >= S) continue;
+        const int32_t row = resident_row(rid[i], x, a.res_block_size);
+        if (row != -1 || (sm.res_s[x >> 5] >> (x & 31)) & 1u) continue;
+        if (hb && sm.tbl_s[x / hb] < 0) continue;
+        miss |= 1u << i;
+    }
+    PackedIdx<KT> arr;
+    uint32_t flags, m_all;
+    number_misses<KT>(miss, 0u, sm.warp_tot, arr, flags, m_all);
+#pragma unroll
+    for (int i = 0; i < KT; ++i)
+        if (arr.get(i) >= 0)
+            sm.left_row[arr.get(i)] = hb ? sm.tbl_s[t[i] / hb] * hb + t[i] % hb : t[i];
+    __syncthreads();
+    const uint8_t *hrow0 = a.store.host + (hb ? 0 : off) * B;
+    uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
+    const int rows = (int)m_all;
+    const CopyMap map = a.aligned_rows
+                            ? CopyMap(true, rows, CH, (c - 1) * (NT / 32) + (tid >> 5), ncopy * (NT / 32))
+                            : CopyMap(false, rows, CH, (c - 1) * NT + tid, ncopy * NT);
+    const int32_t *lrow = sm.left_row;
+    uint4 pv[COPY_WINDOW];
+#pragma unroll
+    for (int u = 0; u < COPY_WINDOW; ++u) {
+        int q, cc;
+        if (map.at(u, lrow, hrow0, B, q, cc)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + cc * 16);
+    }
+    cluster_wait();                       // the victims are in (or no copy)
+    if (sm.pub[1] == 0) return;
+    for (int n0 = 0; n0 < map.items; n0 += COPY_WINDOW) {
+#pragma unroll
+        for (int u = 0; u < COPY_WINDOW; ++u) {
+            int q, cc;
+            if (map.at(n0 + u, lrow, hrow0, B, q, cc))
+                st_v4(drow0 + (int64_t)sm.arr_vict[q] * B + cc * 16, pv[u]);
+            if (map.at(n0 + u + COPY_WINDOW, lrow, hrow0, B, q, cc))
+                pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + cc * 16);
+        }
+    }
+}
+
 template <int KT>
 __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
 {
@@ -470,7 +609,6 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int ncopy = a.ncopy;
     const int r = blockIdx.x / (ncopy + 1);
     const int tid = threadIdx.x;
-    const int lane = tid & 31;
     const int k = a.g.k, D = a.g.D;
     const int DW = (D + 31) >> 5;
     const int64_t B = a.g.B;
@@ -524,7 +662,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
             // stores the resolver's wait (phase 2); it never holds up the next
             // launch, which its resolver's later signal gates.
             if (a.wait_late) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-            copier_main(a, sm, r, rank, ncopy);
+            if (early_classify) copier_self<KT>(a, sm, r, rank, ncopy);
+            else copier_main(a, sm, r, rank, ncopy);
             return;
         }
     }
@@ -719,39 +858,13 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
     PackedIdx<KT> arr;    // arrival index of entry i (a miss), else -1
     uint32_t staged_bytes = 0;
-    {
-        uint32_t in_warp = 0;
-#pragma unroll
-        for (int i = 0; i < KT; ++i) {
-            const bool mine = (miss >> i) & 1u;
-            const unsigned mask = __ballot_sync(0xffffffffu, mine);
-            arr.set(i, mine ? (int32_t)(in_warp + __popc(mask & ((1u << lane) - 1u))) : -1);
-            in_warp += (uint32_t)__popc(mask);
-        }
-        const uint32_t wf = __reduce_or_sync(0xffffffffu, f);
-        if (lane == 0) sm.warp_tot[tid >> 5] = (wf << 16) | in_warp;
-    }
-    if (!sm.res_s) cp_async_wait_all();   // the LRU list, published by this barrier
-    __syncthreads();
-    uint32_t flags, m_all, warp_base;
-    {
-        const uint32_t v = sm.warp_tot[lane];
-        flags = __reduce_or_sync(0xffffffffu, v >> 16);
-        uint32_t incl = v & 0xFFFFu;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += y;
-        }
-        m_all = __shfl_sync(0xffffffffu, incl, 31);
-        const uint32_t before = __shfl_sync(0xffffffffu, incl, ((tid >> 5) + 31) & 31);
-        warp_base = (tid >> 5) ? before : 0u;
-    }
+    uint32_t flags, m_all;
+    if (!sm.res_s) cp_async_wait_all();   // the LRU list, published by the next barrier
+    number_misses<KT>(miss, f, sm.warp_tot, arr, flags, m_all);
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
-        if (arr.get(i) < 0) continue;
-        const int32_t j = (int32_t)warp_base + arr.get(i);
-        arr.set(i, j);
+        const int32_t j = arr.get(i);
+        if (j < 0) continue;
         if (j < SR) staged_bytes += (uint32_t)B;
         else sm.left_row[j - SR] = host_slot(t[i]);
     }
@@ -775,7 +888,13 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     // reads 0 leaves after phase 1.
     __syncthreads();
     const bool copying = ncopy && !flags && m_all > 0u;
-    if (ncopy) {
+    // With the resident-token bitmap the copiers classify for themselves and
+    // build the same list (self_list): one cluster barrier, at which this
+    // CTA arrives once it has filed the victims and set sm.pub[1] (0: no
+    // copy) in their shared memory, on every path.  Otherwise the list goes
+    // to them here, with two barriers.
+    const bool self_list = ncopy && sm.res_s;
+    if (ncopy && !self_list) {
         if (copying) copy_to_copiers(sm.left_row, (m_all * 4u + 15u) / 16u * 16u, ncopy);
         if (tid == 0)
             for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[0], q, flags ? 0u : m_all);
@@ -787,7 +906,13 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
 #pragma unroll
         for (int i = 0; i < KT; ++i) rid[i] = -1;
         finish_untouched<KT>(a, r, t, rid, status_of(flags), tick);
-        if (ncopy) cluster_wait();
+        if (self_list) {
+            if (tid == 0)
+                for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[1], q, 0u);
+            cluster_arrive();
+        } else if (ncopy) {
+            cluster_wait();
+        }
         return;
     }
 
@@ -887,7 +1012,11 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (sm.warp_tot[0]) {
             if (SR) staged_rows_landed(sm.bar, a.status, r);
             finish_untouched<KT>(a, r, t, rid, kStatusCapacity, tick);
-            if (ncopy) {
+            if (self_list) {   // no copy after all
+                if (tid == 0)
+                    for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[1], q, 0u);
+                cluster_arrive();
+            } else if (ncopy) {
                 cluster_wait();
                 if (copying) {   // the copiers wait in phase 2: no copy after all
                     if (tid == 0)
@@ -953,7 +1082,15 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         }
     }
     // The copiers may store their rows now (phase 2): the victims go out.
-    if (ncopy) {
+    if (self_list) {
+        if (copying) {
+            __syncthreads();
+            copy_to_copiers(sm.arr_vict, (m_all * 2u + 15u) / 16u * 16u, ncopy);
+        }
+        if (tid == 0)
+            for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[1], q, copying ? 1u : 0u);
+        cluster_arrive();
+    } else if (ncopy) {
         cluster_wait();
         if (copying) {
             __syncthreads();
@@ -985,7 +1122,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         if (a.deferred) a.deferred[r] = defer ? 1 : 0;
         a.st.tick[r] = tick;
     }
-    if (copying) cluster_wait();
+    if (copying && !self_list) cluster_wait();
 
     // ---- miss copies: pinned host rows -> victim slots ---------------------
     // The leftovers through a window of COPY_WINDOW loads per thread: the
