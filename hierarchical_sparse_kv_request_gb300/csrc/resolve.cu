@@ -12,24 +12,28 @@
 // The miss copies cross the host link and dominate the call, so everything
 // else is arranged around starting them as early as possible and keeping
 // them going:
-//   1. the slot->token row and the LRU list are staged into shared memory
+//   1. the slot->token row and the LRU list (and, where kept, the
+//      request's resident-token bitmap row) are staged into shared memory
 //      with asynchronous copies issued at kernel start, under the first
 //      global round trip; when it fits, the staged row also yields an inverse
 //      token->slot table in shared memory, so the hit lookup needs no gather
 //      of the token->slot map after the top-k row arrives;
-//   2. a miss is known as soon as its lookup returns, long before its victim
-//      slot is: at classification every miss takes an arrival index (a
-//      warp-aggregated shared-memory counter) and its host row goes on a
-//      list.  Right after classification the first chunks of that list are
-//      loaded into registers (or, optionally, the first `stage_rows` rows are
-//      fetched into shared memory by the bulk-copy engine); with copier CTAs
-//      the list goes to them instead (distributed shared memory, released by
-//      a cluster barrier) and they load it at once;
+//   2. a miss is known as soon as its lookup returns (with the bitmap, as
+//      soon as its bit is read), long before its victim slot is: at
+//      classification every miss takes an arrival index (warp ballots and
+//      one barrier) and its host row goes on a list.  Right after
+//      classification the first chunks of that list are loaded into
+//      registers (or, optionally, the first `stage_rows` rows are fetched
+//      into shared memory by the bulk-copy engine).  With copier CTAs the
+//      copiers load the list instead: with the bitmap they stage the same
+//      rows and classify for themselves, in the same arrival order;
+//      otherwise the list goes to them (distributed shared memory, released
+//      by a cluster barrier) and they load it at once;
 //   3. then the block scans give each miss its rank in token order and its
 //      victim; all state writes are plain stores (the slot->token row is
 //      staged, so no write waits on a load of its own), and each victim is
 //      filed under its miss's arrival index (in the copiers' shared memory,
-//      released by the second cluster barrier);
+//      released by a cluster barrier);
 //   4. finally the rows are stored to their victims while a rolling window
 //      of 8 loads per thread keeps the link busy to the end.  Rows under
 //      1 KB are copied in 64-byte-aligned spans of one row per warp load.
