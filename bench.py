@@ -427,8 +427,10 @@ def random_row_ceiling_kernel_only(torch, H, gpu, w, nrows: int, seed: int = 3):
             "rounds_ms": [round(x, 5) for x in per],
             "gbs": round(nrows * w.row_bytes / (t * 1e-3) / 1e9, 1),
             "how": f"graphs of {KONLY_STEPS} (L2 flush, hisparse_link_gather of a fresh draw of "
-                   f"random pool rows, one 1024-thread CTA per SM) with one event pair around "
-                   f"them, minus the same flushes alone; median of {KONLY_ROUNDS} rounds"}
+                   f"random pool rows, one 1024-thread CTA per SM, the miss copy's row mapping: "
+                   f"64-byte-aligned spans below 1 KB rows, a rolling window of 8 loads) with "
+                   f"one event pair around them, minus the same flushes alone; median of "
+                   f"{KONLY_ROUNDS} rounds"}
 
 
 def random_row_ceiling(torch, H, gpu, w, nrows: int, reps: int = 8, seed: int = 2):

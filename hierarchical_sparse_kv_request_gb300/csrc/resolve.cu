@@ -324,39 +324,63 @@ __device__ __forceinline__ void copy_to_copiers(const void *local, uint32_t byte
 // Which 16-byte chunk of the leftover list a thread's n-th copy moves.
 //  - flat: chunk e = first + n * stride of the list, chunk e % CH of
 //    leftover e / CH (consecutive lanes take consecutive chunks);
-//  - unit-aligned: a warp's n-th task is first + n * stride; task (q, h) is
-//    the h-th 512 bytes of the 64-byte-aligned span around leftover q's host
-//    row, one 16-byte piece per lane, and lanes whose piece lies outside the
-//    row move nothing.  No 64-byte unit of host memory is then split between
-//    two warp loads.  Measured on GB300 (gathers of random pinned rows):
-//    656-byte rows 1.7-4% faster this way, 1152-byte rows 1-3% slower.
-struct CopyMap {
-    int CH, H, limit, first, stride, items, lane;
+//  - unit-aligned: a warp's n-th task is e = first + n * stride; task e is
+//    the (e % H)-th 512 bytes of the 64-byte-aligned span around leftover
+//    e / H's host row, one 16-byte piece per lane, and lanes whose piece lies
+//    outside the row move nothing.  No 64-byte unit of host memory is then
+//    split between two warp loads.  Measured on GB300 (gathers of random
+//    pinned rows): 656-byte rows 1.7-4% faster this way, 1152-byte rows 1-3%
+//    slower.
+// A thread walks its items with cursors (leftover q, and x: the chunk, or
+// the task within the row's span), stepping by the stride's quotient and
+// remainder: the one division is at construction.  The walk is issue-bound
+// where it matters (all warps of a CTA issue their first loads at once), and
+// a division per item cost ~1.5 us there on decode-sized calls.
+struct CopyCursor {
+    int q, x;
+};
+
+struct CopyWalk {
+    int rows, CH, X, dq, dx, lane;
     bool aligned;
-    __device__ __forceinline__ CopyMap(bool al, int rows, int ch, int first_, int stride_)
-        : CH(ch), H((ch + 3 + 31) / 32), first(first_), stride(stride_),
-          lane((int)(threadIdx.x & 31)), aligned(al)
+    uint32_t base_lo;   // low bits of the host rows' base: alignment only
+    uint32_t B;
+    CopyCursor start;
+    __device__ __forceinline__ CopyWalk(bool al, int rows_, int ch, int first, int stride,
+                                        const uint8_t *hrow0, int64_t B_)
+        : rows(rows_), CH(ch), X(al ? (ch + 3 + 31) / 32 : ch), lane((int)(threadIdx.x & 31)),
+          aligned(al), base_lo((uint32_t)reinterpret_cast<uintptr_t>(hrow0)), B((uint32_t)B_)
     {
-        limit = rows * (al ? H : ch);
-        items = limit > first ? (limit - first + stride - 1) / stride : 0;
+        dq = stride / X;
+        dx = stride - dq * X;
+        start.q = first / X;
+        start.x = first - start.q * X;
     }
-    // leftover q and chunk c of item n; false if it moves nothing
-    __device__ __forceinline__ bool at(int n, const int32_t *left_row, const uint8_t *hrow0,
-                                       int64_t B, int &q, int &c) const
+    __device__ __forceinline__ void next(CopyCursor &k) const
     {
-        if (n >= items) return false;
-        const int e = first + n * stride;
+        k.q += dq;
+        k.x += dx;
+        if (k.x >= X) {
+            k.x -= X;
+            ++k.q;
+        }
+    }
+    // chunk c of leftover k.q (whose host row is *hr) for cursor k; false
+    // if the item moves nothing
+    __device__ __forceinline__ bool at(const CopyCursor &k, const int32_t *left_row, int32_t &hr,
+                                       int &c) const
+    {
+        if (k.q >= rows) return false;
+        hr = left_row[k.q];
         if (!aligned) {
-            q = e / CH;
-            c = e - q * CH;
+            c = k.x;
             return true;
         }
-        q = e / H;
-        const int h = e - q * H;
-        const int delta = (int)((reinterpret_cast<uintptr_t>(hrow0 + (int64_t)left_row[q] * B) >> 4) & 3);
-        c = h * 32 + lane - delta;
+        const int delta = (int)(((base_lo + (uint32_t)hr * B) >> 4) & 3u);
+        c = k.x * 32 + lane - delta;
         return c >= 0 && c < CH;
     }
+    __device__ __forceinline__ bool done(const CopyCursor &k) const { return k.q >= rows; }
 };
 
 // Resident row of position t from its block id `id` (-1: not resident), or
@@ -410,6 +434,38 @@ __device__ __forceinline__ void finish_untouched(const ResolveLaunch &a, int r,
     }
 }
 
+// A copier's share of the leftover rows: the first COPY_WINDOW loads go out
+// at once; once the cluster barrier has released the victims (filed under
+// the leftovers' indices in arr_vict; *go == 0: nothing to store after all),
+// each stored chunk's register takes the load COPY_WINDOW items ahead.
+__device__ __forceinline__ void copier_rows(const CopyWalk &walk, const int32_t *lrow,
+                                            const uint16_t *arr_vict, const uint8_t *hrow0,
+                                            uint8_t *drow0, int64_t B, const uint32_t *go)
+{
+    uint4 pv[COPY_WINDOW];
+    CopyCursor ld = walk.start, st = walk.start;
+#pragma unroll
+    for (int u = 0; u < COPY_WINDOW; ++u) {
+        int32_t hr;
+        int cc;
+        if (walk.at(ld, lrow, hr, cc)) pv[u] = ld_host_v4(hrow0 + (int64_t)hr * B + cc * 16);
+        walk.next(ld);
+    }
+    cluster_wait();                       // the victims are in (or no copy)
+    if (*go == 0) return;
+    while (!walk.done(st)) {
+#pragma unroll
+        for (int u = 0; u < COPY_WINDOW; ++u) {
+            int32_t hr;
+            int cc;
+            if (walk.at(st, lrow, hr, cc)) st_v4(drow0 + (int64_t)arr_vict[st.q] * B + cc * 16, pv[u]);
+            walk.next(st);
+            if (walk.at(ld, lrow, hr, cc)) pv[u] = ld_host_v4(hrow0 + (int64_t)hr * B + cc * 16);
+            walk.next(ld);
+        }
+    }
+}
+
 // A copier CTA (rank c >= 1 of request r's cluster of 1 + ncopy CTAs).  It
 // resolves nothing and touches no hot state: it loads the miss rows the
 // resolver (rank 0) lists in this CTA's shared memory at classification, and
@@ -439,28 +495,10 @@ __device__ __forceinline__ void copier_main(const ResolveLaunch &a, const Smem &
     // got its loads out (host loads in flight hold up the issue of more).
     cluster_arrive();
     const int rows = (int)sm.pub[0];
-    const CopyMap map = a.aligned_rows
-                            ? CopyMap(true, rows, CH, (c - 1) * (NT / 32) + (tid >> 5), ncopy * (NT / 32))
-                            : CopyMap(false, rows, CH, (c - 1) * NT + tid, ncopy * NT);
-    const int32_t *lrow = sm.left_row;
-    uint4 pv[COPY_WINDOW];
-#pragma unroll
-    for (int u = 0; u < COPY_WINDOW; ++u) {
-        int q, cc;
-        if (map.at(u, lrow, hrow0, B, q, cc)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + cc * 16);
-    }
-    cluster_wait();                       // phase 2: the victims are in
-    if (sm.pub[1] == 0) return;           // no copy after all (protected rows)
-    for (int n0 = 0; n0 < map.items; n0 += COPY_WINDOW) {
-#pragma unroll
-        for (int u = 0; u < COPY_WINDOW; ++u) {
-            int q, cc;
-            if (map.at(n0 + u, lrow, hrow0, B, q, cc))
-                st_v4(drow0 + (int64_t)sm.arr_vict[q] * B + cc * 16, pv[u]);
-            if (map.at(n0 + u + COPY_WINDOW, lrow, hrow0, B, q, cc))
-                pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + cc * 16);
-        }
-    }
+    const CopyWalk walk = a.aligned_rows
+                              ? CopyWalk(true, rows, CH, (c - 1) * (NT / 32) + (tid >> 5), ncopy * (NT / 32), hrow0, B)
+                              : CopyWalk(false, rows, CH, (c - 1) * NT + tid, ncopy * NT, hrow0, B);
+    copier_rows(walk, sm.left_row, sm.arr_vict, hrow0, drow0, B, &sm.pub[1]);
 }
 
 // Misses and their arrival indices, from the staged resident-token bitmap
@@ -578,28 +616,10 @@ __device__ __forceinline__ void copier_self(const ResolveLaunch &a, const Smem &
     const uint8_t *hrow0 = a.store.host + (hb ? 0 : off) * B;
     uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
     const int rows = (int)m_all;
-    const CopyMap map = a.aligned_rows
-                            ? CopyMap(true, rows, CH, (c - 1) * (NT / 32) + (tid >> 5), ncopy * (NT / 32))
-                            : CopyMap(false, rows, CH, (c - 1) * NT + tid, ncopy * NT);
-    const int32_t *lrow = sm.left_row;
-    uint4 pv[COPY_WINDOW];
-#pragma unroll
-    for (int u = 0; u < COPY_WINDOW; ++u) {
-        int q, cc;
-        if (map.at(u, lrow, hrow0, B, q, cc)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + cc * 16);
-    }
-    cluster_wait();                       // the victims are in (or no copy)
-    if (sm.pub[1] == 0) return;
-    for (int n0 = 0; n0 < map.items; n0 += COPY_WINDOW) {
-#pragma unroll
-        for (int u = 0; u < COPY_WINDOW; ++u) {
-            int q, cc;
-            if (map.at(n0 + u, lrow, hrow0, B, q, cc))
-                st_v4(drow0 + (int64_t)sm.arr_vict[q] * B + cc * 16, pv[u]);
-            if (map.at(n0 + u + COPY_WINDOW, lrow, hrow0, B, q, cc))
-                pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + cc * 16);
-        }
-    }
+    const CopyWalk walk = a.aligned_rows
+                              ? CopyWalk(true, rows, CH, (c - 1) * (NT / 32) + (tid >> 5), ncopy * (NT / 32), hrow0, B)
+                              : CopyWalk(false, rows, CH, (c - 1) * NT + tid, ncopy * NT, hrow0, B);
+    copier_rows(walk, sm.left_row, sm.arr_vict, hrow0, drow0, B, &sm.pub[1]);
 }
 
 template <int KT>
@@ -929,14 +949,17 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int m_arr = (int)m_all;
     const bool defer = a.deferred && (int64_t)m_arr * B > a.defer_bytes;
     const int nleft = (a.fused_copy && !defer && !ncopy) ? max(m_arr - SR, 0) : 0;
-    const CopyMap map = a.aligned_rows ? CopyMap(true, nleft, CH, tid >> 5, NT / 32)
-                                       : CopyMap(false, nleft, CH, tid, NT);
+    const CopyWalk walk = a.aligned_rows ? CopyWalk(true, nleft, CH, tid >> 5, NT / 32, hrow0, B)
+                                         : CopyWalk(false, nleft, CH, tid, NT, hrow0, B);
     const int32_t *lrow = sm.left_row;
     uint4 pv[COPY_WINDOW];
+    CopyCursor cur_ld = walk.start;
 #pragma unroll
     for (int u = 0; u < EARLY; ++u) {
-        int q, c;
-        if (map.at(u, lrow, hrow0, B, q, c)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + c * 16);
+        int32_t hr;
+        int c;
+        if (walk.at(cur_ld, lrow, hr, c)) pv[u] = ld_host_v4(hrow0 + (int64_t)hr * B + c * 16);
+        walk.next(cur_ld);
     }
     late_grid_wait(a);   // the first global writes follow
 
@@ -1136,17 +1159,22 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     // COPY_WINDOW loads in flight until its last ones.
 #pragma unroll
     for (int u = EARLY; u < COPY_WINDOW; ++u) {
-        int q, c;
-        if (map.at(u, lrow, hrow0, B, q, c)) pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + c * 16);
+        int32_t hr;
+        int c;
+        if (walk.at(cur_ld, lrow, hr, c)) pv[u] = ld_host_v4(hrow0 + (int64_t)hr * B + c * 16);
+        walk.next(cur_ld);
     }
-    for (int n0 = 0; n0 < map.items; n0 += COPY_WINDOW) {
+    CopyCursor cur_st = walk.start;
+    while (!walk.done(cur_st)) {
 #pragma unroll
         for (int u = 0; u < COPY_WINDOW; ++u) {
-            int q, c;
-            if (map.at(n0 + u, lrow, hrow0, B, q, c))
-                st_v4(drow0 + (int64_t)sm.arr_vict[SR + q] * B + c * 16, pv[u]);
-            if (map.at(n0 + u + COPY_WINDOW, lrow, hrow0, B, q, c))
-                pv[u] = ld_host_v4(hrow0 + (int64_t)lrow[q] * B + c * 16);
+            int32_t hr;
+            int c;
+            if (walk.at(cur_st, lrow, hr, c))
+                st_v4(drow0 + (int64_t)sm.arr_vict[SR + cur_st.q] * B + c * 16, pv[u]);
+            walk.next(cur_st);
+            if (walk.at(cur_ld, lrow, hr, c)) pv[u] = ld_host_v4(hrow0 + (int64_t)hr * B + c * 16);
+            walk.next(cur_ld);
         }
     }
     // the staged rows, once they have all landed, one bulk store per row

@@ -55,7 +55,11 @@ int hisparse_link_probe(const void *src, void *dst, int64_t bytes, int32_t num_c
  * resolver: for i < n, row i of `dst` (device, n * row_bytes bytes) <- row
  * rows[i] of `src` (pinned host memory mapped into the device address
  * space, rows of row_bytes bytes), 16-byte loads with 8 in flight per
- * thread, `num_ctas` CTAs of 1024 threads (0 = one per SM).  rows: device
+ * thread, `num_ctas` CTAs of 1024 threads (0 = one per SM).  Rows under
+ * 1 KB are read as the resolve kernel's miss copy reads them: each warp
+ * load covers 512 bytes of the 64-byte-aligned span around one row, lanes
+ * outside the row idle, and every thread keeps a rolling window of 8 loads;
+ * longer rows are read as consecutive 16-byte chunks.  rows: device
  * int64 [n], each in [0, rows of src) -- the caller guarantees the range;
  * the kernel does not check it.  row_bytes a positive multiple of 16; src
  * and dst 16-byte aligned.  Measures what random rows reach over the host
