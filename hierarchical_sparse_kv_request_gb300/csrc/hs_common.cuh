@@ -161,6 +161,13 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
 //                    for the hits' slots.
 constexpr int32_t kLookupGather = 0, kLookupInverse = 1, kLookupResident = 2;
 
+// Byte offsets of the resolve kernel's shared-memory regions (a launch-time
+// constant: the host lays the regions out once per launch, so no thread
+// recomputes the layout).
+struct ResolveSmem {
+    uint32_t hit, sel, miss, lru, s2t, inv, res, dup, tbl, chunk, vict, lrow, avict, bar, cnt, stage;
+};
+
 struct ResolveLaunch {
     const int32_t *topk;
     const int32_t *seq_lens;
@@ -192,6 +199,7 @@ struct ResolveLaunch {
     int32_t ncopy;            // copier CTAs per request (a cluster of 1 + ncopy CTAs:
                               // the resolver does no copy); 0: the resolver copies.
                               // Needs fused_copy, no deferral and stage_rows == 0.
+    ResolveSmem smem;         // filled by launch_resolve
 };
 
 // Shared-memory bytes the resolve kernel needs for this geometry

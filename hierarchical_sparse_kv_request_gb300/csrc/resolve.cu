@@ -90,7 +90,7 @@ struct SmemPlan {
 // miss rank and by arrival index, the leftover host rows, the staging
 // mbarrier and arrival counter, and `stage_rows` rows of B bytes staged by
 // the bulk-copy engine.
-__host__ __device__ inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t, int lookup,
+inline SmemPlan plan_smem(int k, int D, int max_cap, bool stage_s2t, int lookup,
                                               int tbl_stride, int stage_rows, int64_t B)
 {
     SmemPlan p;
@@ -351,10 +351,16 @@ struct CopyWalk {
         : rows(rows_), CH(ch), X(al ? (ch + 3 + 31) / 32 : ch), lane((int)(threadIdx.x & 31)),
           aligned(al), base_lo((uint32_t)reinterpret_cast<uintptr_t>(hrow0)), B((uint32_t)B_)
     {
-        dq = stride / X;
+        dq = div_small(stride, X);
         dx = stride - dq * X;
-        start.q = first / X;
+        start.q = div_small(first, X);
         start.x = first - start.q * X;
+    }
+    // v / X for v >= 0; the spans of rows under 1 KB take X <= 3 tasks, those
+    // of 480- to 976-byte rows 2 (a shift instead of a division sequence)
+    static __device__ __forceinline__ int div_small(int v, int X)
+    {
+        return X == 1 ? v : X == 2 ? (v >> 1) : v / X;
     }
     __device__ __forceinline__ void next(CopyCursor &k) const
     {
@@ -640,8 +646,7 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     const int SR = a.stage_rows;   // rows the bulk-copy engine may stage (0: none)
 
     const int32_t hb = a.g.hb;
-    const SmemPlan sp = plan_smem(k, D, a.max_cap, a.stage_s2t, a.lookup,
-                                  hb ? a.g.tbl_stride : 0, SR, B);
+    const ResolveSmem &sp = a.smem;   // the layout of plan_smem, laid out by the host
     Smem sm;
     sm.warp_tot = reinterpret_cast<uint32_t *>(smem_raw);
     sm.hitbits = reinterpret_cast<uint32_t *>(smem_raw + sp.hit);
@@ -1284,15 +1289,21 @@ cudaError_t resolve_max_clusters(int k, int ctas, size_t smem, int *clusters)
     return max_clusters_kt<8>(ctas, smem, clusters);
 }
 
-cudaError_t launch_resolve(const ResolveLaunch &a, cudaStream_t s)
+cudaError_t launch_resolve(const ResolveLaunch &a_in, cudaStream_t s)
 {
-    const size_t smem = resolve_smem_bytes(a.g.k, a.g.D, a.max_cap, a.stage_s2t, a.lookup,
-                                           a.g.hb ? a.g.tbl_stride : 0, a.stage_rows, a.g.B);
+    const SmemPlan p = plan_smem(a_in.g.k, a_in.g.D, a_in.max_cap, a_in.stage_s2t, a_in.lookup,
+                                 a_in.g.hb ? a_in.g.tbl_stride : 0, a_in.stage_rows, a_in.g.B);
+    if (p.total > (size_t)UINT32_MAX) return cudaErrorInvalidValue;
+    ResolveLaunch a = a_in;
+    a.smem = ResolveSmem{(uint32_t)p.hit,  (uint32_t)p.sel,   (uint32_t)p.miss, (uint32_t)p.lru,
+                         (uint32_t)p.s2t,  (uint32_t)p.inv,   (uint32_t)p.res,  (uint32_t)p.dup,
+                         (uint32_t)p.tbl,  (uint32_t)p.chunk, (uint32_t)p.vict, (uint32_t)p.lrow,
+                         (uint32_t)p.avict, (uint32_t)p.bar,  (uint32_t)p.cnt,  (uint32_t)p.stage};
     const int kt = (a.g.k + NT - 1) / NT;
-    if (kt <= 1) return launch_kt<1>(a, s, smem);
-    if (kt <= 2) return launch_kt<2>(a, s, smem);
-    if (kt <= 4) return launch_kt<4>(a, s, smem);
-    return launch_kt<8>(a, s, smem);
+    if (kt <= 1) return launch_kt<1>(a, s, p.total);
+    if (kt <= 2) return launch_kt<2>(a, s, p.total);
+    if (kt <= 4) return launch_kt<4>(a, s, p.total);
+    return launch_kt<8>(a, s, p.total);
 }
 
 }  // namespace hs
