@@ -512,9 +512,9 @@ __device__ __forceinline__ void copier_main(const ResolveLaunch &a, const Smem &
 // valid position, not a resident page, its bit is clear and it has a host row.
 // The indices run over [0, m) in (warp, entry, lane) order: warp ballots place
 // each miss within its warp, one barrier publishes the warps' counts (and
-// error flags) through warp_tot, and each warp scans them for its base.  The
-// resolver and self-classifying copiers both number the misses this way, from
-// the same inputs, so they build the same list.
+// error flags) through warp_tot, and each warp scans them for its base.  A
+// self-classifying copier numbers its misses in the same order from the same
+// inputs (without the flags and packed indices), so both build the same list.
 template <int KT>
 __device__ __forceinline__ void number_misses(uint32_t miss, uint32_t f, uint32_t *warp_tot,
                                               PackedIdx<KT> &arr, uint32_t &flags, uint32_t &m_all)
@@ -611,13 +611,35 @@ __device__ __forceinline__ void copier_self(const ResolveLaunch &a, const Smem &
         if (hb && sm.tbl_s[x / hb] < 0) continue;
         miss |= 1u << i;
     }
-    PackedIdx<KT> arr;
-    uint32_t flags, m_all;
-    number_misses<KT>(miss, 0u, sm.warp_tot, arr, flags, m_all);
+    // The list in arrival order, numbered as number_misses numbers it (warp,
+    // entry slot, lane), without its packed indices and error flags: the
+    // copier files each miss's host row at once.
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint32_t below = (1u << lane) - 1u;
+    uint32_t wmask[KT];
+    uint32_t in_warp = 0;
 #pragma unroll
-    for (int i = 0; i < KT; ++i)
-        if (arr.get(i) >= 0)
-            sm.left_row[arr.get(i)] = hb ? sm.tbl_s[t[i] / hb] * hb + t[i] % hb : t[i];
+    for (int i = 0; i < KT; ++i) {
+        wmask[i] = __ballot_sync(0xffffffffu, (miss >> i) & 1u);
+        in_warp += (uint32_t)__popc(wmask[i]);
+    }
+    if (lane == 0) sm.warp_tot[warp] = in_warp;
+    __syncthreads();
+    uint32_t incl = sm.warp_tot[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    const uint32_t m_all = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t pos = __shfl_sync(0xffffffffu, incl, (warp + 31) & 31);
+    if (warp == 0) pos = 0;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        if ((miss >> i) & 1u)
+            sm.left_row[pos + __popc(wmask[i] & below)] = hb ? sm.tbl_s[t[i] / hb] * hb + t[i] % hb : t[i];
+        pos += (uint32_t)__popc(wmask[i]);
+    }
     __syncthreads();
     const uint8_t *hrow0 = a.store.host + (hb ? 0 : off) * B;
     uint8_t *drow0 = a.store.dev + (int64_t)r * D * B;
