@@ -142,7 +142,7 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HISPARSE_OK : HISPARSE_ERR_CUDA; }
 
 // Rows shorter than this are copied in 64-byte-aligned spans (see the
-// resolve kernel's CopyMap): measured faster for 656-byte rows, slower for
+// resolve kernel's CopyWalk): measured faster for 656-byte rows, slower for
 // 1152-byte ones.
 constexpr int64_t kAlignedRowsBelow = 1024;
 

@@ -478,8 +478,9 @@ __device__ __forceinline__ void copier_rows(const CopyWalk &walk, const int32_t 
 // stores them into the victim slots the resolver files there once the block
 // scans have chosen them.  Its SM issues host loads and nothing else, so
 // they queue behind nothing, and the resolver's own stores to the hot state
-// queue behind no host loads.  Copier c takes the rounds n of NT chunks of
-// the list with n % ncopy == c - 1.
+// queue behind no host loads.  Copier c takes the rounds n of the list with
+// n % ncopy == c - 1: rounds of NT chunks (flat mapping) or of 32 warp tasks
+// (aligned spans).
 __device__ __forceinline__ void copier_main(const ResolveLaunch &a, const Smem &sm, int r, int c,
                                             int ncopy)
 {
