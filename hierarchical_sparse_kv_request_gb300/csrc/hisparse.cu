@@ -141,10 +141,6 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HISPARSE_OK : HISPARSE_ERR_CUDA; }
 
-// Rows shorter than this are copied in 64-byte-aligned spans (see the
-// resolve kernel's CopyWalk): measured faster for 656-byte rows, slower for
-// 1152-byte ones.
-constexpr int64_t kAlignedRowsBelow = 1024;
 
 void note_launch_all(hisparse_handle *h, cudaStream_t s)
 {
@@ -753,7 +749,7 @@ int swap_in_impl(hisparse_t h, int32_t layer, const int32_t *topk_idx, const int
     a.stage_rows = (!split && !autom) ? h->stage_rows : 0;
     a.programmatic = h->programmatic;
     a.wait_late = h->programmatic && left_layer_alone(h, as_stream(stream), layer);
-    a.aligned_rows = h->B < kAlignedRowsBelow;
+    a.aligned_rows = h->B < hs::kAlignedRowsBelow;
     // copier CTAs only where the resolving CTA would copy every row itself
     a.ncopy = (!split && !autom && a.stage_rows == 0) ? h->copy_ctas - 1 : 0;
     const bool wide_copy = split || autom;
@@ -1110,7 +1106,7 @@ int hisparse_swap_in_noalloc(hisparse_t h, int32_t layer, const int32_t *topk_id
     a.programmatic = h->programmatic;
     a.ncopy = 0;
     a.wait_late = false;
-    a.aligned_rows = h->B < kAlignedRowsBelow;
+    a.aligned_rows = h->B < hs::kAlignedRowsBelow;
     a.plan_rows = scratch;
     a.plan_counts = scratch + (int64_t)h->R * h->k * 2;
     cudaError_t e = hs::launch_resolve(a, as_stream(stream));

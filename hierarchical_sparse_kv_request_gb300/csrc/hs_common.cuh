@@ -22,6 +22,11 @@ constexpr int kStatusNoHostRow = 6;
 constexpr int kStatusCapacity = 7;
 constexpr int kStatusCopyTimeout = 8;
 constexpr int32_t kResidentFlag = 1 << 30;  // marks a row of the resident pool
+// Rows shorter than this many bytes are copied (and gathered by the link
+// probe) in 64-byte-aligned spans of 512-byte warp tasks; longer rows as
+// consecutive 16-byte chunks.  Measured on GB300: faster for 656-byte rows,
+// slower for 1152-byte ones.
+constexpr int64_t kAlignedRowsBelow = 1024;
 
 // Hot state of one state-owning layer.  Per request r:
 //   tok2slot[host_off[r] + t]  slot holding token t, or -1   (host_cap[r] ints)

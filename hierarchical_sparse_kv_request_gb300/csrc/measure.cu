@@ -49,8 +49,6 @@ __global__ void __launch_bounds__(256) synthetic_compute_kernel(uint4 *buf, int6
 
 constexpr int PROBE_NT = 1024;
 constexpr int PROBE_UNROLL = 8;
-// rows shorter than this are gathered in 64-byte-aligned spans
-constexpr int64_t kGatherAlignedBelow = 1024;
 
 __global__ void __launch_bounds__(PROBE_NT) link_probe_kernel(const uint8_t *src, uint8_t *dst,
                                                               int64_t chunks)
@@ -175,7 +173,7 @@ cudaError_t launch_link_gather(const void *src, int64_t row_bytes, const int64_t
     const int64_t chunks = row_bytes / 16;
     const uint8_t *sp = static_cast<const uint8_t *>(src);
     uint8_t *dp = static_cast<uint8_t *>(dst);
-    if (row_bytes < kGatherAlignedBelow) {
+    if (row_bytes < kAlignedRowsBelow) {
         // tasks: n * H; the last task index, plus one stride, must not wrap
         const int64_t H = (chunks + 3 + 31) / 32;
         const int64_t reach = n * H + (int64_t)num_ctas * (PROBE_NT / 32) * (PROBE_UNROLL + 1);
