@@ -496,19 +496,25 @@ int hisparse_set_stage_rows(hisparse_t h, int32_t rows);
 /*
  * hisparse_set_copy_ctas: how many CTAs serve each request of a fused-copy
  * swap-in (HISPARSE_COPY_FUSED with no staged rows; other modes ignore it).
- * ctas = 1 (the default): the one CTA that resolves the request also loads
- * its miss rows from pinned host memory.  ctas = 2..4: each request gets a
- * thread-block cluster of that many CTAs on different SMs; rank 0 resolves
- * (hit lookup, victims, every state write) and issues no host loads, and the
- * ctas - 1 others copy: at classification rank 0 writes the list of miss rows
- * into their shared memory, and they start loading those rows from the host
- * right away; once the victims are chosen it writes the victim slots there
- * too, and they store the rows.  Each SM then keeps one kind of traffic in
- * flight: on one SM, host loads in flight hold up that SM's stores to the
- * hot state.  Results are identical whatever the count.  Measured on GB300
- * (decode_40k, 32 requests, kernel-only): 47.0 us per call with 1, 45.6 us
- * with 4.  INVALID_ARG unless 1 <= ctas <= 4; UNSUPPORTED if the GPU cannot
- * hold even one such cluster of resolve CTAs.  Read at each swap-in launch.
+ * A new handle starts with the largest count, up to 4, at which the GPU
+ * holds the clusters of all its requests at once (see
+ * hisparse_get_copy_ctas).  ctas = 1: the one CTA that resolves the request
+ * also loads its miss rows from pinned host memory.  ctas = 2..4: each
+ * request gets a thread-block cluster of that many CTAs on different SMs;
+ * rank 0 resolves (hit lookup, victims, every state write) and issues no
+ * host loads, and the ctas - 1 others copy.  With the resident-token bitmap
+ * (the lookup the handle picks when it fits in shared memory) each copier
+ * stages the same rows as rank 0, finds the same misses in the same order
+ * and starts loading their rows from the host at once; otherwise rank 0
+ * writes the list of miss rows into the copiers' shared memory at
+ * classification.  Once the victims are chosen rank 0 writes the victim
+ * slots there, and the copiers store the rows.  Each SM then keeps one kind
+ * of traffic in flight: on one SM, host loads in flight hold up that SM's
+ * stores to the hot state.  Results are identical whatever the count.
+ * Measured on GB300 (decode_40k, 32 requests, kernel-only): 41.5-41.7 us per
+ * call with 4, 42.5 us with 3, 43.3 us with 2.  INVALID_ARG unless
+ * 1 <= ctas <= 4; UNSUPPORTED if the GPU cannot hold even one such cluster of
+ * resolve CTAs.  Read at each swap-in launch.
  */
 int hisparse_set_copy_ctas(hisparse_t h, int32_t ctas);
 
