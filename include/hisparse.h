@@ -486,7 +486,8 @@ int hisparse_set_copy_mode(hisparse_t h, int32_t mode);
  * the shared memory left over by the resolver holds (~259 rows of 656 B at
  * k 2048, D 6144); a larger count is clamped to that.  Results are
  * identical whatever the count; only the route of the bytes differs.
- * Measured on GB300 (kernel-only step time): decode_40k 45.6 us with 0,
+ * Measured on GB300 with an earlier kernel of this design, one CTA per
+ * request (kernel-only step time): decode_40k 45.6 us with 0,
  * 46.5 us with 16, 48.9 us with 64 and 57.6 us with all; mixed_len 1.009 ms
  * with 0, 1.003 ms with all; spec_verify 3.576 ms with 0, 3.591 ms with
  * all.  Read at each swap-in launch.  INVALID_ARG for rows < -1.
