@@ -1103,14 +1103,15 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
     }
     __syncthreads();
 
-    // The resident-token bitmap row in global memory, if kept: evicted tokens
-    // leave it, misses enter it (atomics: threads share its words).
-    uint32_t *resg = a.st.resbits ? a.st.resbits + (int64_t)r * a.st.res_words : nullptr;
-    // State writes (stores only: no load of their own to wait for).  Misses
-    // take victims by ascending token rank; each victim is also filed under
-    // the miss's arrival index, where the copies below look it up.
+    // Each miss's victim: misses take victims by ascending token rank, and
+    // each victim is also filed under the miss's arrival index, where the
+    // copies look it up.  With self-classifying copiers the victims go out
+    // before this CTA's global state writes, so the copiers' stores wait for
+    // nothing else.
+    int32_t vict[KT];
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
+        vict[i] = -1;
         const int j = tid + i * NT;
         const int32_t x = t[i];
         if (j >= k || x < 0 || rid[i] >= 0 || s[i] >= 0) continue;
@@ -1121,6 +1122,28 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
         rank += __popc(sm.missbits[w] & ((1u << (x & 31)) - 1u));
         const int v = sm.victims[rank];
         sm.arr_vict[arr.get(i)] = (uint16_t)v;
+        vict[i] = v | (int32_t)(rank << 16);   // slot (< 65536) and rank (< k)
+    }
+    if (self_list) {
+        if (copying) {
+            __syncthreads();
+            copy_to_copiers(sm.arr_vict, (m_all * 2u + 15u) / 16u * 16u, ncopy);
+        }
+        if (tid == 0)
+            for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[1], q, copying ? 1u : 0u);
+        cluster_arrive();
+    }
+    // The resident-token bitmap row in global memory, if kept: evicted tokens
+    // leave it, misses enter it (atomics: threads share its words).
+    uint32_t *resg = a.st.resbits ? a.st.resbits + (int64_t)r * a.st.res_words : nullptr;
+    // State writes (stores only: no load of their own to wait for).
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+        if (vict[i] < 0) continue;
+        const int j = tid + i * NT;
+        const int32_t x = t[i];
+        const int v = vict[i] & 0xFFFF;
+        const uint32_t rank = (uint32_t)vict[i] >> 16;
         const int32_t old = sm.s2t_s ? sm.s2t_s[v] : slot2tok[v];
         if (old >= 0 && (int64_t)old < cap) {
             tok2slot[old] = -1;
@@ -1136,16 +1159,8 @@ __global__ void __launch_bounds__(NT, 1) resolve_kernel(ResolveLaunch a)
             pr[1] = v;
         }
     }
-    // The copiers may store their rows now (phase 2): the victims go out.
-    if (self_list) {
-        if (copying) {
-            __syncthreads();
-            copy_to_copiers(sm.arr_vict, (m_all * 2u + 15u) / 16u * 16u, ncopy);
-        }
-        if (tid == 0)
-            for (int q = 1; q <= ncopy; ++q) st_remote_u32(&sm.pub[1], q, copying ? 1u : 0u);
-        cluster_arrive();
-    } else if (ncopy) {
+    // Message protocol: the copiers may store their rows now (phase 2).
+    if (!self_list && ncopy) {
         cluster_wait();
         if (copying) {
             __syncthreads();
