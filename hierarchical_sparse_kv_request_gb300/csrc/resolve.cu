@@ -30,13 +30,18 @@
 //      otherwise the list goes to them (distributed shared memory, released
 //      by a cluster barrier) and they load it at once;
 //   3. then the block scans give each miss its rank in token order and its
-//      victim; all state writes are plain stores (the slot->token row is
-//      staged, so no write waits on a load of its own), and each victim is
-//      filed under its miss's arrival index (in the copiers' shared memory,
-//      released by a cluster barrier);
+//      victim, and each victim is filed under its miss's arrival index (in
+//      the copiers' shared memory, released by a cluster barrier; copiers
+//      that classify for themselves get their victims before the resolver
+//      writes the hot state); all state writes are plain stores (the
+//      slot->token row is staged, so no write waits on a load of its own);
 //   4. finally the rows are stored to their victims while a rolling window
 //      of 8 loads per thread keeps the link busy to the end.  Rows under
 //      1 KB are copied in 64-byte-aligned spans of one row per warp load.
+//      Each thread walks its items with cursors (no division per item): all
+//      warps issue their first loads at once, so the issue slots spent
+//      before them are on the critical path, and for the same reason the
+//      host lays out the shared memory once per launch.
 // Only the bytes' route differs from a copy in rank order; where each row
 // lands is fixed by its rank, so the results are the same.
 //
